@@ -1,0 +1,466 @@
+#!/usr/bin/env python3
+"""Benchmark of the KIVI hot path on GB300 (libkivi through its C ABI).
+
+One step = one pass of the whole path over one batch of the workload:
+prefix encode of keys and values (quantize + pack + residual copy),
+materialize both back to fp16, append one decoded token per sequence, and
+fused-dequant decode attention (q.K_hat^T, softmax, p.V_hat).  The default
+workload is the Llama-2-7B-shaped layer: K, V fp16 [8, 32, 4096, 128],
+int2 keys and values, G = 32, R = 128, q [8, 32, 1, 128].
+
+Metric: fp16-equivalent KV gigabytes per second over the step (the fp16 bytes
+of K and V the step encodes, materializes and attends over, divided by the
+step time), with decode tokens/s and per-kernel HBM roofline fractions.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+    python bench.py --impl reference ...   # the CPU oracle, timed on host cores
+
+Under torchrun each rank runs an independent replica on its own GPU (the path
+has no cross-GPU exchange); the timed region is bracketed by barriers and the
+slowest rank's time is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV quant/dequant GB/s (fp16-equiv) & decode-attn tok/s; % of HBM roofline"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+# ------------------------------------------------------------------ setup --
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--impl", default="kivi", choices=["kivi", "reference"])
+    p.add_argument("--workload", default="llama2_7b_layer")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "kivi_bit_kv_gb300", "csrc", "*"))):
+        with open(p, "rb") as f:
+            h.update(os.path.basename(p).encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if the kernel
+    sources are unchanged since it was taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        e = d[workload][kernel]
+        if e.get("source_hash") != kernel_source_hash():
+            return None
+        return float(e["dram_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi SM clock / throttle-reason samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.out = ""
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                self.out, _ = self.proc.communicate(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for line in (self.out or "").strip().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 7:
+                continue
+            try:
+                rows.append((float(parts[0]), float(parts[1]), parts[2:]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for _, _, flags in rows:
+            for n, v in zip(names, flags[1:]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+# ------------------------------------------------------- byte accounting --
+
+def alg_bytes(w, T: int, n_dec: int) -> dict:
+    """Algorithmic HBM bytes (read + write) of each call in one step.
+
+    T: prefix tokens encoded / materialized; n_dec: tokens attended over by
+    the decode (T + 1 after the append)."""
+    BH, D, G, Rr = w.B * w.H, w.D, w.G, w.R
+    def split(n):
+        tq = max(0, (n - Rr) // G * G)
+        return tq, n - tq
+    tq, res = split(T)
+    kcodes = BH * tq * D * w.bits_k // 8
+    vcodes = BH * tq * D * w.bits_v // 8
+    kstats = BH * (tq // G) * D * 8
+    vstats = BH * tq * (D // G) * 8
+    resb = BH * res * D * 2
+    fp16 = BH * T * D * 2
+    tqd, resd = split(n_dec)
+    kcd = BH * tqd * D * w.bits_k // 8 + BH * (tqd // G) * D * 8 + BH * resd * D * 2
+    vcd = BH * tqd * D * w.bits_v // 8 + BH * tqd * (D // G) * 8 + BH * resd * D * 2
+    qb = w.B * w.Hq * D * 2
+    lg = w.B * w.Hq * n_dec * 4
+    return {
+        "quant_keys": fp16 + kcodes + kstats + resb,
+        "quant_values": fp16 + vcodes + vstats + resb,
+        "dequant_keys": kcodes + kstats + resb + fp16,
+        "dequant_values": vcodes + vstats + resb + fp16,
+        "append": 2 * BH * D * 2 * 2,
+        "decode_qk": kcd + qb + lg,
+        "decode_pv": vcd + lg + w.B * w.Hq * D * 4,
+    }
+
+
+def fp16_equiv_bytes(w, T: int, n_dec: int) -> int:
+    """fp16 K+V bytes the step encodes, materializes and attends over."""
+    BH, D = w.B * w.H, w.D
+    return 2 * BH * T * D * 2 + 2 * BH * T * D * 2 + 2 * BH * n_dec * D * 2 + 2 * BH * D * 2
+
+
+# --------------------------------------------------------------- GPU arm --
+
+CALLS = ["quant_keys", "quant_values", "dequant_keys", "dequant_values", "append",
+         "decode_qk", "decode_pv"]
+LAUNCHES_PER_STEP = 9  # append and decode_pv enqueue two kernels each
+
+
+def run_kivi(args, rank, world, local):
+    import torch
+    from kivi_bit_kv_gb300 import KiviCache, abi
+    from kivi_bit_kv_gb300 import workloads as W
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if dist.is_nccl_available() else "gloo")
+    w = W.WORKLOADS[args.workload]
+    T = w.T
+    Tmax = (T + 1 + w.G - 1) // w.G * w.G + w.G
+    K, V = W.make_kv(w, device=dev)
+    q = W.make_q(w, device=dev)
+    kn, vn = W.make_step_tokens(w, 1, device=dev)
+    kn, vn = kn[0].contiguous(), vn[0].contiguous()
+    cache = KiviCache(w.B, w.H, w.D, w.bits_k, w.bits_v, w.G, w.R, Tmax, device=dev)
+    kh = torch.empty((w.B, w.H, T, w.D), dtype=torch.float16, device=dev)
+    vh = torch.empty_like(kh)
+    ld = (Tmax + 3) // 4 * 4
+    logits = torch.empty((w.B, w.Hq, ld), dtype=torch.float32, device=dev)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    ws = cache.workspace(w.Hq)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        fns = [lambda: abi.kivi_quant_keys(cache, K), lambda: abi.kivi_quant_values(cache, V),
+               lambda: abi.kivi_dequant(cache, 0, kh), lambda: abi.kivi_dequant(cache, 1, vh),
+               lambda: abi.kivi_append_token(cache, kn, vn, status),
+               lambda: abi.kivi_decode_qk(cache, q, logits), lambda: abi.kivi_decode_pv(cache, logits, out, ws)]
+        for i, fn in enumerate(fns):
+            if ev is not None:
+                ev[2 * i].record(stream)
+            fn()
+            if ev is not None:
+                ev[2 * i + 1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(CALLS))] for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        t0.record(stream)
+        for s in range(args.steps):
+            step(evs[s])
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1)
+    per_call = {c: sum(evs[s][2 * i].elapsed_time(evs[s][2 * i + 1]) for s in range(args.steps)) / args.steps
+                for i, c in enumerate(CALLS)}
+    assert int(status.item()) == 0
+    if world > 1:
+        import torch.distributed as dist
+        tmax = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
+        ms = float(tmax.item())
+
+    ms_step = ms / args.steps
+    n_dec = T + 1
+    eq = fp16_equiv_bytes(w, T, n_dec)
+    value = eq * world / (ms_step * 1e-3) / 1e9
+    ab = alg_bytes(w, T, n_dec)
+    hbm, src = peaks()
+    kernels = {}
+    for c in CALLS:
+        gbs = ab[c] / (per_call[c] * 1e-3) / 1e9
+        kernels[c] = {"ms": round(per_call[c], 5), "alg_bytes": ab[c], "gbs": round(gbs, 1),
+                      "frac": round(gbs / hbm, 3)}
+    dominant = max(CALLS, key=lambda c: per_call[c])
+    dk = kernels[dominant]
+    quant_ms = per_call["quant_keys"] + per_call["quant_values"]
+    deq_ms = per_call["dequant_keys"] + per_call["dequant_values"]
+    dec_ms = per_call["decode_qk"] + per_call["decode_pv"]
+    BH = w.B * w.H
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u2 codes / f32 stats / f16 KV",
+        "data": "synthetic (seeded N(0,1) fp16, outlier key channels)",
+        "config": {"workload": w.name, "shape": [w.B, w.H, T, w.D], "Hq": w.Hq, "bits_k": w.bits_k,
+                   "bits_v": w.bits_v, "G": w.G, "R": w.R, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (K, V 268 MB each)"},
+        "breakdown": {
+            "quant_gbs_fp16eq": round(2 * BH * T * w.D * 2 / (quant_ms * 1e-3) / 1e9, 1),
+            "dequant_gbs_fp16eq": round(2 * BH * T * w.D * 2 / (deq_ms * 1e-3) / 1e9, 1),
+            "decode_tok_s": round(w.B / (dec_ms * 1e-3), 1),
+            "decode_gbs_fp16eq": round(2 * BH * n_dec * w.D * 2 / (dec_ms * 1e-3) / 1e9, 1),
+            "kernels": kernels,
+        },
+        "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": hbm,
+                     "peak_source": src, "unit": "GB/s", "frac": dk["frac"],
+                     "traffic": recorded_traffic(dominant, w.name)},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clk.summary(),
+    }
+    if not args.no_e2e:
+        line["e2e"] = run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, K, V, q, kn, vn)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line if rank == 0 else None
+
+
+def run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq):
+    """Same step through the public API from pinned host buffers: H2D of the
+    step's K, V, q and new token, the step, D2H of the attention output."""
+    import torch
+    from kivi_bit_kv_gb300 import abi
+    from kivi_bit_kv_gb300 import workloads as W
+    Kh, Vh = (t.pin_memory() for t in W.make_kv(w, device="cpu"))
+    qh = W.make_q(w, "cpu").pin_memory()
+    knh, vnh = (t[0].contiguous().pin_memory() for t in W.make_step_tokens(w, 1, "cpu"))
+    Kd, Vd = torch.empty_like(Kh, device=dev), torch.empty_like(Vh, device=dev)
+    qd, knd, vnd = (torch.empty_like(t, device=dev) for t in (qh, knh, vnh))
+    outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    n = max(3, args.steps // 20)
+
+    def step():
+        for d, h in ((Kd, Kh), (Vd, Vh), (qd, qh), (knd, knh), (vnd, vnh)):
+            d.copy_(h, non_blocking=True)
+        abi.kivi_quant_keys(cache, Kd)
+        abi.kivi_quant_values(cache, Vd)
+        abi.kivi_dequant(cache, 0, kh)
+        abi.kivi_dequant(cache, 1, vh)
+        abi.kivi_append_token(cache, knd, vnd, status)
+        abi.kivi_decode_qk(cache, qd, logits)
+        abi.kivi_decode_pv(cache, logits, out, ws)
+        outh.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize(dev)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    t0.record(stream)
+    for _ in range(n):
+        step()
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        import torch.distributed as dist
+        tm = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ms = float(tm.item())
+    bi = sum(t.numel() * t.element_size() for t in (Kh, Vh, qh, knh, vnh))
+    bo = outh.numel() * outh.element_size()
+    return {"value": round(eq * world / (ms / n * 1e-3) / 1e9, 1), "unit": UNIT,
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n}
+
+
+# ------------------------------------------------------ CPU oracle legs --
+
+def _oracle_pass(R, w, Ks, Vs, qs, kn, vn, threads):
+    """The whole step on the oracle for a sample of (b, h) slices, each
+    treated as its own single-head sequence."""
+    n, T, D = Ks.shape[0], Ks.shape[2], w.D
+    Tmax = (T + 1 + w.G - 1) // w.G * w.G + w.G
+    rc = R.RefCache(n, 1, D, w.bits_k, w.bits_v, w.G, w.R, Tmax)
+    rc.encode(Ks, Vs, threads=threads)
+    rc.decode(0, threads=threads)
+    rc.decode(1, threads=threads)
+    rc.append(kn, vn)
+    rc.attention(qs, threads=threads)
+
+
+def _sample(w, K, V, q, kn, vn, n, T):
+    import numpy as np
+    import torch
+    idx = [(i * 7) % (w.B * w.H) for i in range(n)]
+    bs = torch.tensor([i // w.H for i in idx])
+    hs = torch.tensor([i % w.H for i in idx])
+    Ks = K[bs, hs, :T].unsqueeze(1).cpu().numpy().view(np.uint16)
+    Vs = V[bs, hs, :T].unsqueeze(1).cpu().numpy().view(np.uint16)
+    qs = q[bs, hs * (w.Hq // w.H)].unsqueeze(1).cpu().numpy().view(np.uint16)
+    ks = kn[bs, hs].unsqueeze(1).cpu().numpy().view(np.uint16)
+    vs = vn[bs, hs].unsqueeze(1).cpu().numpy().view(np.uint16)
+    return Ks, Vs, qs, ks, vs
+
+
+def _slice_fp16eq(w, T):
+    return 2 * T * w.D * 2 * 3 + 2 * w.D * 2
+
+
+def cpu_baseline(w, K, V, q, kn, vn, budget_s: float = 10.0):
+    """The oracle as it stands on a bounded sample (about 10 s of CPU work)."""
+    from oracle import ref as R
+    cores = R.host_threads()
+    Ks, Vs, qs, ks, vs = _sample(w, K, V, q, kn, vn, cores, w.T)
+    done, t_start = 0, time.perf_counter()
+    while True:
+        _oracle_pass(R, w, Ks, Vs, qs, ks, vs, cores)
+        done += 1
+        el = time.perf_counter() - t_start
+        if el >= budget_s:
+            break
+    value = done * cores * _slice_fp16eq(w, w.T) / el / 1e9
+    return {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{done} rounds x {cores} (b,h) slices of {w.name} ({w.T} tokens each, full step "
+                      f"per slice: encode, materialize K and V, append, decode), {el:.1f} s"}
+
+
+def run_reference(args, rank, world):
+    """The oracle as the reference arm: every step is a bounded sample of the
+    workload, sized so the whole run stays within a few minutes."""
+    if rank != 0:
+        return None
+    import torch
+    from kivi_bit_kv_gb300 import workloads as W
+    from oracle import ref as R
+    w = W.WORKLOADS[args.workload]
+    cores = R.host_threads()
+    K, V = W.make_kv(w, "cpu")
+    q = W.make_q(w, "cpu")
+    kn, vn = (t[0] for t in W.make_step_tokens(w, 1, "cpu"))
+    # calibrate one full slice on one thread
+    Ks, Vs, qs, ks, vs = _sample(w, K, V, q, kn, vn, 1, w.T)
+    t = time.perf_counter()
+    _oracle_pass(R, w, Ks, Vs, qs, ks, vs, 1)
+    t1 = time.perf_counter() - t
+    per_step = min(10.0, 150.0 / max(1, args.steps + args.warmup))
+    Tw = int(min(w.T, max(w.R + w.G, w.T * per_step / t1)))
+    Tw = max(w.R + w.G, Tw // w.G * w.G)
+    Ks, Vs, qs, ks, vs = _sample(w, K, V, q, kn, vn, cores, Tw)
+    for _ in range(args.warmup):
+        _oracle_pass(R, w, Ks, Vs, qs, ks, vs, cores)
+    t = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_pass(R, w, Ks, Vs, qs, ks, vs, cores)
+    el = time.perf_counter() - t
+    ms_step = el / args.steps * 1e3
+    value = cores * _slice_fp16eq(w, Tw) / (ms_step * 1e-3) / 1e9
+    sample = f"per step {cores} (b,h) slices of {w.name} truncated to {Tw} tokens"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32/f64 (CPU oracle)",
+        "data": "synthetic (seeded N(0,1) fp16, outlier key channels)",
+        "config": {"workload": w.name, "shape": [w.B, w.H, w.T, w.D], "Hq": w.Hq, "bits_k": w.bits_k,
+                   "bits_v": w.bits_v, "G": w.G, "R": w.R, "parallelism": "host threads"},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+    else:
+        line = run_kivi(args, rank, world, local)
+    if line is not None and rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,219 @@
+/*
+ * kivi.h -- C ABI of libkivi: KIVI grouped asymmetric KV-cache quantization
+ * on one NVIDIA GB300 (sm_103a).
+ *
+ * The method (KIVI, "A Tuning-Free Asymmetric 2bit Quantization for KV
+ * Cache", as described on the CacheForge README, section "How it works", and
+ * in CacheSeek PR #4 "add KIVI KV-cache quantization for exact-prefix reuse"):
+ * keys are quantized per channel over groups of G tokens, values per token
+ * over groups of G channels, each group with its own min/max statistics; the
+ * most recent tokens stay in fp16.  The pages print no formula; this library
+ * fixes the arithmetic as follows, and every entry point below follows it:
+ *
+ *   M     = 2^b - 1, b in {2, 4, 8}            (CacheForge "Example": k_bits,
+ *                                               v_bits; CacheSeek: int4/int8)
+ *   scale = (max - min) / M     fp32 subtraction, IEEE fp32 division
+ *   zero  = min                 (the "offset" of CacheSeek's qdata/scale/offset)
+ *   code  = clamp(rne((x - zero) / scale), 0, M)   fp32, IEEE division,
+ *           round half to even; code = 0 when scale == 0
+ *   x_hat = fp16_rne(fmaf(code, scale, zero))
+ *
+ * Inputs equal to -0 are treated as +0 when forming min/max, so the stored
+ * statistics never hold -0.  NaN and infinity inputs are not supported.
+ *
+ * Codes are packed little-endian into int32 words, P = 32/b codes per word
+ * (16 x int2, 8 x int4, 4 x int8; code i occupies bits [i*b, i*b+b)), along
+ * the grouping axis: key words run along tokens, value words along channels.
+ *
+ * Residual (CacheForge "Example": residual_length = number of recent fp16
+ * tokens).  A sequence of T tokens keeps its first
+ *     Tq = max(0, floor((T - R) / G) * G)
+ * tokens quantized and the remaining T - Tq tokens (R <= T - Tq < R + G once
+ * T >= R) in fp16, in a ring of R + G slots: token t lives in slot t mod (R+G).
+ * Appending a token that makes the residual reach R + G quantizes its oldest
+ * G tokens as one group and drops them from the ring ("quantization flow
+ * during prefill and decoding", CacheForge README, "How it works").
+ *
+ * Conventions for every call:
+ *   - All tensors are caller-allocated device memory (the library never
+ *     allocates or frees), contiguous, row-major, 16-byte aligned.
+ *   - fp16 tensors are passed as uint16_t bit patterns (IEEE binary16).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     only enqueues work on it and returns; no call synchronizes the host.
+ *   - Every call returns KIVI_OK or an error code; a failed call enqueues
+ *     nothing (argument errors) or reports the launch error (KIVI_ECUDA).
+ *     kivi_last_error() then describes the problem (per host thread).
+ *   - The per-sequence token counts `len` live on the device, so ragged
+ *     batches never need a host round trip.
+ */
+#ifndef KIVI_H
+#define KIVI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define KIVI_ABI_VERSION 1
+
+/* Status codes. */
+#define KIVI_OK         0
+#define KIVI_EINVAL     1 /* bad descriptor, shape, pointer or alignment       */
+#define KIVI_ECAPACITY  2 /* a sequence would exceed Tmax tokens (device flag) */
+#define KIVI_ECUDA      3 /* the CUDA launch reported an error                  */
+#define KIVI_ETIMEOUT   4 /* reserved: a bounded device wait gave up            */
+#define KIVI_EWORKSPACE 5 /* workspace smaller than kivi_workspace_bytes()      */
+
+/*
+ * Cache descriptor: a plain struct of sizes and device pointers, owned and
+ * filled by the caller.  Shapes (P_k = 32/bits_k, P_v = 32/bits_v):
+ *
+ *   kq      int32 [B][H][Tmax/P_k][D]   key codes; word (w, d) = tokens
+ *                                        w*P_k .. w*P_k+P_k-1 of channel d
+ *   kscale  fp32  [B][H][Tmax/G][D]     per (token group, channel)
+ *   kzero   fp32  [B][H][Tmax/G][D]
+ *   vq      int32 [B][H][Tmax][D/P_v]   value codes; word (t, w) = channels
+ *                                        w*P_v .. w*P_v+P_v-1 of token t
+ *   vscale  fp32  [B][H][Tmax][D/G]     per (token, channel group)
+ *   vzero   fp32  [B][H][Tmax][D/G]
+ *   kres    fp16  [B][H][R+G][D]        residual ring of keys
+ *   vres    fp16  [B][H][R+G][D]        residual ring of values
+ *   len     int32 [B]                   tokens held by each sequence
+ *
+ * Constraints (checked, KIVI_EINVAL otherwise): B, H >= 1; D in {64, 128,
+ * 256}; bits in {2, 4, 8}; G in {32, 64, 128} with D % G == 0; R >= 0 with
+ * R % G == 0; 1 <= Tmax <= 2^24 with Tmax % G == 0; R <= 2^24; all pointers
+ * non-NULL and 16-byte aligned.
+ */
+typedef struct kivi_cache {
+    int32_t B, H, D;
+    int32_t bits_k, bits_v;
+    int32_t G, R, Tmax;
+    int32_t*  kq;
+    float*    kscale;
+    float*    kzero;
+    int32_t*  vq;
+    float*    vscale;
+    float*    vzero;
+    uint16_t* kres;
+    uint16_t* vres;
+    int32_t*  len;
+} kivi_cache;
+
+/* Buffer ids for kivi_buffer_bytes(). */
+#define KIVI_BUF_KQ     0
+#define KIVI_BUF_KSCALE 1
+#define KIVI_BUF_KZERO  2
+#define KIVI_BUF_VQ     3
+#define KIVI_BUF_VSCALE 4
+#define KIVI_BUF_VZERO  5
+#define KIVI_BUF_KRES   6
+#define KIVI_BUF_VRES   7
+#define KIVI_BUF_LEN    8
+
+/* Library ABI version (KIVI_ABI_VERSION). */
+int32_t kivi_abi_version(void);
+
+/* Message for a status code; never NULL. */
+const char* kivi_status_string(int32_t status);
+
+/* Description of the last error returned on this host thread ("" if none). */
+const char* kivi_last_error(void);
+
+/* Checks the descriptor's sizes, pointers and alignment.  Host only. */
+int32_t kivi_cache_validate(const kivi_cache* c);
+
+/* Bytes the caller must allocate for one buffer of the descriptor (sizes
+ * only are read; pointers may be NULL).  Returns 0 for a bad id or bad sizes. */
+size_t kivi_buffer_bytes(const kivi_cache* c, int32_t buffer);
+
+/*
+ * Bytes a sequence of T tokens occupies in the cache for one (batch, head)
+ * slice -- codes + fp32 scale/zero + fp16 residual (CacheSeek PR #4:
+ * "manager-side accounting so stored payload sizes reflect optional
+ * quantization"):
+ *   keys   (which = 0): Tq*D*b/8 + (Tq/G)*D*8 + (T-Tq)*D*2
+ *   values (which = 1): Tq*D*b/8 + Tq*(D/G)*8 + (T-Tq)*D*2
+ * Host only.  Returns 0 for invalid arguments.
+ */
+size_t kivi_cache_bytes(int32_t T, int32_t D, int32_t bits, int32_t G,
+                        int32_t R, int32_t which);
+
+/*
+ * Prefix encode of keys (CacheForge "How it works": keys per channel).
+ * K: fp16 [B][H][T][D].  Sequence b keeps its first n_b tokens, where
+ * n_b = seq_lens[b] (device int32 [B], each 0 <= n_b <= T) or n_b = T when
+ * seq_lens is NULL; T <= Tmax.  Writes kq, kscale, kzero for the Tq(n_b)
+ * quantized tokens, copies tokens [Tq, n_b) into the key ring, and sets
+ * len[b] = n_b.  One pass: each (channel, G-token group) tile is read once,
+ * reduced to min/max, and its codes are packed in place.
+ */
+int32_t kivi_quant_keys(const kivi_cache* c, const uint16_t* K, int32_t T,
+                        const int32_t* seq_lens, void* stream);
+
+/*
+ * Prefix encode of values (CacheForge "How it works": values per token).
+ * V: fp16 [B][H][T][D]; seq_lens, T as for kivi_quant_keys.  Writes vq,
+ * vscale, vzero, the value ring, and len[b] = n_b.
+ */
+int32_t kivi_quant_values(const kivi_cache* c, const uint16_t* V, int32_t T,
+                          const int32_t* seq_lens, void* stream);
+
+/*
+ * Materialize (CacheSeek PR #4: "decode after materialize"): unpack and
+ * dequantize keys (which = 0) or values (which = 1) into out, fp16
+ * [B][H][T_out][D].  Rows t < len[b] are written (quantized rows as x_hat,
+ * residual rows copied from the ring); rows t >= len[b] are not touched.
+ * Requires len[b] <= T_out <= Tmax for every b (len is not checked on the
+ * host; rows past T_out are never written).
+ */
+int32_t kivi_dequant(const kivi_cache* c, int32_t which, uint16_t* out,
+                     int32_t T_out, void* stream);
+
+/*
+ * Append one decoded token to every sequence: k, v fp16 [B][H][D].
+ * Writes them into ring slot len[b] mod (R+G) and increments len[b]; when
+ * the residual reaches R + G tokens, the oldest G are quantized (keys: one
+ * G-token group per channel; values: G tokens, per-token groups) and
+ * appended to the packed cache.  A sequence with len[b] == Tmax is left
+ * unchanged and *status (device int32, caller-owned) is set to
+ * KIVI_ECAPACITY; *status is otherwise not written.  Two kernels on `stream`.
+ */
+int32_t kivi_append_token(const kivi_cache* c, const uint16_t* k,
+                          const uint16_t* v, int32_t* status, void* stream);
+
+/*
+ * Decode logits with dequantization fused into the load:
+ *   logits[b][hq][t] = sm_scale * sum_d q[b][hq][d] * K_hat[b][h][t][d]
+ * for t < len[b], where h = hq / (Hq / H) (grouped-query attention) and
+ * K_hat = code*scale + zero evaluated in fp32 (quantized tokens) or the fp16
+ * residual.  q: fp16 [B][Hq][D]; logits: fp32 [B][Hq][ld_logits],
+ * ld_logits >= Tmax, a multiple of 4; entries t >= len[b] are not written.
+ * Hq must be a multiple of H with Hq / H <= 16.
+ */
+int32_t kivi_decode_qk(const kivi_cache* c, const uint16_t* q, int32_t Hq,
+                       float sm_scale, float* logits, int32_t ld_logits,
+                       void* stream);
+
+/*
+ * Decode output with dequantization fused into the load:
+ *   p = softmax over t < len[b] of logits[b][hq][t]     (fp32, max-subtracted)
+ *   out[b][hq][d] = sum_t p_t * V_hat[b][h][t][d]
+ * out: fp32 [B][Hq][D].  The token range is split into chunks processed in
+ * parallel; per-chunk partial results go to the caller's workspace `ws`
+ * (device, >= kivi_workspace_bytes(c, Hq) bytes, 16-byte aligned) and a
+ * second kernel combines them.  A sequence with len[b] == 0 gets out = 0.
+ */
+int32_t kivi_decode_pv(const kivi_cache* c, const float* logits,
+                       int32_t ld_logits, int32_t Hq, float* out, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/* Workspace bytes kivi_decode_pv needs for this descriptor and Hq. */
+size_t kivi_workspace_bytes(const kivi_cache* c, int32_t Hq);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* KIVI_H */

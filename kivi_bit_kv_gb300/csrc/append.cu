@@ -1,0 +1,106 @@
+// append.cu -- append one decoded token per sequence, flushing the oldest G
+// residual tokens into the packed cache when the residual reaches R + G
+// (CacheForge README, "How it works": recent tokens stay at higher precision;
+// the quantization flow during decoding).
+//
+// Kernel 1, one CTA per (h, b): writes k, v into ring slot len mod (R+G) and,
+// on a flush step, quantizes the G oldest ring tokens exactly like a prefix
+// group (same lane quantizers as the encode kernels).  Kernel 2 advances
+// len[b]; it runs after every CTA of kernel 1 has read the old length, so no
+// CTA can observe a half-updated count.
+#include "kivi_device.cuh"
+#include "kivi_launch.h"
+
+namespace kivi {
+
+template <int BK, int BV>
+__global__ void __launch_bounds__(128)
+append_kernel(kivi_cache c, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+              int32_t* status)
+{
+    const size_t bh = blockIdx.x;
+    const int b = (int)(bh / c.H), h = (int)(bh % c.H);
+    const int L = c.len[b];
+    if (L + 1 > c.Tmax) {
+        if (h == 0 && threadIdx.x == 0)
+            atomicExch(status, KIVI_ECAPACITY);
+        return;
+    }
+    const int D = c.D, G = c.G, RG = c.R + c.G;
+    const int slot = L % RG;
+    for (int i = threadIdx.x; i < D / kLaneChans; i += blockDim.x) {
+        const size_t o = (bh * RG + slot) * D + (size_t)i * kLaneChans;
+        const size_t in = bh * D + (size_t)i * kLaneChans;
+        *reinterpret_cast<uint4*>(c.kres + o) = *reinterpret_cast<const uint4*>(k + in);
+        *reinterpret_cast<uint4*>(c.vres + o) = *reinterpret_cast<const uint4*>(v + in);
+    }
+    const int Tq = quantized_tokens(L, G, c.R);
+    if (L + 1 - Tq != RG)
+        return;  // uniform over the CTA
+    __syncthreads();  // the new token is visible to every thread of the CTA
+
+    const int lane = threadIdx.x & 31;
+    // keys: one G-token group per channel, lanes (s, j) with s fastest
+    {
+        const int S = G / kLaneTokens, NC = D / kLaneChans;
+        const unsigned smask = (((1u << S) - 1u) << (lane & ~(S - 1)));
+        for (int task = threadIdx.x; task < S * NC; task += blockDim.x) {
+            const int s = task % S, j = task / S;
+            const int t0 = Tq + s * kLaneTokens;
+            uint4 raw[kLaneTokens];
+#pragma unroll
+            for (int i = 0; i < kLaneTokens; ++i)
+                raw[i] = *reinterpret_cast<const uint4*>(
+                    c.kres + (bh * RG + (t0 + i) % RG) * D + (size_t)j * kLaneChans);
+            quant_store_key_lane<BK>(c, bh, t0, Tq / G, j, s, S, smask, raw);
+        }
+    }
+    // values: G token rows, 8-channel lanes
+    {
+        const int NC = D / kLaneChans, LPG = G / kLaneChans;
+        const unsigned gmask = (((1u << LPG) - 1u) << (lane & ~(LPG - 1)));
+        for (int task = threadIdx.x; task < G * NC; task += blockDim.x) {
+            const int j = task % NC, r = task / NC;
+            const int t = Tq + r;
+            const uint4 raw = *reinterpret_cast<const uint4*>(
+                c.vres + (bh * RG + t % RG) * D + (size_t)j * kLaneChans);
+            store_value_lane<BV>(c, bh, t, j, raw, gmask);
+        }
+    }
+}
+
+__global__ void advance_len_kernel(int32_t* len, int B, int Tmax)
+{
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b < B) {
+        const int L = len[b];
+        if (L + 1 <= Tmax)
+            len[b] = L + 1;
+    }
+}
+
+template <int BK>
+static void launch_append_bk(const kivi_cache& c, const uint16_t* k, const uint16_t* v,
+                             int32_t* status, cudaStream_t s)
+{
+    const dim3 grid(c.B * c.H);
+    switch (c.bits_v) {
+    case 2: append_kernel<BK, 2><<<grid, 128, 0, s>>>(c, k, v, status); break;
+    case 4: append_kernel<BK, 4><<<grid, 128, 0, s>>>(c, k, v, status); break;
+    default: append_kernel<BK, 8><<<grid, 128, 0, s>>>(c, k, v, status); break;
+    }
+}
+
+cudaError_t launch_append(const kivi_cache& c, const uint16_t* k, const uint16_t* v,
+                          int32_t* status, cudaStream_t s)
+{
+    switch (c.bits_k) {
+    case 2: launch_append_bk<2>(c, k, v, status, s); break;
+    case 4: launch_append_bk<4>(c, k, v, status, s); break;
+    default: launch_append_bk<8>(c, k, v, status, s); break;
+    }
+    advance_len_kernel<<<(c.B + 127) / 128, 128, 0, s>>>(c.len, c.B, c.Tmax);
+    return cudaGetLastError();
+}
+
+}  // namespace kivi

@@ -1,0 +1,35 @@
+// kivi_launch.h -- host-side launchers behind the C ABI (internal).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kivi.h"
+
+namespace kivi {
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count();
+
+// Tokens per decode_qk CTA and per decode_pv chunk for head dim D.
+int qk_chunk_tokens(int D);
+int pv_chunk_tokens(int D);
+int pv_chunks(const kivi_cache& c);
+
+cudaError_t launch_quant_keys(const kivi_cache& c, const uint16_t* K, int T,
+                              const int32_t* seq_lens, cudaStream_t s);
+cudaError_t launch_quant_values(const kivi_cache& c, const uint16_t* V, int T,
+                                const int32_t* seq_lens, cudaStream_t s);
+cudaError_t launch_dequant(const kivi_cache& c, int which, uint16_t* out, int T_out,
+                           cudaStream_t s);
+cudaError_t launch_append(const kivi_cache& c, const uint16_t* k, const uint16_t* v,
+                          int32_t* status, cudaStream_t s);
+cudaError_t launch_decode_qk(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale,
+                             float* logits, int ld_logits, cudaStream_t s);
+// ws_o: [B*Hq][nchunks][D], ws_m / ws_l: [B*Hq][nchunks] (fp32).
+cudaError_t launch_decode_pv(const kivi_cache& c, const float* logits, int ld_logits, int Hq,
+                             float* out, float* ws_o, float* ws_m, float* ws_l,
+                             cudaStream_t s);
+
+}  // namespace kivi
