@@ -213,6 +213,34 @@ int32_t kivi_decode_pv(const kivi_cache* c, const float* logits,
 /* Workspace bytes kivi_decode_pv needs for this descriptor and Hq. */
 size_t kivi_workspace_bytes(const kivi_cache* c, int32_t Hq);
 
+/* Size of the fixed device scratch behind kivi_decode_pv_noalloc. */
+#define KIVI_NOALLOC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+/*
+ * kivi_decode_pv for callers that cannot allocate device memory.  This entry
+ * point has no counterpart on the KIVI pages; it exists for callers with no
+ * way to hand over a workspace -- an engine that reserves all of HBM for its
+ * own KV pool and exposes no allocator, a custom op inside another runtime
+ * that must not allocate outside that runtime's accounting, a decode loop
+ * that must not call cudaMalloc / cudaFree because they can synchronize the
+ * device.  Same arguments, results and validation as kivi_decode_pv, minus
+ * ws / ws_bytes: the per-chunk partials go to a KIVI_NOALLOC_SCRATCH_BYTES
+ * (16 MiB) array compiled into the library, one per GPU that loads it, held
+ * until the process exits.  The call allocates nothing.
+ *   - Shapes with kivi_workspace_bytes(c, Hq) > KIVI_NOALLOC_SCRATCH_BYTES are
+ *     rejected with KIVI_EWORKSPACE before anything is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call on a device shares the one array and it keeps the last
+ *     call's contents.  Calls whose kernels may overlap on the GPU (unordered
+ *     streams) race and corrupt each other's results: order them.  No part
+ *     of the array needs to start at zero.
+ */
+int32_t kivi_decode_pv_noalloc(const kivi_cache* c, const float* logits,
+                               int32_t ld_logits, int32_t Hq, float* out,
+                               void* stream);
+
 #ifdef __cplusplus
 }
 #endif

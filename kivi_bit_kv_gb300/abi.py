@@ -31,8 +31,10 @@ EXPORTS = (
     "kivi_abi_version", "kivi_status_string", "kivi_last_error", "kivi_cache_validate",
     "kivi_buffer_bytes", "kivi_cache_bytes", "kivi_quant_keys", "kivi_quant_values",
     "kivi_dequant", "kivi_append_token", "kivi_decode_qk", "kivi_decode_pv",
-    "kivi_workspace_bytes",
+    "kivi_workspace_bytes", "kivi_decode_pv_noalloc",
 )
+
+KIVI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
 
 class KiviError(RuntimeError):
@@ -82,6 +84,7 @@ def load(path: str | None = None):
         "kivi_decode_qk": ([cp, vp, i32, f32, vp, i32, vp], i32),
         "kivi_decode_pv": ([cp, vp, i32, i32, vp, vp, sz, vp], i32),
         "kivi_workspace_bytes": ([cp, i32], sz),
+        "kivi_decode_pv_noalloc": ([cp, vp, i32, i32, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -225,3 +228,18 @@ def kivi_decode_pv(cache, logits: torch.Tensor, out: torch.Tensor, ws: torch.Ten
                                  ld, Hq, _dev(out, torch.float32, "out", cache.device), wp,
                                  ws.numel() * ws.element_size(), _stream(stream, cache.device)),
            "kivi_decode_pv")
+
+
+def kivi_decode_pv_noalloc(cache, logits: torch.Tensor, out: torch.Tensor, stream=None):
+    """kivi_decode_pv without a workspace argument, for callers that cannot
+    allocate device memory: the library's fixed 16 MiB per-device scratch
+    holds the partial results.  Calls sharing a device must not overlap on
+    the GPU (order them on one stream); the first call on a device should
+    come before any stream capture."""
+    B, Hq, ld = logits.shape
+    if tuple(out.shape) not in ((B, Hq, cache.D), (B, Hq, 1, cache.D)):
+        raise ValueError(f"out shape {tuple(out.shape)}; expected {(B, Hq, cache.D)}")
+    _check(load().kivi_decode_pv_noalloc(C.byref(cache.desc),
+                                         _dev(logits, torch.float32, "logits", cache.device), ld, Hq,
+                                         _dev(out, torch.float32, "out", cache.device),
+                                         _stream(stream, cache.device)), "kivi_decode_pv_noalloc")

@@ -295,3 +295,14 @@ int sm_count()
 }
 
 }  // namespace kivi
+
+namespace kivi {
+
+// Lets entry points defined in other translation units report through
+// kivi_last_error().
+int32_t record_error(int32_t status, const char* message)
+{
+    return fail(status, "%s", message);
+}
+
+}  // namespace kivi

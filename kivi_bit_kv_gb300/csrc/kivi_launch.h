@@ -32,4 +32,7 @@ cudaError_t launch_decode_pv(const kivi_cache& c, const float* logits, int ld_lo
                              float* out, float* ws_o, float* ws_m, float* ws_l,
                              cudaStream_t s);
 
+// Sets the message kivi_last_error() returns on this host thread; returns status.
+int32_t record_error(int32_t status, const char* message);
+
 }  // namespace kivi
