@@ -13,6 +13,22 @@
 
 namespace kivi {
 
+template <int BV, int G>
+__device__ __forceinline__ void flush_values(const kivi_cache& c, size_t bh, int Tq)
+{
+    const int D = c.D, NG = D / G, RG = c.R + c.G;
+    for (int task = threadIdx.x; task < G * NG; task += blockDim.x) {
+        const int gi = task % NG, r = task / NG;
+        const int t = Tq + r;
+        const uint16_t* src = c.vres + (bh * RG + t % RG) * D + gi * G;
+        uint4 raw[G / 8];
+#pragma unroll
+        for (int v = 0; v < G / 8; ++v)
+            raw[v] = *reinterpret_cast<const uint4*>(src + v * 8);
+        quant_store_value_group<BV, G>(c, bh, t, gi, raw);
+    }
+}
+
 template <int BK, int BV>
 __global__ void __launch_bounds__(128)
 append_kernel(kivi_cache c, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
@@ -55,17 +71,11 @@ append_kernel(kivi_cache c, const uint16_t* __restrict__ k, const uint16_t* __re
             quant_store_key_lane<BK>(c, bh, t0, Tq / G, j, s, S, smask, raw);
         }
     }
-    // values: G token rows, 8-channel lanes
-    {
-        const int NC = D / kLaneChans, LPG = G / kLaneChans;
-        const unsigned gmask = (((1u << LPG) - 1u) << (lane & ~(LPG - 1)));
-        for (int task = threadIdx.x; task < G * NC; task += blockDim.x) {
-            const int j = task % NC, r = task / NC;
-            const int t = Tq + r;
-            const uint4 raw = *reinterpret_cast<const uint4*>(
-                c.vres + (bh * RG + t % RG) * D + (size_t)j * kLaneChans);
-            store_value_lane<BV>(c, bh, t, j, raw, gmask);
-        }
+    // values: G token rows x D/G channel groups, one lane per group
+    switch (G) {
+    case 32: flush_values<BV, 32>(c, bh, Tq); break;
+    case 64: flush_values<BV, 64>(c, bh, Tq); break;
+    default: flush_values<BV, 128>(c, bh, Tq); break;
     }
 }
 

@@ -83,41 +83,52 @@ decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_
                 for (int i = 0; i < kLaneTokens; ++i)
                     acc[hq][i] = 0.0f;
             }
-#pragma unroll 2
-            for (int cb = 0; cb < kSegChans / 4; ++cb) {
-                uint4 W[Cd::kWordRows];
+            // Load phases of LB channel batches (4 channels each): every load
+            // of a phase is issued before any of its data is used.
+            constexpr int LB = BITS == 2 ? 8 : BITS == 4 ? 4 : 2;
+#pragma unroll 1
+            for (int cb0 = 0; cb0 < kSegChans / 4; cb0 += LB) {
+                uint4 W[LB][Cd::kWordRows];
+                float4 SC[LB], ZR[LB];
 #pragma unroll
-                for (int w = 0; w < Cd::kWordRows; ++w)
-                    W[w] = ld_nc(kw + (size_t)w * D + cb * 4);
-                const float4 sc = ld_nc_f4(c.kscale + so + cb * 4);
-                const float4 zr = ld_nc_f4(c.kzero + so + cb * 4);
-                const float scv[4] = {sc.x, sc.y, sc.z, sc.w};
-                const float zrv[4] = {zr.x, zr.y, zr.z, zr.w};
-                float qsw[NQB][4][Win::kNumPos];
+                for (int l = 0; l < LB; ++l) {
 #pragma unroll
-                for (int hq = 0; hq < NQB; ++hq) {
-                    const float4 qv = *reinterpret_cast<const float4*>(qseg + hq * hq_stride + cb * 4);
-                    const float qq[4] = {qv.x, qv.y, qv.z, qv.w};
-#pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        const float qs = qq[k] * scv[k];
-                        Ssum[hq] += qs;
-                        Zsum[hq] = fmaf(qq[k], zrv[k], Zsum[hq]);
-#pragma unroll
-                        for (int p = 0; p < Win::kNumPos; ++p)
-                            qsw[hq][k][p] = qs * Win::mult_of_index(p);
-                    }
+                    for (int w = 0; w < Cd::kWordRows; ++w)
+                        W[l][w] = ld_nc(kw + (size_t)w * D + (cb0 + l) * 4);
+                    SC[l] = ld_nc_f4(c.kscale + so + (cb0 + l) * 4);
+                    ZR[l] = ld_nc_f4(c.kzero + so + (cb0 + l) * 4);
                 }
 #pragma unroll
-                for (int k = 0; k < 4; ++k)
+                for (int l = 0; l < LB; ++l) {
+                    const int cb = cb0 + l;
+                    const float scv[4] = {SC[l].x, SC[l].y, SC[l].z, SC[l].w};
+                    const float zrv[4] = {ZR[l].x, ZR[l].y, ZR[l].z, ZR[l].w};
+                    float qsw[NQB][4][Win::kNumPos];
 #pragma unroll
-                    for (int i = 0; i < kLaneTokens; ++i) {
-                        const int ci = i % Cd::P;
-                        const float f = window_value<BITS>(u4_word(W[i / Cd::P], k), ci);
+                    for (int hq = 0; hq < NQB; ++hq) {
+                        const float4 qv = *reinterpret_cast<const float4*>(qseg + hq * hq_stride + cb * 4);
+                        const float qq[4] = {qv.x, qv.y, qv.z, qv.w};
 #pragma unroll
-                        for (int hq = 0; hq < NQB; ++hq)
-                            acc[hq][i] = fmaf(qsw[hq][k][Win::pos_index(ci)], f, acc[hq][i]);
+                        for (int k = 0; k < 4; ++k) {
+                            const float qs = qq[k] * scv[k];
+                            Ssum[hq] += qs;
+                            Zsum[hq] = fmaf(qq[k], zrv[k], Zsum[hq]);
+#pragma unroll
+                            for (int p = 0; p < Win::kNumPos; ++p)
+                                qsw[hq][k][p] = qs * Win::mult_of_index(p);
+                        }
                     }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+#pragma unroll
+                        for (int i = 0; i < kLaneTokens; ++i) {
+                            const int ci = i % Cd::P;
+                            const float f = window_value<BITS>(u4_word(W[l][i / Cd::P], k), ci);
+#pragma unroll
+                            for (int hq = 0; hq < NQB; ++hq)
+                                acc[hq][i] = fmaf(qsw[hq][k][Win::pos_index(ci)], f, acc[hq][i]);
+                        }
+                }
             }
 #pragma unroll
             for (int hq = 0; hq < NQB; ++hq)
@@ -279,50 +290,67 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
                 acc[hq][k] = 0.0f;
         }
         const int tq_end = min(t_end, Tq);
-#pragma unroll 2
-        for (int t = t_begin + warp * TPW + tl; t < tq_end; t += NW * TPW) {
-            const size_t vrow = bh * (size_t)c.Tmax + t;
-            const int32_t* vw = c.vq + vrow * (D / Cd::P) + seg * WPL;
-            uint32_t W[WPL];
-            if constexpr (WPL == 1) {
-                W[0] = (uint32_t)__ldg(vw);
-            } else if constexpr (WPL == 2) {
-                const uint2 x = __ldg(reinterpret_cast<const uint2*>(vw));
-                W[0] = x.x;
-                W[1] = x.y;
-            } else {
+        constexpr int UNR = NQB == 1 ? 8 : 4;  // tokens whose loads are in flight per lane
+        for (int t0 = t_begin + warp * TPW + tl; t0 < tq_end; t0 += NW * TPW * UNR) {
+            uint32_t W[UNR][WPL];
+            float SV[UNR], ZV[UNR];
 #pragma unroll
-                for (int w = 0; w < WPL; w += 4) {
-                    const uint4 x = ld_nc(vw + w);
-                    W[w] = x.x;
-                    W[w + 1] = x.y;
-                    W[w + 2] = x.z;
-                    W[w + 3] = x.w;
+            for (int u = 0; u < UNR; ++u) {
+                const int t = t0 + u * NW * TPW;
+                SV[u] = ZV[u] = 0.0f;
+#pragma unroll
+                for (int w = 0; w < WPL; ++w)
+                    W[u][w] = 0u;
+                if (t < tq_end) {
+                    const size_t vrow = bh * (size_t)c.Tmax + t;
+                    const int32_t* vw = c.vq + vrow * (D / Cd::P) + seg * WPL;
+                    if constexpr (WPL == 1) {
+                        W[u][0] = (uint32_t)__ldg(vw);
+                    } else if constexpr (WPL == 2) {
+                        const uint2 x = __ldg(reinterpret_cast<const uint2*>(vw));
+                        W[u][0] = x.x;
+                        W[u][1] = x.y;
+                    } else {
+#pragma unroll
+                        for (int w = 0; w < WPL; w += 4) {
+                            const uint4 x = ld_nc(vw + w);
+                            W[u][w] = x.x;
+                            W[u][w + 1] = x.y;
+                            W[u][w + 2] = x.z;
+                            W[u][w + 3] = x.w;
+                        }
+                    }
+                    SV[u] = __ldg(c.vscale + vrow * NGv + g);
+                    ZV[u] = __ldg(c.vzero + vrow * NGv + g);
                 }
             }
-            const float sv = __ldg(c.vscale + vrow * NGv + g);
-            const float zv = __ldg(c.vzero + vrow * NGv + g);
-            float psw[NQB][Win::kNumPos];
 #pragma unroll
-            for (int hq = 0; hq < NQB; ++hq) {
-                const float pt = p_sm[(t - t_begin) * NQB + hq];
-                const float ps = pt * sv;
-                Ssum[hq] += ps;
-                Zsum[hq] = fmaf(pt, zv, Zsum[hq]);
+            for (int u = 0; u < UNR; ++u) {
+                const int t = t0 + u * NW * TPW;
+                if (t >= tq_end)
+                    break;
+                float psw[NQB][Win::kNumPos];
 #pragma unroll
-                for (int p = 0; p < Win::kNumPos; ++p)
-                    psw[hq][p] = ps * Win::mult_of_index(p);
-            }
+                for (int hq = 0; hq < NQB; ++hq) {
+                    const float pt = p_sm[(t - t_begin) * NQB + hq];
+                    const float ps = pt * SV[u];
+                    Ssum[hq] += ps;
+                    Zsum[hq] = fmaf(pt, ZV[u], Zsum[hq]);
 #pragma unroll
-            for (int w = 0; w < WPL; ++w)
-#pragma unroll
-                for (int i = 0; i < Cd::P; ++i) {
-                    const float f = window_value<BITS>(W[w], i);
-#pragma unroll
-                    for (int hq = 0; hq < NQB; ++hq)
-                        acc[hq][w * Cd::P + i] =
-                            fmaf(psw[hq][Win::pos_index(i)], f, acc[hq][w * Cd::P + i]);
+                    for (int p = 0; p < Win::kNumPos; ++p)
+                        psw[hq][p] = ps * Win::mult_of_index(p);
                 }
+#pragma unroll
+                for (int w = 0; w < WPL; ++w)
+#pragma unroll
+                    for (int i = 0; i < Cd::P; ++i) {
+                        const float f = window_value<BITS>(W[u][w], i);
+#pragma unroll
+                        for (int hq = 0; hq < NQB; ++hq)
+                            acc[hq][w * Cd::P + i] =
+                                fmaf(psw[hq][Win::pos_index(i)], f, acc[hq][w * Cd::P + i]);
+                    }
+            }
         }
 #pragma unroll
         for (int hq = 0; hq < NQB; ++hq)
@@ -408,7 +436,7 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int TC, in
 
 // ---------------------------------------------------------------- launch ---
 
-int qk_chunk_tokens(int D) { return (kDecodeThreads / (D / kSegChans)) * kLaneTokens; }
+int qk_chunk_tokens(int D) { return 2 * (kDecodeThreads / (D / kSegChans)) * kLaneTokens; }
 int pv_chunk_tokens(int) { return 1024; }
 int pv_chunks(const kivi_cache& c)
 {

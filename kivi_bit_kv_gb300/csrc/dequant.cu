@@ -4,52 +4,49 @@
 // the compact qdata/scale/offset to the device and dequantizes there.
 //
 // HBM-bound: reads b/8 bytes of code plus the statistics per element and
-// writes 2 bytes per element with 16-byte stores.
+// writes 2 bytes per element with 16-byte stores.  2-D grids (x: token tiles,
+// y: (b, h) slices), 32-bit index arithmetic.
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
 namespace kivi {
 
+constexpr int kDequantThreads = 256;
+
+__device__ __forceinline__ int lg2(int x) { return __ffs(x) - 1; }
+
 // Keys: one lane = 16 tokens x 8 channels of a G-token group.
 template <int BITS>
-__global__ void __launch_bounds__(256)
-dequant_keys_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out, int units_per_bh)
+__global__ void __launch_bounds__(kDequantThreads)
+dequant_keys_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
 {
     using Cd = Codec<BITS>;
     const int D = c.D;
-    const int S = c.G / kLaneTokens;
-    const int NC = D / kLaneChans;
-    const int lanes_per_unit = S * NC;
-    const long long total = (long long)c.B * c.H * units_per_bh * lanes_per_unit;
-    const long long stride = (long long)gridDim.x * blockDim.x;
+    const int S = c.G / kLaneTokens, lgS = lg2(S);
+    const int NC = D / kLaneChans, lgNC = lg2(NC);
+    const int s = threadIdx.x & (S - 1);
+    const int j = (threadIdx.x >> lgS) & (NC - 1);
+    const int g = blockIdx.x * (kDequantThreads >> (lgS + lgNC)) + (threadIdx.x >> (lgS + lgNC));
+    const int t0 = g * c.G + s * kLaneTokens;
     const int RG = c.R + c.G;
 
-    for (long long task = (long long)blockIdx.x * blockDim.x + threadIdx.x; task < total;
-         task += stride) {
-        const int s = (int)(task % S);
-        const int j = (int)((task / S) % NC);
-        const long long unit = task / lanes_per_unit;
-        const int g = (int)(unit % units_per_bh);
-        const size_t bh = (size_t)(unit / units_per_bh);
-        const int b = (int)(bh / c.H);
-        const int len = c.len[b];
+    for (int bh = blockIdx.y; bh < c.B * c.H; bh += gridDim.y) {
+        const int len = c.len[bh / c.H];
         const int n = min(len, T_out);
-        const int t0 = g * c.G + s * kLaneTokens;
         if (t0 >= n)
             continue;
         const int Tq = quantized_tokens(len, c.G, c.R);
-        uint16_t* dst = out + (bh * T_out) * D + (size_t)j * kLaneChans;
-
+        uint16_t* dst = out + (size_t)bh * T_out * D + j * kLaneChans;
         if (t0 + kLaneTokens <= Tq) {
-            const int32_t* src = c.kq + (bh * (size_t)(c.Tmax / Cd::P) + t0 / Cd::P) * D +
-                                 (size_t)j * kLaneChans;
+            const int32_t* src = c.kq + ((size_t)bh * (c.Tmax / Cd::P) + t0 / Cd::P) * D +
+                                 j * kLaneChans;
             uint4 wlo[Cd::kWordRows], whi[Cd::kWordRows];
 #pragma unroll
             for (int w = 0; w < Cd::kWordRows; ++w) {
                 wlo[w] = ld_stream(src + (size_t)w * D);
                 whi[w] = ld_stream(src + (size_t)w * D + 4);
             }
-            const size_t so = (bh * (size_t)(c.Tmax / c.G) + g) * D + (size_t)j * kLaneChans;
+            const size_t so = ((size_t)bh * (c.Tmax / c.G) + g) * D + j * kLaneChans;
             const float4 s0 = ld_nc_f4(c.kscale + so), s1 = ld_nc_f4(c.kscale + so + 4);
             const float4 z0 = ld_nc_f4(c.kzero + so), z1 = ld_nc_f4(c.kzero + so + 4);
             const float sc[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
@@ -74,91 +71,104 @@ dequant_keys_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out, int uni
                 const int t = t0 + i;
                 if (t >= Tq && t < n)
                     st_stream(dst + (size_t)t * D,
-                              ld_nc(c.kres + (bh * RG + t % RG) * D + (size_t)j * kLaneChans));
+                              ld_nc(c.kres + ((size_t)bh * RG + t % RG) * D + j * kLaneChans));
             }
         }
     }
 }
 
-// Values: one lane = 8 channels of one token; four rows in flight per thread.
-template <int BITS>
-__global__ void __launch_bounds__(256)
+// Values: one lane = one channel group (G channels) of U token rows: the
+// group's words, scale and zero are loaded once and G fp16 values stored.
+template <int BITS, int G>
+__global__ void __launch_bounds__(kDequantThreads)
 dequant_values_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
 {
     using Cd = Codec<BITS>;
-    constexpr int U = 4;
+    constexpr int U = G == 32 ? 4 : G == 64 ? 2 : 1;
+    constexpr int NW = G * BITS / 32;  // words per group
     const int D = c.D;
-    const int NC = D / kLaneChans;
-    const int LPG = c.G / kLaneChans;
-    const long long total = (long long)c.B * c.H * T_out * NC;
-    const long long stride = (long long)gridDim.x * blockDim.x;
+    const int NG = D / G, lgNG = lg2(NG);
+    const int gi = threadIdx.x & (NG - 1);
+    const int rows_per_pass = kDequantThreads >> lgNG;
+    const int r0 = blockIdx.x * rows_per_pass * U + (threadIdx.x >> lgNG);
     const int RG = c.R + c.G;
 
-    for (long long base = (long long)blockIdx.x * blockDim.x + threadIdx.x; base < total;
-         base += U * stride) {
-        uint32_t wl[U], wh[U];
+    for (int bh = blockIdx.y; bh < c.B * c.H; bh += gridDim.y) {
+        const int len = c.len[bh / c.H];
+        const int n = min(len, T_out);
+        const int Tq = quantized_tokens(len, c.G, c.R);
+        uint32_t words[U][NW];
         float sc[U], zr[U];
-        uint4 rr[U];
-        int kind[U];  // 0 nothing, 1 quantized, 2 residual
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const long long task = base + u * stride;
-            kind[u] = 0;
-            wl[u] = wh[u] = 0u;
+            const int t = r0 + u * rows_per_pass;
             sc[u] = zr[u] = 0.0f;
-            rr[u] = make_uint4(0u, 0u, 0u, 0u);
-            if (task >= total)
-                continue;
-            const int j = (int)(task % NC);
-            const long long row = task / NC;
-            const int t = (int)(row % T_out);
-            const size_t bh = (size_t)(row / T_out);
-            const int len = c.len[(int)(bh / c.H)];
-            if (t >= len)
-                continue;
-            const int Tq = quantized_tokens(len, c.G, c.R);
-            if (t < Tq) {
-                kind[u] = 1;
-                const size_t vrow = bh * (size_t)c.Tmax + t;
-                const int32_t* vw = c.vq + vrow * (D / Cd::P);
-                if (BITS == 2) {
-                    wl[u] = (uint32_t)__ldcs(vw + (j >> 1)) >> ((j & 1) * 16);
-                } else if (BITS == 4) {
-                    wl[u] = (uint32_t)__ldcs(vw + j);
+            if (t < Tq && t < n) {
+                const size_t row = (size_t)bh * c.Tmax + t;
+                const uint32_t* src = reinterpret_cast<const uint32_t*>(c.vq) + row * (D / Cd::P) + gi * NW;
+                if constexpr (NW == 2) {
+                    const uint2 x = __ldcs(reinterpret_cast<const uint2*>(src));
+                    words[u][0] = x.x;
+                    words[u][1] = x.y;
                 } else {
-                    const uint2 p = __ldcs(reinterpret_cast<const uint2*>(vw) + j);
-                    wl[u] = p.x;
-                    wh[u] = p.y;
+#pragma unroll
+                    for (int w = 0; w < NW; w += 4) {
+                        const uint4 x = ld_stream(src + w);
+                        words[u][w] = x.x;
+                        words[u][w + 1] = x.y;
+                        words[u][w + 2] = x.z;
+                        words[u][w + 3] = x.w;
+                    }
                 }
-                const size_t so = vrow * (D / c.G) + j / LPG;
-                sc[u] = __ldg(c.vscale + so);
-                zr[u] = __ldg(c.vzero + so);
-            } else {
-                kind[u] = 2;
-                rr[u] = ld_nc(c.vres + (bh * RG + t % RG) * D + (size_t)j * kLaneChans);
+                sc[u] = __ldcs(c.vscale + row * NG + gi);
+                zr[u] = __ldcs(c.vzero + row * NG + gi);
             }
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            if (kind[u] == 0)
+            const int t = r0 + u * rows_per_pass;
+            if (t >= n)
                 continue;
-            const long long task = base + u * stride;
-            const int j = (int)(task % NC);
-            const long long row = task / NC;
-            uint4 v = rr[u];
-            if (kind[u] == 1) {
-                uint32_t h[8];
+            uint16_t* dst = out + ((size_t)bh * T_out + t) * D + gi * G;
+            if (t < Tq) {
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t code = BITS == 8 ? ((k < 4 ? wl[u] : wh[u]) >> ((k & 3) * 8)) & 0xffu
-                                                    : (wl[u] >> (k * BITS)) & Cd::M;
-                    h[k] = dequant_h(code, sc[u], zr[u]);
+                for (int v = 0; v < G / 8; ++v) {
+                    uint32_t h[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const int e = v * 8 + k;
+                        h[k] = dequant_h((words[u][e / Cd::P] >> ((e % Cd::P) * BITS)) & Cd::M,
+                                         sc[u], zr[u]);
+                    }
+                    st_stream(dst + v * 8, make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16),
+                                                      h[4] | (h[5] << 16), h[6] | (h[7] << 16)));
                 }
-                v = make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16), h[4] | (h[5] << 16),
-                               h[6] | (h[7] << 16));
+            } else {
+                const uint16_t* rs = c.vres + ((size_t)bh * RG + t % RG) * D + gi * G;
+#pragma unroll
+                for (int v = 0; v < G / 8; ++v)
+                    st_stream(dst + v * 8, ld_nc(rs + v * 8));
             }
-            st_stream(out + (size_t)row * D + (size_t)j * kLaneChans, v);
         }
+    }
+}
+
+static dim3 dq_grid(const kivi_cache& c, int tiles)
+{
+    const int bh = c.B * c.H;
+    return dim3((unsigned)(tiles > 0 ? tiles : 1), (unsigned)(bh < 65535 ? bh : 65535));
+}
+
+template <int BITS>
+static void dequant_values_bits(const kivi_cache& c, uint16_t* out, int T_out, cudaStream_t s)
+{
+    const int U = c.G == 32 ? 4 : c.G == 64 ? 2 : 1;
+    const int rows_per_cta = kDequantThreads / (c.D / c.G) * U;
+    const dim3 grid = dq_grid(c, (T_out + rows_per_cta - 1) / rows_per_cta);
+    switch (c.G) {
+    case 32: dequant_values_kernel<BITS, 32><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;
+    case 64: dequant_values_kernel<BITS, 64><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;
+    default: dequant_values_kernel<BITS, 128><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;
     }
 }
 
@@ -167,28 +177,20 @@ cudaError_t launch_dequant(const kivi_cache& c, int which, uint16_t* out, int T_
 {
     if (T_out <= 0)
         return cudaGetLastError();
-    const int cap = sm_count() * 16;
     if (which == 0) {
-        const int units = (T_out + c.G - 1) / c.G;
-        const long long threads = (long long)c.B * c.H * units * (c.G / kLaneTokens) *
-                                  (c.D / kLaneChans);
-        long long grid = (threads + 255) / 256;
-        if (grid > cap)
-            grid = cap;
+        const int groups_per_cta = kDequantThreads / ((c.G / kLaneTokens) * (c.D / kLaneChans));
+        const int groups = (T_out + c.G - 1) / c.G;
+        const dim3 grid = dq_grid(c, (groups + groups_per_cta - 1) / groups_per_cta);
         switch (c.bits_k) {
-        case 2: dequant_keys_kernel<2><<<(int)grid, 256, 0, s>>>(c, out, T_out, units); break;
-        case 4: dequant_keys_kernel<4><<<(int)grid, 256, 0, s>>>(c, out, T_out, units); break;
-        default: dequant_keys_kernel<8><<<(int)grid, 256, 0, s>>>(c, out, T_out, units); break;
+        case 2: dequant_keys_kernel<2><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;
+        case 4: dequant_keys_kernel<4><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;
+        default: dequant_keys_kernel<8><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;
         }
     } else {
-        const long long threads = (long long)c.B * c.H * T_out * (c.D / kLaneChans);
-        long long grid = ((threads + 3) / 4 + 255) / 256;
-        if (grid > cap)
-            grid = cap;
         switch (c.bits_v) {
-        case 2: dequant_values_kernel<2><<<(int)grid, 256, 0, s>>>(c, out, T_out); break;
-        case 4: dequant_values_kernel<4><<<(int)grid, 256, 0, s>>>(c, out, T_out); break;
-        default: dequant_values_kernel<8><<<(int)grid, 256, 0, s>>>(c, out, T_out); break;
+        case 2: dequant_values_bits<2>(c, out, T_out, s); break;
+        case 4: dequant_values_bits<4>(c, out, T_out, s); break;
+        default: dequant_values_bits<8>(c, out, T_out, s); break;
         }
     }
     return cudaGetLastError();

@@ -152,13 +152,30 @@ __device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens], 
             mn[c] = __hmin2(mn[c], as_h2(__shfl_xor_sync(mask, h2_bits(mn[c]), m)));
             mx[c] = __hmax2(mx[c], as_h2(__shfl_xor_sync(mask, h2_bits(mx[c]), m)));
         }
+    // Every lane of the tile column now holds the same min / max.  The S lanes
+    // split the eight divisions (lane s takes channels k with k % S == s) and
+    // exchange the results.
     float inv[8], nzero[8];
+    const int s_lane = (int)(threadIdx.x & 31) & (S - 1);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const float lo = (k & 1) ? __high2float(mn[k >> 1]) : __low2float(mn[k >> 1]);
         const float hi = (k & 1) ? __high2float(mx[k >> 1]) : __low2float(mx[k >> 1]);
-        group_stats<BITS>(lo, hi, scale[k], zero[k], inv[k]);
+        zero[k] = __fadd_rn(lo, 0.0f);
         nzero[k] = -zero[k];
+        scale[k] = 0.0f;
+        inv[k] = 0.0f;
+        if ((k & (S - 1)) == s_lane)  // S is a power of two <= 8
+            group_stats<BITS>(lo, hi, scale[k], zero[k], inv[k]);
+    }
+    if (S > 1) {
+        const int base = (int)(threadIdx.x & 31) & ~(S - 1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int src = base + (k & (S - 1));
+            scale[k] = __shfl_sync(mask, scale[k], src);
+            inv[k] = __shfl_sync(mask, inv[k], src);
+        }
     }
 #pragma unroll
     for (int w = 0; w < Cd::kWordRows; ++w)
@@ -175,40 +192,38 @@ __device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens], 
         }
 }
 
-// Value lane: 8 consecutive channels of one token.  The G/8 lanes holding one
-// channel group are adjacent and aligned; `mask` names the warp lanes taking
-// part (all lanes of every group involved).  Returns the group statistics and
-// this lane's 8 codes packed little-endian into `bits_lo` (b = 2: 16 bits;
-// b = 4: one word; b = 8: bits_lo = channels 0-3, bits_hi = channels 4-7).
-template <int BITS>
-__device__ __forceinline__ void quant_value_lane(const uint4& raw, int lanes_per_group,
-                                                 unsigned mask, float& scale, float& zero,
-                                                 uint32_t& bits_lo, uint32_t& bits_hi)
+// Value group lane: one token's G consecutive channels (raw[i] = channels
+// 8i..8i+7), reduced and coded by a single lane -- no shuffles.  words[w]
+// holds channels w*P .. w*P+P-1 of the group.
+template <int BITS, int G>
+__device__ __forceinline__ void quant_value_group(const uint4 (&raw)[G / 8], float& scale,
+                                                  float& zero,
+                                                  uint32_t (&words)[G * BITS / 32])
 {
-    __half2 mn = __hmin2(__hmin2(as_h2(raw.x), as_h2(raw.y)), __hmin2(as_h2(raw.z), as_h2(raw.w)));
-    __half2 mx = __hmax2(__hmax2(as_h2(raw.x), as_h2(raw.y)), __hmax2(as_h2(raw.z), as_h2(raw.w)));
-    for (int m = 1; m < lanes_per_group; m <<= 1) {
-        mn = __hmin2(mn, as_h2(__shfl_xor_sync(mask, h2_bits(mn), m)));
-        mx = __hmax2(mx, as_h2(__shfl_xor_sync(mask, h2_bits(mx), m)));
-    }
+    using Cd = Codec<BITS>;
+    __half2 mn = as_h2(raw[0].x), mx = mn;
+#pragma unroll
+    for (int i = 0; i < G / 8; ++i)
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            if (i == 0 && c == 0)
+                continue;
+            const __half2 v = as_h2(u4_word(raw[i], c));
+            mn = __hmin2(mn, v);
+            mx = __hmax2(mx, v);
+        }
     const float lo = fminf(__low2float(mn), __high2float(mn));
     const float hi = fmaxf(__low2float(mx), __high2float(mx));
     float inv;
     group_stats<BITS>(lo, hi, scale, zero, inv);
     const float nz = -zero;
-    bits_lo = 0u;
-    bits_hi = 0u;
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const uint32_t code = quant_code<BITS>(add_h_f(u4_half(raw, k), nz), scale, inv);
-        if (BITS == 8) {
-            if (k < 4)
-                bits_lo |= code << (8 * k);
-            else
-                bits_hi |= code << (8 * (k - 4));
-        } else {
-            bits_lo |= code << (BITS * k);
-        }
+    for (int w = 0; w < G * BITS / 32; ++w)
+        words[w] = 0u;
+#pragma unroll
+    for (int e = 0; e < G; ++e) {
+        const uint32_t code = quant_code<BITS>(add_h_f(u4_half(raw[e / 8], e % 8), nz), scale, inv);
+        words[e / Cd::P] |= code << ((e % Cd::P) * BITS);
     }
 }
 
@@ -245,36 +260,29 @@ __device__ __forceinline__ void quant_store_key_lane(const kivi_cache& c, size_t
     }
 }
 
-// Quantize the 8-channel slice `raw` (channels 8j..8j+7) of token t in slice
-// bh and store its codes and -- on the first lane of the channel group -- the
-// group statistics.  The G/8 lanes of the channel group (`gmask`) must call
-// this together.
-template <int BITS>
-__device__ __forceinline__ void store_value_lane(const kivi_cache& c, size_t bh, int t, int j,
-                                                 const uint4& raw, unsigned gmask)
+// Quantize value group gi (channels gi*G .. gi*G+G-1) of token t in slice bh
+// from `raw` and store its codes and statistics.
+template <int BITS, int G>
+__device__ __forceinline__ void quant_store_value_group(const kivi_cache& c, size_t bh, int t,
+                                                        int gi, const uint4 (&raw)[G / 8])
 {
     using Cd = Codec<BITS>;
-    const int D = c.D;
-    const int LPG = c.G / kLaneChans;
+    constexpr int NW = G * BITS / 32;  // 2, 4 or 8 words for G = 32
     float scale, zero;
-    uint32_t lo, hi;
-    quant_value_lane<BITS>(raw, LPG, gmask, scale, zero, lo, hi);
+    uint32_t words[NW];
+    quant_value_group<BITS, G>(raw, scale, zero, words);
     const size_t row = bh * (size_t)c.Tmax + t;
-    int32_t* vrow = c.vq + row * (D / Cd::P);
-    if (BITS == 2) {
-        const uint32_t other = __shfl_xor_sync(gmask, lo, 1);
-        if ((j & 1) == 0)
-            vrow[j >> 1] = (int32_t)(lo | (other << 16));
-    } else if (BITS == 4) {
-        vrow[j] = (int32_t)lo;
+    uint32_t* dst = reinterpret_cast<uint32_t*>(c.vq) + row * (c.D / Cd::P) + (size_t)gi * NW;
+    if constexpr (NW == 2) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
     } else {
-        reinterpret_cast<uint2*>(vrow)[j] = make_uint2(lo, hi);
+#pragma unroll
+        for (int w = 0; w < NW; w += 4)
+            *reinterpret_cast<uint4*>(dst + w) = make_uint4(words[w], words[w + 1], words[w + 2], words[w + 3]);
     }
-    if (j % LPG == 0) {
-        const size_t so = row * (D / c.G) + j / LPG;
-        c.vscale[so] = scale;
-        c.vzero[so] = zero;
-    }
+    const size_t so = row * (c.D / G) + gi;
+    c.vscale[so] = scale;
+    c.vzero[so] = zero;
 }
 
 // ------------------------------------------------- fused-dequant windows ---
