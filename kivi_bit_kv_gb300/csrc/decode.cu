@@ -54,6 +54,7 @@ decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_
     const int rows_per_cta = kDecodeThreads / LPR;
     const int hq_stride = (D / kSegChans) * kSegStride;
     const int TPL = kLaneTokens / LPR;  // logits each lane stores per row
+    const uint32_t one = one_bits();
 
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = h * NQ + pass * NQB;
@@ -121,12 +122,15 @@ decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_
 #pragma unroll
                     for (int k = 0; k < 4; ++k)
 #pragma unroll
-                        for (int i = 0; i < kLaneTokens; ++i) {
-                            const int ci = i % Cd::P;
-                            const float f = window_value<BITS>(u4_word(W[l][i / Cd::P], k), ci);
+                        for (int w = 0; w < Cd::kWordRows; ++w) {
+                            float f[Cd::P];
+                            window_values<BITS>(u4_word(W[l][w], k), one, f);
 #pragma unroll
-                            for (int hq = 0; hq < NQB; ++hq)
-                                acc[hq][i] = fmaf(qsw[hq][k][Win::pos_index(ci)], f, acc[hq][i]);
+                            for (int ci = 0; ci < Cd::P; ++ci)
+#pragma unroll
+                                for (int hq = 0; hq < NQB; ++hq)
+                                    acc[hq][w * Cd::P + ci] = fmaf(qsw[hq][k][Win::pos_index(ci)], f[ci],
+                                                                   acc[hq][w * Cd::P + ci]);
                         }
                 }
             }
@@ -248,6 +252,7 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
     const int seg = lane % LPT, tl = lane / LPT;
     constexpr int NW = kDecodeThreads / 32;
     const int g = (seg * CPL) / c.G;         // channel group of this segment
+    const uint32_t one = one_bits();
     const int NGv = D / c.G;
 
     for (int pass = 0; pass < NQ / NQB; ++pass) {
@@ -341,15 +346,16 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
                         psw[hq][p] = ps * Win::mult_of_index(p);
                 }
 #pragma unroll
-                for (int w = 0; w < WPL; ++w)
+                for (int w = 0; w < WPL; ++w) {
+                    float f[Cd::P];
+                    window_values<BITS>(W[u][w], one, f);
 #pragma unroll
-                    for (int i = 0; i < Cd::P; ++i) {
-                        const float f = window_value<BITS>(W[u][w], i);
+                    for (int i = 0; i < Cd::P; ++i)
 #pragma unroll
                         for (int hq = 0; hq < NQB; ++hq)
                             acc[hq][w * Cd::P + i] =
-                                fmaf(psw[hq][Win::pos_index(i)], f, acc[hq][w * Cd::P + i]);
-                    }
+                                fmaf(psw[hq][Win::pos_index(i)], f[i], acc[hq][w * Cd::P + i]);
+                }
             }
         }
 #pragma unroll

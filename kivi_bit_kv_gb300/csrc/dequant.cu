@@ -29,6 +29,7 @@ dequant_keys_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
     const int g = blockIdx.x * (kDequantThreads >> (lgS + lgNC)) + (threadIdx.x >> (lgS + lgNC));
     const int t0 = g * c.G + s * kLaneTokens;
     const int RG = c.R + c.G;
+    const uint32_t two23 = two23_bits();
 
     for (int bh = blockIdx.y; bh < c.B * c.H; bh += gridDim.y) {
         const int len = c.len[bh / c.H];
@@ -56,15 +57,16 @@ dequant_keys_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
                 if (t0 + i >= n)
                     break;  // out holds only T_out rows
                 const int w = i / Cd::P, sh = (i % Cd::P) * BITS;
-                uint32_t h[8];
+                uint32_t h2[4];
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const uint32_t word = k < 4 ? u4_word(wlo[w], k) : u4_word(whi[w], k - 4);
-                    h[k] = dequant_h((word >> sh) & Cd::M, sc[k], zr[k]);
+                for (int k = 0; k < 8; k += 2) {
+                    const uint32_t w0 = k < 4 ? u4_word(wlo[w], k) : u4_word(whi[w], k - 4);
+                    const uint32_t w1 = k < 4 ? u4_word(wlo[w], k + 1) : u4_word(whi[w], k - 3);
+                    h2[k / 2] = dequant_h2(code_float(w0 >> sh, Cd::M, two23),
+                                           code_float(w1 >> sh, Cd::M, two23), sc[k], zr[k],
+                                           sc[k + 1], zr[k + 1]);
                 }
-                st_stream(dst + (size_t)(t0 + i) * D,
-                          make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16),
-                                     h[4] | (h[5] << 16), h[6] | (h[7] << 16)));
+                st_stream(dst + (size_t)(t0 + i) * D, make_uint4(h2[0], h2[1], h2[2], h2[3]));
             }
         } else {
             for (int i = 0; i < kLaneTokens; ++i) {
@@ -92,6 +94,7 @@ dequant_values_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
     const int rows_per_pass = kDequantThreads >> lgNG;
     const int r0 = blockIdx.x * rows_per_pass * U + (threadIdx.x >> lgNG);
     const int RG = c.R + c.G;
+    const uint32_t two23 = two23_bits();
 
     for (int bh = blockIdx.y; bh < c.B * c.H; bh += gridDim.y) {
         const int len = c.len[bh / c.H];
@@ -133,15 +136,16 @@ dequant_values_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
             if (t < Tq) {
 #pragma unroll
                 for (int v = 0; v < G / 8; ++v) {
-                    uint32_t h[8];
+                    uint32_t h2[4];
 #pragma unroll
-                    for (int k = 0; k < 8; ++k) {
+                    for (int k = 0; k < 8; k += 2) {
                         const int e = v * 8 + k;
-                        h[k] = dequant_h((words[u][e / Cd::P] >> ((e % Cd::P) * BITS)) & Cd::M,
-                                         sc[u], zr[u]);
+                        h2[k / 2] = dequant_h2(
+                            code_float(words[u][e / Cd::P] >> ((e % Cd::P) * BITS), Cd::M, two23),
+                            code_float(words[u][(e + 1) / Cd::P] >> (((e + 1) % Cd::P) * BITS), Cd::M, two23),
+                            sc[u], zr[u], sc[u], zr[u]);
                     }
-                    st_stream(dst + v * 8, make_uint4(h[0] | (h[1] << 16), h[2] | (h[3] << 16),
-                                                      h[4] | (h[5] << 16), h[6] | (h[7] << 16)));
+                    st_stream(dst + v * 8, make_uint4(h2[0], h2[1], h2[2], h2[3]));
                 }
             } else {
                 const uint16_t* rs = c.vres + ((size_t)bh * RG + t % RG) * D + gi * G;

@@ -95,29 +95,69 @@ __device__ __forceinline__ void group_stats(float mn, float mx, float& scale,
     inv = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
 }
 
-// code = clamp(rne(a / scale), 0, M) for a = x - zero >= 0, bit-identical to
-// rounding the IEEE quotient.  Fast path: q0 = a * rn(1/scale).  For
-// y = a/scale <= M(1 + 2^-23) < 256, |q0 - y| <= 2.0001 * 2^-24 * y and
-// |rn(y) - y| <= 2^-24 * y, so |q0 - rn(y)| < 2^-14.  Unless q0 lies within
-// 2^-12 of a half-integer, q0 and rn(y) sit strictly on the same side of
-// every rounding boundary and round to the same integer; otherwise the IEEE
-// quotient is formed and rounded.  scale == 0 gives inv == 0, q0 == 0, code 0.
-template <int BITS>
-__device__ __forceinline__ uint32_t quant_code(float a, float scale, float inv)
+// Exact code: round-half-even of the IEEE quotient a / scale (scale > 0).
+// Kept out of line: it runs only for quotients near a rounding boundary.
+static __device__ __noinline__ uint32_t exact_code(float a, float scale)
+{
+    return (uint32_t)__float2int_rn(__fdiv_rn(a, scale));
+}
+
+// Fast code for a = x - zero >= 0, without branches.  With inv = rn(1/scale),
+// q0 = rn(a * inv) satisfies, for y = a/scale <= M(1 + 2^-23) < 256,
+// |q0 - y| <= 2.0001 * 2^-24 * y and |rn(y) - y| <= 2^-24 * y, so
+// |q0 - rn(y)| < 2^-14.  Unless q0 lies within 2^-12 of a half-integer, q0
+// and rn(y) sit strictly on the same side of every rounding boundary and
+// round to the same integer; `near` flags the other case, which the caller
+// resolves with exact_code().  The code never exceeds M here:
+// q0 <= M (1 + u)^2 / (1 - u) < M + 1/2.  Returns the bits of
+// t = q0 + 1.5 * 2^23, whose integer part is the code:
+// code = t_bits - 0x4B400000.  scale == 0 gives inv == 0 and code 0.
+__device__ __forceinline__ uint32_t fast_code_bits(float a, float inv, bool& near)
 {
     const float q0 = __fmul_rn(a, inv);
     const float t = __fadd_rn(q0, 12582912.0f);  // 1.5 * 2^23: ulp 1, RNE
     const float r = __fsub_rn(t, 12582912.0f);
-    const float d = __fsub_rn(q0, r);            // exact, in [-0.5, 0.5]
-    uint32_t c = __float_as_uint(t) - 0x4B400000u;
-    if (fabsf(d) >= 0.5f - 0x1p-12f)
-        c = (uint32_t)__float2int_rn(__fdiv_rn(a, scale));
-    return min(c, Codec<BITS>::M);
+    near = fabsf(__fsub_rn(q0, r)) >= 0.5f - 0x1p-12f;
+    return __float_as_uint(t);
+}
+constexpr uint32_t kCodeBias = 0x4B400000u;
+
+// code = clamp(rne(a / scale), 0, M), bit-identical to rounding the IEEE
+// quotient (see fast_code_bits).
+template <int BITS>
+__device__ __forceinline__ uint32_t quant_code(float a, float scale, float inv)
+{
+    bool near;
+    uint32_t c = fast_code_bits(a, inv, near) - kCodeBias;
+    if (near)
+        c = exact_code(a, scale);
+    return c;
 }
 
-__device__ __forceinline__ uint16_t dequant_h(uint32_t code, float scale, float zero)
+// 2^23 as an opaque register value (see one_bits).
+__device__ __forceinline__ uint32_t two23_bits()
 {
-    return __half_as_ushort(__float2half_rn(__fmaf_rn((float)code, scale, zero)));
+    uint32_t v = 0x4B000000u;
+    asm volatile("" : "+r"(v));
+    return v;
+}
+
+// (float)((word >> sh) & M) without a conversion instruction: one LOP3 places
+// the code in the mantissa of 2^23, one exact subtraction removes 2^23.
+__device__ __forceinline__ float code_float(uint32_t shifted, uint32_t mask, uint32_t two23)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(shifted), "r"(mask), "r"(two23));
+    return __fsub_rn(__uint_as_float(r), 8388608.0f);
+}
+
+// Two dequantized values fp16_rne(fmaf(code, scale, zero)) packed as half2
+// bits (first in the low half); f0, f1 are the codes as floats.
+__device__ __forceinline__ uint32_t dequant_h2(float f0, float f1, float s0, float z0, float s1,
+                                               float z1)
+{
+    const __half2 h = __floats2half2_rn(__fmaf_rn(f0, s0, z0), __fmaf_rn(f1, s1, z1));
+    return h2_bits(h);
 }
 
 // ------------------------------------------------------ lane quantizers ---
@@ -177,19 +217,38 @@ __device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens], 
             inv[k] = __shfl_sync(mask, inv[k], src);
         }
     }
+    // Pack t_bits * 2^sh (IMAD) and remove the constant bias once per word:
+    // sum_i (bias + c_i) 2^(b i) - bias * sum_i 2^(b i) = sum_i c_i 2^(b i) (mod 2^32).
+    constexpr uint32_t kWordBias = kCodeBias * (uint32_t)(((1ull << (Cd::P * BITS)) - 1) /
+                                                          ((1ull << BITS) - 1));
 #pragma unroll
     for (int w = 0; w < Cd::kWordRows; ++w)
 #pragma unroll
         for (int k = 0; k < 8; ++k)
-            words[w][k] = 0u;
+            words[w][k] = 0u - kWordBias;
 #pragma unroll
-    for (int i = 0; i < kLaneTokens; ++i)
+    for (int i = 0; i < kLaneTokens; ++i) {
+        bool any = false;
+        uint32_t tb[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const float a = add_h_f(u4_half(raw[i], k), nzero[k]);
-            const uint32_t code = quant_code<BITS>(a, scale[k], inv[k]);
-            words[i / Cd::P][k] |= code << ((i % Cd::P) * BITS);
+            bool near;
+            tb[k] = fast_code_bits(a, inv[k], near);
+            any |= near;
+            words[i / Cd::P][k] += tb[k] * (1u << ((i % Cd::P) * BITS));
         }
+        if (any) {  // rare: a quotient within 2^-12 of a rounding boundary
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float a = add_h_f(u4_half(raw[i], k), nzero[k]);
+                bool near;
+                const uint32_t fast = fast_code_bits(a, inv[k], near) - kCodeBias;
+                if (near)
+                    words[i / Cd::P][k] += (exact_code(a, scale[k]) - fast) << ((i % Cd::P) * BITS);
+            }
+        }
+    }
 }
 
 // Value group lane: one token's G consecutive channels (raw[i] = channels
@@ -217,13 +276,31 @@ __device__ __forceinline__ void quant_value_group(const uint4 (&raw)[G / 8], flo
     float inv;
     group_stats<BITS>(lo, hi, scale, zero, inv);
     const float nz = -zero;
+    constexpr uint32_t kWordBias = kCodeBias * (uint32_t)(((1ull << (Cd::P * BITS)) - 1) /
+                                                          ((1ull << BITS) - 1));
 #pragma unroll
     for (int w = 0; w < G * BITS / 32; ++w)
-        words[w] = 0u;
+        words[w] = 0u - kWordBias;
 #pragma unroll
-    for (int e = 0; e < G; ++e) {
-        const uint32_t code = quant_code<BITS>(add_h_f(u4_half(raw[e / 8], e % 8), nz), scale, inv);
-        words[e / Cd::P] |= code << ((e % Cd::P) * BITS);
+    for (int e0 = 0; e0 < G; e0 += 8) {
+        bool any = false;
+#pragma unroll
+        for (int e = e0; e < e0 + 8; ++e) {
+            bool near;
+            const uint32_t tb = fast_code_bits(add_h_f(u4_half(raw[e / 8], e % 8), nz), inv, near);
+            any |= near;
+            words[e / Cd::P] += tb * (1u << ((e % Cd::P) * BITS));
+        }
+        if (any) {
+#pragma unroll
+            for (int e = e0; e < e0 + 8; ++e) {
+                const float a = add_h_f(u4_half(raw[e / 8], e % 8), nz);
+                bool near;
+                const uint32_t fast = fast_code_bits(a, inv, near) - kCodeBias;
+                if (near)
+                    words[e / Cd::P] += (exact_code(a, scale) - fast) << ((e % Cd::P) * BITS);
+            }
+        }
     }
 }
 
@@ -297,69 +374,78 @@ __device__ __forceinline__ void quant_store_value_group(const kivi_cache& c, siz
 template <int BITS>
 struct Window;
 
-// int2: code i of a word at bits [2i, 2i+2); windows at mantissa bits 17/19/21.
+// int2: code i of a word at bits [2i, 2i+2).  Codes go in threes to mantissa
+// bits 17/19/21 after one shift each: shift(i) = 19 - 6*floor((i+1)/3)
+// (i = 0,1: <<19; 2-4: <<13; 5-7: <<7; 8-10: <<1; 11-13: >>5; 14,15: >>11),
+// pos(i) = 2i + shift(i), pos_index(i) = (i+1) % 3, mult = 64, 16, 4.
 template <>
 struct Window<2> {
-    static constexpr int kCodes = 16;
-    __device__ static __forceinline__ int pos(int i)
-    {
-        constexpr int t[16] = {19, 21, 17, 19, 21, 17, 19, 21, 17, 19, 21, 17, 19, 21, 17, 19};
-        return t[i];
-    }
-    // shift applied to the word before masking code i (positive = left)
-    __device__ static __forceinline__ int shift(int i)
-    {
-        constexpr int t[16] = {19, 19, 13, 13, 13, 7, 7, 7, 1, 1, 1, -5, -5, -5, -11, -11};
-        return t[i];
-    }
     static constexpr int kNumPos = 3;
-    __device__ static __forceinline__ int pos_index(int i) { return (pos(i) - 17) / 2; }   // 0,1,2
-    __device__ static __forceinline__ float mult_of_index(int k) { return k == 0 ? 64.0f : k == 1 ? 16.0f : 4.0f; }
+    __host__ __device__ static constexpr int shift(int i) { return 19 - 6 * ((i + 1) / 3); }
+    __host__ __device__ static constexpr int pos(int i) { return 2 * i + shift(i); }
+    __host__ __device__ static constexpr int pos_index(int i) { return (i + 1) % 3; }
+    __host__ __device__ static constexpr float mult_of_index(int k) { return (float)(64 >> (2 * k)); }
 };
 
-// int4: code i at bits [4i, 4i+4); windows at mantissa bits 15/19.
+// int4: code i at bits [4i, 4i+4); pairs go to mantissa bits 15/19 after
+// shift(i) = 15 - 8*floor(i/2) (<<15, <<7, >>1, >>9); pos_index = i & 1;
+// mult = 256, 16.
 template <>
 struct Window<4> {
-    static constexpr int kCodes = 8;
-    __device__ static __forceinline__ int pos(int i)
-    {
-        constexpr int t[8] = {15, 19, 15, 19, 15, 19, 15, 19};
-        return t[i];
-    }
-    __device__ static __forceinline__ int shift(int i)
-    {
-        constexpr int t[8] = {15, 15, 7, 7, -1, -1, -9, -9};
-        return t[i];
-    }
     static constexpr int kNumPos = 2;
-    __device__ static __forceinline__ int pos_index(int i) { return i & 1; }   // 15 -> 0, 19 -> 1
-    __device__ static __forceinline__ float mult_of_index(int k) { return k == 0 ? 256.0f : 16.0f; }
+    __host__ __device__ static constexpr int shift(int i) { return 15 - 8 * (i / 2); }
+    __host__ __device__ static constexpr int pos(int i) { return 4 * i + shift(i); }
+    __host__ __device__ static constexpr int pos_index(int i) { return i & 1; }
+    __host__ __device__ static constexpr float mult_of_index(int k) { return (float)(256 >> (4 * k)); }
 };
 
-// int8: code i at bits [8i, 8i+8); one window at mantissa bits 15.
+// int8: code i at bits [8i, 8i+8); each goes to mantissa bits 15..22 after
+// shift(i) = 15 - 8i (<<15, <<7, >>1, >>9); mult = 256.
 template <>
 struct Window<8> {
-    static constexpr int kCodes = 4;
-    __device__ static __forceinline__ int pos(int) { return 15; }
-    __device__ static __forceinline__ int shift(int i)
-    {
-        constexpr int t[4] = {15, 7, -1, -9};
-        return t[i];
-    }
     static constexpr int kNumPos = 1;
-    __device__ static __forceinline__ int pos_index(int) { return 0; }
-    __device__ static __forceinline__ float mult_of_index(int) { return 256.0f; }
+    __host__ __device__ static constexpr int shift(int i) { return 15 - 8 * i; }
+    __host__ __device__ static constexpr int pos(int i) { return 8 * i + shift(i); }
+    __host__ __device__ static constexpr int pos_index(int) { return 0; }
+    __host__ __device__ static constexpr float mult_of_index(int) { return 256.0f; }
 };
 
-// f(c) for code i of `word`: 1 + c * 2^(pos(i)-23).  All arguments but `word`
-// are compile-time constants once the caller's loop over i is unrolled.
-template <int BITS>
-__device__ __forceinline__ float window_value(uint32_t word, int i)
+static_assert(Window<2>::pos(0) == 19 && Window<2>::pos(1) == 21 && Window<2>::pos(2) == 17 &&
+                  Window<2>::pos(10) == 21 && Window<2>::pos(11) == 17 && Window<2>::pos(15) == 19,
+              "int2 windows");
+static_assert(Window<4>::pos(0) == 15 && Window<4>::pos(1) == 19 && Window<4>::pos(6) == 15 &&
+                  Window<4>::pos(7) == 19, "int4 windows");
+static_assert(Window<8>::pos(3) == 15, "int8 windows");
+
+// 1.0f as an opaque register value: keeps the exponent operand of the
+// per-code mask in a register instead of being rematerialized per use.
+__device__ __forceinline__ uint32_t one_bits()
 {
-    const int sh = Window<BITS>::shift(i);
-    const uint32_t s = sh >= 0 ? (word << sh) : (word >> (-sh));
-    const uint32_t m = ((1u << BITS) - 1u) << Window<BITS>::pos(i);
-    return __uint_as_float((s & m) | 0x3F800000u);
+    uint32_t v = 0x3F800000u;
+    asm volatile("" : "+r"(v));
+    return v;
+}
+
+// (a & mask) | one in a single LOP3.
+__device__ __forceinline__ float mask_or(uint32_t a, uint32_t mask, uint32_t one)
+{
+    uint32_t r;
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(one));
+    return __uint_as_float(r);
+}
+
+// All P window values of one word: f[i] = 1 + c_i * 2^(pos(i)-23).  Each
+// distinct shift is formed once; every code then costs one LOP3.
+template <int BITS>
+__device__ __forceinline__ void window_values(uint32_t word, uint32_t one,
+                                              float (&f)[32 / BITS])
+{
+#pragma unroll
+    for (int i = 0; i < 32 / BITS; ++i) {
+        const int sh = Window<BITS>::shift(i);
+        const uint32_t sw = sh >= 0 ? (word << sh) : (word >> (-sh));
+        f[i] = mask_or(sw, ((1u << BITS) - 1u) << Window<BITS>::pos(i), one);
+    }
 }
 
 }  // namespace kivi
