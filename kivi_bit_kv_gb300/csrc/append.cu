@@ -68,7 +68,9 @@ append_kernel(kivi_cache c, const uint16_t* __restrict__ k, const uint16_t* __re
             for (int i = 0; i < kLaneTokens; ++i)
                 raw[i] = *reinterpret_cast<const uint4*>(
                     c.kres + (bh * RG + (t0 + i) % RG) * D + (size_t)j * kLaneChans);
-            quant_store_key_lane<BK>(c, bh, t0, Tq / G, j, s, S, smask, raw);
+            // RG and t0 are multiples of 16: the lane's 16 ring rows never wrap
+            quant_store_key_lane<BK>(c, bh, t0, Tq / G, j, s, S, smask, raw,
+                                     c.kres + (bh * RG + t0 % RG) * D + (size_t)j * kLaneChans, D);
         }
     }
     // values: G token rows x D/G channel groups, one lane per group

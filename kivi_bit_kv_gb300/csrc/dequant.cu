@@ -24,9 +24,10 @@ dequant_keys_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
     const int D = c.D;
     const int S = c.G / kLaneTokens, lgS = lg2(S);
     const int NC = D / kLaneChans, lgNC = lg2(NC);
-    const int s = threadIdx.x & (S - 1);
-    const int j = (threadIdx.x >> lgS) & (NC - 1);
-    const int g = blockIdx.x * (kDequantThreads >> (lgS + lgNC)) + (threadIdx.x >> (lgS + lgNC));
+    const int id = blockIdx.x * kDequantThreads + threadIdx.x;  // lane task within the slice
+    const int s = id & (S - 1);
+    const int j = (id >> lgS) & (NC - 1);
+    const int g = id >> (lgS + lgNC);
     const int t0 = g * c.G + s * kLaneTokens;
     const int RG = c.R + c.G;
     const uint32_t two23 = two23_bits();
@@ -182,9 +183,8 @@ cudaError_t launch_dequant(const kivi_cache& c, int which, uint16_t* out, int T_
     if (T_out <= 0)
         return cudaGetLastError();
     if (which == 0) {
-        const int groups_per_cta = kDequantThreads / ((c.G / kLaneTokens) * (c.D / kLaneChans));
-        const int groups = (T_out + c.G - 1) / c.G;
-        const dim3 grid = dq_grid(c, (groups + groups_per_cta - 1) / groups_per_cta);
+        const int lanes = ((T_out + c.G - 1) / c.G) * (c.G / kLaneTokens) * (c.D / kLaneChans);
+        const dim3 grid = dq_grid(c, (lanes + kDequantThreads - 1) / kDequantThreads);
         switch (c.bits_k) {
         case 2: dequant_keys_kernel<2><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;
         case 4: dequant_keys_kernel<4><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;

@@ -14,8 +14,10 @@
 
 namespace kivi {
 
-// Tokens one lane covers in a key tile (one int2 word; two int4 / four int8).
+// Tokens one lane covers in a key tile (one int2 word; two int4 / four int8)
+// and in a decode_qk row.
 constexpr int kLaneTokens = 16;
+constexpr int kRowTokens = kLaneTokens;
 // Channels one lane covers in an encode / materialize tile (one 16-byte vector).
 constexpr int kLaneChans = 8;
 
@@ -31,6 +33,18 @@ __host__ __device__ __forceinline__ int quantized_tokens(int T, int G, int R)
     const int n = T - R;
     return n <= 0 ? 0 : (n / G) * G;
 }
+
+// ------------------------------------------------------------- cp.async ---
+// 16-byte asynchronous global -> shared copies (cached in L2 only).  A thread
+// waits for its own groups with cp.async.wait_group -- a hardware wait, no
+// spinning -- and a warp barrier then publishes them to the warp.
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
+{
+    const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;\n" ::: "memory"); }
 
 // ---------------------------------------------------------------- loads ---
 
@@ -102,24 +116,26 @@ static __device__ __noinline__ uint32_t exact_code(float a, float scale)
     return (uint32_t)__float2int_rn(__fdiv_rn(a, scale));
 }
 
-// Fast code for a = x - zero >= 0, without branches.  With inv = rn(1/scale),
-// q0 = rn(a * inv) satisfies, for y = a/scale <= M(1 + 2^-23) < 256,
-// |q0 - y| <= 2.0001 * 2^-24 * y and |rn(y) - y| <= 2^-24 * y, so
-// |q0 - rn(y)| < 2^-14.  Unless q0 lies within 2^-12 of a half-integer, q0
-// and rn(y) sit strictly on the same side of every rounding boundary and
-// round to the same integer; `near` flags the other case, which the caller
-// resolves with exact_code().  The code never exceeds M here:
-// q0 <= M (1 + u)^2 / (1 - u) < M + 1/2.  Returns the bits of
-// t = q0 + 1.5 * 2^23, whose integer part is the code:
-// code = t_bits - 0x4B400000.  scale == 0 gives inv == 0 and code 0.
-__device__ __forceinline__ uint32_t fast_code_bits(float a, float inv, bool& near)
+// Fast code for a = x - zero >= 0, without branches.  With inv = rn(1/scale)
+// the exact product p = a * inv equals y = a / scale up to a factor
+// (1 + d), |d| <= 2^-24, and y <= M (1 + 2^-23) < 256.
+//   t = rn(p + C), C = 1.5 * 2^23 (ulp 1): t - C = r, the nearest integer to
+//   p, ties to even (one FFMA, the product is not rounded first);
+//   dlt = rn(p - r) = fma(a, inv, C - t) (C - t is exact).
+// |rn(y) - p| <= 2^-24 y + 2^-24 y <= 2^-15, so when |dlt| < 1/2 - 2^-12 the
+// IEEE quotient rn(y) lies strictly within 1/2 of r and rounds to r; `near`
+// flags the other case, which the caller resolves with exact_code().  The
+// code never exceeds M: p <= M (1 + 2^-24)^2 / (1 - 2^-24) < M + 1/2.
+// Returns the bits of t: code = t_bits - 0x4B400000.  scale == 0 gives
+// inv == 0, p == 0 and code 0.
+__device__ __forceinline__ uint32_t fast_code_bits(float a, float inv, float& worst)
 {
-    const float q0 = __fmul_rn(a, inv);
-    const float t = __fadd_rn(q0, 12582912.0f);  // 1.5 * 2^23: ulp 1, RNE
-    const float r = __fsub_rn(t, 12582912.0f);
-    near = fabsf(__fsub_rn(q0, r)) >= 0.5f - 0x1p-12f;
+    const float t = __fmaf_rn(a, inv, 12582912.0f);
+    const float dlt = __fmaf_rn(a, inv, __fsub_rn(12582912.0f, t));
+    worst = fmaxf(worst, fabsf(dlt));  // flags are tested once per batch of codes
     return __float_as_uint(t);
 }
+constexpr float kNearTie = 0.5f - 0x1p-12f;  // |dlt| at or above this: use exact_code
 constexpr uint32_t kCodeBias = 0x4B400000u;
 
 // code = clamp(rne(a / scale), 0, M), bit-identical to rounding the IEEE
@@ -127,9 +143,9 @@ constexpr uint32_t kCodeBias = 0x4B400000u;
 template <int BITS>
 __device__ __forceinline__ uint32_t quant_code(float a, float scale, float inv)
 {
-    bool near;
-    uint32_t c = fast_code_bits(a, inv, near) - kCodeBias;
-    if (near)
+    float worst = 0.0f;
+    uint32_t c = fast_code_bits(a, inv, worst) - kCodeBias;
+    if (worst >= kNearTie)
         c = exact_code(a, scale);
     return c;
 }
@@ -170,8 +186,9 @@ __device__ __forceinline__ uint32_t dequant_h2(float f0, float f1, float s0, flo
 template <int BITS>
 __device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens], int S,
                                                unsigned mask, float (&scale)[8],
-                                               float (&zero)[8],
-                                               uint32_t (&words)[Codec<BITS>::kWordRows][8])
+                                               float (&zero)[8], float (&inv)[8],
+                                               uint32_t (&words)[Codec<BITS>::kWordRows][8],
+                                               unsigned& flagged)
 {
     using Cd = Codec<BITS>;
     __half2 mn[4], mx[4];
@@ -195,7 +212,7 @@ __device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens], 
     // Every lane of the tile column now holds the same min / max.  The S lanes
     // split the eight divisions (lane s takes channels k with k % S == s) and
     // exchange the results.
-    float inv[8], nzero[8];
+    float nzero[8];
     const int s_lane = (int)(threadIdx.x & 31) & (S - 1);
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -226,26 +243,47 @@ __device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens], 
 #pragma unroll
         for (int k = 0; k < 8; ++k)
             words[w][k] = 0u - kWordBias;
+    flagged = 0u;
 #pragma unroll
     for (int i = 0; i < kLaneTokens; ++i) {
-        bool any = false;
-        uint32_t tb[8];
+        float worst = 0.0f;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const float a = add_h_f(u4_half(raw[i], k), nzero[k]);
-            bool near;
-            tb[k] = fast_code_bits(a, inv[k], near);
-            any |= near;
-            words[i / Cd::P][k] += tb[k] * (1u << ((i % Cd::P) * BITS));
+            const uint32_t tb = fast_code_bits(a, inv[k], worst);
+            words[i / Cd::P][k] += tb * (1u << ((i % Cd::P) * BITS));
         }
-        if (any) {  // rare: a quotient within 2^-12 of a rounding boundary
+        flagged |= (worst >= kNearTie ? 1u : 0u) << i;
+    }
+}
+
+// Rows of a key lane whose fast codes need the exact quotient (bit i of
+// `flagged`), re-read from `row0 + i * stride`: one small loop, kept out of
+// the unrolled main body.
+template <int BITS>
+__device__ __forceinline__ void key_lane_fixup(unsigned flagged, const uint16_t* row0, size_t stride,
+                                               const float (&scale)[8], const float (&inv)[8],
+                                               const float (&zero)[8],
+                                               uint32_t (&words)[Codec<BITS>::kWordRows][8])
+{
+    using Cd = Codec<BITS>;
+#pragma unroll 1
+    while (flagged) {
+        const int i = __ffs(flagged) - 1;
+        flagged &= flagged - 1;
+        const uint4 r = *reinterpret_cast<const uint4*>(row0 + (size_t)i * stride);
+        const int sh = (i % Cd::P) * BITS;
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                const float a = add_h_f(u4_half(raw[i], k), nzero[k]);
-                bool near;
-                const uint32_t fast = fast_code_bits(a, inv[k], near) - kCodeBias;
-                if (near)
-                    words[i / Cd::P][k] += (exact_code(a, scale[k]) - fast) << ((i % Cd::P) * BITS);
+        for (int k = 0; k < 8; ++k) {
+            const float a = add_h_f(u4_half(r, k), -zero[k]);
+            float w1 = 0.0f;
+            const uint32_t fast = fast_code_bits(a, inv[k], w1) - kCodeBias;
+            if (w1 >= kNearTie) {
+                const uint32_t fix = (exact_code(a, scale[k]) - fast) << sh;
+#pragma unroll
+                for (int w = 0; w < Cd::kWordRows; ++w)
+                    if (w == i / Cd::P)
+                        words[w][k] += fix;
             }
         }
     }
@@ -283,21 +321,19 @@ __device__ __forceinline__ void quant_value_group(const uint4 (&raw)[G / 8], flo
         words[w] = 0u - kWordBias;
 #pragma unroll
     for (int e0 = 0; e0 < G; e0 += 8) {
-        bool any = false;
+        float worst = 0.0f;
 #pragma unroll
         for (int e = e0; e < e0 + 8; ++e) {
-            bool near;
-            const uint32_t tb = fast_code_bits(add_h_f(u4_half(raw[e / 8], e % 8), nz), inv, near);
-            any |= near;
+            const uint32_t tb = fast_code_bits(add_h_f(u4_half(raw[e / 8], e % 8), nz), inv, worst);
             words[e / Cd::P] += tb * (1u << ((e % Cd::P) * BITS));
         }
-        if (any) {
+        if (__builtin_expect(worst >= kNearTie, 0)) {
 #pragma unroll
             for (int e = e0; e < e0 + 8; ++e) {
                 const float a = add_h_f(u4_half(raw[e / 8], e % 8), nz);
-                bool near;
-                const uint32_t fast = fast_code_bits(a, inv, near) - kCodeBias;
-                if (near)
+                float w1 = 0.0f;
+                const uint32_t fast = fast_code_bits(a, inv, w1) - kCodeBias;
+                if (w1 >= kNearTie)
                     words[e / Cd::P] += (exact_code(a, scale) - fast) << ((e % Cd::P) * BITS);
             }
         }
@@ -313,13 +349,17 @@ __device__ __forceinline__ void quant_value_group(const uint4 (&raw)[G / 8], flo
 template <int BITS>
 __device__ __forceinline__ void quant_store_key_lane(const kivi_cache& c, size_t bh, int t0,
                                                      int g, int j, int s, int S, unsigned smask,
-                                                     const uint4 (&raw)[kLaneTokens])
+                                                     const uint4 (&raw)[kLaneTokens],
+                                                     const uint16_t* row0, size_t row_stride)
 {
     using Cd = Codec<BITS>;
     const int D = c.D;
-    float scale[8], zero[8];
+    float scale[8], zero[8], inv[8];
     uint32_t words[Cd::kWordRows][8];
-    quant_key_lane<BITS>(raw, S, smask, scale, zero, words);
+    unsigned flagged;
+    quant_key_lane<BITS>(raw, S, smask, scale, zero, inv, words, flagged);
+    if (__builtin_expect(flagged != 0u, 0))
+        key_lane_fixup<BITS>(flagged, row0, row_stride, scale, inv, zero, words);
     int32_t* dst = c.kq + (bh * (size_t)(c.Tmax / Cd::P) + t0 / Cd::P) * D + (size_t)j * kLaneChans;
 #pragma unroll
     for (int w = 0; w < Cd::kWordRows; ++w) {

@@ -53,7 +53,7 @@ quant_keys_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
 #pragma unroll
             for (int i = 0; i < kLaneTokens; ++i)
                 raw[i] = ld_stream(src + (size_t)(t0 + i) * D);
-            quant_store_key_lane<BITS>(c, bh, t0, g, j, s, S, smask, raw);
+            quant_store_key_lane<BITS>(c, bh, t0, g, j, s, S, smask, raw, src + (size_t)t0 * D, D);
         } else {
             for (int i = 0; i < kLaneTokens; ++i) {
                 const int t = t0 + i;
