@@ -149,52 +149,90 @@ class ClockSampler:
 
 # ------------------------------------------------------- byte accounting --
 
-def alg_bytes(w, T: int, n_dec: int) -> dict:
-    """Algorithmic HBM bytes (read + write) of each call in one step.
+# How each workload is stepped: "full" = encode + materialize + append +
+# decode of one batch; "store" = encode + materialize (the exact-prefix store
+# round trip); "decode" / "stream" = append + decode on a cache encoded once
+# before the timed region (the cache grows by one token per step).
+KINDS = {"tiny": "full", "llama2_7b_layer": "full", "prefix_store_int4": "store",
+         "prefix_store_int8": "store", "mistral_gqa": "decode", "streaming": "stream"}
+STEP_CALLS = {
+    "full": ["quant_keys", "quant_values", "dequant_keys", "dequant_values", "append",
+             "decode_qk", "decode_pv"],
+    "store": ["quant_keys", "quant_values", "dequant_keys", "dequant_values"],
+    "decode": ["append", "decode_qk", "decode_pv"],
+    "stream": ["append", "decode_qk", "decode_pv"],
+}
+LAUNCHES = {"quant_keys": 1, "quant_values": 1, "dequant_keys": 1, "dequant_values": 1,
+            "append": 2, "decode_qk": 1, "decode_pv": 2}  # append / decode_pv enqueue two kernels
 
-    T: prefix tokens encoded / materialized; n_dec: tokens attended over by
-    the decode (T + 1 after the append)."""
-    BH, D, G, Rr = w.B * w.H, w.D, w.G, w.R
-    def split(n):
-        tq = max(0, (n - Rr) // G * G)
-        return tq, n - tq
-    tq, res = split(T)
-    kcodes = BH * tq * D * w.bits_k // 8
-    vcodes = BH * tq * D * w.bits_v // 8
-    kstats = BH * (tq // G) * D * 8
-    vstats = BH * tq * (D // G) * 8
-    resb = BH * res * D * 2
-    fp16 = BH * T * D * 2
-    tqd, resd = split(n_dec)
-    kcd = BH * tqd * D * w.bits_k // 8 + BH * (tqd // G) * D * 8 + BH * resd * D * 2
-    vcd = BH * tqd * D * w.bits_v // 8 + BH * tqd * (D // G) * 8 + BH * resd * D * 2
-    qb = w.B * w.Hq * D * 2
-    lg = w.B * w.Hq * n_dec * 4
+
+def _split(n, G, R):
+    tq = max(0, (int(n) - R) // G * G)
+    return tq, int(n) - tq
+
+
+def slice_bytes(w, n: int, which: int) -> int:
+    """Stored bytes of one (b, h) slice holding n tokens: codes + fp32
+    scale/zero + fp16 residual (keys: which = 0, values: which = 1)."""
+    tq, res = _split(n, w.G, w.R)
+    bits = w.bits_k if which == 0 else w.bits_v
+    stats = (tq // w.G) * w.D * 8 if which == 0 else tq * (w.D // w.G) * 8
+    return tq * w.D * bits // 8 + stats + res * w.D * 2
+
+
+def call_bytes(w, enc_lens, dec_lens) -> dict:
+    """Algorithmic HBM bytes (read + write) of each call of one step.
+
+    enc_lens[b]: tokens of sequence b encoded / materialized; dec_lens[b]:
+    tokens the decode attends over (after the append)."""
+    H, Hq, D = w.H, w.Hq, w.D
+    fp16 = sum(H * int(n) * D * 2 for n in enc_lens)
+    kst = sum(H * slice_bytes(w, n, 0) for n in enc_lens)
+    vst = sum(H * slice_bytes(w, n, 1) for n in enc_lens)
+    kdec = sum(H * slice_bytes(w, n, 0) for n in dec_lens)
+    vdec = sum(H * slice_bytes(w, n, 1) for n in dec_lens)
+    logits = sum(Hq * int(n) * 4 for n in dec_lens)
+    B = len(dec_lens)
     return {
-        "quant_keys": fp16 + kcodes + kstats + resb,
-        "quant_values": fp16 + vcodes + vstats + resb,
-        "dequant_keys": kcodes + kstats + resb + fp16,
-        "dequant_values": vcodes + vstats + resb + fp16,
-        "append": 2 * BH * D * 2 * 2,
-        "decode_qk": kcd + qb + lg,
-        "decode_pv": vcd + lg + w.B * w.Hq * D * 4,
+        "quant_keys": fp16 + kst, "quant_values": fp16 + vst,
+        "dequant_keys": kst + fp16, "dequant_values": vst + fp16,
+        "append": B * H * D * 2 * 4,
+        "decode_qk": kdec + B * Hq * D * 2 + logits,
+        "decode_pv": vdec + logits + B * Hq * D * 4,
     }
 
 
-def fp16_equiv_bytes(w, T: int, n_dec: int) -> int:
+def fp16_equiv_bytes(w, kind: str, enc_lens, dec_lens) -> int:
     """fp16 K+V bytes the step encodes, materializes and attends over."""
-    BH, D = w.B * w.H, w.D
-    return 2 * BH * T * D * 2 + 2 * BH * T * D * 2 + 2 * BH * n_dec * D * 2 + 2 * BH * D * 2
+    H, D = w.H, w.D
+    enc = sum(2 * H * int(n) * D * 2 for n in enc_lens)
+    dec = sum(2 * H * int(n) * D * 2 for n in dec_lens)
+    app = 2 * len(dec_lens) * H * D * 2
+    return {"full": 2 * enc + dec + app, "store": 2 * enc}.get(kind, dec + app)
+
+
+def reduce_max(value: float, device="cpu") -> float:
+    """Max of `value` over the ranks of the default process group (identity
+    when there is none): the slowest replica defines the job time."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_value(bytes_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Job throughput in GB/s: every replica moves the same bytes per step,
+    and the step lasts as long as the slowest replica."""
+    return bytes_per_rank * world / (ms_per_step * 1e-3) / 1e9
 
 
 # --------------------------------------------------------------- GPU arm --
 
-CALLS = ["quant_keys", "quant_values", "dequant_keys", "dequant_values", "append",
-         "decode_qk", "decode_pv"]
-LAUNCHES_PER_STEP = 9  # append and decode_pv enqueue two kernels each
-
-
 def run_kivi(args, rank, world, local):
+    import numpy as np
     import torch
     from kivi_bit_kv_gb300 import KiviCache, abi
     from kivi_bit_kv_gb300 import workloads as W
@@ -205,38 +243,55 @@ def run_kivi(args, rank, world, local):
         import torch.distributed as dist
         dist.init_process_group("nccl" if dist.is_nccl_available() else "gloo")
     w = W.WORKLOADS[args.workload]
-    T = w.T
-    Tmax = (T + 1 + w.G - 1) // w.G * w.G + w.G
+    kind = KINDS[w.name]
+    calls = STEP_CALLS[kind]
+    grows = kind in ("decode", "stream")
+    n_app = (args.warmup + args.steps) if grows else 1
+    lens0 = W.make_lengths(w).numpy().astype(np.int64)
+    Tmax = (int(lens0.max()) + n_app + w.G) // w.G * w.G + w.G
     K, V = W.make_kv(w, device=dev)
-    q = W.make_q(w, device=dev)
-    kn, vn = W.make_step_tokens(w, 1, device=dev)
-    kn, vn = kn[0].contiguous(), vn[0].contiguous()
     cache = KiviCache(w.B, w.H, w.D, w.bits_k, w.bits_v, w.G, w.R, Tmax, device=dev)
-    kh = torch.empty((w.B, w.H, T, w.D), dtype=torch.float16, device=dev)
-    vh = torch.empty_like(kh)
+    seq_lens = None if w.ragged is None else torch.as_tensor(lens0.astype(np.int32), device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
     ld = (Tmax + 3) // 4 * 4
     logits = torch.empty((w.B, w.Hq, ld), dtype=torch.float32, device=dev)
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
     ws = cache.workspace(w.Hq)
-    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    kn, vn = W.make_step_tokens(w, n_app, device=dev)
+    qs = torch.stack([W.make_q(w, dev, step=s) for s in range(n_app)]) if grows else W.make_q(w, dev)[None]
+    if kind in ("full", "store"):
+        kh = torch.empty((w.B, w.H, w.T, w.D), dtype=torch.float16, device=dev)
+        vh = torch.empty_like(kh)
+    else:  # encode the prefix once; the timed steps only append and decode
+        abi.kivi_quant_keys(cache, K, seq_lens)
+        abi.kivi_quant_values(cache, V, seq_lens)
+        torch.cuda.synchronize(dev)
+        del K, V
+        torch.cuda.empty_cache()
     stream = torch.cuda.current_stream(dev)
 
-    def step(ev=None):
-        fns = [lambda: abi.kivi_quant_keys(cache, K), lambda: abi.kivi_quant_values(cache, V),
-               lambda: abi.kivi_dequant(cache, 0, kh), lambda: abi.kivi_dequant(cache, 1, vh),
-               lambda: abi.kivi_append_token(cache, kn, vn, status),
-               lambda: abi.kivi_decode_qk(cache, q, logits), lambda: abi.kivi_decode_pv(cache, logits, out, ws)]
-        for i, fn in enumerate(fns):
+    def step(i, ev=None):
+        j = i if grows else 0
+        fns = {
+            "quant_keys": lambda: abi.kivi_quant_keys(cache, K, seq_lens),
+            "quant_values": lambda: abi.kivi_quant_values(cache, V, seq_lens),
+            "dequant_keys": lambda: abi.kivi_dequant(cache, 0, kh),
+            "dequant_values": lambda: abi.kivi_dequant(cache, 1, vh),
+            "append": lambda: abi.kivi_append_token(cache, kn[j], vn[j], status),
+            "decode_qk": lambda: abi.kivi_decode_qk(cache, qs[j], logits),
+            "decode_pv": lambda: abi.kivi_decode_pv(cache, logits, out, ws),
+        }
+        for c_i, name in enumerate(calls):
             if ev is not None:
-                ev[2 * i].record(stream)
-            fn()
+                ev[2 * c_i].record(stream)
+            fns[name]()
             if ev is not None:
-                ev[2 * i + 1].record(stream)
+                ev[2 * c_i + 1].record(stream)
 
-    for _ in range(args.warmup):
-        step()
+    for i in range(args.warmup):
+        step(i)
     torch.cuda.synchronize(dev)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(CALLS))] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(calls))] for _ in range(args.steps)]
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -244,63 +299,70 @@ def run_kivi(args, rank, world, local):
     with ClockSampler(local) as clk:
         t0.record(stream)
         for s in range(args.steps):
-            step(evs[s])
+            step(args.warmup + s, evs[s])
         t1.record(stream)
         torch.cuda.synchronize(dev)
     if world > 1:
         torch.distributed.barrier()
-    ms = t0.elapsed_time(t1)
+    assert int(status.item()) == 0, "a sequence ran out of capacity"
     per_call = {c: sum(evs[s][2 * i].elapsed_time(evs[s][2 * i + 1]) for s in range(args.steps)) / args.steps
-                for i, c in enumerate(CALLS)}
-    assert int(status.item()) == 0
-    if world > 1:
-        import torch.distributed as dist
-        tmax = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tmax, op=dist.ReduceOp.MAX)
-        ms = float(tmax.item())
+                for i, c in enumerate(calls)}
+    ms_step = reduce_max(t0.elapsed_time(t1), dev) / args.steps
 
-    ms_step = ms / args.steps
-    n_dec = T + 1
-    eq = fp16_equiv_bytes(w, T, n_dec)
-    value = eq * world / (ms_step * 1e-3) / 1e9
-    ab = alg_bytes(w, T, n_dec)
+    # bytes per step, averaged over the timed steps (decode caches grow)
+    if grows:
+        timed = [lens0 + args.warmup + s + 1 for s in range(args.steps)]
+        pick = timed[:: max(1, len(timed) // 16)]
+        ab_list = [call_bytes(w, d, d) for d in pick]
+        ab = {k: sum(a[k] for a in ab_list) / len(ab_list) for k in ab_list[0]}
+        eq = sum(fp16_equiv_bytes(w, kind, d, d) for d in pick) / len(pick)
+    else:
+        dec = lens0 + 1
+        ab = call_bytes(w, lens0, dec)
+        eq = fp16_equiv_bytes(w, kind, lens0, dec)
+    value = whole_job_value(eq, world, ms_step)
     hbm, src = peaks()
     kernels = {}
-    for c in CALLS:
+    for c in calls:
         gbs = ab[c] / (per_call[c] * 1e-3) / 1e9
-        kernels[c] = {"ms": round(per_call[c], 5), "alg_bytes": ab[c], "gbs": round(gbs, 1),
+        kernels[c] = {"ms": round(per_call[c], 5), "alg_bytes": int(ab[c]), "gbs": round(gbs, 1),
                       "frac": round(gbs / hbm, 3)}
-    dominant = max(CALLS, key=lambda c: per_call[c])
+    dominant = max(calls, key=lambda c: per_call[c])
     dk = kernels[dominant]
-    quant_ms = per_call["quant_keys"] + per_call["quant_values"]
-    deq_ms = per_call["dequant_keys"] + per_call["dequant_values"]
-    dec_ms = per_call["decode_qk"] + per_call["decode_pv"]
-    BH = w.B * w.H
+    breakdown = {"kernels": kernels}
+    H, D = w.H, w.D
+    if kind in ("full", "store"):
+        enc = sum(2 * H * int(n) * D * 2 for n in lens0)
+        qms = per_call["quant_keys"] + per_call["quant_values"]
+        dms = per_call["dequant_keys"] + per_call["dequant_values"]
+        breakdown["quant_gbs_fp16eq"] = round(enc / (qms * 1e-3) / 1e9, 1)
+        breakdown["dequant_gbs_fp16eq"] = round(enc / (dms * 1e-3) / 1e9, 1)
+    if kind != "store":
+        dec_ms = per_call["decode_qk"] + per_call["decode_pv"]
+        breakdown["decode_tok_s"] = round(w.B * world / (dec_ms * 1e-3), 1)
+        breakdown["step_tok_s"] = round(w.B * world / (ms_step * 1e-3), 1)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u2 codes / f32 stats / f16 KV",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": f"u{w.bits_k}/u{w.bits_v} codes, f32 stats, f16 KV, f32 accumulate",
         "data": "synthetic (seeded N(0,1) fp16, outlier key channels)",
-        "config": {"workload": w.name, "shape": [w.B, w.H, T, w.D], "Hq": w.Hq, "bits_k": w.bits_k,
-                   "bits_v": w.bits_v, "G": w.G, "R": w.R, "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (K, V 268 MB each)"},
-        "breakdown": {
-            "quant_gbs_fp16eq": round(2 * BH * T * w.D * 2 / (quant_ms * 1e-3) / 1e9, 1),
-            "dequant_gbs_fp16eq": round(2 * BH * T * w.D * 2 / (deq_ms * 1e-3) / 1e9, 1),
-            "decode_tok_s": round(w.B / (dec_ms * 1e-3), 1),
-            "decode_gbs_fp16eq": round(2 * BH * n_dec * w.D * 2 / (dec_ms * 1e-3) / 1e9, 1),
-            "kernels": kernels,
-        },
+        "config": {"workload": w.name, "step": kind, "shape": [w.B, w.H, w.T, w.D], "Hq": w.Hq,
+                   "bits_k": w.bits_k, "bits_v": w.bits_v, "G": w.G, "R": w.R,
+                   "ragged": list(w.ragged) if w.ragged else None,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "packed cache and fp16 K/V larger than L2 (no flush needed)"},
+        "breakdown": breakdown,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": hbm,
                      "peak_source": src, "unit": "GB/s", "frac": dk["frac"],
                      "traffic": recorded_traffic(dominant, w.name)},
-        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "gpu_launches": sum(LAUNCHES[c] for c in calls) * args.steps,
         "clocks": clk.summary(),
     }
-    if not args.no_e2e:
+    if kind == "full" and not args.no_e2e:
         line["e2e"] = run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, K, V, q, kn, vn)
+    if rank == 0 and world == 1 and kind == "full" and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, K, V, qs[0], kn[0], vn[0])
     if world > 1:
         torch.distributed.destroy_process_group()
     return line if rank == 0 else None
@@ -344,15 +406,10 @@ def run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq):
         step()
     t1.record(stream)
     torch.cuda.synchronize(dev)
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        import torch.distributed as dist
-        tm = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
+    ms = reduce_max(t0.elapsed_time(t1), dev)
     bi = sum(t.numel() * t.element_size() for t in (Kh, Vh, qh, knh, vnh))
     bo = outh.numel() * outh.element_size()
-    return {"value": round(eq * world / (ms / n * 1e-3) / 1e9, 1), "unit": UNIT,
+    return {"value": round(whole_job_value(eq, world, ms / n), 1), "unit": UNIT,
             "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n}
 
 

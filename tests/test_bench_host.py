@@ -1,0 +1,92 @@
+"""Host logic of bench.py, without a GPU: the replica timing across ranks (two
+gloo processes on the CPU), and the byte accounting behind the roofline
+numbers, checked against the library's closed-form kivi_cache_bytes."""
+import os
+import socket
+import sys
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def _free_port() -> int:
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _replica(rank, world, port, ms, q):
+    import torch.distributed as dist
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        slowest = bench.reduce_max(ms[rank])
+        q.put((rank, slowest, bench.whole_job_value(2e9, world, slowest)))
+    finally:
+        dist.destroy_process_group()
+
+
+def test_replicas_take_the_slowest_rank():
+    """Each rank times its own replica; every rank ends with the max, and
+    the job value counts all ranks' bytes over that time (weak scaling)."""
+    import torch.multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    world, port, ms = 2, _free_port(), [4.0, 5.0]
+    procs = [ctx.Process(target=_replica, args=(r, world, port, ms, q)) for r in range(world)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in range(world))
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [r[1] for r in res] == [5.0, 5.0]
+    assert res[0][2] == pytest.approx(2e9 * 2 / 5e-3 / 1e9)
+
+
+def test_reduce_max_without_process_group():
+    assert bench.reduce_max(3.5) == 3.5
+    assert bench.whole_job_value(1e9, 1, 1.0) == pytest.approx(1000.0)
+
+
+def test_dist_env_defaults(monkeypatch):
+    for k in ("RANK", "WORLD_SIZE", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    assert bench.dist_env() == (0, 1, 0)
+    monkeypatch.setenv("RANK", "3")
+    monkeypatch.setenv("WORLD_SIZE", "4")
+    monkeypatch.setenv("LOCAL_RANK", "1")
+    assert bench.dist_env() == (3, 4, 1)
+
+
+@pytest.mark.parametrize("name", ["llama2_7b_layer", "prefix_store_int4", "prefix_store_int8",
+                                  "mistral_gqa", "tiny"])
+def test_step_bytes_match_library_closed_form(kivi_lib, name):
+    """The stored-bytes part of the encode accounting equals H x
+    kivi_cache_bytes per sequence, for keys and values."""
+    from kivi_bit_kv_gb300 import abi
+    from kivi_bit_kv_gb300 import workloads as W
+    w = W.WORKLOADS[name]
+    lens = np.array([w.T - 3 * b for b in range(w.B)])
+    ab = bench.call_bytes(w, lens, lens + 1)
+    fp16 = sum(w.H * int(n) * w.D * 2 for n in lens)
+    for which, key in ((0, "quant_keys"), (1, "quant_values")):
+        bits = w.bits_k if which == 0 else w.bits_v
+        lib = sum(w.H * abi.kivi_cache_bytes(int(n), w.D, bits, w.G, w.R, which) for n in lens)
+        assert ab[key] - fp16 == lib
+
+
+def test_fp16_equivalent_bytes_per_kind():
+    from kivi_bit_kv_gb300 import workloads as W
+    w = W.WORKLOADS["llama2_7b_layer"]
+    lens = np.full(w.B, w.T)
+    kv = 2 * w.B * w.H * w.T * w.D * 2
+    assert bench.fp16_equiv_bytes(w, "store", lens, lens) == 2 * kv
+    assert bench.fp16_equiv_bytes(w, "decode", lens, lens) == kv + 2 * w.B * w.H * w.D * 2
+    assert bench.fp16_equiv_bytes(w, "full", lens, lens) == 3 * kv + 2 * w.B * w.H * w.D * 2
