@@ -210,6 +210,22 @@ int32_t kivi_decode_pv(const kivi_cache* c, const float* logits,
                        int32_t ld_logits, int32_t Hq, float* out, void* ws,
                        size_t ws_bytes, void* stream);
 
+/*
+ * Decode attention in one pass over the cache: the logits of kivi_decode_qk,
+ * the softmax and the weighted sum of kivi_decode_pv, fused per (KV head,
+ * 1024-token chunk) so that the logits stay on chip:
+ *   out[b][hq][d] = sum_t softmax_t(sm_scale q . K_hat_t) V_hat[t][d]
+ * over t < len[b] (CacheSeek PR #4: decode from the quantized KV).  q: fp16
+ * [B][Hq][D]; out: fp32 [B][Hq][D]; ws as for kivi_decode_pv (>=
+ * kivi_workspace_bytes(c, Hq) bytes, 16-byte aligned).  Requires
+ * bits_k == bits_v (KIVI_EINVAL otherwise: use kivi_decode_qk followed by
+ * kivi_decode_pv).  A sequence with len[b] == 0 gets out = 0.  Two kernels on
+ * `stream`.
+ */
+int32_t kivi_decode_attention(const kivi_cache* c, const uint16_t* q,
+                              int32_t Hq, float sm_scale, float* out,
+                              void* ws, size_t ws_bytes, void* stream);
+
 /* Workspace bytes kivi_decode_pv needs for this descriptor and Hq. */
 size_t kivi_workspace_bytes(const kivi_cache* c, int32_t Hq);
 

@@ -31,7 +31,7 @@ EXPORTS = (
     "kivi_abi_version", "kivi_status_string", "kivi_last_error", "kivi_cache_validate",
     "kivi_buffer_bytes", "kivi_cache_bytes", "kivi_quant_keys", "kivi_quant_values",
     "kivi_dequant", "kivi_append_token", "kivi_decode_qk", "kivi_decode_pv",
-    "kivi_workspace_bytes", "kivi_decode_pv_noalloc",
+    "kivi_workspace_bytes", "kivi_decode_pv_noalloc", "kivi_decode_attention",
 )
 
 KIVI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
@@ -85,6 +85,7 @@ def load(path: str | None = None):
         "kivi_decode_pv": ([cp, vp, i32, i32, vp, vp, sz, vp], i32),
         "kivi_workspace_bytes": ([cp, i32], sz),
         "kivi_decode_pv_noalloc": ([cp, vp, i32, i32, vp, vp], i32),
+        "kivi_decode_attention": ([cp, vp, i32, f32, vp, vp, sz, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -243,3 +244,21 @@ def kivi_decode_pv_noalloc(cache, logits: torch.Tensor, out: torch.Tensor, strea
                                          _dev(logits, torch.float32, "logits", cache.device), ld, Hq,
                                          _dev(out, torch.float32, "out", cache.device),
                                          _stream(stream, cache.device)), "kivi_decode_pv_noalloc")
+
+
+def kivi_decode_attention(cache, q: torch.Tensor, out: torch.Tensor, ws: torch.Tensor,
+                          sm_scale: float | None = None, stream=None):
+    """out fp32 [B, Hq, D] <- softmax(sm_scale q . K_hat^T) . V_hat in one fused
+    pass (logits stay on chip); q fp16 [B, Hq, D] (or [B, Hq, 1, D]), ws a
+    device workspace of at least kivi_workspace_bytes(cache, Hq) bytes."""
+    B, Hq = q.shape[0], q.shape[1]
+    if B != cache.B or q.shape[-1] != cache.D or q.numel() != B * Hq * cache.D:
+        raise ValueError(f"q shape {tuple(q.shape)} does not match cache")
+    if tuple(out.shape) not in ((B, Hq, cache.D), (B, Hq, 1, cache.D)):
+        raise ValueError(f"out shape {tuple(out.shape)}; expected {(B, Hq, cache.D)}")
+    sm = float(cache.D ** -0.5) if sm_scale is None else float(sm_scale)
+    wp = _dev(ws, ws.dtype, "ws", cache.device)
+    _check(load().kivi_decode_attention(C.byref(cache.desc), _dev(q, torch.float16, "q", cache.device),
+                                        Hq, sm, _dev(out, torch.float32, "out", cache.device), wp,
+                                        ws.numel() * ws.element_size(), _stream(stream, cache.device)),
+           "kivi_decode_attention")

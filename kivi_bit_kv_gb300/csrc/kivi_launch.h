@@ -32,6 +32,12 @@ cudaError_t launch_decode_pv(const kivi_cache& c, const float* logits, int ld_lo
                              float* out, float* ws_o, float* ws_m, float* ws_l,
                              cudaStream_t s);
 
+// q . K, softmax and p . V in one kernel per (KV head, chunk) plus the combine
+// kernel; requires c.bits_k == c.bits_v.  Workspace as for launch_decode_pv.
+cudaError_t launch_decode_attention(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale,
+                                    float* out, float* ws_o, float* ws_m, float* ws_l,
+                                    cudaStream_t s);
+
 // Sets the message kivi_last_error() returns on this host thread; returns status.
 int32_t record_error(int32_t status, const char* message);
 

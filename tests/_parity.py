@@ -40,15 +40,22 @@ def gpu_encode(cache: KiviCache, K: torch.Tensor, V: torch.Tensor, seq_lens=None
 
 
 def gpu_decode(cache: KiviCache, q: torch.Tensor, sm_scale=None):
+    """Two-kernel decode (logits, out) and, when bits_k == bits_v, the fused
+    kivi_decode_attention output (else None)."""
     B, Hq, D = q.shape
     ld = roundup(cache.Tmax, 4)
     logits = torch.zeros((B, Hq, ld), dtype=torch.float32, device=cache.device)
     out = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=cache.device)
     ws = cache.workspace(Hq)
-    abi.kivi_decode_qk(cache, q.to(cache.device), logits, sm_scale)
+    qd = q.to(cache.device)
+    abi.kivi_decode_qk(cache, qd, logits, sm_scale)
     abi.kivi_decode_pv(cache, logits, out, ws)
+    fused = None
+    if cache.bits_k == cache.bits_v:
+        fused = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=cache.device)
+        abi.kivi_decode_attention(cache, qd, fused, cache.workspace(Hq), sm_scale)
     torch.cuda.synchronize(cache.device)
-    return logits.cpu().numpy(), out.cpu().numpy()
+    return logits.cpu().numpy(), out.cpu().numpy(), None if fused is None else fused.cpu().numpy()
 
 
 def state(cache: KiviCache, rows=None) -> dict:
@@ -113,9 +120,14 @@ def row_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
     return float(num / den) if den > 0 else float(num)
 
 
-def compare_attention(lg, out, ref_lg, ref_out, lens, heads=None, rtol=ATTN_RTOL):
+def compare_attention(lg, out, ref_lg, ref_out, lens, heads=None, rtol=ATTN_RTOL, fused=None):
     """Per-row relative error of logits and outputs; rows of empty sequences
-    must be exactly zero.  Returns the worst (logit, output) errors."""
+    must be exactly zero.  The fused kernel runs the same tile arithmetic with
+    the logits kept on chip, so its output must equal the two-kernel output
+    bit for bit.  Returns the worst (logit, output) errors."""
+    if fused is not None:
+        assert np.array_equal(fused, out), (
+            f"fused output differs from the two-kernel path at {np.argwhere(fused != out)[:5].tolist()}")
     worst_l = worst_o = 0.0
     B, Hq = out.shape[:2]
     for b in range(B):

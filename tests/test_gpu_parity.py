@@ -73,9 +73,9 @@ def test_encode_dequant_decode_small(cuda, case):
         ex, tot = compare_dequant(np16(out).view(np.uint16), rc.decode(which, T_out=T), lens)
         assert ex == tot  # same fmaf + fp16 rounding on both sides
 
-    lg, o = gpu_decode(cache, q)
+    lg, o, fo = gpu_decode(cache, q)
     rlg, ro = rc.attention(np16(q))
-    compare_attention(lg, o, rlg, ro, lens)
+    compare_attention(lg, o, rlg, ro, lens, fused=fo)
 
 
 def test_decode_is_deterministic(cuda):
@@ -86,7 +86,7 @@ def test_decode_is_deterministic(cuda):
     gpu_encode(cache, K, V)
     a = gpu_decode(cache, q)
     b = gpu_decode(cache, q)
-    assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
 
 
 @pytest.mark.parametrize("bk,bv,G,Rr,T0,n", [(2, 2, 32, 128, 100, 300), (4, 8, 32, 0, 17, 150),
@@ -113,9 +113,9 @@ def test_append_stream_small(cuda, bk, bv, G, Rr, T0, n):
         rc.append(np16(kn[s]), np16(vn[s]))
         if s in check_at:
             q = f16_host((B, Hq, D), 100 + s)
-            lg, o = gpu_decode(cache, q)
+            lg, o, fo = gpu_decode(cache, q)
             rlg, ro = rc.attention(np16(q))
-            compare_attention(lg, o, rlg, ro, rc.lens)
+            compare_attention(lg, o, rlg, ro, rc.lens, fused=fo)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     compare_state(state(cache), rc)
@@ -174,9 +174,9 @@ def test_workload_tiny(cuda):
         ex, tot = compare_dequant(np16(out).view(np.uint16), rc.decode(which), rc.lens)
         assert ex == tot
     q = W.make_q(w, cuda)
-    lg, o = gpu_decode(cache, q)
+    lg, o, fo = gpu_decode(cache, q)
     rlg, ro = rc.attention(np16(q))
-    compare_attention(lg, o, rlg, ro, rc.lens)
+    compare_attention(lg, o, rlg, ro, rc.lens, fused=fo)
 
 
 @pytest.mark.slow
@@ -192,9 +192,9 @@ def test_workload_llama2_layer_full(cuda):
         ex, tot = compare_dequant(np16(out).view(np.uint16), rc.decode(which, threads=THREADS), rc.lens)
         assert ex == tot
     q = W.make_q(w, cuda)
-    lg, o = gpu_decode(cache, q)
+    lg, o, fo = gpu_decode(cache, q)
     rlg, ro = rc.attention(np16(q), threads=THREADS)
-    compare_attention(lg, o, rlg, ro, rc.lens)
+    compare_attention(lg, o, rlg, ro, rc.lens, fused=fo)
 
 
 @pytest.mark.slow
@@ -226,9 +226,9 @@ def test_workload_mistral_gqa(cuda):
     cache, rc, K, V, rows = _workload_encode(w, cuda)
     compare_state(state(cache), rc)
     q = W.make_q(w, cuda)
-    lg, o = gpu_decode(cache, q)
+    lg, o, fo = gpu_decode(cache, q)
     rlg, ro = rc.attention(np16(q), threads=THREADS)
-    compare_attention(lg, o, rlg, ro, rc.lens)
+    compare_attention(lg, o, rlg, ro, rc.lens, fused=fo)
 
 
 @pytest.mark.slow
@@ -247,16 +247,20 @@ def test_workload_streaming(cuda):
     logits = torch.zeros((w.B, w.Hq, ld), dtype=torch.float32, device=cuda)
     out = torch.zeros((w.B, w.Hq, w.D), dtype=torch.float32, device=cuda)
     ws = cache.workspace(w.Hq)
+    fused = torch.zeros((w.B, w.Hq, w.D), dtype=torch.float32, device=cuda)
+    ws2 = cache.workspace(w.Hq)
     for s in range(w.steps):
         abi.kivi_append_token(cache, kn[s], vn[s], status)
         rc.append(np16(kn[s][rows]), np16(vn[s][rows]))
         q = W.make_q(w, cuda, step=s)
         abi.kivi_decode_qk(cache, q, logits)
         abi.kivi_decode_pv(cache, logits, out, ws)
+        abi.kivi_decode_attention(cache, q, fused, ws2)
         if s in check:
             torch.cuda.synchronize()
             rlg, ro = rc.attention(np16(q[rows]), threads=THREADS)
-            compare_attention(logits[rows].cpu().numpy(), out[rows].cpu().numpy(), rlg, ro, rc.lens)
+            compare_attention(logits[rows].cpu().numpy(), out[rows].cpu().numpy(), rlg, ro, rc.lens,
+                              fused=fused[rows].cpu().numpy())
     torch.cuda.synchronize()
     assert int(status.item()) == 0
     compare_state(state(cache, rows), rc)
