@@ -50,6 +50,8 @@ def parse():
     p.add_argument("--workload", default="llama2_7b_layer")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--decode", default="fused", choices=["fused", "split"],
+                   help="decode through kivi_decode_attention (fused) or kivi_decode_qk + kivi_decode_pv")
     return p.parse_args()
 
 
@@ -156,14 +158,25 @@ class ClockSampler:
 KINDS = {"tiny": "full", "llama2_7b_layer": "full", "prefix_store_int4": "store",
          "prefix_store_int8": "store", "mistral_gqa": "decode", "streaming": "stream"}
 STEP_CALLS = {
-    "full": ["quant_keys", "quant_values", "dequant_keys", "dequant_values", "append",
-             "decode_qk", "decode_pv"],
+    "full": ["quant_keys", "quant_values", "dequant_keys", "dequant_values", "append", "decode"],
     "store": ["quant_keys", "quant_values", "dequant_keys", "dequant_values"],
-    "decode": ["append", "decode_qk", "decode_pv"],
-    "stream": ["append", "decode_qk", "decode_pv"],
+    "decode": ["append", "decode"],
+    "stream": ["append", "decode"],
 }
+# "decode" is the fused kivi_decode_attention (--decode fused, the default) or
+# kivi_decode_qk followed by kivi_decode_pv (--decode split, and always when
+# bits_k != bits_v).
+DECODE_CALLS = {"fused": ["decode_attn"], "split": ["decode_qk", "decode_pv"]}
 LAUNCHES = {"quant_keys": 1, "quant_values": 1, "dequant_keys": 1, "dequant_values": 1,
-            "append": 2, "decode_qk": 1, "decode_pv": 2}  # append / decode_pv enqueue two kernels
+            "append": 2, "decode_qk": 1, "decode_pv": 2, "decode_attn": 2}  # + combine kernels
+
+
+def step_calls(w, kind: str, decode: str) -> list:
+    mode = decode if w.bits_k == w.bits_v else "split"
+    out = []
+    for c in STEP_CALLS[kind]:
+        out += DECODE_CALLS[mode] if c == "decode" else [c]
+    return out
 
 
 def _split(n, G, R):
@@ -199,6 +212,7 @@ def call_bytes(w, enc_lens, dec_lens) -> dict:
         "append": B * H * D * 2 * 4,
         "decode_qk": kdec + B * Hq * D * 2 + logits,
         "decode_pv": vdec + logits + B * Hq * D * 4,
+        "decode_attn": kdec + vdec + B * Hq * D * 2 + B * Hq * D * 4,
     }
 
 
@@ -244,7 +258,7 @@ def run_kivi(args, rank, world, local):
         dist.init_process_group("nccl" if dist.is_nccl_available() else "gloo")
     w = W.WORKLOADS[args.workload]
     kind = KINDS[w.name]
-    calls = STEP_CALLS[kind]
+    calls = step_calls(w, kind, args.decode)
     grows = kind in ("decode", "stream")
     n_app = (args.warmup + args.steps) if grows else 1
     lens0 = W.make_lengths(w).numpy().astype(np.int64)
@@ -280,6 +294,7 @@ def run_kivi(args, rank, world, local):
             "append": lambda: abi.kivi_append_token(cache, kn[j], vn[j], status),
             "decode_qk": lambda: abi.kivi_decode_qk(cache, qs[j], logits),
             "decode_pv": lambda: abi.kivi_decode_pv(cache, logits, out, ws),
+            "decode_attn": lambda: abi.kivi_decode_attention(cache, qs[j], out, ws),
         }
         for c_i, name in enumerate(calls):
             if ev is not None:
@@ -338,7 +353,7 @@ def run_kivi(args, rank, world, local):
         breakdown["quant_gbs_fp16eq"] = round(enc / (qms * 1e-3) / 1e9, 1)
         breakdown["dequant_gbs_fp16eq"] = round(enc / (dms * 1e-3) / 1e9, 1)
     if kind != "store":
-        dec_ms = per_call["decode_qk"] + per_call["decode_pv"]
+        dec_ms = sum(per_call[c] for c in calls if c.startswith("decode"))
         breakdown["decode_tok_s"] = round(w.B * world / (dec_ms * 1e-3), 1)
         breakdown["step_tok_s"] = round(w.B * world / (ms_step * 1e-3), 1)
     line = {
@@ -360,7 +375,7 @@ def run_kivi(args, rank, world, local):
         "clocks": clk.summary(),
     }
     if kind == "full" and not args.no_e2e:
-        line["e2e"] = run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq)
+        line["e2e"] = run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq, calls)
     if rank == 0 and world == 1 and kind == "full" and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, K, V, qs[0], kn[0], vn[0])
     if world > 1:
@@ -368,7 +383,7 @@ def run_kivi(args, rank, world, local):
     return line if rank == 0 else None
 
 
-def run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq):
+def run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq, calls):
     """Same step through the public API from pinned host buffers: H2D of the
     step's K, V, q and new token, the step, D2H of the attention output."""
     import torch
@@ -391,8 +406,11 @@ def run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq):
         abi.kivi_dequant(cache, 0, kh)
         abi.kivi_dequant(cache, 1, vh)
         abi.kivi_append_token(cache, knd, vnd, status)
-        abi.kivi_decode_qk(cache, qd, logits)
-        abi.kivi_decode_pv(cache, logits, out, ws)
+        if "decode_attn" in calls:
+            abi.kivi_decode_attention(cache, qd, out, ws)
+        else:
+            abi.kivi_decode_qk(cache, qd, logits)
+            abi.kivi_decode_pv(cache, logits, out, ws)
         outh.copy_(out, non_blocking=True)
 
     for _ in range(2):

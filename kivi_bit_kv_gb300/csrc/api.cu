@@ -100,7 +100,7 @@ int32_t launched(cudaError_t e)
 
 size_t ws_bytes(const kivi_cache& c, int Hq)
 {
-    const size_t rows = (size_t)c.B * Hq * kivi::pv_chunks(c);
+    const size_t rows = (size_t)c.B * Hq * kivi::pv_chunks(c, Hq);
     return rows * ((size_t)c.D + 2) * sizeof(float);
 }
 
@@ -267,7 +267,7 @@ int32_t kivi_decode_pv(const kivi_cache* c, const float* logits, int32_t ld_logi
     const size_t need = ws_bytes(*c, Hq);
     if (ws_bytes_given < need)
         return fail(KIVI_EWORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes_given, need);
-    const size_t rows = (size_t)c->B * Hq * kivi::pv_chunks(*c);
+    const size_t rows = (size_t)c->B * Hq * kivi::pv_chunks(*c, Hq);
     float* ws_o = static_cast<float*>(ws);
     float* ws_m = ws_o + rows * c->D;
     float* ws_l = ws_m + rows;
@@ -288,7 +288,7 @@ int32_t kivi_decode_attention(const kivi_cache* c, const uint16_t* q, int32_t Hq
     const size_t need = ws_bytes(*c, Hq);
     if (ws_bytes_given < need)
         return fail(KIVI_EWORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes_given, need);
-    const size_t rows = (size_t)c->B * Hq * kivi::pv_chunks(*c);
+    const size_t rows = (size_t)c->B * Hq * kivi::pv_chunks(*c, Hq);
     float* ws_o = static_cast<float*>(ws);
     float* ws_m = ws_o + rows * c->D;
     float* ws_l = ws_m + rows;

@@ -7,8 +7,9 @@
 //   decode_pv_kernel         softmax + p . V from given logits (kivi_decode_pv)
 //   decode_attention_kernel  both, logits kept in shared memory
 //                            (kivi_decode_attention)
-// Each CTA owns one KV head and one 1024-token chunk; the pv and fused kernels
-// leave per-chunk (o, m, l) partials that decode_combine_kernel merges.
+// Each CTA owns one KV head and one chunk of decode_chunk_tokens() tokens,
+// staged into shared memory at launch; the pv and fused kernels leave
+// per-chunk (o, m, l) partials that decode_combine_kernel merges.
 #include <math.h>
 
 #include "decode_mma.cuh"
@@ -16,183 +17,354 @@
 
 namespace kivi {
 
-// Per-CTA coordinates of a decode chunk.
+// Per-CTA coordinates of a decode chunk of TC tokens.
 struct ChunkRange {
     int b, h, n, t_begin, t_end, Tq, tq_end;
 };
 
-__device__ __forceinline__ bool chunk_range(const kivi_cache& c, ChunkRange& r)
+__device__ __forceinline__ bool chunk_range(const kivi_cache& c, int TC, ChunkRange& r)
 {
-    const size_t bh = blockIdx.x;
-    r.b = (int)(bh / c.H);
-    r.h = (int)(bh % c.H);
+    const int bh = (int)blockIdx.x;
+    r.b = bh / c.H;
+    r.h = bh - r.b * c.H;
     r.n = c.len[r.b];
-    r.t_begin = blockIdx.y * kChunkTokens;
+    r.t_begin = blockIdx.y * TC;
     if (r.t_begin >= r.n)
         return false;
-    r.t_end = min(r.t_begin + kChunkTokens, r.n);
+    r.t_end = min(r.t_begin + TC, r.n);
     r.Tq = quantized_tokens(r.n, c.G, c.R);
     r.tq_end = max(r.t_begin, min(r.t_end, r.Tq));
     return true;
 }
 
+// Pointers into the dynamic shared memory of a decode kernel (decode_layout),
+// for item buffer `buf`.
+struct DecodeSmem {
+    uint32_t *kw, *vw;
+    float *ks, *kz, *vs, *vz, *p, *part, *zs;
+    uint16_t* q16;
+    uint2* bb;
+};
+
+__device__ __forceinline__ DecodeSmem carve(float* base, const DecodeLayout& L, int buf)
+{
+    float* b = base + L.buf * buf;
+    DecodeSmem m;
+    m.kw = reinterpret_cast<uint32_t*>(b + L.kw);
+    m.ks = b + L.ks;
+    m.kz = b + L.kz;
+    m.vw = reinterpret_cast<uint32_t*>(b + L.vw);
+    m.vs = b + L.vs;
+    m.vz = b + L.vz;
+    m.q16 = reinterpret_cast<uint16_t*>(b + L.q16);
+    m.p = base + L.p;
+    m.bb = reinterpret_cast<uint2*>(L.bb_on_keys ? b + L.bb : base + L.bb);
+    m.part = L.part_on_vstats ? b + L.part : base + L.part;
+    m.zs = base + L.zs;
+    return m;
+}
+
+
 // ---------------------------------------------------------------- q . K ---
 
 template <int BITS, int NQB>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 3)
 decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_scale,
-                 float* __restrict__ logits, int ldl)
+                 float* __restrict__ logits, int ldl, int TC, const DecodeLayout L)
 {
+    extern __shared__ __align__(16) float dsm[];
     __shared__ __align__(16) float qs[NQB * qstride_of(256)];
     __shared__ float fac[NQB];
+    using T = KeyTile<BITS, NQB>;
     ChunkRange r;
-    if (!chunk_range(c, r))
+    if (!chunk_range(c, TC, r))
         return;
     const size_t bh = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const DecodeSmem m = carve(dsm, L, 0);
+    stage_keys<BITS, T::TOK>(c, bh, r.t_begin, r.tq_end, m.kw, m.ks, m.kz);
+    cp_async_commit();
     const int NQ = Hq / c.H;
+    const int rows = 32 / (c.D / 32);  // residual tokens per warp step
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = r.h * NQ + pass * NQB;
         __syncthreads();
         stage_q<NQB>(q + ((size_t)r.b * Hq + hq0) * c.D, c.D, sm_scale, qs, fac);
+        cp_async_wait_all();
         __syncthreads();
         float* out = logits + ((size_t)r.b * Hq + hq0) * ldl;
         auto sink = [&](int h, int t, float s) { out[(size_t)h * ldl + t] = s; };
-        qk_quantized<BITS, NQB>(c, bh, r.t_begin, r.tq_end, qs, fac, sink);
-        qk_residual<NQB>(c, bh, r.tq_end, r.t_end, qs, fac, sink);
+        qk_quantized<BITS, NQB>(c.D, c.G, r.t_begin, r.tq_end, r.t_begin + warp * T::TOK, r.tq_end,
+                                kDecodeWarps * T::TOK, m.kw, m.ks, m.kz, qs, fac, sink);
+        qk_residual<NQB>(c, bh, r.tq_end + warp * rows, kDecodeWarps * rows, r.t_end, qs, fac, sink);
+        (void)lane;
     }
 }
 
 // ---------------------------------------------------------------- p . V ---
 
-// Dynamic shared memory of the pv / fused kernels: p [NQB][1024], then the
-// split partials.
-__host__ __device__ constexpr size_t pv_smem_bytes(int NQB, int D, int G)
+// Softmax statistics, B fragments and the weighted value sum of one pass
+// (p_sm holds the chunk's logits), then the chunk's partials.  Whole CTA.
+template <int BITS, int NQB>
+__device__ __forceinline__ void pv_pass(const kivi_cache& c, size_t bh, int TC, const ChunkRange& r,
+                                        const DecodeSmem& m, float* red, size_t row0, int nchunks,
+                                        float* ws_o, float* ws_m, float* ws_l, bool first_pass)
 {
-    return ((size_t)NQB * kChunkTokens + pv_part_floats(NQB, D, G)) * sizeof(float);
+    const int ps = prob_stride(TC), NGv = c.D >> ilog2(c.G);
+    const int n = r.t_end - r.t_begin, nq = r.tq_end - r.t_begin;
+    float mx[NQB], l[NQB];
+    chunk_softmax<NQB>(m.p, ps, n, mx, l, red);
+    if (first_pass) {
+        cp_async_wait_all();  // the staged values
+        __syncthreads();
+    }
+    pv_weights<NQB>(n, nq, NGv, threadIdx.x, pv_pairs(n, nq), kDecodeThreads, 0, m.p, ps, m.vs, m.vz,
+                    m.bb, bb_stride(TC), m.zs);
+    __syncthreads();
+    pv_chunk<BITS, NQB>(c, bh, TC, r.t_begin, r.tq_end, r.t_end, m.vw, m.bb, m.part);
+    __syncthreads();
+    write_partials<NQB>(c.D, c.G, pv_splits(pv_seg_groups<BITS>(c.D)), m.part, m.zs, mx, l, row0,
+                        nchunks, ws_o, ws_m, ws_l);
 }
 
 template <int BITS, int NQB>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 3)
 decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq,
                  float* __restrict__ ws_o, float* __restrict__ ws_m, float* __restrict__ ws_l,
-                 int nchunks)
+                 int nchunks, int TC, const DecodeLayout L)
 {
-    extern __shared__ __align__(16) float pv_smem[];
+    extern __shared__ __align__(16) float dsm[];
     __shared__ float red[kDecodeWarps * NQB];
-    float* p_sm = pv_smem;
-    float* o_part = p_sm + NQB * kChunkTokens;
-    float* z_part = o_part + kDecodeWarps * NQB * c.D;
     ChunkRange r;
-    if (!chunk_range(c, r))
+    if (!chunk_range(c, TC, r))
         return;
     const size_t bh = blockIdx.x;
+    const DecodeSmem m = carve(dsm, L, 0);
+    stage_values<BITS>(c, bh, r.t_begin, r.tq_end, m.vw, m.vs, m.vz);
+    cp_async_commit();
     const int NQ = Hq / c.H;
     const int n = r.t_end - r.t_begin;
-    const int NCB = (c.D / (32 / BITS)) / ValTile<BITS, NQB>::WC;
+    const int ps = prob_stride(TC);
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = r.h * NQ + pass * NQB;
         __syncthreads();
-        for (int i = threadIdx.x; i < NQB * n; i += kDecodeThreads) {
-            const int h = i / n, t = i % n;
-            p_sm[h * kChunkTokens + t] = logits[((size_t)r.b * Hq + hq0 + h) * ldl + r.t_begin + t];
+#pragma unroll
+        for (int h = 0; h < NQB; ++h) {
+            const float* lrow = logits + ((size_t)r.b * Hq + hq0 + h) * ldl + r.t_begin;
+            for (int t = threadIdx.x; t < n; t += kDecodeThreads)
+                m.p[h * ps + t] = lrow[t];
         }
         __syncthreads();
-        float m[NQB], l[NQB];
-        chunk_softmax<NQB>(p_sm, n, m, l, red);
-        pv_chunk<BITS, NQB>(c, bh, r.t_begin, r.tq_end, r.t_end, p_sm, o_part, z_part);
-        __syncthreads();
-        const size_t row0 = ((size_t)r.b * Hq + hq0) * nchunks + blockIdx.y;
-        write_partials<NQB>(c.D, c.G, pv_splits(NCB), o_part, z_part, m, l, row0, nchunks, ws_o,
-                            ws_m, ws_l);
+        pv_pass<BITS, NQB>(c, bh, TC, r, m, red, ((size_t)r.b * Hq + hq0) * nchunks + blockIdx.y,
+                           nchunks, ws_o, ws_m, ws_l, pass == 0);
     }
 }
 
 // ------------------------------------------------------------ attention ---
 
+// One CTA per (KV head, chunk); after the chunk's keys and values are staged,
+// each warp works through its own quarter of the chunk alone -- logits, its
+// softmax statistics, its B fragments, its share of p . V -- and the CTA
+// merges the four warp partials once at the end, so the warps meet at two
+// barriers per pass.
 template <int BITS, int NQB>
-__global__ void __launch_bounds__(kDecodeThreads)
+__global__ void __launch_bounds__(kDecodeThreads, 3)
 decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_scale,
                         float* __restrict__ ws_o, float* __restrict__ ws_m,
-                        float* __restrict__ ws_l, int nchunks)
+                        float* __restrict__ ws_l, int nchunks, int TC, const WarpLayout L)
 {
-    extern __shared__ __align__(16) float pv_smem[];
+    extern __shared__ __align__(16) float dsm[];
     __shared__ __align__(16) float qs[NQB * qstride_of(256)];
     __shared__ float fac[NQB];
-    __shared__ float red[kDecodeWarps * NQB];
-    float* p_sm = pv_smem;
-    float* o_part = p_sm + NQB * kChunkTokens;
-    float* z_part = o_part + kDecodeWarps * NQB * c.D;
+    __shared__ float wm[kDecodeWarps * NQB], wl[kDecodeWarps * NQB];
+    using T = KeyTile<BITS, NQB>;
     ChunkRange r;
-    if (!chunk_range(c, r))
+    if (!chunk_range(c, TC, r))
         return;
     const size_t bh = blockIdx.x;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NQ = Hq / c.H;
-    const int NCB = (c.D / (32 / BITS)) / ValTile<BITS, NQB>::WC;
+    uint32_t* kw = reinterpret_cast<uint32_t*>(dsm + L.kw);
+    uint32_t* vw = reinterpret_cast<uint32_t*>(dsm + L.vw);
+    float* p = dsm + L.p;
+    stage_keys<BITS, T::TOK>(c, bh, r.t_begin, r.tq_end, kw, dsm + L.ks, dsm + L.kz);
+    stage_values<BITS>(c, bh, r.t_begin, r.tq_end, vw, dsm + L.vs, dsm + L.vz);
+    cp_async_commit();
+
+    const int D = c.D, NGv = D >> ilog2(c.G), ps = prob_stride(TC);
+    const int q4 = TC / 4;
+    const int a = r.t_begin + warp * q4, b = min(a + q4, r.t_end);  // this warp's tokens
+    const int aq = min(b, r.tq_end);                                // ... quantized below aq
+    const int ra = max(a, r.tq_end);                                // ... residual from ra
+    const int n = r.t_end - r.t_begin, nq = r.tq_end - r.t_begin;
+    // this warp's B fragments and output partial
+    uint2* bbw = reinterpret_cast<uint2*>(L.bb_on_keys ? dsm + L.kw + (size_t)(q4 / (32 / BITS)) * D * warp
+                                                       : dsm + L.bb + L.bb_w * warp);
+    float* pw = L.part_on_vals ? dsm + L.vw + (size_t)q4 * (D / (32 / BITS)) * warp : dsm + L.part + L.part_w * warp;
+    float* const part_all[kDecodeWarps] = {
+        L.part_on_vals ? dsm + L.vw : dsm + L.part,
+        L.part_on_vals ? dsm + L.vw + (size_t)q4 * (D / (32 / BITS)) : dsm + L.part + L.part_w,
+        L.part_on_vals ? dsm + L.vw + (size_t)q4 * (D / (32 / BITS)) * 2 : dsm + L.part + L.part_w * 2,
+        L.part_on_vals ? dsm + L.vw + (size_t)q4 * (D / (32 / BITS)) * 3 : dsm + L.part + L.part_w * 3};
+    const int i0 = (a - r.t_begin) / 2;                      // first pair of this warp
+    const int i1 = min(pv_pairs(n, nq), (a + q4 - r.t_begin) / 2);
+    const int rows = 32 / (D / 32);
+
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = r.h * NQ + pass * NQB;
-        __syncthreads();
-        stage_q<NQB>(q + ((size_t)r.b * Hq + hq0) * c.D, c.D, sm_scale, qs, fac);
-        __syncthreads();
-        auto sink = [&](int h, int t, float s) { p_sm[h * kChunkTokens + t - r.t_begin] = s; };
-        qk_quantized<BITS, NQB>(c, bh, r.t_begin, r.tq_end, qs, fac, sink);
-        qk_residual<NQB>(c, bh, r.tq_end, r.t_end, qs, fac, sink);
+        __syncthreads();  // the previous pass's merge is done
+        stage_q<NQB>(q + ((size_t)r.b * Hq + hq0) * D, D, sm_scale, qs, fac);
+        cp_async_wait_all();
         __syncthreads();
         float m[NQB], l[NQB];
-        chunk_softmax<NQB>(p_sm, r.t_end - r.t_begin, m, l, red);
-        pv_chunk<BITS, NQB>(c, bh, r.t_begin, r.tq_end, r.t_end, p_sm, o_part, z_part);
+#pragma unroll
+        for (int h = 0; h < NQB; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.0f;
+        }
+        if (a < b) {
+            auto sink = [&](int h, int t, float s) { p[h * ps + t - r.t_begin] = s; };
+            if (a < aq)
+                qk_quantized<BITS, NQB>(D, c.G, r.t_begin, r.tq_end, a, aq, T::TOK, kw, dsm + L.ks,
+                                        dsm + L.kz, qs, fac, sink);
+            qk_residual<NQB>(c, bh, ra, rows, b, qs, fac, sink);
+            __syncwarp();
+            warp_softmax<NQB>(p, ps, a - r.t_begin, b - r.t_begin, m, l);
+            pv_weights<NQB>(n, nq, NGv, i0 + lane, i1, 32, i0, p, ps, dsm + L.vs, dsm + L.vz, bbw, q4 / 2,
+                            dsm + L.zw);
+            __syncwarp();
+            const int kq = (a - r.t_begin) / 16, kq_end = a < aq ? (aq - r.t_begin) / 16 : kq;
+            const int kr = (ra - r.tq_end) / 16, kr_end = ra < b ? (b - r.tq_end + 15) / 16 : kr;
+            const int nsp = pv_seg_groups<BITS>(D);
+            for (int sp = 0; sp < nsp; ++sp)
+                pv_unit<BITS, NQB>(c, bh, r.t_begin, r.tq_end, r.t_end, vw, bbw, q4 / 2, i0, sp, kq, kq_end,
+                                   kr, kr_end, 1, pw);
+        }
+        if (lane == 0)
+#pragma unroll
+            for (int h = 0; h < NQB; ++h) {
+                wm[warp * NQB + h] = m[h];
+                wl[warp * NQB + h] = l[h];
+            }
         __syncthreads();
-        const size_t row0 = ((size_t)r.b * Hq + hq0) * nchunks + blockIdx.y;
-        write_partials<NQB>(c.D, c.G, pv_splits(NCB), o_part, z_part, m, l, row0, nchunks, ws_o,
-                            ws_m, ws_l);
+        merge_warps<NQB>(D, c.G, part_all, dsm + L.zw, wm, wl,
+                         ((size_t)r.b * Hq + hq0) * nchunks + blockIdx.y, nchunks, ws_o, ws_m, ws_l);
     }
 }
 
-// out[b][hq][d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M), M = max m_c.
-__global__ void __launch_bounds__(256)
-decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunks,
+// out[b][hq][d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M), M = max m_c
+// over the chunks c that hold tokens of sequence b.  One CTA per (b, hq): the
+// chunk weights go to shared memory, each warp sums a quarter of the chunks
+// with 16-byte loads, and the four warp sums are added in a fixed order.
+constexpr int kCombineThreads = 128;
+
+__global__ void __launch_bounds__(kCombineThreads)
+decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunks, int TC,
                       const float* __restrict__ ws_o, const float* __restrict__ ws_m,
                       const float* __restrict__ ws_l, float* __restrict__ out)
 {
+    extern __shared__ __align__(16) float cmb[];  // e[nchunks], then [4][D] warp sums
+    __shared__ float red[kDecodeWarps];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t bhq = blockIdx.x;
-    const int b = (int)(bhq / Hq);
-    const int n = len[b];
-    const int nv = (n + kChunkTokens - 1) / kChunkTokens;
+    const int n = len[bhq / Hq];
+    const int nv = (n + TC - 1) / TC;
     const float* mrow = ws_m + bhq * nchunks;
     const float* lrow = ws_l + bhq * nchunks;
-    float M = -INFINITY;
-    for (int k = 0; k < nv; ++k)
-        M = fmaxf(M, mrow[k]);
+    float mx = -INFINITY;
+    for (int k = threadIdx.x; k < nv; k += kCombineThreads)
+        mx = fmaxf(mx, mrow[k]);
+    for (int m = 16; m > 0; m >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+    if (lane == 0)
+        red[warp] = mx;
+    __syncthreads();
+    const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    __syncthreads();
     float L = 0.0f;
-    for (int k = 0; k < nv; ++k)
-        L += lrow[k] * expf(mrow[k] - M);
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        float o = 0.0f;
-        for (int k = 0; k < nv; ++k)
-            o = fmaf(ws_o[(bhq * nchunks + k) * D + d], expf(mrow[k] - M), o);
+    for (int k = threadIdx.x; k < nv; k += kCombineThreads) {
+        const float e = expf(mrow[k] - M);
+        cmb[k] = e;
+        L = fmaf(lrow[k], e, L);
+    }
+    for (int m = 16; m > 0; m >>= 1)
+        L += __shfl_xor_sync(0xffffffffu, L, m);
+    if (lane == 0)
+        red[warp] = L;
+    __syncthreads();  // also publishes cmb[0 .. nv)
+    L = (red[0] + red[1]) + (red[2] + red[3]);
+    float* wsum = cmb + ((nchunks + 3) & ~3);
+    const float4* o4 = reinterpret_cast<const float4*>(ws_o + bhq * nchunks * D);
+    for (int d4 = lane; d4 < D / 4; d4 += 32) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int k = warp; k < nv; k += kDecodeWarps) {
+            const float4 o = o4[(size_t)k * (D / 4) + d4];
+            const float e = cmb[k];
+            acc.x = fmaf(o.x, e, acc.x);
+            acc.y = fmaf(o.y, e, acc.y);
+            acc.z = fmaf(o.z, e, acc.z);
+            acc.w = fmaf(o.w, e, acc.w);
+        }
+        reinterpret_cast<float4*>(wsum + warp * D)[d4] = acc;
+    }
+    __syncthreads();
+    for (int d = threadIdx.x; d < D; d += kCombineThreads) {
+        const float o = (wsum[d] + wsum[D + d]) + (wsum[2 * D + d] + wsum[3 * D + d]);
         out[bhq * D + d] = nv > 0 ? o / L : 0.0f;
     }
 }
 
 // ---------------------------------------------------------------- launch ---
 
-int pv_chunk_tokens(int) { return kChunkTokens; }
-int qk_chunk_tokens(int) { return kChunkTokens; }
-int pv_chunks(const kivi_cache& c) { return (c.Tmax + kChunkTokens - 1) / kChunkTokens; }
-
-static cudaError_t combine(const kivi_cache& c, int Hq, int nch, const float* ws_o,
-                           const float* ws_m, const float* ws_l, float* out, cudaStream_t s)
+int chunk_tokens(const kivi_cache& c, int Hq)
 {
-    decode_combine_kernel<<<c.B * Hq, c.D < 256 ? c.D : 256, 0, s>>>(c.len, Hq, c.D, nch, ws_o,
-                                                                     ws_m, ws_l, out);
+    return decode_chunk_tokens(c.D, c.bits_k, c.bits_v, c.G, Hq / c.H);
+}
+int pv_chunks(const kivi_cache& c, int Hq)
+{
+    const int TC = chunk_tokens(c, Hq);
+    return (c.Tmax + TC - 1) / TC;
+}
+
+static cudaError_t combine(const kivi_cache& c, int Hq, const float* ws_o, const float* ws_m,
+                           const float* ws_l, float* out, cudaStream_t s)
+{
+    const int nch = pv_chunks(c, Hq);
+    const size_t smem = (((size_t)nch + 3) / 4 * 4 + (size_t)kDecodeWarps * c.D) * sizeof(float);
+    cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    decode_combine_kernel<<<c.B * Hq, kCombineThreads, smem, s>>>(c.len, Hq, c.D, nch, chunk_tokens(c, Hq),
+                                                                  ws_o, ws_m, ws_l, out);
     return cudaGetLastError();
+}
+
+template <class K>
+static cudaError_t set_smem(K kern, size_t bytes)
+{
+    return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+}
+
+static DecodeLayout cta_layout(const kivi_cache& c, int Hq, bool keys, bool values)
+{
+    const int NQ = Hq / c.H, NQB = heads_per_pass(NQ);
+    return decode_layout(chunk_tokens(c, Hq), c.D, c.bits_k, c.bits_v, c.G, NQB, NQ > NQB, keys, values, 1);
 }
 
 template <int BITS, int NQB>
 static cudaError_t qk_launch(const kivi_cache& c, const uint16_t* q, int Hq, float sm,
                              float* logits, int ldl, cudaStream_t s)
 {
-    const dim3 grid(c.B * c.H, pv_chunks(c));
-    decode_qk_kernel<BITS, NQB><<<grid, kDecodeThreads, 0, s>>>(c, q, Hq, sm, logits, ldl);
+    auto kern = decode_qk_kernel<BITS, NQB>;
+    const DecodeLayout L = cta_layout(c, Hq, true, false);
+    const size_t smem = 4 * L.total;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess)
+        return e;
+    kern<<<dim3(c.B * c.H, pv_chunks(c, Hq)), kDecodeThreads, smem, s>>>(c, q, Hq, sm, logits, ldl,
+                                                                        chunk_tokens(c, Hq), L);
     return cudaGetLastError();
 }
 
@@ -201,7 +373,6 @@ static cudaError_t qk_bits(const kivi_cache& c, const uint16_t* q, int Hq, float
                            float* logits, int ldl, cudaStream_t s)
 {
     switch (heads_per_pass(Hq / c.H)) {
-    case 8: return qk_launch<BITS, 8>(c, q, Hq, sm, logits, ldl, s);
     case 4: return qk_launch<BITS, 4>(c, q, Hq, sm, logits, ldl, s);
     case 2: return qk_launch<BITS, 2>(c, q, Hq, sm, logits, ldl, s);
     default: return qk_launch<BITS, 1>(c, q, Hq, sm, logits, ldl, s);
@@ -222,13 +393,15 @@ template <int BITS, int NQB>
 static cudaError_t pv_launch(const kivi_cache& c, const float* logits, int ldl, int Hq,
                              float* ws_o, float* ws_m, float* ws_l, cudaStream_t s)
 {
-    const size_t smem = pv_smem_bytes(NQB, c.D, c.G);
     auto kern = decode_pv_kernel<BITS, NQB>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const DecodeLayout L = cta_layout(c, Hq, false, true);
+    const size_t smem = 4 * L.total;
+    cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
-    const int nch = pv_chunks(c);
-    kern<<<dim3(c.B * c.H, nch), kDecodeThreads, smem, s>>>(c, logits, ldl, Hq, ws_o, ws_m, ws_l, nch);
+    const int nch = pv_chunks(c, Hq);
+    kern<<<dim3(c.B * c.H, nch), kDecodeThreads, smem, s>>>(c, logits, ldl, Hq, ws_o, ws_m, ws_l, nch,
+                                                           chunk_tokens(c, Hq), L);
     return cudaGetLastError();
 }
 
@@ -237,7 +410,6 @@ static cudaError_t pv_bits(const kivi_cache& c, const float* logits, int ldl, in
                            float* ws_m, float* ws_l, cudaStream_t s)
 {
     switch (heads_per_pass(Hq / c.H)) {
-    case 8: return pv_launch<BITS, 8>(c, logits, ldl, Hq, ws_o, ws_m, ws_l, s);
     case 4: return pv_launch<BITS, 4>(c, logits, ldl, Hq, ws_o, ws_m, ws_l, s);
     case 2: return pv_launch<BITS, 2>(c, logits, ldl, Hq, ws_o, ws_m, ws_l, s);
     default: return pv_launch<BITS, 1>(c, logits, ldl, Hq, ws_o, ws_m, ws_l, s);
@@ -255,20 +427,23 @@ cudaError_t launch_decode_pv(const kivi_cache& c, const float* logits, int ld_lo
     }
     if (e != cudaSuccess)
         return e;
-    return combine(c, Hq, pv_chunks(c), ws_o, ws_m, ws_l, out, s);
+    return combine(c, Hq, ws_o, ws_m, ws_l, out, s);
 }
 
 template <int BITS, int NQB>
 static cudaError_t attn_launch(const kivi_cache& c, const uint16_t* q, int Hq, float sm,
                                float* ws_o, float* ws_m, float* ws_l, cudaStream_t s)
 {
-    const size_t smem = pv_smem_bytes(NQB, c.D, c.G);
     auto kern = decode_attention_kernel<BITS, NQB>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    const int NQ = Hq / c.H;
+    const WarpLayout L = warp_layout(chunk_tokens(c, Hq), c.D, c.bits_k, c.bits_v, c.G, NQB, NQ > NQB);
+    const size_t smem = 4 * L.total;
+    cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)
         return e;
-    const int nch = pv_chunks(c);
-    kern<<<dim3(c.B * c.H, nch), kDecodeThreads, smem, s>>>(c, q, Hq, sm, ws_o, ws_m, ws_l, nch);
+    const int nch = pv_chunks(c, Hq);
+    kern<<<dim3(c.B * c.H, nch), kDecodeThreads, smem, s>>>(c, q, Hq, sm, ws_o, ws_m, ws_l, nch,
+                                                           chunk_tokens(c, Hq), L);
     return cudaGetLastError();
 }
 
@@ -277,7 +452,6 @@ static cudaError_t attn_bits(const kivi_cache& c, const uint16_t* q, int Hq, flo
                              float* ws_o, float* ws_m, float* ws_l, cudaStream_t s)
 {
     switch (heads_per_pass(Hq / c.H)) {
-    case 8: return attn_launch<BITS, 8>(c, q, Hq, sm, ws_o, ws_m, ws_l, s);
     case 4: return attn_launch<BITS, 4>(c, q, Hq, sm, ws_o, ws_m, ws_l, s);
     case 2: return attn_launch<BITS, 2>(c, q, Hq, sm, ws_o, ws_m, ws_l, s);
     default: return attn_launch<BITS, 1>(c, q, Hq, sm, ws_o, ws_m, ws_l, s);
@@ -296,7 +470,7 @@ cudaError_t launch_decode_attention(const kivi_cache& c, const uint16_t* q, int 
     }
     if (e != cudaSuccess)
         return e;
-    return combine(c, Hq, pv_chunks(c), ws_o, ws_m, ws_l, out, s);
+    return combine(c, Hq, ws_o, ws_m, ws_l, out, s);
 }
 
 }  // namespace kivi

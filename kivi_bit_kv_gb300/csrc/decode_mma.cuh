@@ -10,15 +10,26 @@
 // and whose B operand holds the weights w = q s or p s; the second is a plain
 // fp32 dot product per group.
 //
-// A operand.  Packed words run along the output axis (keys: 32/b tokens of one
-// channel; values: 32/b channels of one token), while an A register pairs two
-// values along the contraction axis.  One PRMT moves byte y of two words (two
-// channels of a key word-row, or two tokens of a value word-column) into bytes
-// 0 and 2 of a register; one AND then keeps the code at position m of that
-// byte in both halves.  Each half is the fp16 subnormal c * 2^(b m) * 2^-24,
-// exact for every code (c 2^(b m) <= 255 < 2^10); the factor 2^(24 - b m) is
-// applied to the fp32 accumulator at the end.  No conversion instruction runs
-// per code.
+// Staging.  A CTA owns one KV head and one chunk of TC tokens.  The chunk's
+// packed keys (word-rows and per-channel statistics) and packed values (token
+// rows and per-token statistics) are contiguous in HBM; at launch every thread
+// issues its share of 16-byte cp.async copies of both into shared memory (two
+// commit groups, keys first), so the whole chunk is in flight at once and the
+// tiles read shared memory only.  The 16-byte chunks are placed with an XOR
+// swizzle so that the tile reads are free of bank conflicts.
+//
+// A operand, codes as fp16 subnormals.  A code c at bit position p of a
+// 16-bit half (p + b <= 10) is the fp16 subnormal c 2^(p - 24) once the other
+// bits are cleared: one AND yields two A values, exact for every code, and the
+// factor 2^(24 - p) is applied to the fp32 accumulator afterwards.  No
+// conversion instruction runs per code.
+//   keys: a key word holds 32/b tokens of one channel, while an A register
+//   pairs two channels of one token; one PRMT moves byte y of two channel
+//   words into bytes 0 and 2 of a register, then ANDs pick the positions.
+//   values: a value word holds 32/b channels of one token, an A register pairs
+//   two tokens of one channel; ldmatrix.trans delivers exactly that pairing at
+//   16-bit granularity (half h of tokens 2 tg and 2 tg + 1), so ANDs alone (and
+//   one shift for the top positions) build the operand.
 //
 // B operand.  w is split into two fp16 terms, hi = w with its low 13
 // mantissa bits cleared (exact in fp16) and lo = fp16(w - hi), and both MMAs
@@ -27,13 +38,9 @@
 // for keys q is pre-scaled per head by a power of two so that max |q| < 1
 // (the factor returns exactly in the epilogue).
 //
-// Warp tile.  The 8 lane groups g of a warp (lanes 4g .. 4g+3) own the 16
-// rows of an MMA tile, two rows each; rows g and g+8 of tile j are the code
-// positions 2 pi and 2 pi + 1 (pi = v NT + j) of the word-row (keys) or
-// word-column (values) the lane group loads.  A tile's N = 8 columns are
-// (group, query head) pairs, so one B fragment serves tokens (channels) from
-// several statistic groups and several heads of a grouped-query set; each
-// output reads the column of its own group.
+// Columns.  A tile's N = 8 columns are (statistic group, query head) pairs,
+// so one B fragment serves rows from several groups and several heads of a
+// grouped-query set; each output reads the column of its own group.
 #pragma once
 
 #include <math.h>
@@ -44,20 +51,13 @@ namespace kivi {
 
 constexpr int kDecodeThreads = 128;
 constexpr int kDecodeWarps = kDecodeThreads / 32;
-constexpr int kChunkTokens = 1024;  // tokens per decode CTA (one split-T chunk)
 
 __host__ __device__ constexpr int cmin(int a, int b) { return a < b ? a : b; }
+__host__ __device__ constexpr int cmax(int a, int b) { return a > b ? a : b; }
+__host__ __device__ constexpr int ilog2(int x) { return x <= 1 ? 0 : 1 + ilog2(x >> 1); }
 
-// Query heads processed together per KV head: 8, 4, 2 or 1.
-__host__ __device__ constexpr int heads_per_pass(int NQ)
-{
-    return NQ % 8 == 0 ? 8 : NQ % 4 == 0 ? 4 : NQ % 2 == 0 ? 2 : 1;
-}
-
-// fp32 q row in shared memory: channel d at qpad(d) (4 floats of padding per
-// 16 channels spread the LDS.128 of the four lanes of a lane group over banks).
-__host__ __device__ constexpr int qstride_of(int D) { return D + D / 4; }
-__device__ __forceinline__ int qpad(int d) { return d + ((d >> 4) << 2); }
+// Query heads processed together per KV head: 4, 2 or 1.
+__host__ __device__ constexpr int heads_per_pass(int NQ) { return NQ % 4 == 0 ? 4 : NQ % 2 == 0 ? 2 : 1; }
 
 // D += A * B, m16n8k16, fp16 operands, fp32 accumulate.
 __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2,
@@ -69,20 +69,32 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], uint32_t a0, uint32_t a1,
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// PRMT selector: byte y of the first word to byte 0, byte y of the second to
-// byte 2 (bytes 1 and 3 are don't-care; the AND clears them).
-__host__ __device__ constexpr uint32_t pair_sel(int y) { return (uint32_t)y | ((uint32_t)(4 + y) << 8); }
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
-template <int BITS>
-__device__ __forceinline__ uint32_t code_pair(uint32_t w0, uint32_t w1, uint32_t sel, int m)
+// Four 8x8 b16 matrices, transposed: lanes 8i .. 8i+7 give the row addresses
+// of matrix i; r[i] of lane (g, tg) holds rows 2 tg and 2 tg + 1 of column g.
+__device__ __forceinline__ void ldsm_x4_t(uint32_t (&r)[4], uint32_t addr)
 {
-    const uint32_t hm = ((1u << BITS) - 1u) << (BITS * m);
-    return __byte_perm(w0, w1, sel) & (hm | (hm << 16));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t (&r)[4], uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(addr));
 }
 
-// fp32 factor that undoes the 2^(b m - 24) of a code at byte position m.
+// Two-bit ... eight-bit code field at position p of both 16-bit halves.
 template <int BITS>
-__host__ __device__ constexpr float code_unscale(int m) { return (float)(1u << (24 - BITS * m)); }
+__host__ __device__ constexpr uint32_t half_pair_mask(int p)
+{
+    return (((1u << BITS) - 1u) << p) | ((((1u << BITS) - 1u) << p) << 16);
+}
+
+// fp32 factor that undoes the 2^(p - 24) of a code at bit position p of a half.
+__host__ __device__ constexpr float code_unscale_bits(int p) { return (float)(1u << (24 - p)); }
 
 // w = hi + lo as two fp16 pairs (see the B operand note above).
 __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint32_t& lo)
@@ -93,31 +105,320 @@ __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint
     lo = h2_bits(__floats2half2_rn(__fsub_rn(a, ah), __fsub_rn(b, bh)));
 }
 
-// Positions of the rows of tile j for sub-lane v (see the warp-tile note).
-template <int BITS, int NT>
-struct TileRows {
-    static constexpr int CPB = 8 / BITS;  // codes per byte
-    // byte and in-byte position of rows g (a) and g + 8 (b) of tile j, v = 0
-    __host__ __device__ static constexpr int ya(int j) { return (2 * j) / CPB; }
-    __host__ __device__ static constexpr int yb(int j) { return (2 * j + 1) / CPB; }
-    __host__ __device__ static constexpr int ma(int j) { return (2 * j) % CPB; }
-    __host__ __device__ static constexpr int mb(int j) { return (2 * j + 1) % CPB; }
-    // selector offset of sub-lane v: its positions start at 2 v NT, a whole
-    // number of bytes (2 NT is a multiple of CPB for every shape used)
-    __device__ static uint32_t sel_offset(int v) { return (uint32_t)(2 * v * NT / CPB) * 0x101u; }
-    static_assert((2 * NT) % CPB == 0, "sub-lane positions must start on a byte");
-};
+// -------------------------------------------------------------- shapes ---
 
-// ------------------------------------------------------------------ keys ---
-
+// Keys: the 8 lane groups g of a warp take WR word-rows (LPW = 8 / WR lane
+// groups per word-row, sub-lane v = g / WR); rows g and g + 8 of MMA tile j
+// are code positions 2 pi and 2 pi + 1, pi = v NT + j, of the lane group's
+// word-row; TOK tokens per warp tile.
 template <int BITS, int NQB>
 struct KeyTile {
     static constexpr int P = 32 / BITS;
+    static constexpr int CPB = 8 / BITS;                    // codes per byte
     static constexpr int WR = cmin(8, (8 / NQB) * 32 / P);  // word-rows per warp tile
-    static constexpr int LPW = 8 / WR;                      // lane groups per word-row
     static constexpr int TOK = WR * P;                      // tokens per warp tile
     static constexpr int NT = TOK / 16;                     // MMA tiles per warp tile
+    // byte / bit position of rows g (a) and g + 8 (b) of tile j for v = 0
+    __host__ __device__ static constexpr int ya(int j) { return (2 * j) / CPB; }
+    __host__ __device__ static constexpr int yb(int j) { return (2 * j + 1) / CPB; }
+    __host__ __device__ static constexpr int pa(int j) { return BITS * ((2 * j) % CPB); }
+    __host__ __device__ static constexpr int pb(int j) { return BITS * ((2 * j + 1) % CPB); }
+    static_assert((2 * NT) % CPB == 0, "sub-lane positions must start on a byte");
 };
+
+// Values: a 16-byte segment of a token row holds 8 halves of HC codes; the
+// lane group g owns half g, and tile j its positions 2j (row g) and 2j + 1
+// (row g + 8).  Positions whose field would reach the fp16 exponent are read
+// after one right shift by SHIFT bits.
+template <int BITS>
+struct ValTile {
+    static constexpr int P = 32 / BITS;
+    static constexpr int HC = 16 / BITS;                    // codes per 16-bit half
+    static constexpr int CS = 8 * HC;                       // channels per segment
+    static constexpr int NT = HC / 2;                       // MMA tiles per segment
+    static constexpr int NDIRECT = BITS == 2 ? 5 : HC / 2;  // positions read unshifted
+    static constexpr int SHIFT = NDIRECT * BITS;
+    __host__ __device__ static constexpr bool shifted(int m) { return m >= NDIRECT; }
+    __host__ __device__ static constexpr int bitpos(int m) { return BITS * (shifted(m) ? m - NDIRECT : m); }
+};
+
+// ------------------------------------------------------- shared memory ---
+
+// Staged keys: word-rows [TC/P][D] then scales and zeros [TC/G][D] (words).
+__host__ __device__ constexpr size_t key_stage_words(int TC, int D, int bits_k, int G)
+{
+    return (size_t)(TC / (32 / bits_k)) * D + 2 * (size_t)(TC / G) * D;
+}
+// Staged values: token rows [TC][D/P] then scales and zeros [TC][D/G].
+__host__ __device__ constexpr size_t val_stage_words(int TC, int D, int bits_v, int G)
+{
+    return (size_t)TC * (D / (32 / bits_v)) + 2 * (size_t)TC * (D / G);
+}
+// Probability rows [NQB][TC + 8] (the pad spreads heads over banks).
+__host__ __device__ constexpr int prob_stride(int TC) { return TC + 8; }
+// B fragments of p . V: [(D/G) NQB rows][TC/2] uint2 (hi pair, lo pair of
+// tokens 2i, 2i+1), pair i of row r stored at i ^ bb_swz(r).
+__host__ __device__ constexpr int bb_stride(int TC) { return TC / 2; }
+__host__ __device__ constexpr int bb_swz(int r) { return (r & 3) << 2; }
+__host__ __device__ constexpr size_t bb_words(int TC, int D, int G, int NQB)
+{
+    return 2 * (size_t)(D / G) * NQB * bb_stride(TC);
+}
+// Split partials [4][NQB][D]; per-warp zero terms [4][NQB][D/G].
+__host__ __device__ constexpr size_t part_words(int D, int NQB) { return (size_t)kDecodeWarps * NQB * D; }
+__host__ __device__ constexpr size_t zs_words(int D, int G, int NQB) { return (size_t)kDecodeWarps * NQB * (D / G); }
+
+// Word offsets into a decode kernel's dynamic shared memory.  `buffers` item
+// buffers (two for the persistent attention kernel, which fills one while it
+// computes from the other), each with the staged keys and / or values and the
+// fp16 q rows, then the probabilities, the B fragments and split partials
+// when they do not overlay a dead region of the buffer in use, and the zero
+// terms.
+struct DecodeLayout {
+    size_t kw, ks, kz, vw, vs, vz, q16;  // within a buffer
+    size_t buf;                          // words per buffer
+    size_t p, bb, part, zs, total;       // bb / part: absolute, or within the buffer if overlaid
+    bool bb_on_keys, part_on_vstats;
+};
+
+// keys / values: whether the kernel stages them.  The B fragments overlay the
+// staged keys (dead once the logits exist), the split partials the value
+// statistics (dead once the B fragments exist) when one pass covers all query
+// heads of the staged chunk.
+__host__ __device__ inline DecodeLayout decode_layout(int TC, int D, int bits_k, int bits_v, int G,
+                                                      int NQB, bool multipass, bool keys, bool values,
+                                                      int buffers)
+{
+    DecodeLayout L{};
+    size_t o = 0;
+    if (keys) {
+        const size_t kwn = (size_t)(TC / (32 / bits_k)) * D, ksn = (size_t)(TC / G) * D;
+        L.kw = o;
+        L.ks = o + kwn;
+        L.kz = L.ks + ksn;
+        o = L.kz + ksn;
+    }
+    size_t vsn = 0;
+    if (values) {
+        const size_t vwn = (size_t)TC * (D / (32 / bits_v));
+        vsn = (size_t)TC * (D / G);
+        L.vw = o;
+        L.vs = o + vwn;
+        L.vz = L.vs + vsn;
+        o = L.vz + vsn;
+    }
+    if (buffers > 1) {  // q rows travel with the item
+        L.q16 = o;
+        o += ((size_t)NQB * D / 2 + 3) & ~(size_t)3;
+    }
+    L.buf = o;
+    o *= buffers;
+    if (values) {
+        L.p = o;
+        o += (size_t)NQB * prob_stride(TC);
+        const size_t bbn = bb_words(TC, D, G, NQB);
+        L.bb_on_keys = keys && bbn <= key_stage_words(TC, D, bits_k, G);
+        if (L.bb_on_keys) {
+            L.bb = L.kw;
+        } else {
+            L.bb = o;
+            o += bbn;
+        }
+        L.part_on_vstats = !multipass && part_words(D, NQB) <= 2 * vsn;
+        if (L.part_on_vstats) {
+            L.part = L.vs;
+        } else {
+            L.part = o;
+            o += part_words(D, NQB);
+        }
+        L.zs = o;
+        o += zs_words(D, G, NQB);
+    }
+    L.total = o;
+    return L;
+}
+
+// Shared memory of the fused attention kernel, where each warp owns a
+// quarter of the chunk: staged keys and values, probabilities [NQB][TC + 8],
+// per-warp zero terms [4][NQB][D/G], and per warp its B fragments
+// ([(D/G) NQB][TC/8] uint2) and output partial ([NQB][D]).  A warp's B
+// fragments overlay its own key word-rows (dead once its logits exist) and
+// its partial its own value rows (dead after its last ldmatrix) when they fit
+// and one pass covers all query heads; otherwise they get regions of their own.
+struct WarpLayout {
+    size_t kw, ks, kz, vw, vs, vz, p, zw;
+    size_t bb, part;       // base of the per-warp regions (when not overlaid)
+    size_t bb_w, part_w;   // words per warp region
+    bool bb_on_keys, part_on_vals;
+    size_t total;
+};
+
+__host__ __device__ inline WarpLayout warp_layout(int TC, int D, int bits_k, int bits_v, int G, int NQB,
+                                                  bool multipass)
+{
+    WarpLayout L{};
+    const int Pk = 32 / bits_k, Pv = 32 / bits_v, NGv = D / G, q4 = TC / 4;
+    size_t o = 0;
+    L.kw = o;
+    L.ks = L.kw + (size_t)(TC / Pk) * D;
+    L.kz = L.ks + (size_t)(TC / G) * D;
+    L.vw = L.kz + (size_t)(TC / G) * D;
+    L.vs = L.vw + (size_t)TC * (D / Pv);
+    L.vz = L.vs + (size_t)TC * NGv;
+    o = L.vz + (size_t)TC * NGv;
+    L.p = o;
+    o += (size_t)NQB * prob_stride(TC);
+    L.zw = o;
+    o += zs_words(D, G, NQB);
+    L.bb_w = 2 * (size_t)NGv * NQB * (q4 / 2);
+    L.part_w = (size_t)NQB * D;
+    const int nsp = D / Pv / 4 >= 2 ? D / Pv / 8 : 1;  // segment groups of the value rows
+    L.bb_on_keys = !multipass && L.bb_w <= (size_t)(q4 / Pk) * D;
+    L.part_on_vals = !multipass && nsp == 1 && L.part_w <= (size_t)q4 * (D / Pv);
+    if (!L.bb_on_keys) {
+        L.bb = o;
+        o += kDecodeWarps * L.bb_w;
+    }
+    if (!L.part_on_vals) {
+        L.part = o;
+        o += kDecodeWarps * L.part_w;
+    }
+    L.total = o;
+    return L;
+}
+
+// Tokens per decode chunk: the largest of 1024 ... 64 that is a multiple of
+// G, whose quarter holds a whole key warp tile, and whose fused-kernel layout
+// fits three CTAs per SM (else two, else one); ctas_per_sm receives that count.
+__host__ __device__ inline int decode_chunk_tokens(int D, int bits_k, int bits_v, int G, int NQ,
+                                                   int* ctas_per_sm = nullptr)
+{
+    const int NQB = heads_per_pass(NQ);
+    const int P = 32 / bits_k;
+    const int tok = cmin(8, (8 / NQB) * 32 / P) * P;
+    const int tc_min = cmax(cmax(4 * tok, G), 64);
+    const size_t budgets[3] = {74 * 1024, 110 * 1024, 220 * 1024};
+    for (int bi = NQB >= 4 ? 1 : 0; bi < 3; ++bi)
+        for (int TC = 1024; TC >= tc_min; TC >>= 1)
+            if (4 * warp_layout(TC, D, bits_k, bits_v, G, NQB, NQ > NQB).total <= budgets[bi]) {
+                if (ctas_per_sm)
+                    *ctas_per_sm = 3 - bi;
+                return TC;
+            }
+    if (ctas_per_sm)
+        *ctas_per_sm = 1;
+    return tc_min;
+}
+
+// ------------------------------------------------------------- staging ---
+
+// Physical 16-byte chunk of logical chunk x in key row r (word-row or
+// statistics group row).  qk_quantized's lanes 0-7 read chunks 4 tg + i
+// (tg = 0..3) of two consecutive rows; the XOR spreads those eight chunks
+// over the eight 16-byte bank groups.  It changes bits 0-1 only, so a chunk
+// stays in its row.
+__device__ __forceinline__ int key_swz(int r, int x) { return x ^ (((x >> 3) & 1) | ((r & 1) << 1)); }
+
+// Physical segment of segment s in value row t, for NSEG segments per row:
+// ldmatrix reads one segment of 8 consecutive rows per phase; the XOR puts
+// those 8 x 16 bytes into distinct bank groups.
+__device__ __forceinline__ int val_swz(int t, int s, int NSEG)
+{
+    const int sh = NSEG >= 8 ? 0 : ilog2(8 / NSEG);
+    const int msk = (NSEG >= 8 ? 8 : NSEG) - 1;
+    return s ^ ((t >> sh) & msk);
+}
+
+// cp.async copies of the chunk's quantized keys [t_begin, tq_end) into kw /
+// ks / kz (key_swz layout); rows from tq_end up to the next multiple of TOK
+// tokens are zero-filled so that whole warp tiles can be read unguarded.  A
+// thread's 16-byte chunks are kDecodeThreads apart, i.e. a fixed column of
+// every (kDecodeThreads / chunks-per-row)-th row, so its swizzled column is
+// fixed (the row step is even) and the loops only advance pointers.
+template <int BITS, int TOK>
+__device__ __forceinline__ void stage_keys(const kivi_cache& c, size_t bh, int t_begin, int tq_end,
+                                           uint32_t* kw, float* ks, float* kz)
+{
+    constexpr int P = 32 / BITS;
+    const int D = c.D, lgG = ilog2(c.G);
+    const int lg = ilog2(D / 4);                    // 16-byte chunks per row: D / 4
+    const int step = kDecodeThreads >> lg;          // rows per sweep (even)
+    const int x = threadIdx.x & (D / 4 - 1), r0 = threadIdx.x >> lg;
+    const int xs = key_swz(r0, x);
+    const int n = tq_end - t_begin, npad = (n + TOK - 1) / TOK * TOK;
+    const size_t adv = (size_t)step * D;            // words per sweep
+    {
+        const int nw = n / P, nwp = npad / P;
+        const int32_t* src = c.kq + (bh * (size_t)(c.Tmax / P) + t_begin / P) * D + (size_t)r0 * D + 4 * x;
+        uint32_t* dst = kw + (size_t)r0 * D + 4 * xs;
+        int r = r0;
+        for (; r < nw; r += step, src += adv, dst += adv)
+            cp_async16(dst, src);
+        for (; r < nwp; r += step, dst += adv)
+            *reinterpret_cast<uint4*>(dst) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    {
+        const int ng = n >> lgG, ngp = (npad + c.G - 1) >> lgG;
+        const size_t so = (bh * (size_t)(c.Tmax >> lgG) + (t_begin >> lgG)) * D + (size_t)r0 * D + 4 * x;
+        const float* s1 = c.kscale + so;
+        const float* s2 = c.kzero + so;
+        const size_t d0 = (size_t)r0 * D + 4 * xs;
+        float* d1 = ks + d0;
+        float* d2 = kz + d0;
+        int r = r0;
+        for (; r < ng; r += step, s1 += adv, s2 += adv, d1 += adv, d2 += adv) {
+            cp_async16(d1, s1);
+            cp_async16(d2, s2);
+        }
+        for (; r < ngp; r += step, d1 += adv, d2 += adv) {
+            *reinterpret_cast<float4*>(d1) = make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<float4*>(d2) = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+    }
+}
+
+// cp.async copies of the chunk's quantized values [t_begin, tq_end): token
+// rows into vw (val_swz layout), statistics into vs / vz [t - t_begin][D/G].
+// As for the keys, a thread's segment (and its swizzled place) is fixed.
+template <int BITS>
+__device__ __forceinline__ void stage_values(const kivi_cache& c, size_t bh, int t_begin, int tq_end,
+                                             uint32_t* vw, float* vs, float* vz)
+{
+    constexpr int P = 32 / BITS;
+    const int D = c.D, DW = D / P, NSEG = DW / 4, NGv = D >> ilog2(c.G);
+    const int lg = ilog2(NSEG);
+    const int n = tq_end - t_begin;
+    const int seg = threadIdx.x & (NSEG - 1), t0 = threadIdx.x >> lg;
+    const int step = kDecodeThreads >> lg;          // tokens per sweep (a multiple of 8)
+    const size_t adv = (size_t)kDecodeThreads * 4;  // words per sweep
+    {
+        const int32_t* src = c.vq + (bh * (size_t)c.Tmax + t_begin) * DW + (size_t)threadIdx.x * 4;
+        uint32_t* dst = vw + (size_t)t0 * DW + val_swz(t0, seg, NSEG) * 4;
+        for (int t = t0; t < n; t += step, src += adv, dst += adv)
+            cp_async16(dst, src);
+    }
+    {
+        const int nf = (n * NGv) / 4;  // n is a multiple of 32
+        const size_t so = (bh * (size_t)c.Tmax + t_begin) * NGv + (size_t)threadIdx.x * 4;
+        const float* s1 = c.vscale + so;
+        const float* s2 = c.vzero + so;
+        float* d1 = vs + threadIdx.x * 4;
+        float* d2 = vz + threadIdx.x * 4;
+        for (int i = threadIdx.x; i < nf; i += kDecodeThreads, s1 += adv, s2 += adv, d1 += adv, d2 += adv) {
+            cp_async16(d1, s1);
+            cp_async16(d2, s2);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ keys ---
+
+// fp32 q row in shared memory: channel d at qpad(d) (4 floats of padding per
+// 16 channels spread the LDS.128 of the four lanes of a lane group over banks)
+// and rows D + D/4 (+16) floats apart, 16 (mod 32), so that two heads read by
+// one quarter-warp use the other half of the banks.
+__host__ __device__ constexpr int qstride_of(int D) { return D + D / 4 + ((D + D / 4) % 32 == 0 ? 16 : 0); }
+__device__ __forceinline__ int qpad(int d) { return d + ((d >> 4) << 2); }
 
 // Stages query heads hq0 .. hq0+NQB-1 of sequence b: qs[h][qpad(d)] = q 2^-e_h
 // with 2^-e_h the power of two that brings max_d |q| into [1/2, 1), and
@@ -148,66 +449,69 @@ __device__ __forceinline__ void stage_q(const uint16_t* __restrict__ q, int D, f
     }
 }
 
-// Logits of the quantized tokens [t_begin, tq_end) of KV head bh for NQB
-// query heads; sink(h, t, s) receives each one.  t_begin and tq_end are
-// multiples of G (tq_end may also be a chunk end, a multiple of 1024).
+// Logits of quantized tokens for NQB query heads from the staged keys of the
+// chunk starting at t_begin (zero-filled up to a whole warp tile); the calling
+// warp takes the warp tiles that start at tok_first, tok_first + tok_step, ...
+// below tok_end (<= tq_end, the end of the quantized tokens); sink(h, t, s)
+// receives each logit.
 template <int BITS, int NQB, class Sink>
-__device__ __forceinline__ void qk_quantized(const kivi_cache& c, size_t bh, int t_begin, int tq_end,
-                                             const float* qs, const float* fac, Sink sink)
+__device__ __forceinline__ void qk_quantized(int D, int G, int t_begin, int tq_end, int tok_first,
+                                             int tok_end, int tok_step, const uint32_t* kw,
+                                             const float* ks, const float* kz, const float* qs,
+                                             const float* fac, Sink sink)
 {
     using T = KeyTile<BITS, NQB>;
-    using Rows = TileRows<BITS, T::NT>;
-    const int D = c.D, G = c.G;
     const int qstride = qstride_of(D);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int cpr = D / 4;  // 16-byte chunks per staged row
+    const int lgG = ilog2(G);
+    const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tg = lane & 3;
     const int wr = g % T::WR, v = g / T::WR;
-    const uint32_t soff = Rows::sel_offset(v);
-    const int NGW = T::TOK / G > 1 ? T::TOK / G : 1;  // statistic groups per warp tile
-    const int gi = g / NQB, hq = g % NQB;              // B column of this lane group
-    const float* qrow = qs + hq * qstride;
-    const int gi_row = (wr * T::P) / G;                // group of this lane group's rows
+    const uint32_t soff = (uint32_t)(2 * v * T::NT / T::CPB) * 0x101u;  // byte offset of sub-lane v
+    const int NGW = cmax(1, T::TOK >> lgG);         // statistic groups per warp tile
+    const int gi = cmin(g / NQB, NGW - 1);          // B column group (clamped; extra columns unused)
+    const int hq = g % NQB;
+    const float* qrow = qs + hq * qstride + qpad(tg * 16);
+    const int gi_row = (wr * T::P) >> lgG;          // group of this lane group's rows
 
-    for (int tok0 = t_begin + warp * T::TOK; tok0 < tq_end; tok0 += kDecodeWarps * T::TOK) {
+    for (int tok0 = tok_first; tok0 < tok_end; tok0 += tok_step) {
         float acc[T::NT][4];
 #pragma unroll
         for (int j = 0; j < T::NT; ++j)
             acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
         float zacc = 0.0f;
-        const int grp = tok0 / G + gi;
-        const bool col_ok = gi < NGW && grp * G < tq_end;
-        const bool row_ok = tok0 + wr * T::P < tq_end;
-        const int32_t* kw = c.kq + (bh * (size_t)(c.Tmax / T::P) + tok0 / T::P + wr) * D + tg * 16;
-        const size_t so = (bh * (size_t)(c.Tmax / G) + grp) * D + tg * 16;
+        const int lr = (tok0 - t_begin) / T::P + wr;    // staged word-row
+        const int lgp = ((tok0 - t_begin) >> lgG) + gi; // staged group row of the B column
+        const int xr = (tg >> 1) | ((lr & 1) << 1);     // key_swz of this lane's chunks
+        const int xg = (tg >> 1) | ((lgp & 1) << 1);
+        const uint4* wrow = reinterpret_cast<const uint4*>(kw) + lr * cpr + 4 * tg;
+        const float4* srow = reinterpret_cast<const float4*>(ks) + lgp * cpr + 4 * tg;
+        const float4* zrow = reinterpret_cast<const float4*>(kz) + lgp * cpr + 4 * tg;
 
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 64) {
-            uint4 W[4];
-            float4 S[4], Z[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                W[i] = row_ok ? ld_nc(kw + c0 + 4 * i) : make_uint4(0u, 0u, 0u, 0u);
-                S[i] = col_ok ? ld_nc_f4(c.kscale + so + c0 + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-                Z[i] = col_ok ? ld_nc_f4(c.kzero + so + c0 + 4 * i) : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
+        for (int c0 = 0; c0 < cpr; c0 += 16) {
 #pragma unroll
             for (int s = 0; s < 4; ++s) {
-                const float4 qv = *reinterpret_cast<const float4*>(qrow + qpad(c0 + tg * 16 + 4 * s));
-                zacc = fmaf(qv.x, Z[s].x, zacc);
-                zacc = fmaf(qv.y, Z[s].y, zacc);
-                zacc = fmaf(qv.z, Z[s].z, zacc);
-                zacc = fmaf(qv.w, Z[s].w, zacc);
+                const uint4 W = wrow[c0 + (s ^ xr)];
+                const float4 S = srow[c0 + (s ^ xg)];
+                const float4 Z = zrow[c0 + (s ^ xg)];
+                const float4 qv = *reinterpret_cast<const float4*>(qrow + 5 * c0 + 4 * s);
+                zacc = fmaf(qv.x, Z.x, zacc);
+                zacc = fmaf(qv.y, Z.y, zacc);
+                zacc = fmaf(qv.z, Z.z, zacc);
+                zacc = fmaf(qv.w, Z.w, zacc);
                 uint32_t bh0, bl0, bh1, bl1;
-                split_hi_lo(qv.x * S[s].x, qv.y * S[s].y, bh0, bl0);
-                split_hi_lo(qv.z * S[s].z, qv.w * S[s].w, bh1, bl1);
+                split_hi_lo(qv.x * S.x, qv.y * S.y, bh0, bl0);
+                split_hi_lo(qv.z * S.z, qv.w * S.w, bh1, bl1);
 #pragma unroll
                 for (int j = 0; j < T::NT; ++j) {
-                    const uint32_t sa = pair_sel(Rows::ya(j)) + soff;
-                    const uint32_t sb = pair_sel(Rows::yb(j)) + soff;
-                    const uint32_t a0 = code_pair<BITS>(W[s].x, W[s].y, sa, Rows::ma(j));
-                    const uint32_t a1 = code_pair<BITS>(W[s].x, W[s].y, sb, Rows::mb(j));
-                    const uint32_t a2 = code_pair<BITS>(W[s].z, W[s].w, sa, Rows::ma(j));
-                    const uint32_t a3 = code_pair<BITS>(W[s].z, W[s].w, sb, Rows::mb(j));
+                    const uint32_t sa = ((uint32_t)T::ya(j) | ((uint32_t)(4 + T::ya(j)) << 8)) + soff;
+                    const uint32_t sb = ((uint32_t)T::yb(j) | ((uint32_t)(4 + T::yb(j)) << 8)) + soff;
+                    const uint32_t ma = half_pair_mask<BITS>(T::pa(j)), mb = half_pair_mask<BITS>(T::pb(j));
+                    const uint32_t a0 = __byte_perm(W.x, W.y, sa) & ma;
+                    const uint32_t a1 = __byte_perm(W.x, W.y, sb) & mb;
+                    const uint32_t a2 = __byte_perm(W.z, W.w, sa) & ma;
+                    const uint32_t a3 = __byte_perm(W.z, W.w, sb) & mb;
                     mma_f16(acc[j], a0, a1, a2, a3, bh0, bh1);
                     mma_f16(acc[j], a0, a1, a2, a3, bl0, bl1);
                 }
@@ -218,7 +522,7 @@ __device__ __forceinline__ void qk_quantized(const kivi_cache& c, size_t bh, int
         zacc += __shfl_xor_sync(0xffffffffu, zacc, 2);
         const float zc[2] = {__shfl_sync(0xffffffffu, zacc, 8 * tg),
                              __shfl_sync(0xffffffffu, zacc, 8 * tg + 4)};
-        if (!row_ok)
+        if (tok0 + wr * T::P >= tq_end)
             continue;
 #pragma unroll
         for (int cc = 0; cc < 2; ++cc) {
@@ -230,26 +534,26 @@ __device__ __forceinline__ void qk_quantized(const kivi_cache& c, size_t bh, int
             const int tbase = tok0 + wr * T::P + 2 * v * T::NT;
 #pragma unroll
             for (int j = 0; j < T::NT; ++j) {
-                sink(h, tbase + 2 * j, f * fmaf(code_unscale<BITS>(Rows::ma(j)), acc[j][cc], zc[cc]));
-                sink(h, tbase + 2 * j + 1, f * fmaf(code_unscale<BITS>(Rows::mb(j)), acc[j][2 + cc], zc[cc]));
+                sink(h, tbase + 2 * j, f * fmaf(code_unscale_bits(T::pa(j)), acc[j][cc], zc[cc]));
+                sink(h, tbase + 2 * j + 1, f * fmaf(code_unscale_bits(T::pb(j)), acc[j][2 + cc], zc[cc]));
             }
         }
     }
 }
 
-// Logits of the fp16 residual tokens [t0, t_end): D/32 lanes per token, each
-// a 32-channel segment, fp32 FMA.
+// Logits of fp16 residual tokens (read from the ring in global memory): D/32
+// lanes per token, each a 32-channel segment, fp32 FMA; the calling warp
+// takes 32 / (D/32) tokens from base0, then every `step` tokens, below t_end.
 template <int NQB, class Sink>
-__device__ __forceinline__ void qk_residual(const kivi_cache& c, size_t bh, int t0, int t_end,
+__device__ __forceinline__ void qk_residual(const kivi_cache& c, size_t bh, int base0, int step, int t_end,
                                             const float* qs, const float* fac, Sink sink)
 {
     const int D = c.D, RG = c.R + c.G;
     const int qstride = qstride_of(D);
     const int LPR = D / 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int seg = lane % LPR;
-    const int rows = 32 / LPR;
-    for (int base = t0 + warp * rows; base < t_end; base += kDecodeWarps * rows) {
+    for (int base = base0; base < t_end; base += step) {
         const int t = base + lane / LPR;
         float acc[NQB];
 #pragma unroll
@@ -286,200 +590,23 @@ __device__ __forceinline__ void qk_residual(const kivi_cache& c, size_t bh, int 
 
 // ---------------------------------------------------------------- values ---
 
-template <int BITS, int NQB>
-struct ValTile {
-    static constexpr int P = 32 / BITS;
-    static constexpr int WC = cmin(BITS == 2 ? 4 : 8, (8 / NQB) * 32 / P);  // word-columns per block
-    static constexpr int LPW = 8 / WC;   // lane groups per word-column
-    static constexpr int CH = WC * P;    // channels per block
-    static constexpr int NT = CH / 16;   // MMA tiles per block
-};
-
-// Shared-memory floats the p . V phase needs beyond p: per split, NQB x D
-// partial outputs and NQB x (D / G) zero terms.
-__host__ __device__ constexpr int pv_part_floats(int NQB, int D, int G)
-{
-    return kDecodeWarps * NQB * (D + D / G);
-}
-
-// Splits of the token range across the warps for a block count NCB.
-__device__ __forceinline__ int pv_splits(int NCB) { return NCB >= kDecodeWarps ? 1 : kDecodeWarps / NCB; }
-
-// p . V_hat over tokens [t_begin, t_end) of KV head bh for NQB query heads:
-// p_sm[h][t - t_begin] holds the unnormalized probabilities.  Quantized
-// tokens [t_begin, tq_end) go through the code MMA, residual tokens
-// [tq_end, t_end) (from the fp16 ring) through the same tiles with the raw
-// values as A and p as B.  Writes o_part[split][h][d] (without zero terms)
-// and z_part[split][h][g]; each entry is written by exactly one lane, so the
-// CTA's sum over splits is deterministic.
-template <int BITS, int NQB>
-__device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int t_begin, int tq_end,
-                                         int t_end, const float* p_sm, float* o_part, float* z_part)
-{
-    using T = ValTile<BITS, NQB>;
-    using Rows = TileRows<BITS, T::NT>;
-    const int D = c.D, G = c.G, NGv = D / G, RG = c.R + c.G;
-    const int DW = D / T::P;       // words per token row
-    const int NCB = DW / T::WC;    // channel blocks
-    const int NSPLIT = pv_splits(NCB);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int g = lane >> 2, tg = lane & 3;
-    const int wcl = g % T::WC, v = g / T::WC;
-    const uint32_t soff = Rows::sel_offset(v);
-    const int NGW = T::CH / G > 1 ? T::CH / G : 1;
-    const int gi = g / NQB, hq = g % NQB;
-    const bool col_ok = gi < NGW;
-    const float* prow = p_sm + hq * kChunkTokens;  // p of token t at prow[t - t_begin]
-    const int nq_slices = (tq_end - t_begin) / 16;          // quantized part: whole slices
-    const int nr_slices = (t_end - tq_end + 15) / 16;       // residual part: last one ragged
-
-    for (int unit = warp; unit < NCB * NSPLIT; unit += kDecodeWarps) {
-        const int cb = unit % NCB, split = unit / NCB;
-        const int grp0 = (cb * T::CH) / G;
-        const int grp = grp0 + gi;
-        float acc[T::NT][4];
-#pragma unroll
-        for (int j = 0; j < T::NT; ++j)
-            acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
-        float zacc = 0.0f;
-        const int32_t* vw = c.vq + bh * (size_t)c.Tmax * DW + cb * T::WC + wcl;
-        const float* vs = c.vscale + bh * (size_t)c.Tmax * NGv + grp;
-        const float* vz = c.vzero + bh * (size_t)c.Tmax * NGv + grp;
-
-        constexpr int UNR = 4;
-#pragma unroll 1
-        for (int k0 = split; k0 < nq_slices; k0 += NSPLIT * UNR) {
-            uint32_t W[UNR][4];
-            float S[UNR][4], Z[UNR][4];
-#pragma unroll
-            for (int u = 0; u < UNR; ++u) {
-                const bool ok = k0 + u * NSPLIT < nq_slices;
-                const size_t t = (size_t)t_begin + (k0 + u * NSPLIT) * 16 + 4 * tg;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    W[u][i] = ok ? (uint32_t)__ldg(vw + (t + i) * DW) : 0u;
-                    S[u][i] = ok && col_ok ? __ldg(vs + (t + i) * NGv) : 0.0f;
-                    Z[u][i] = ok && col_ok ? __ldg(vz + (t + i) * NGv) : 0.0f;
-                }
-            }
-#pragma unroll
-            for (int u = 0; u < UNR; ++u) {
-                const int k = k0 + u * NSPLIT;
-                if (k >= nq_slices)
-                    break;
-                const float4 pv = *reinterpret_cast<const float4*>(prow + k * 16 + 4 * tg);
-                zacc = fmaf(pv.x, Z[u][0], zacc);
-                zacc = fmaf(pv.y, Z[u][1], zacc);
-                zacc = fmaf(pv.z, Z[u][2], zacc);
-                zacc = fmaf(pv.w, Z[u][3], zacc);
-                uint32_t bh0, bl0, bh1, bl1;
-                split_hi_lo(pv.x * S[u][0], pv.y * S[u][1], bh0, bl0);
-                split_hi_lo(pv.z * S[u][2], pv.w * S[u][3], bh1, bl1);
-#pragma unroll
-                for (int j = 0; j < T::NT; ++j) {
-                    const uint32_t sa = pair_sel(Rows::ya(j)) + soff;
-                    const uint32_t sb = pair_sel(Rows::yb(j)) + soff;
-                    const uint32_t a0 = code_pair<BITS>(W[u][0], W[u][1], sa, Rows::ma(j));
-                    const uint32_t a1 = code_pair<BITS>(W[u][0], W[u][1], sb, Rows::mb(j));
-                    const uint32_t a2 = code_pair<BITS>(W[u][2], W[u][3], sa, Rows::ma(j));
-                    const uint32_t a3 = code_pair<BITS>(W[u][2], W[u][3], sb, Rows::mb(j));
-                    mma_f16(acc[j], a0, a1, a2, a3, bh0, bh1);
-                    mma_f16(acc[j], a0, a1, a2, a3, bl0, bl1);
-                }
-            }
-        }
-        // undo the code scaling before the residual tokens join the sums
-#pragma unroll
-        for (int j = 0; j < T::NT; ++j) {
-            acc[j][0] *= code_unscale<BITS>(Rows::ma(j));
-            acc[j][1] *= code_unscale<BITS>(Rows::ma(j));
-            acc[j][2] *= code_unscale<BITS>(Rows::mb(j));
-            acc[j][3] *= code_unscale<BITS>(Rows::mb(j));
-        }
-        // residual tokens: A = (v[t][d], v[t+1][d]) pairs, B = p (hi / lo)
-        // the lane's 2 NT channels ch0 .. ch0 + 2 NT - 1 are contiguous: one
-        // 16-byte (NT = 4) or 8-byte (NT = 2) load per residual token
-        static_assert(T::NT == 2 || T::NT == 4, "value tiles per block");
-        const int ch0 = (cb * T::WC + wcl) * T::P + 2 * v * T::NT;
-#pragma unroll 1
-        for (int k = split; k < nr_slices; k += NSPLIT) {
-            const int tb = tq_end + k * 16 + 4 * tg;
-            uint32_t X[4][T::NT];
-            float pr[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = tb + i;
-                const bool ok = t < t_end;
-                pr[i] = ok && col_ok ? prow[t - t_begin] : 0.0f;
-                const uint16_t* vr = c.vres + (bh * RG + (ok ? t : 0) % RG) * D + ch0;
-                if constexpr (T::NT == 4) {
-                    const uint4 x = ok ? ld_nc(vr) : make_uint4(0u, 0u, 0u, 0u);
-                    X[i][0] = x.x;
-                    X[i][1] = x.y;
-                    X[i][2] = x.z;
-                    X[i][3] = x.w;
-                } else {
-                    const uint2 x = ok ? __ldg(reinterpret_cast<const uint2*>(vr)) : make_uint2(0u, 0u);
-                    X[i][0] = x.x;
-                    X[i][1] = x.y;
-                }
-            }
-            uint32_t bh0, bl0, bh1, bl1;
-            split_hi_lo(pr[0], pr[1], bh0, bl0);
-            split_hi_lo(pr[2], pr[3], bh1, bl1);
-#pragma unroll
-            for (int j = 0; j < T::NT; ++j) {
-                const uint32_t a0 = __byte_perm(X[0][j], X[1][j], 0x5410);
-                const uint32_t a1 = __byte_perm(X[0][j], X[1][j], 0x7632);
-                const uint32_t a2 = __byte_perm(X[2][j], X[3][j], 0x5410);
-                const uint32_t a3 = __byte_perm(X[2][j], X[3][j], 0x7632);
-                mma_f16(acc[j], a0, a1, a2, a3, bh0, bh1);
-                mma_f16(acc[j], a0, a1, a2, a3, bl0, bl1);
-            }
-        }
-
-        zacc += __shfl_xor_sync(0xffffffffu, zacc, 1);
-        zacc += __shfl_xor_sync(0xffffffffu, zacc, 2);
-        float* op = o_part + (size_t)split * NQB * D;
-        float* zp = z_part + (size_t)split * NQB * NGv;
-        if (tg == 0 && col_ok)
-            zp[hq * NGv + grp] = zacc;
-#pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int u = 2 * tg + cc;
-            const int ugi = u / NQB, uh = u % NQB;
-            if (ugi >= NGW)
-                continue;
-#pragma unroll
-            for (int j = 0; j < T::NT; ++j) {
-                const int cha = ch0 + 2 * j;
-                if (grp0 + ugi != cha / G)
-                    continue;
-                op[uh * D + cha] = acc[j][cc];
-                op[uh * D + cha + 1] = acc[j][2 + cc];
-            }
-        }
-    }
-}
-
-// Chunk softmax statistics over p_sm[h][0 .. n) (holding logits on entry):
-// m_h = max, p = exp(s - m_h) in place, l_h = sum p.  Whole CTA.
+// Chunk softmax over p_sm[h][0 .. n) (row stride ps; logits on entry):
+// m_h = max, p = exp(s - m_h) in place, l_h = sum p.  Whole CTA; ends with a
+// barrier that publishes p_sm.
 template <int NQB>
-__device__ __forceinline__ void chunk_softmax(float* p_sm, int n, float (&m)[NQB], float (&l)[NQB],
-                                              float* red)
+__device__ __forceinline__ void chunk_softmax(float* p_sm, int ps, int n, float (&m)[NQB],
+                                              float (&l)[NQB], float* red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int h = 0; h < NQB; ++h) {
         float mx = -INFINITY;
         for (int t = threadIdx.x; t < n; t += kDecodeThreads)
-            mx = fmaxf(mx, p_sm[h * kChunkTokens + t]);
+            mx = fmaxf(mx, p_sm[h * ps + t]);
+        for (int k = 16; k > 0; k >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
         m[h] = mx;
     }
-#pragma unroll
-    for (int h = 0; h < NQB; ++h)
-        for (int k = 16; k > 0; k >>= 1)
-            m[h] = fmaxf(m[h], __shfl_xor_sync(0xffffffffu, m[h], k));
     if (lane == 0)
 #pragma unroll
         for (int h = 0; h < NQB; ++h)
@@ -498,21 +625,19 @@ __device__ __forceinline__ void chunk_softmax(float* p_sm, int n, float (&m)[NQB
     for (int h = 0; h < NQB; ++h) {
         float s = 0.0f;
         for (int t = threadIdx.x; t < n; t += kDecodeThreads) {
-            const float e = expf(p_sm[h * kChunkTokens + t] - m[h]);
-            p_sm[h * kChunkTokens + t] = e;
+            const float e = expf(p_sm[h * ps + t] - m[h]);
+            p_sm[h * ps + t] = e;
             s += e;
         }
+        for (int k = 16; k > 0; k >>= 1)
+            s += __shfl_xor_sync(0xffffffffu, s, k);
         l[h] = s;
     }
-#pragma unroll
-    for (int h = 0; h < NQB; ++h)
-        for (int k = 16; k > 0; k >>= 1)
-            l[h] += __shfl_xor_sync(0xffffffffu, l[h], k);
     if (lane == 0)
 #pragma unroll
         for (int h = 0; h < NQB; ++h)
             red[warp * NQB + h] = l[h];
-    __syncthreads();  // also publishes p_sm
+    __syncthreads();
 #pragma unroll
     for (int h = 0; h < NQB; ++h) {
         float r = red[h];
@@ -523,21 +648,358 @@ __device__ __forceinline__ void chunk_softmax(float* p_sm, int n, float (&m)[NQB
     }
 }
 
+// B fragments of p . V for the chunk: bb row r = g NQB + h, pair i (stored at
+// i ^ bb_swz(r)) holds the (hi, lo) fp16 pairs of tokens 2i, 2i+1 of
+// w = p_ht s_tg for quantized tokens (t < nq) and of w = p_ht for residual
+// tokens (nq <= t < n), zero up to the end of the last 16-token slice.
+// zw[warp][h][g] = the warp's share of sum over quantized t of p_ht z_tg.
+// One thread per token pair; whole CTA, the caller's barrier publishes both.
+template <int NQB, int NGV>
+__device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_end, int i_step, int i_base,
+                                             const float* p_sm, int ps, const float* vs,
+                                             const float* vz, uint2* bb, int bbs, float* zw)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float z[NQB][NGV];
+#pragma unroll
+    for (int h = 0; h < NQB; ++h)
+#pragma unroll
+        for (int gg = 0; gg < NGV; ++gg)
+            z[h][gg] = 0.0f;
+    for (int i = i_first; i < i_end; i += i_step) {
+        const int t = 2 * i;
+        float s0[NGV], s1[NGV];
+        const bool quant = t < nq;  // nq is even: t + 1 is quantized too
+        if (quant) {
+            float z0[NGV], z1[NGV];
+#pragma unroll
+            for (int gg = 0; gg < NGV; ++gg) {
+                s0[gg] = vs[t * NGV + gg];
+                s1[gg] = vs[(t + 1) * NGV + gg];
+                z0[gg] = vz[t * NGV + gg];
+                z1[gg] = vz[(t + 1) * NGV + gg];
+            }
+#pragma unroll
+            for (int h = 0; h < NQB; ++h) {
+                const float2 pp = *reinterpret_cast<const float2*>(p_sm + h * ps + t);
+#pragma unroll
+                for (int gg = 0; gg < NGV; ++gg)
+                    z[h][gg] = fmaf(pp.x, z0[gg], fmaf(pp.y, z1[gg], z[h][gg]));
+            }
+        } else {
+#pragma unroll
+            for (int gg = 0; gg < NGV; ++gg)
+                s0[gg] = s1[gg] = 1.0f;
+        }
+#pragma unroll
+        for (int h = 0; h < NQB; ++h) {
+            const float p0 = t < n ? p_sm[h * ps + t] : 0.0f;
+            const float p1 = t + 1 < n ? p_sm[h * ps + t + 1] : 0.0f;
+#pragma unroll
+            for (int gg = 0; gg < NGV; ++gg) {
+                const int r = gg * NQB + h;
+                uint2 hl;
+                split_hi_lo(p0 * s0[gg], p1 * s1[gg], hl.x, hl.y);
+                bb[r * bbs + ((i - i_base) ^ bb_swz(r))] = hl;
+            }
+        }
+    }
+#pragma unroll
+    for (int h = 0; h < NQB; ++h)
+#pragma unroll
+        for (int gg = 0; gg < NGV; ++gg) {
+            float v = z[h][gg];
+            for (int k = 16; k > 0; k >>= 1)
+                v += __shfl_xor_sync(0xffffffffu, v, k);
+            if (lane == 0)
+                zw[(warp * NQB + h) * NGV + gg] = v;
+        }
+}
+
+// Pairs i_first, i_first + i_step, ... below i_end; bb holds pairs from
+// i_base on (i_base = 0 for a whole-chunk array, the warp's first pair for a
+// warp-private one).  Pairs past the last token (up to the end of the last
+// 16-token slice) get zero weights.
+template <int NQB>
+__device__ __forceinline__ void pv_weights(int n, int nq, int NGv, int i_first, int i_end, int i_step,
+                                           int i_base, const float* p_sm, int ps, const float* vs,
+                                           const float* vz, uint2* bb, int bbs, float* zw)
+{
+    switch (NGv) {
+    case 1: pv_weights_g<NQB, 1>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, vs, vz, bb, bbs, zw); break;
+    case 2: pv_weights_g<NQB, 2>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, vs, vz, bb, bbs, zw); break;
+    case 4: pv_weights_g<NQB, 4>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, vs, vz, bb, bbs, zw); break;
+    default: pv_weights_g<NQB, 8>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, vs, vz, bb, bbs, zw); break;
+    }
+}
+// Pairs a chunk of n tokens (nq quantized) needs: through the last residual slice.
+__host__ __device__ constexpr int pv_pairs(int n, int nq) { return (nq + ((n - nq + 15) & ~15)) / 2; }
+
+// Splits of the token range across the warps for NSP segment groups.
+__host__ __device__ constexpr int pv_splits(int NSP) { return NSP >= kDecodeWarps ? 1 : kDecodeWarps / NSP; }
+template <int BITS>
+__host__ __device__ constexpr int pv_segs_per_load(int D) { return D / (32 / BITS) / 4 >= 2 ? 2 : 1; }
+template <int BITS>
+__host__ __device__ constexpr int pv_seg_groups(int D) { return D / (32 / BITS) / 4 / pv_segs_per_load<BITS>(D); }
+
+// p . V_hat for NQB query heads and the channels of segment group sp (SPL
+// segments of 8 halves each) with the staged values of the chunk at t_begin
+// (vw, val_swz layout) and B fragments of pv_weights (pair i of the chunk at
+// bb pair i - i_base).  Quantized 16-token slices k = kq, kq + kstep, ...
+// below kq_end through ldmatrix.trans; residual slices kr, kr + kstep, ...
+// below kr_end (tokens tq_end + 16 kr ...) from the fp16 ring with the raw
+// values as A.  Writes o_out[h][d] (no zero terms) for the segment group's
+// channels, each entry by exactly one lane.
+template <int BITS, int NQB>
+__device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_begin, int tq_end,
+                                        int t_end, const uint32_t* vw, const uint2* bb, int bbs,
+                                        int i_base, int sp, int kq, int kq_end, int kr, int kr_end,
+                                        int kstep, float* o_out)
+{
+    using T = ValTile<BITS>;
+    const int D = c.D, G = c.G, lgG = ilog2(G), RG = c.R + c.G;
+    const int DW = D / T::P, NSEG = DW / 4;
+    const int SPL = pv_segs_per_load<BITS>(D);  // segments per ldmatrix (x4: 2, x2: 1)
+    const int NGS = cmax(1, T::CS >> lgG);      // groups per segment
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tg = lane & 3;
+    const int gl = cmin(g / NQB, NGS - 1), hq = g % NQB;  // B column (clamped; extras unused)
+    // ldmatrix row of this lane: matrix mi = lane / 8 = 2 s + (token half)
+    const int mi = lane >> 3, lrow = (lane & 7) + 8 * (mi & 1), lseg = SPL == 2 ? mi >> 1 : 0;
+    const int seg0 = sp * SPL;
+    float acc[2][T::NT][4];
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int j = 0; j < T::NT; ++j)
+            acc[s][j][0] = acc[s][j][1] = acc[s][j][2] = acc[s][j][3] = 0.0f;
+    const uint2* bp[2];
+    int bx[2];  // bb_swz of the lane's row
+    int grp_first[2];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        grp_first[s] = ((seg0 + s) * T::CS) >> lgG;
+        const int r = (grp_first[s] + gl) * NQB + hq;
+        bp[s] = bb + (size_t)r * bbs;
+        bx[s] = bb_swz(r);
+    }
+    // swizzled address of this lane's ldmatrix row (val_swz depends on the
+    // row within its 8-token group only)
+    const uint32_t a0 = smem_addr(vw + (size_t)lrow * DW + val_swz(lrow, seg0 + lseg, NSEG) * 4);
+    const uint32_t astep = 16u * DW * 4u;  // one 16-token slice
+
+#pragma unroll 1
+    for (int k = kq; k < kq_end; k += kstep) {
+        uint32_t R[4];
+        if (SPL == 2)
+            ldsm_x4_t(R, a0 + k * astep);
+        else
+            ldsm_x2_t(R, a0 + k * astep);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            if (s >= SPL)
+                break;
+            const uint2 b01 = bp[s][(k * 8 + tg - i_base) ^ bx[s]];
+            const uint2 b23 = bp[s][(k * 8 + 4 + tg - i_base) ^ bx[s]];
+            const uint32_t Rl = R[2 * s], Rh = R[2 * s + 1];
+            const uint32_t Rls = Rl >> T::SHIFT, Rhs = Rh >> T::SHIFT;
+#pragma unroll
+            for (int j = 0; j < T::NT; ++j) {
+                const int m0 = 2 * j, m1 = 2 * j + 1;
+                const uint32_t mk0 = half_pair_mask<BITS>(T::bitpos(m0));
+                const uint32_t mk1 = half_pair_mask<BITS>(T::bitpos(m1));
+                const uint32_t x0 = (T::shifted(m0) ? Rls : Rl) & mk0;
+                const uint32_t x1 = (T::shifted(m1) ? Rls : Rl) & mk1;
+                const uint32_t x2 = (T::shifted(m0) ? Rhs : Rh) & mk0;
+                const uint32_t x3 = (T::shifted(m1) ? Rhs : Rh) & mk1;
+                mma_f16(acc[s][j], x0, x1, x2, x3, b01.x, b23.x);
+                mma_f16(acc[s][j], x0, x1, x2, x3, b01.y, b23.y);
+            }
+        }
+    }
+    // undo the code scaling before the residual tokens join the sums
+#pragma unroll
+    for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int j = 0; j < T::NT; ++j) {
+            const float f0 = code_unscale_bits(T::bitpos(2 * j)), f1 = code_unscale_bits(T::bitpos(2 * j + 1));
+            acc[s][j][0] *= f0;
+            acc[s][j][1] *= f0;
+            acc[s][j][2] *= f1;
+            acc[s][j][3] *= f1;
+        }
+    // residual tokens: A = (v[t][d], v[t+1][d]) pairs, B = p (hi / lo).
+    // The lane's HC channels of a segment are contiguous: one 16 / 8 /
+    // 4-byte load per token and segment.
+    const int nq2 = (tq_end - t_begin) / 2;  // pair index of the first residual token
+#pragma unroll 1
+    for (int k = kr; k < kr_end; k += kstep) {
+        const int tb = tq_end + k * 16 + 2 * tg;
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+            if (s >= SPL)
+                break;
+            const int ch0 = (seg0 + s) * T::CS + g * T::HC;
+            uint32_t X[4][T::NT];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int t = tb + (i & 1) + 8 * (i >> 1);
+                const bool ok = t < t_end;
+                const uint16_t* vr = c.vres + (bh * RG + (ok ? t : 0) % RG) * D + ch0;
+                if constexpr (T::NT == 4) {
+                    const uint4 x = ok ? ld_nc(vr) : make_uint4(0u, 0u, 0u, 0u);
+                    X[i][0] = x.x;
+                    X[i][1] = x.y;
+                    X[i][2] = x.z;
+                    X[i][3] = x.w;
+                } else if constexpr (T::NT == 2) {
+                    const uint2 x = ok ? __ldg(reinterpret_cast<const uint2*>(vr)) : make_uint2(0u, 0u);
+                    X[i][0] = x.x;
+                    X[i][1] = x.y;
+                } else {
+                    X[i][0] = ok ? __ldg(reinterpret_cast<const uint32_t*>(vr)) : 0u;
+                }
+            }
+            const uint2 b01 = bp[s][(nq2 + k * 8 + tg - i_base) ^ bx[s]];
+            const uint2 b23 = bp[s][(nq2 + k * 8 + 4 + tg - i_base) ^ bx[s]];
+#pragma unroll
+            for (int j = 0; j < T::NT; ++j) {
+                const uint32_t x0 = __byte_perm(X[0][j], X[1][j], 0x5410);
+                const uint32_t x1 = __byte_perm(X[0][j], X[1][j], 0x7632);
+                const uint32_t x2 = __byte_perm(X[2][j], X[3][j], 0x5410);
+                const uint32_t x3 = __byte_perm(X[2][j], X[3][j], 0x7632);
+                mma_f16(acc[s][j], x0, x1, x2, x3, b01.x, b23.x);
+                mma_f16(acc[s][j], x0, x1, x2, x3, b01.y, b23.y);
+            }
+        }
+    }
+
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+        if (s >= SPL)
+            break;
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int u = 2 * tg + cc;
+            const int ugl = u / NQB, uh = u % NQB;
+            if (ugl >= NGS)
+                continue;
+            const int ch0 = (seg0 + s) * T::CS + g * T::HC;
+            if (grp_first[s] + ugl != (ch0 >> lgG))
+                continue;
+#pragma unroll
+            for (int j = 0; j < T::NT; ++j) {
+                o_out[uh * D + ch0 + 2 * j] = acc[s][j][cc];
+                o_out[uh * D + ch0 + 2 * j + 1] = acc[s][j][2 + cc];
+            }
+        }
+    }
+}
+
+// p . V_hat of the whole chunk by the CTA: each warp takes units (segment
+// group, token split) and writes o_part[split] (splits of one segment group
+// are different warps).
+template <int BITS, int NQB>
+__device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TC, int t_begin,
+                                         int tq_end, int t_end, const uint32_t* vw, const uint2* bb,
+                                         float* o_part)
+{
+    const int NSP = pv_seg_groups<BITS>(c.D);
+    const int NSPLIT = pv_splits(NSP);
+    const int nq_slices = (tq_end - t_begin) / 16;
+    const int nr_slices = (t_end - tq_end + 15) / 16;
+    for (int unit = threadIdx.x >> 5; unit < NSP * NSPLIT; unit += kDecodeWarps) {
+        const int sp = unit % NSP, split = unit / NSP;
+        pv_unit<BITS, NQB>(c, bh, t_begin, tq_end, t_end, vw, bb, bb_stride(TC), 0, sp, split, nq_slices,
+                           split, nr_slices, NSPLIT, o_part + (size_t)split * NQB * c.D);
+    }
+}
+
+// Softmax statistics of one warp's tokens p_sm[h][lo .. hi) (row stride ps;
+// logits on entry): m_h = max, p = exp(s - m_h) in place, l_h = sum p.  The
+// whole warp takes part; an empty range gives m = -inf, l = 0.
+template <int NQB>
+__device__ __forceinline__ void warp_softmax(float* p_sm, int ps, int lo, int hi, float (&m)[NQB],
+                                             float (&l)[NQB])
+{
+    const int lane = threadIdx.x & 31;
+#pragma unroll
+    for (int h = 0; h < NQB; ++h) {
+        float* row = p_sm + h * ps;
+        float mx = -INFINITY;
+        for (int t = lo + lane; t < hi; t += 32)
+            mx = fmaxf(mx, row[t]);
+        for (int k = 16; k > 0; k >>= 1)
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
+        __syncwarp();
+        float sum = 0.0f;
+        for (int t = lo + lane; t < hi; t += 32) {
+            const float e = expf(row[t] - mx);
+            row[t] = e;
+            sum += e;
+        }
+        for (int k = 16; k > 0; k >>= 1)
+            sum += __shfl_xor_sync(0xffffffffu, sum, k);
+        m[h] = mx;
+        l[h] = sum;
+    }
+    __syncwarp();
+}
+
+// Merges the per-warp partials of a chunk (each relative to its warp's own
+// maximum wm[w][h]; wl[w][h] = 0 for a warp without tokens) into the chunk's
+// (o, m, l): M = max_w wm, o[h][d] = sum_w e^(wm - M) (o_w[h][d] + z_w[h][g(d)]),
+// l = sum_w e^(wm - M) wl.  Whole CTA, after a barrier; fixed order.
+template <int NQB>
+__device__ __forceinline__ void merge_warps(int D, int G, float* const (&o_w)[kDecodeWarps],
+                                            const float* zw, const float* wm, const float* wl,
+                                            size_t row0, int nchunks, float* ws_o, float* ws_m,
+                                            float* ws_l)
+{
+    const int lgD = ilog2(D), lgG = ilog2(G), NGv = D >> lgG;
+    for (int idx = threadIdx.x; idx < NQB * D; idx += kDecodeThreads) {
+        const int h = idx >> lgD, d = idx & (D - 1);
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kDecodeWarps; ++w)
+            if (wl[w * NQB + h] > 0.0f)
+                M = fmaxf(M, wm[w * NQB + h]);
+        float o = 0.0f, L = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kDecodeWarps; ++w)
+            if (wl[w * NQB + h] > 0.0f) {
+                const float e = expf(wm[w * NQB + h] - M);
+                o = fmaf(e, o_w[w][idx] + zw[(w * NQB + h) * NGv + (d >> lgG)], o);
+                L = fmaf(e, wl[w * NQB + h], L);
+            }
+        ws_o[(row0 + (size_t)h * nchunks) * D + d] = o;
+        if (d == 0) {
+            ws_m[row0 + (size_t)h * nchunks] = M;
+            ws_l[row0 + (size_t)h * nchunks] = L;
+        }
+    }
+}
+
 // Writes the chunk's partial (o, m, l) for query heads hq0 .. hq0+NQB-1:
-// o[h][d] = sum over splits of o_part + z_part of d's group.  Whole CTA,
-// after a barrier that follows pv_chunk.
+// o[h][d] = sum over warps of zs[w][h][group of d] + sum over splits of
+// o_part (a fixed order: the result is deterministic).  Whole CTA, after
+// a barrier that follows pv_chunk.
 template <int NQB>
 __device__ __forceinline__ void write_partials(int D, int G, int nsplit, const float* o_part,
-                                               const float* z_part, const float (&m)[NQB],
+                                               const float* zs, const float (&m)[NQB],
                                                const float (&l)[NQB], size_t row0, int nchunks,
                                                float* ws_o, float* ws_m, float* ws_l)
 {
-    const int NGv = D / G;
+    const int lgD = ilog2(D), lgG = ilog2(G), NGv = D >> lgG;
     for (int idx = threadIdx.x; idx < NQB * D; idx += kDecodeThreads) {
-        const int h = idx / D, d = idx % D;
-        float s = 0.0f;
+        const int h = idx >> lgD, d = idx & (D - 1);
+        const int zi = h * NGv + (d >> lgG);
+        float s = zs[zi];
+#pragma unroll
+        for (int w = 1; w < kDecodeWarps; ++w)
+            s += zs[w * NQB * NGv + zi];
         for (int sp = 0; sp < nsplit; ++sp)
-            s += o_part[((size_t)sp * NQB + h) * D + d] + z_part[((size_t)sp * NQB + h) * NGv + d / G];
+            s += o_part[(size_t)sp * NQB * D + idx];
         ws_o[(row0 + (size_t)h * nchunks) * D + d] = s;
     }
 #pragma unroll

@@ -12,10 +12,10 @@ namespace kivi {
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
-// Tokens per decode_qk CTA and per decode_pv chunk for head dim D.
-int qk_chunk_tokens(int D);
-int pv_chunk_tokens(int D);
-int pv_chunks(const kivi_cache& c);
+// Tokens per decode chunk (one CTA per KV head and chunk) and the number of
+// chunks that cover Tmax.
+int chunk_tokens(const kivi_cache& c, int Hq);
+int pv_chunks(const kivi_cache& c, int Hq);
 
 cudaError_t launch_quant_keys(const kivi_cache& c, const uint16_t* K, int T,
                               const int32_t* seq_lens, cudaStream_t s);

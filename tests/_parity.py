@@ -122,12 +122,9 @@ def row_rel_err(gpu: np.ndarray, ref: np.ndarray) -> float:
 
 def compare_attention(lg, out, ref_lg, ref_out, lens, heads=None, rtol=ATTN_RTOL, fused=None):
     """Per-row relative error of logits and outputs; rows of empty sequences
-    must be exactly zero.  The fused kernel runs the same tile arithmetic with
-    the logits kept on chip, so its output must equal the two-kernel output
-    bit for bit.  Returns the worst (logit, output) errors."""
-    if fused is not None:
-        assert np.array_equal(fused, out), (
-            f"fused output differs from the two-kernel path at {np.argwhere(fused != out)[:5].tolist()}")
+    must be exactly zero.  The fused kernel's output (which merges per-warp
+    softmax partials, a different rounding order) is held to the same bound
+    against the oracle.  Returns the worst (logit, output) errors."""
     worst_l = worst_o = 0.0
     B, Hq = out.shape[:2]
     for b in range(B):
@@ -135,10 +132,15 @@ def compare_attention(lg, out, ref_lg, ref_out, lens, heads=None, rtol=ATTN_RTOL
         for h in range(Hq) if heads is None else heads:
             if n == 0:
                 assert (out[b, h] == 0).all()
+                assert fused is None or (fused[b, h] == 0).all()
                 continue
             el = row_rel_err(lg[b, h, :n], ref_lg[b, h, :n])
             eo = row_rel_err(out[b, h], ref_out[b, h])
             assert el <= rtol, f"logits b={b} hq={h}: rel err {el:.3g}"
             assert eo <= rtol, f"out b={b} hq={h}: rel err {eo:.3g}"
+            if fused is not None:
+                ef = row_rel_err(fused[b, h], ref_out[b, h])
+                assert ef <= rtol, f"fused out b={b} hq={h}: rel err {ef:.3g}"
+                eo = max(eo, ef)
             worst_l, worst_o = max(worst_l, el), max(worst_o, eo)
     return worst_l, worst_o
