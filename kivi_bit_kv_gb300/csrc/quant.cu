@@ -11,6 +11,8 @@
 // and written once as a b-bit code; statistics add 8 bytes per group column.
 // Grids are 2-D -- x over token tiles, y over (b, h) slices -- so all index
 // arithmetic is 32-bit shifts and masks.
+#include <algorithm>
+
 #include "kivi_device.cuh"
 #include "kivi_launch.h"
 
@@ -63,6 +65,210 @@ quant_keys_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
             }
         }
     }
+}
+
+// Keys, staged.  A persistent CTA of 128 threads walks token tiles of
+// 128 * 128 / D tokens (32 KB of fp16 K): while it encodes one tile from
+// shared memory, the cp.async copies of its next tile fill the other buffer,
+// so the loads stay in flight without holding registers.  Lane layout and
+// arithmetic are those of quant_keys_kernel (16 tokens x 8 channels per
+// lane, the G/16 lanes of a group column adjacent).  In shared memory the
+// 16-byte chunk x of row r sits at x ^ (s * 8/S), s = (r mod G) / 16, so that
+// the eight lanes of an LDS.128 phase read eight different bank groups.
+constexpr int kKeyStageThreads = 128;
+constexpr int kKeyStageBytes = 32 * 1024;
+
+__device__ __forceinline__ int key_stage_swz(int r, int x, int lgS)
+{
+    return x ^ (((r >> 4) & ((1 << lgS) - 1)) << (3 - lgS));
+}
+
+// Encode one key lane (16 tokens x 8 channels) whose rows are staged in
+// shared memory at lrow[i * stride], i = 0..15: statistics as in
+// quant_key_lane, then the codes in short unrolled runs of four tokens, each
+// word-row stored (after its near-tie fix-up) as soon as it is complete.
+template <int BITS>
+__device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, size_t bh, int t0, int g,
+                                                          int j, int s, int S, unsigned smask,
+                                                          const uint4* lrow, int stride)
+{
+    using Cd = Codec<BITS>;
+    const int D = c.D;
+    __half2 mn[4], mx[4];
+    {
+        const uint4 r0 = lrow[0];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            mn[k] = mx[k] = as_h2(u4_word(r0, k));
+    }
+#pragma unroll 5
+    for (int i = 1; i < kLaneTokens; ++i) {
+        const uint4 r = lrow[i * stride];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const __half2 v = as_h2(u4_word(r, k));
+            mn[k] = __hmin2(mn[k], v);
+            mx[k] = __hmax2(mx[k], v);
+        }
+    }
+    for (int m = 1; m < S; m <<= 1)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            mn[k] = __hmin2(mn[k], as_h2(__shfl_xor_sync(smask, h2_bits(mn[k]), m)));
+            mx[k] = __hmax2(mx[k], as_h2(__shfl_xor_sync(smask, h2_bits(mx[k]), m)));
+        }
+    float scale[8], zero[8], inv[8], nzero[8];
+    const int s_lane = (int)(threadIdx.x & 31) & (S - 1);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float lo = (k & 1) ? __high2float(mn[k >> 1]) : __low2float(mn[k >> 1]);
+        const float hi = (k & 1) ? __high2float(mx[k >> 1]) : __low2float(mx[k >> 1]);
+        zero[k] = __fadd_rn(lo, 0.0f);
+        nzero[k] = -zero[k];
+        scale[k] = 0.0f;
+        inv[k] = 0.0f;
+        if ((k & (S - 1)) == s_lane)  // the S lanes of the column split the divisions
+            group_stats<BITS>(lo, hi, scale[k], zero[k], inv[k]);
+    }
+    if (S > 1) {
+        const int base = (int)(threadIdx.x & 31) & ~(S - 1);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int src = base + (k & (S - 1));
+            scale[k] = __shfl_sync(smask, scale[k], src);
+            inv[k] = __shfl_sync(smask, inv[k], src);
+        }
+    }
+    if (s == 0) {
+        const size_t so = (bh * (size_t)(c.Tmax / c.G) + g) * D + (size_t)j * kLaneChans;
+        float4* sp = reinterpret_cast<float4*>(c.kscale + so);
+        float4* zp = reinterpret_cast<float4*>(c.kzero + so);
+        sp[0] = make_float4(scale[0], scale[1], scale[2], scale[3]);
+        sp[1] = make_float4(scale[4], scale[5], scale[6], scale[7]);
+        zp[0] = make_float4(zero[0], zero[1], zero[2], zero[3]);
+        zp[1] = make_float4(zero[4], zero[5], zero[6], zero[7]);
+    }
+    // codes: word = sum_i t_bits_i 2^(b i) - bias * sum_i 2^(b i) (mod 2^32)
+    constexpr uint32_t kWordBias = kCodeBias * (uint32_t)(((1ull << (Cd::P * BITS)) - 1) /
+                                                          ((1ull << BITS) - 1));
+    int32_t* dst = c.kq + (bh * (size_t)(c.Tmax / Cd::P) + t0 / Cd::P) * D + (size_t)j * kLaneChans;
+#pragma unroll 1
+    for (int w = 0; w < Cd::kWordRows; ++w) {
+        uint32_t words[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            words[k] = 0u - kWordBias;
+        unsigned flagged = 0u;
+        uint32_t mul = 1u;
+#pragma unroll 1
+        for (int i0 = 0; i0 < Cd::P; i0 += 4) {
+#pragma unroll
+            for (int ii = 0; ii < 4; ++ii) {
+                const uint4 r = lrow[(w * Cd::P + i0 + ii) * stride];
+                float worst = 0.0f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float a = add_h_f(u4_half(r, k), nzero[k]);
+                    words[k] += fast_code_bits(a, inv[k], worst) * mul;
+                }
+                flagged |= (worst >= kNearTie ? 1u : 0u) << (i0 + ii);
+                mul <<= BITS;
+            }
+        }
+        if (__builtin_expect(flagged != 0u, 0)) {
+#pragma unroll 1
+            while (flagged) {
+                const int i = __ffs(flagged) - 1;
+                flagged &= flagged - 1;
+                const uint4 r = lrow[(w * Cd::P + i) * stride];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const float a = add_h_f(u4_half(r, k), nzero[k]);
+                    float w1 = 0.0f;
+                    const uint32_t fast = fast_code_bits(a, inv[k], w1) - kCodeBias;
+                    if (w1 >= kNearTie)
+                        words[k] += (exact_code(a, scale[k]) - fast) << (i * BITS);
+                }
+            }
+        }
+        st_stream(dst + (size_t)w * D, make_uint4(words[0], words[1], words[2], words[3]));
+        st_stream(dst + (size_t)w * D + 4, make_uint4(words[4], words[5], words[6], words[7]));
+    }
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kKeyStageThreads, 3)
+quant_keys_staged_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
+                         const int32_t* __restrict__ seq_lens, int tiles_per_seq)
+{
+    extern __shared__ __align__(16) uint4 kst[];  // two buffers of kKeyStageBytes
+    const int D = c.D;
+    const int S = c.G / kLaneTokens, lgS = log2_pow2(S);
+    const int NC = D / kLaneChans, lgNC = log2_pow2(NC);
+    const int TT = (kKeyStageBytes / 2) / D;       // tokens per tile
+    const int lane = threadIdx.x & 31;
+    const unsigned smask = (((1u << S) - 1u) << (lane & ~(S - 1)));
+    const int s = threadIdx.x & (S - 1);
+    const int j = (threadIdx.x >> lgS) & (NC - 1);
+    const int gl = threadIdx.x >> (lgS + lgNC);   // group within the tile
+    const int RG = c.R + c.G;
+    const int ntiles = c.B * c.H * tiles_per_seq;
+    const int cpr = NC;                            // 16-byte chunks per row
+    const int rsweep = kKeyStageThreads / cpr;    // rows per copy sweep
+    const int cx = threadIdx.x & (cpr - 1), cr = threadIdx.x / cpr;
+
+    auto tile_of = [&](int tile, int& bh, int& tt0, int& n) {
+        bh = tile / tiles_per_seq;
+        tt0 = (tile - bh * tiles_per_seq) * TT;
+        const int b = bh / c.H;
+        n = seq_lens ? min(max(seq_lens[b], 0), T) : T;
+    };
+    auto prefetch = [&](int tile, int buf) {
+        if (tile < ntiles) {
+            int bh, tt0, n;
+            tile_of(tile, bh, tt0, n);
+            const int rows = min(TT, n - tt0);
+            if (rows > 0) {
+                const uint16_t* src = K + ((size_t)bh * T + tt0) * D + cx * 8;
+                uint4* dst = kst + (size_t)buf * (kKeyStageBytes / 16);
+                for (int r = cr; r < rows; r += rsweep)
+                    cp_async16(dst + r * cpr + key_stage_swz(r, cx, lgS), src + (size_t)r * D);
+            }
+        }
+        cp_async_commit();
+    };
+
+    int tile = blockIdx.x;
+    prefetch(tile, 0);
+    for (int k = 0; tile < ntiles; ++k, tile += gridDim.x) {
+        prefetch(tile + gridDim.x, (k + 1) & 1);
+        cp_async_wait_prior();
+        __syncthreads();
+        int bh, tt0, n;
+        tile_of(tile, bh, tt0, n);
+        if (tt0 == 0 && threadIdx.x == 0 && bh % c.H == 0)
+            c.len[bh / c.H] = n;
+        const int g = tt0 / c.G + gl;
+        const int t0 = g * c.G + s * kLaneTokens;
+        const int lr = gl * c.G + s * kLaneTokens;  // first tile row of this lane
+        if (g * c.G < n) {
+            const uint4* buf = kst + (size_t)(k & 1) * (kKeyStageBytes / 16);
+            const int Tq = quantized_tokens(n, c.G, c.R);
+            // the lane's 16 rows share one swizzled column (r / 16 is fixed)
+            const uint4* lrow = buf + lr * cpr + key_stage_swz(lr, j, lgS);
+            if ((g + 1) * c.G <= Tq) {
+                quant_store_key_lane_smem<BITS>(c, bh, t0, g, j, s, S, smask, lrow, cpr);
+            } else {
+                for (int i = 0; i < kLaneTokens; ++i) {
+                    const int t = t0 + i;
+                    if (t >= Tq && t < n)
+                        st_stream(c.kres + ((size_t)bh * RG + t % RG) * D + j * kLaneChans, lrow[i * cpr]);
+                }
+            }
+        }
+        __syncthreads();  // the buffer is refilled by the next iteration's prefetch
+    }
+    cp_async_wait_all();
 }
 
 // Values.  One lane = one channel group (G channels) of U token rows, so
@@ -130,8 +336,29 @@ static dim3 encode_grid(const kivi_cache& c, int tiles)
 cudaError_t launch_quant_keys(const kivi_cache& c, const uint16_t* K, int T,
                               const int32_t* seq_lens, cudaStream_t s)
 {
-    if (T > 0) {
-        const int groups_per_cta = kEncodeThreads / ((c.G / kLaneTokens) * (c.D / kLaneChans));
+    const int lanes_per_group = (c.G / kLaneTokens) * (c.D / kLaneChans);
+    if (T > 0 && lanes_per_group <= kKeyStageThreads) {
+        const int TT = (kKeyStageBytes / 2) / c.D;
+        const int tiles_per_seq = (T + TT - 1) / TT;
+        const long ntiles = (long)c.B * c.H * tiles_per_seq;
+        const int grid = (int)std::min<long>(ntiles, (long)sm_count() * 3);
+        const size_t smem = 2 * kKeyStageBytes;
+        switch (c.bits_k) {
+        case 2:
+            cudaFuncSetAttribute(quant_keys_staged_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            quant_keys_staged_kernel<2><<<grid, kKeyStageThreads, smem, s>>>(c, K, T, seq_lens, tiles_per_seq);
+            break;
+        case 4:
+            cudaFuncSetAttribute(quant_keys_staged_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            quant_keys_staged_kernel<4><<<grid, kKeyStageThreads, smem, s>>>(c, K, T, seq_lens, tiles_per_seq);
+            break;
+        default:
+            cudaFuncSetAttribute(quant_keys_staged_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            quant_keys_staged_kernel<8><<<grid, kKeyStageThreads, smem, s>>>(c, K, T, seq_lens, tiles_per_seq);
+            break;
+        }
+    } else if (T > 0) {
+        const int groups_per_cta = kEncodeThreads / lanes_per_group;
         const int groups = (T + c.G - 1) / c.G;
         const dim3 grid = encode_grid(c, (groups + groups_per_cta - 1) / groups_per_cta);
         switch (c.bits_k) {
