@@ -81,7 +81,12 @@ dequant_keys_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
 }
 
 // Values: one lane = one channel group (G channels) of U token rows: the
-// group's words, scale and zero are loaded once and G fp16 values stored.
+// group's words, scale and zero are loaded once and G fp16 values produced.
+// A lane's 16-byte output chunks lie 64 bytes apart (G = 32), so each warp
+// passes its rows through shared memory and stores them back with every
+// instruction writing 512 contiguous bytes.  In shared memory chunk c of warp
+// row r sits at c ^ ((r NG ^ c / (G/8)) & 7), which keeps both the group-wise
+// writes and the row-wise reads free of bank conflicts.
 template <int BITS, int G>
 __global__ void __launch_bounds__(kDequantThreads)
 dequant_values_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
@@ -89,13 +94,22 @@ dequant_values_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
     using Cd = Codec<BITS>;
     constexpr int U = G == 32 ? 4 : G == 64 ? 2 : 1;
     constexpr int NW = G * BITS / 32;  // words per group
+    constexpr int NV = G / 8;          // 16-byte chunks per group
+    constexpr int lgNV = G == 32 ? 2 : G == 64 ? 3 : 4;
+    extern __shared__ __align__(16) uint4 dq_rows[];
     const int D = c.D;
     const int NG = D / G, lgNG = lg2(NG);
+    const int CPR = D / 8, lgCPR = lg2(CPR);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int gi = threadIdx.x & (NG - 1);
     const int rows_per_pass = kDequantThreads >> lgNG;
+    const int rows_w = 32 >> lgNG;                      // rows per warp and pass
+    const int wr = lane >> lgNG;                        // this lane's row in the warp
     const int r0 = blockIdx.x * rows_per_pass * U + (threadIdx.x >> lgNG);
     const int RG = c.R + c.G;
     const uint32_t two23 = two23_bits();
+    uint4* wsm = dq_rows + (size_t)warp * rows_w * CPR;
+    auto phys = [&](int r, int ch) { return ch ^ (((r << lgNG) ^ (ch >> lgNV)) & 7); };
 
     for (int bh = blockIdx.y; bh < c.B * c.H; bh += gridDim.y) {
         const int len = c.len[bh / c.H];
@@ -130,30 +144,43 @@ dequant_values_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            const int tw = r0 - (threadIdx.x >> lgNG) + warp * rows_w + u * rows_per_pass;  // warp's first row
+            if (tw >= n)
+                break;  // uniform over the warp
             const int t = r0 + u * rows_per_pass;
-            if (t >= n)
-                continue;
-            uint16_t* dst = out + ((size_t)bh * T_out + t) * D + gi * G;
-            if (t < Tq) {
+            if (t < n) {
+                uint4* dst = wsm + (size_t)wr * CPR;
+                if (t < Tq) {
 #pragma unroll
-                for (int v = 0; v < G / 8; ++v) {
-                    uint32_t h2[4];
+                    for (int v = 0; v < NV; ++v) {
+                        uint32_t h2[4];
 #pragma unroll
-                    for (int k = 0; k < 8; k += 2) {
-                        const int e = v * 8 + k;
-                        h2[k / 2] = dequant_h2(
-                            code_float(words[u][e / Cd::P] >> ((e % Cd::P) * BITS), Cd::M, two23),
-                            code_float(words[u][(e + 1) / Cd::P] >> (((e + 1) % Cd::P) * BITS), Cd::M, two23),
-                            sc[u], zr[u], sc[u], zr[u]);
+                        for (int k = 0; k < 8; k += 2) {
+                            const int e = v * 8 + k;
+                            h2[k / 2] = dequant_h2(
+                                code_float(words[u][e / Cd::P] >> ((e % Cd::P) * BITS), Cd::M, two23),
+                                code_float(words[u][(e + 1) / Cd::P] >> (((e + 1) % Cd::P) * BITS), Cd::M, two23),
+                                sc[u], zr[u], sc[u], zr[u]);
+                        }
+                        dst[phys(wr, gi * NV + v)] = make_uint4(h2[0], h2[1], h2[2], h2[3]);
                     }
-                    st_stream(dst + v * 8, make_uint4(h2[0], h2[1], h2[2], h2[3]));
-                }
-            } else {
-                const uint16_t* rs = c.vres + ((size_t)bh * RG + t % RG) * D + gi * G;
+                } else {
+                    const uint16_t* rs = c.vres + ((size_t)bh * RG + t % RG) * D + gi * G;
 #pragma unroll
-                for (int v = 0; v < G / 8; ++v)
-                    st_stream(dst + v * 8, ld_nc(rs + v * 8));
+                    for (int v = 0; v < NV; ++v)
+                        dst[phys(wr, gi * NV + v)] = ld_nc(rs + v * 8);
+                }
             }
+            __syncwarp();
+            uint16_t* orow = out + ((size_t)bh * T_out + tw) * D;
+#pragma unroll
+            for (int k = 0; k < NV; ++k) {
+                const int q = k * 32 + lane;
+                const int rr = q >> lgCPR, x = q & (CPR - 1);
+                if (tw + rr < n)
+                    st_stream(orow + (size_t)rr * D + x * 8, wsm[(size_t)rr * CPR + phys(rr, x)]);
+            }
+            __syncwarp();
         }
     }
 }
@@ -170,10 +197,16 @@ static void dequant_values_bits(const kivi_cache& c, uint16_t* out, int T_out, c
     const int U = c.G == 32 ? 4 : c.G == 64 ? 2 : 1;
     const int rows_per_cta = kDequantThreads / (c.D / c.G) * U;
     const dim3 grid = dq_grid(c, (T_out + rows_per_cta - 1) / rows_per_cta);
+    // per warp: (32 / (D/G)) rows of D fp16 values
+    const size_t smem = (size_t)(kDequantThreads / 32) * 64 * c.G;
     switch (c.G) {
-    case 32: dequant_values_kernel<BITS, 32><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;
-    case 64: dequant_values_kernel<BITS, 64><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;
-    default: dequant_values_kernel<BITS, 128><<<grid, kDequantThreads, 0, s>>>(c, out, T_out); break;
+    case 32: dequant_values_kernel<BITS, 32><<<grid, kDequantThreads, smem, s>>>(c, out, T_out); break;
+    case 64: dequant_values_kernel<BITS, 64><<<grid, kDequantThreads, smem, s>>>(c, out, T_out); break;
+    default:
+        cudaFuncSetAttribute(dequant_values_kernel<BITS, 128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        dequant_values_kernel<BITS, 128><<<grid, kDequantThreads, smem, s>>>(c, out, T_out);
+        break;
     }
 }
 
