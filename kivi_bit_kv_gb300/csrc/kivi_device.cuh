@@ -120,16 +120,19 @@ static __device__ __noinline__ uint32_t exact_code(float a, float scale)
 
 // Fast code for a = x - zero >= 0, without branches.  With inv = rn(1/scale)
 // the exact product p = a * inv equals y = a / scale up to a factor
-// (1 + d), |d| <= 2^-24, and y <= M (1 + 2^-23) < 256.
+// (1 + d1), |d1| <= 2^-24, and y <= M (1 + 2^-23).
 //   t = rn(p + C), C = 1.5 * 2^23 (ulp 1): t - C = r, the nearest integer to
 //   p, ties to even (one FFMA, the product is not rounded first);
-//   dlt = rn(p - r) = fma(a, inv, C - t) (C - t is exact).
-// |rn(y) - p| <= 2^-24 y + 2^-24 y <= 2^-15, so when |dlt| < 1/2 - 2^-12 the
-// IEEE quotient rn(y) lies strictly within 1/2 of r and rounds to r; `near`
-// flags the other case, which the caller resolves with exact_code().  The
-// code never exceeds M: p <= M (1 + 2^-24)^2 / (1 - 2^-24) < M + 1/2.
-// Returns the bits of t: code = t_bits - 0x4B400000.  scale == 0 gives
-// inv == 0, p == 0 and code 0.
+//   dlt = rn(p - r) = fma(a, inv, C - t) (C - t is exact), so
+//   |dlt - (p - r)| <= 2^-26.
+// The IEEE quotient rn(y) = y (1 + d2), |d2| <= 2^-24, so
+// |rn(y) - p| <= 2^-23 y <= 2^-23 M (1 + 2^-23), and
+// |rn(y) - r| <= |dlt| + 2^-23 M + 2^-23 2^-23 M + 2^-26 < |dlt| + 2^(b-23).
+// Hence when |dlt| < 1/2 - 2^(b-23) (near_tie<b>) rn(y) lies strictly within
+// 1/2 of r and rounds to r; the caller resolves the other case (about 2^(b-21)
+// of the codes) with exact_code().  The code never exceeds M:
+// p <= M (1 + 2^-24)^2 / (1 - 2^-24) < M + 1/2.  Returns the bits of t:
+// code = t_bits - 0x4B400000.  scale == 0 gives inv == 0, p == 0 and code 0.
 __device__ __forceinline__ uint32_t fast_code_bits(float a, float inv, float& worst)
 {
     const float t = __fmaf_rn(a, inv, 12582912.0f);
@@ -137,7 +140,9 @@ __device__ __forceinline__ uint32_t fast_code_bits(float a, float inv, float& wo
     worst = fmaxf(worst, fabsf(dlt));  // flags are tested once per batch of codes
     return __float_as_uint(t);
 }
-constexpr float kNearTie = 0.5f - 0x1p-12f;  // |dlt| at or above this: use exact_code
+// |dlt| at or above this: use exact_code (see fast_code_bits).
+template <int BITS>
+__host__ __device__ constexpr float near_tie() { return 0.5f - (float)(1u << BITS) * 0x1p-23f; }
 constexpr uint32_t kCodeBias = 0x4B400000u;
 
 // code = clamp(rne(a / scale), 0, M), bit-identical to rounding the IEEE
@@ -147,7 +152,7 @@ __device__ __forceinline__ uint32_t quant_code(float a, float scale, float inv)
 {
     float worst = 0.0f;
     uint32_t c = fast_code_bits(a, inv, worst) - kCodeBias;
-    if (worst >= kNearTie)
+    if (worst >= near_tie<BITS>())
         c = exact_code(a, scale);
     return c;
 }
@@ -255,7 +260,7 @@ __device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens], 
             const uint32_t tb = fast_code_bits(a, inv[k], worst);
             words[i / Cd::P][k] += tb * (1u << ((i % Cd::P) * BITS));
         }
-        flagged |= (worst >= kNearTie ? 1u : 0u) << i;
+        flagged |= (worst >= near_tie<BITS>() ? 1u : 0u) << i;
     }
 }
 
@@ -280,7 +285,7 @@ __device__ __forceinline__ void key_lane_fixup(unsigned flagged, const uint16_t*
             const float a = add_h_f(u4_half(r, k), -zero[k]);
             float w1 = 0.0f;
             const uint32_t fast = fast_code_bits(a, inv[k], w1) - kCodeBias;
-            if (w1 >= kNearTie) {
+            if (w1 >= near_tie<BITS>()) {
                 const uint32_t fix = (exact_code(a, scale[k]) - fast) << sh;
 #pragma unroll
                 for (int w = 0; w < Cd::kWordRows; ++w)
@@ -329,13 +334,13 @@ __device__ __forceinline__ void quant_value_group(const uint4 (&raw)[G / 8], flo
             const uint32_t tb = fast_code_bits(add_h_f(u4_half(raw[e / 8], e % 8), nz), inv, worst);
             words[e / Cd::P] += tb * (1u << ((e % Cd::P) * BITS));
         }
-        if (__builtin_expect(worst >= kNearTie, 0)) {
+        if (__builtin_expect(worst >= near_tie<BITS>(), 0)) {
 #pragma unroll
             for (int e = e0; e < e0 + 8; ++e) {
                 const float a = add_h_f(u4_half(raw[e / 8], e % 8), nz);
                 float w1 = 0.0f;
                 const uint32_t fast = fast_code_bits(a, inv, w1) - kCodeBias;
-                if (w1 >= kNearTie)
+                if (w1 >= near_tie<BITS>())
                     words[e / Cd::P] += (exact_code(a, scale) - fast) << ((e % Cd::P) * BITS);
             }
         }

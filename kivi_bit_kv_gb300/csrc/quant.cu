@@ -171,7 +171,7 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
                     const float a = add_h_f(u4_half(r, k), nzero[k]);
                     words[k] += fast_code_bits(a, inv[k], worst) * mul;
                 }
-                flagged |= (worst >= kNearTie ? 1u : 0u) << (i0 + ii);
+                flagged |= (worst >= near_tie<BITS>() ? 1u : 0u) << (i0 + ii);
                 mul <<= BITS;
             }
         }
@@ -186,7 +186,7 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
                     const float a = add_h_f(u4_half(r, k), nzero[k]);
                     float w1 = 0.0f;
                     const uint32_t fast = fast_code_bits(a, inv[k], w1) - kCodeBias;
-                    if (w1 >= kNearTie)
+                    if (w1 >= near_tie<BITS>())
                         words[k] += (exact_code(a, scale[k]) - fast) << (i * BITS);
                 }
             }
