@@ -162,93 +162,56 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
 
 // ------------------------------------------------------------ attention ---
 
-// One CTA per (KV head, chunk); after the chunk's keys and values are staged,
-// each warp works through its own quarter of the chunk alone -- logits, its
-// softmax statistics, its B fragments, its share of p . V -- and the CTA
-// merges the four warp partials once at the end, so the warps meet at two
-// barriers per pass.
+// One CTA per (KV head, chunk): the chunk's keys and values are staged at
+// launch (two cp.async groups, keys first); q . K_hat^T runs as soon as the
+// keys have landed and leaves the logits in shared memory, then the softmax,
+// the B fragments and p . V_hat run as in decode_pv_kernel.  The logits never
+// reach HBM.
 template <int BITS, int NQB>
 __global__ void __launch_bounds__(kDecodeThreads, 3)
 decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_scale,
                         float* __restrict__ ws_o, float* __restrict__ ws_m,
-                        float* __restrict__ ws_l, int nchunks, int TC, const WarpLayout L)
+                        float* __restrict__ ws_l, int nchunks, int TC, const DecodeLayout L)
 {
     extern __shared__ __align__(16) float dsm[];
     __shared__ __align__(16) float qs[NQB * qstride_of(256)];
     __shared__ float fac[NQB];
-    __shared__ float wm[kDecodeWarps * NQB], wl[kDecodeWarps * NQB];
+    __shared__ float red[kDecodeWarps * NQB];
     using T = KeyTile<BITS, NQB>;
     ChunkRange r;
     if (!chunk_range(c, TC, r))
         return;
     const size_t bh = blockIdx.x;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int warp = threadIdx.x >> 5;
     const int NQ = Hq / c.H;
-    uint32_t* kw = reinterpret_cast<uint32_t*>(dsm + L.kw);
-    uint32_t* vw = reinterpret_cast<uint32_t*>(dsm + L.vw);
-    float* p = dsm + L.p;
-    stage_keys<BITS, T::TOK>(c, bh, r.t_begin, r.tq_end, kw, dsm + L.ks, dsm + L.kz);
-    stage_values<BITS>(c, bh, r.t_begin, r.tq_end, vw, dsm + L.vs, dsm + L.vz);
+    const DecodeSmem m = carve(dsm, L, 0);
+    stage_keys<BITS, T::TOK>(c, bh, r.t_begin, r.tq_end, m.kw, m.ks, m.kz);
     cp_async_commit();
-
-    const int D = c.D, NGv = D >> ilog2(c.G), ps = prob_stride(TC);
-    const int q4 = TC / 4;
-    const int a = r.t_begin + warp * q4, b = min(a + q4, r.t_end);  // this warp's tokens
-    const int aq = min(b, r.tq_end);                                // ... quantized below aq
-    const int ra = max(a, r.tq_end);                                // ... residual from ra
-    const int n = r.t_end - r.t_begin, nq = r.tq_end - r.t_begin;
-    // this warp's B fragments and output partial
-    uint2* bbw = reinterpret_cast<uint2*>(L.bb_on_keys ? dsm + L.kw + (size_t)(q4 / (32 / BITS)) * D * warp
-                                                       : dsm + L.bb + L.bb_w * warp);
-    float* pw = L.part_on_vals ? dsm + L.vw + (size_t)q4 * (D / (32 / BITS)) * warp : dsm + L.part + L.part_w * warp;
-    float* const part_all[kDecodeWarps] = {
-        L.part_on_vals ? dsm + L.vw : dsm + L.part,
-        L.part_on_vals ? dsm + L.vw + (size_t)q4 * (D / (32 / BITS)) : dsm + L.part + L.part_w,
-        L.part_on_vals ? dsm + L.vw + (size_t)q4 * (D / (32 / BITS)) * 2 : dsm + L.part + L.part_w * 2,
-        L.part_on_vals ? dsm + L.vw + (size_t)q4 * (D / (32 / BITS)) * 3 : dsm + L.part + L.part_w * 3};
-    const int i0 = (a - r.t_begin) / 2;                      // first pair of this warp
-    const int i1 = min(pv_pairs(n, nq), (a + q4 - r.t_begin) / 2);
-    const int rows = 32 / (D / 32);
-
+    stage_values<BITS>(c, bh, r.t_begin, r.tq_end, m.vw, m.vs, m.vz);
+    cp_async_commit();
+    const int ps = prob_stride(TC);
+    const int rows = 32 / (c.D / 32);  // residual tokens per warp step
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = r.h * NQ + pass * NQB;
-        __syncthreads();  // the previous pass's merge is done
-        stage_q<NQB>(q + ((size_t)r.b * Hq + hq0) * D, D, sm_scale, qs, fac);
-        cp_async_wait_all();
         __syncthreads();
-        float m[NQB], l[NQB];
-#pragma unroll
-        for (int h = 0; h < NQB; ++h) {
-            m[h] = -INFINITY;
-            l[h] = 0.0f;
+        if (pass > 0 && L.bb_on_keys) {
+            // the previous pass's B fragments overwrote the staged keys
+            stage_keys<BITS, T::TOK>(c, bh, r.t_begin, r.tq_end, m.kw, m.ks, m.kz);
+            cp_async_commit();
         }
-        if (a < b) {
-            auto sink = [&](int h, int t, float s) { p[h * ps + t - r.t_begin] = s; };
-            if (a < aq)
-                qk_quantized<BITS, NQB>(D, c.G, r.t_begin, r.tq_end, a, aq, T::TOK, kw, dsm + L.ks,
-                                        dsm + L.kz, qs, fac, sink);
-            qk_residual<NQB>(c, bh, ra, rows, b, qs, fac, sink);
-            __syncwarp();
-            warp_softmax<NQB>(p, ps, a - r.t_begin, b - r.t_begin, m, l);
-            pv_weights<NQB>(n, nq, NGv, i0 + lane, i1, 32, i0, p, ps, dsm + L.vs, dsm + L.vz, bbw, q4 / 2,
-                            dsm + L.zw);
-            __syncwarp();
-            const int kq = (a - r.t_begin) / 16, kq_end = a < aq ? (aq - r.t_begin) / 16 : kq;
-            const int kr = (ra - r.tq_end) / 16, kr_end = ra < b ? (b - r.tq_end + 15) / 16 : kr;
-            const int nsp = pv_seg_groups<BITS>(D);
-            for (int sp = 0; sp < nsp; ++sp)
-                pv_unit<BITS, NQB>(c, bh, r.t_begin, r.tq_end, r.t_end, vw, bbw, q4 / 2, i0, sp, kq, kq_end,
-                                   kr, kr_end, 1, pw);
-        }
-        if (lane == 0)
-#pragma unroll
-            for (int h = 0; h < NQB; ++h) {
-                wm[warp * NQB + h] = m[h];
-                wl[warp * NQB + h] = l[h];
-            }
+        stage_q<NQB>(q + ((size_t)r.b * Hq + hq0) * c.D, c.D, sm_scale, qs, fac);
+        if (pass == 0)
+            cp_async_wait_prior();  // the keys have landed; the values may still be in flight
+        else
+            cp_async_wait_all();
         __syncthreads();
-        merge_warps<NQB>(D, c.G, part_all, dsm + L.zw, wm, wl,
-                         ((size_t)r.b * Hq + hq0) * nchunks + blockIdx.y, nchunks, ws_o, ws_m, ws_l);
+        auto sink = [&](int h, int t, float s) { m.p[h * ps + t - r.t_begin] = s; };
+        qk_quantized<BITS, NQB>(c.D, c.G, r.t_begin, r.tq_end, r.t_begin + warp * T::TOK, r.tq_end,
+                                kDecodeWarps * T::TOK, m.kw, m.ks, m.kz, qs, fac, sink);
+        qk_residual<NQB>(c, bh, r.tq_end + warp * rows, kDecodeWarps * rows, r.t_end, qs, fac, sink);
+        __syncthreads();
+        pv_pass<BITS, NQB>(c, bh, TC, r, m, red, ((size_t)r.b * Hq + hq0) * nchunks + blockIdx.y,
+                           nchunks, ws_o, ws_m, ws_l, pass == 0);
     }
 }
 
@@ -435,8 +398,7 @@ static cudaError_t attn_launch(const kivi_cache& c, const uint16_t* q, int Hq, f
                                float* ws_o, float* ws_m, float* ws_l, cudaStream_t s)
 {
     auto kern = decode_attention_kernel<BITS, NQB>;
-    const int NQ = Hq / c.H;
-    const WarpLayout L = warp_layout(chunk_tokens(c, Hq), c.D, c.bits_k, c.bits_v, c.G, NQB, NQ > NQB);
+    const DecodeLayout L = cta_layout(c, Hq, true, true);
     const size_t smem = 4 * L.total;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess)

@@ -238,69 +238,21 @@ __host__ __device__ inline DecodeLayout decode_layout(int TC, int D, int bits_k,
     return L;
 }
 
-// Shared memory of the fused attention kernel, where each warp owns a
-// quarter of the chunk: staged keys and values, probabilities [NQB][TC + 8],
-// per-warp zero terms [4][NQB][D/G], and per warp its B fragments
-// ([(D/G) NQB][TC/8] uint2) and output partial ([NQB][D]).  A warp's B
-// fragments overlay its own key word-rows (dead once its logits exist) and
-// its partial its own value rows (dead after its last ldmatrix) when they fit
-// and one pass covers all query heads; otherwise they get regions of their own.
-struct WarpLayout {
-    size_t kw, ks, kz, vw, vs, vz, p, zw;
-    size_t bb, part;       // base of the per-warp regions (when not overlaid)
-    size_t bb_w, part_w;   // words per warp region
-    bool bb_on_keys, part_on_vals;
-    size_t total;
-};
-
-__host__ __device__ inline WarpLayout warp_layout(int TC, int D, int bits_k, int bits_v, int G, int NQB,
-                                                  bool multipass)
-{
-    WarpLayout L{};
-    const int Pk = 32 / bits_k, Pv = 32 / bits_v, NGv = D / G, q4 = TC / 4;
-    size_t o = 0;
-    L.kw = o;
-    L.ks = L.kw + (size_t)(TC / Pk) * D;
-    L.kz = L.ks + (size_t)(TC / G) * D;
-    L.vw = L.kz + (size_t)(TC / G) * D;
-    L.vs = L.vw + (size_t)TC * (D / Pv);
-    L.vz = L.vs + (size_t)TC * NGv;
-    o = L.vz + (size_t)TC * NGv;
-    L.p = o;
-    o += (size_t)NQB * prob_stride(TC);
-    L.zw = o;
-    o += zs_words(D, G, NQB);
-    L.bb_w = 2 * (size_t)NGv * NQB * (q4 / 2);
-    L.part_w = (size_t)NQB * D;
-    const int nsp = D / Pv / 4 >= 2 ? D / Pv / 8 : 1;  // segment groups of the value rows
-    L.bb_on_keys = !multipass && L.bb_w <= (size_t)(q4 / Pk) * D;
-    L.part_on_vals = !multipass && nsp == 1 && L.part_w <= (size_t)q4 * (D / Pv);
-    if (!L.bb_on_keys) {
-        L.bb = o;
-        o += kDecodeWarps * L.bb_w;
-    }
-    if (!L.part_on_vals) {
-        L.part = o;
-        o += kDecodeWarps * L.part_w;
-    }
-    L.total = o;
-    return L;
-}
-
 // Tokens per decode chunk: the largest of 1024 ... 64 that is a multiple of
-// G, whose quarter holds a whole key warp tile, and whose fused-kernel layout
-// fits three CTAs per SM (else two, else one); ctas_per_sm receives that count.
+// G and of the key warp tile and whose fused-kernel layout (staged keys and
+// values, probabilities, B fragments, partials) fits three CTAs per SM (else
+// two, else one); ctas_per_sm receives that count.
 __host__ __device__ inline int decode_chunk_tokens(int D, int bits_k, int bits_v, int G, int NQ,
                                                    int* ctas_per_sm = nullptr)
 {
     const int NQB = heads_per_pass(NQ);
     const int P = 32 / bits_k;
     const int tok = cmin(8, (8 / NQB) * 32 / P) * P;
-    const int tc_min = cmax(cmax(4 * tok, G), 64);
+    const int tc_min = cmax(cmax(tok, G), 64);
     const size_t budgets[3] = {74 * 1024, 110 * 1024, 220 * 1024};
     for (int bi = NQB >= 4 ? 1 : 0; bi < 3; ++bi)
         for (int TC = 1024; TC >= tc_min; TC >>= 1)
-            if (4 * warp_layout(TC, D, bits_k, bits_v, G, NQB, NQ > NQB).total <= budgets[bi]) {
+            if (4 * decode_layout(TC, D, bits_k, bits_v, G, NQB, NQ > NQB, true, true, 1).total <= budgets[bi]) {
                 if (ctas_per_sm)
                     *ctas_per_sm = 3 - bi;
                 return TC;
@@ -912,71 +864,6 @@ __device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TC,
         const int sp = unit % NSP, split = unit / NSP;
         pv_unit<BITS, NQB>(c, bh, t_begin, tq_end, t_end, vw, bb, bb_stride(TC), 0, sp, split, nq_slices,
                            split, nr_slices, NSPLIT, o_part + (size_t)split * NQB * c.D);
-    }
-}
-
-// Softmax statistics of one warp's tokens p_sm[h][lo .. hi) (row stride ps;
-// logits on entry): m_h = max, p = exp(s - m_h) in place, l_h = sum p.  The
-// whole warp takes part; an empty range gives m = -inf, l = 0.
-template <int NQB>
-__device__ __forceinline__ void warp_softmax(float* p_sm, int ps, int lo, int hi, float (&m)[NQB],
-                                             float (&l)[NQB])
-{
-    const int lane = threadIdx.x & 31;
-#pragma unroll
-    for (int h = 0; h < NQB; ++h) {
-        float* row = p_sm + h * ps;
-        float mx = -INFINITY;
-        for (int t = lo + lane; t < hi; t += 32)
-            mx = fmaxf(mx, row[t]);
-        for (int k = 16; k > 0; k >>= 1)
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
-        __syncwarp();
-        float sum = 0.0f;
-        for (int t = lo + lane; t < hi; t += 32) {
-            const float e = expf(row[t] - mx);
-            row[t] = e;
-            sum += e;
-        }
-        for (int k = 16; k > 0; k >>= 1)
-            sum += __shfl_xor_sync(0xffffffffu, sum, k);
-        m[h] = mx;
-        l[h] = sum;
-    }
-    __syncwarp();
-}
-
-// Merges the per-warp partials of a chunk (each relative to its warp's own
-// maximum wm[w][h]; wl[w][h] = 0 for a warp without tokens) into the chunk's
-// (o, m, l): M = max_w wm, o[h][d] = sum_w e^(wm - M) (o_w[h][d] + z_w[h][g(d)]),
-// l = sum_w e^(wm - M) wl.  Whole CTA, after a barrier; fixed order.
-template <int NQB>
-__device__ __forceinline__ void merge_warps(int D, int G, float* const (&o_w)[kDecodeWarps],
-                                            const float* zw, const float* wm, const float* wl,
-                                            size_t row0, int nchunks, float* ws_o, float* ws_m,
-                                            float* ws_l)
-{
-    const int lgD = ilog2(D), lgG = ilog2(G), NGv = D >> lgG;
-    for (int idx = threadIdx.x; idx < NQB * D; idx += kDecodeThreads) {
-        const int h = idx >> lgD, d = idx & (D - 1);
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w)
-            if (wl[w * NQB + h] > 0.0f)
-                M = fmaxf(M, wm[w * NQB + h]);
-        float o = 0.0f, L = 0.0f;
-#pragma unroll
-        for (int w = 0; w < kDecodeWarps; ++w)
-            if (wl[w * NQB + h] > 0.0f) {
-                const float e = expf(wm[w * NQB + h] - M);
-                o = fmaf(e, o_w[w][idx] + zw[(w * NQB + h) * NGv + (d >> lgG)], o);
-                L = fmaf(e, wl[w * NQB + h], L);
-            }
-        ws_o[(row0 + (size_t)h * nchunks) * D + d] = o;
-        if (d == 0) {
-            ws_m[row0 + (size_t)h * nchunks] = M;
-            ws_l[row0 + (size_t)h * nchunks] = L;
-        }
     }
 }
 
