@@ -7,7 +7,7 @@
 //   decode_pv_kernel         softmax + p . V from given logits (kivi_decode_pv)
 //   decode_attention_kernel  both, logits kept in shared memory
 //                            (kivi_decode_attention)
-// Each CTA owns one KV head and one chunk of decode_chunk_tokens() tokens,
+// Each CTA owns one KV head and one chunk of tokens (decode_chunk_plan),
 // staged into shared memory at launch; the pv and fused kernels leave
 // per-chunk (o, m, l) partials that decode_combine_kernel merges.
 #include <math.h>
@@ -17,49 +17,50 @@
 
 namespace kivi {
 
-// Per-CTA coordinates of a decode chunk of TC tokens.
+// Per-CTA coordinates of decode chunk ci: TC tokens, or up to TC + S for the
+// last chunk of a sequence (decode_chunks).  Chunks run in reverse order of
+// blockIdx.y, so the last chunks of the sequences, which also carry the
+// residual tokens, are dispatched first and full chunks fill the tail.
 struct ChunkRange {
-    int b, h, n, t_begin, t_end, Tq, tq_end;
+    int b, h, n, ci, t_begin, t_end, Tq, tq_end;
 };
 
-__device__ __forceinline__ bool chunk_range(const kivi_cache& c, int TC, ChunkRange& r)
+__device__ __forceinline__ bool chunk_range(const kivi_cache& c, int TC, int S, ChunkRange& r)
 {
     const int bh = (int)blockIdx.x;
     r.b = bh / c.H;
     r.h = bh - r.b * c.H;
     r.n = c.len[r.b];
-    r.t_begin = blockIdx.y * TC;
-    if (r.t_begin >= r.n)
+    const int nch = decode_chunks(r.n, TC, S);
+    r.ci = (int)(gridDim.y - 1 - blockIdx.y);
+    if (r.ci >= nch)
         return false;
-    r.t_end = min(r.t_begin + TC, r.n);
+    r.t_begin = r.ci * TC;
+    r.t_end = r.ci == nch - 1 ? r.n : r.t_begin + TC;
     r.Tq = quantized_tokens(r.n, c.G, c.R);
     r.tq_end = max(r.t_begin, min(r.t_end, r.Tq));
     return true;
 }
 
-// Pointers into the dynamic shared memory of a decode kernel (decode_layout),
-// for item buffer `buf`.
+// Pointers into the dynamic shared memory of a decode kernel (decode_layout).
 struct DecodeSmem {
     uint32_t *kw, *vw;
     float *ks, *kz, *vs, *vz, *p, *part, *zs;
-    uint16_t* q16;
     uint2* bb;
 };
 
-__device__ __forceinline__ DecodeSmem carve(float* base, const DecodeLayout& L, int buf)
+__device__ __forceinline__ DecodeSmem carve(float* base, const DecodeLayout& L)
 {
-    float* b = base + L.buf * buf;
     DecodeSmem m;
-    m.kw = reinterpret_cast<uint32_t*>(b + L.kw);
-    m.ks = b + L.ks;
-    m.kz = b + L.kz;
-    m.vw = reinterpret_cast<uint32_t*>(b + L.vw);
-    m.vs = b + L.vs;
-    m.vz = b + L.vz;
-    m.q16 = reinterpret_cast<uint16_t*>(b + L.q16);
+    m.kw = reinterpret_cast<uint32_t*>(base + L.kw);
+    m.ks = base + L.ks;
+    m.kz = base + L.kz;
+    m.vw = reinterpret_cast<uint32_t*>(base + L.vw);
+    m.vs = base + L.vs;
+    m.vz = base + L.vz;
     m.p = base + L.p;
-    m.bb = reinterpret_cast<uint2*>(L.bb_on_keys ? b + L.bb : base + L.bb);
-    m.part = L.part_on_vstats ? b + L.part : base + L.part;
+    m.bb = reinterpret_cast<uint2*>(base + L.bb);
+    m.part = base + L.part;
     m.zs = base + L.zs;
     return m;
 }
@@ -70,18 +71,18 @@ __device__ __forceinline__ DecodeSmem carve(float* base, const DecodeLayout& L, 
 template <int BITS, int NQB>
 __global__ void __launch_bounds__(kDecodeThreads, 3)
 decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_scale,
-                 float* __restrict__ logits, int ldl, int TC, const DecodeLayout L)
+                 float* __restrict__ logits, int ldl, int TC, int S, const DecodeLayout L)
 {
     extern __shared__ __align__(16) float dsm[];
     __shared__ __align__(16) float qs[NQB * qstride_of(256)];
     __shared__ float fac[NQB];
     using T = KeyTile<BITS, NQB>;
     ChunkRange r;
-    if (!chunk_range(c, TC, r))
+    if (!chunk_range(c, TC, S, r))
         return;
     const size_t bh = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const DecodeSmem m = carve(dsm, L, 0);
+    const DecodeSmem m = carve(dsm, L);
     stage_keys<BITS, T::TOK>(c, bh, r.t_begin, r.tq_end, m.kw, m.ks, m.kz);
     cp_async_commit();
     const int NQ = Hq / c.H;
@@ -106,11 +107,11 @@ decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_
 // Softmax statistics, B fragments and the weighted value sum of one pass
 // (p_sm holds the chunk's logits), then the chunk's partials.  Whole CTA.
 template <int BITS, int NQB>
-__device__ __forceinline__ void pv_pass(const kivi_cache& c, size_t bh, int TC, const ChunkRange& r,
+__device__ __forceinline__ void pv_pass(const kivi_cache& c, size_t bh, int TX, const ChunkRange& r,
                                         const DecodeSmem& m, float* red, size_t row0, int nchunks,
                                         float* ws_o, float* ws_m, float* ws_l, bool first_pass)
 {
-    const int ps = prob_stride(TC), NGv = c.D >> ilog2(c.G);
+    const int ps = prob_stride(TX), NGv = c.D >> ilog2(c.G);
     const int n = r.t_end - r.t_begin, nq = r.tq_end - r.t_begin;
     float mx[NQB], l[NQB];
     chunk_softmax<NQB>(m.p, ps, n, mx, l, red);
@@ -119,9 +120,9 @@ __device__ __forceinline__ void pv_pass(const kivi_cache& c, size_t bh, int TC, 
         __syncthreads();
     }
     pv_weights<NQB>(n, nq, NGv, threadIdx.x, pv_pairs(n, nq), kDecodeThreads, 0, m.p, ps, m.vs, m.vz,
-                    m.bb, bb_stride(TC), m.zs);
+                    m.bb, bb_stride(TX), m.zs);
     __syncthreads();
-    pv_chunk<BITS, NQB>(c, bh, TC, r.t_begin, r.tq_end, r.t_end, m.vw, m.bb, m.part);
+    pv_chunk<BITS, NQB>(c, bh, TX, r.t_begin, r.tq_end, r.t_end, m.vw, m.bb, m.part);
     __syncthreads();
     write_partials<NQB>(c.D, c.G, pv_splits(pv_seg_groups<BITS>(c.D)), m.part, m.zs, mx, l, row0,
                         nchunks, ws_o, ws_m, ws_l);
@@ -131,20 +132,20 @@ template <int BITS, int NQB>
 __global__ void __launch_bounds__(kDecodeThreads, 3)
 decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq,
                  float* __restrict__ ws_o, float* __restrict__ ws_m, float* __restrict__ ws_l,
-                 int nchunks, int TC, const DecodeLayout L)
+                 int nchunks, int TC, int S, const DecodeLayout L)
 {
     extern __shared__ __align__(16) float dsm[];
     __shared__ float red[kDecodeWarps * NQB];
     ChunkRange r;
-    if (!chunk_range(c, TC, r))
+    if (!chunk_range(c, TC, S, r))
         return;
     const size_t bh = blockIdx.x;
-    const DecodeSmem m = carve(dsm, L, 0);
+    const DecodeSmem m = carve(dsm, L);
     stage_values<BITS>(c, bh, r.t_begin, r.tq_end, m.vw, m.vs, m.vz);
     cp_async_commit();
     const int NQ = Hq / c.H;
     const int n = r.t_end - r.t_begin;
-    const int ps = prob_stride(TC);
+    const int ps = prob_stride(TC + S);
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = r.h * NQ + pass * NQB;
         __syncthreads();
@@ -155,7 +156,7 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
                 m.p[h * ps + t] = lrow[t];
         }
         __syncthreads();
-        pv_pass<BITS, NQB>(c, bh, TC, r, m, red, ((size_t)r.b * Hq + hq0) * nchunks + blockIdx.y,
+        pv_pass<BITS, NQB>(c, bh, TC + S, r, m, red, ((size_t)r.b * Hq + hq0) * nchunks + r.ci,
                            nchunks, ws_o, ws_m, ws_l, pass == 0);
     }
 }
@@ -171,7 +172,7 @@ template <int BITS, int NQB>
 __global__ void __launch_bounds__(kDecodeThreads, 3)
 decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_scale,
                         float* __restrict__ ws_o, float* __restrict__ ws_m,
-                        float* __restrict__ ws_l, int nchunks, int TC, const DecodeLayout L)
+                        float* __restrict__ ws_l, int nchunks, int TC, int S, const DecodeLayout L)
 {
     extern __shared__ __align__(16) float dsm[];
     __shared__ __align__(16) float qs[NQB * qstride_of(256)];
@@ -179,17 +180,17 @@ decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, fl
     __shared__ float red[kDecodeWarps * NQB];
     using T = KeyTile<BITS, NQB>;
     ChunkRange r;
-    if (!chunk_range(c, TC, r))
+    if (!chunk_range(c, TC, S, r))
         return;
     const size_t bh = blockIdx.x;
     const int warp = threadIdx.x >> 5;
     const int NQ = Hq / c.H;
-    const DecodeSmem m = carve(dsm, L, 0);
+    const DecodeSmem m = carve(dsm, L);
     stage_keys<BITS, T::TOK>(c, bh, r.t_begin, r.tq_end, m.kw, m.ks, m.kz);
     cp_async_commit();
     stage_values<BITS>(c, bh, r.t_begin, r.tq_end, m.vw, m.vs, m.vz);
     cp_async_commit();
-    const int ps = prob_stride(TC);
+    const int ps = prob_stride(TC + S);
     const int rows = 32 / (c.D / 32);  // residual tokens per warp step
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = r.h * NQ + pass * NQB;
@@ -210,7 +211,7 @@ decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, fl
                                 kDecodeWarps * T::TOK, m.kw, m.ks, m.kz, qs, fac, sink);
         qk_residual<NQB>(c, bh, r.tq_end + warp * rows, kDecodeWarps * rows, r.t_end, qs, fac, sink);
         __syncthreads();
-        pv_pass<BITS, NQB>(c, bh, TC, r, m, red, ((size_t)r.b * Hq + hq0) * nchunks + blockIdx.y,
+        pv_pass<BITS, NQB>(c, bh, TC + S, r, m, red, ((size_t)r.b * Hq + hq0) * nchunks + r.ci,
                            nchunks, ws_o, ws_m, ws_l, pass == 0);
     }
 }
@@ -222,7 +223,7 @@ decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, fl
 constexpr int kCombineThreads = 128;
 
 __global__ void __launch_bounds__(kCombineThreads)
-decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunks, int TC,
+decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunks, int TC, int S,
                       const float* __restrict__ ws_o, const float* __restrict__ ws_m,
                       const float* __restrict__ ws_l, float* __restrict__ out)
 {
@@ -231,7 +232,7 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t bhq = blockIdx.x;
     const int n = len[bhq / Hq];
-    const int nv = (n + TC - 1) / TC;
+    const int nv = decode_chunks(n, TC, S);
     const float* mrow = ws_m + bhq * nchunks;
     const float* lrow = ws_l + bhq * nchunks;
     float mx = -INFINITY;
@@ -280,14 +281,15 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
 
 // ---------------------------------------------------------------- launch ---
 
-int chunk_tokens(const kivi_cache& c, int Hq)
+static ChunkPlan plan(const kivi_cache& c, int Hq)
 {
-    return decode_chunk_tokens(c.D, c.bits_k, c.bits_v, c.G, Hq / c.H);
+    return decode_chunk_plan(c.D, c.bits_k, c.bits_v, c.G, c.R, Hq / c.H);
 }
+int chunk_tokens(const kivi_cache& c, int Hq) { return plan(c, Hq).TC; }
 int pv_chunks(const kivi_cache& c, int Hq)
 {
-    const int TC = chunk_tokens(c, Hq);
-    return (c.Tmax + TC - 1) / TC;
+    const ChunkPlan cp = plan(c, Hq);
+    return decode_chunks(c.Tmax, cp.TC, cp.S);
 }
 
 static cudaError_t combine(const kivi_cache& c, int Hq, const float* ws_o, const float* ws_m,
@@ -299,7 +301,8 @@ static cudaError_t combine(const kivi_cache& c, int Hq, const float* ws_o, const
                                          (int)smem);
     if (e != cudaSuccess)
         return e;
-    decode_combine_kernel<<<c.B * Hq, kCombineThreads, smem, s>>>(c.len, Hq, c.D, nch, chunk_tokens(c, Hq),
+    const ChunkPlan cp = plan(c, Hq);
+    decode_combine_kernel<<<c.B * Hq, kCombineThreads, smem, s>>>(c.len, Hq, c.D, nch, cp.TC, cp.S,
                                                                   ws_o, ws_m, ws_l, out);
     return cudaGetLastError();
 }
@@ -313,7 +316,9 @@ static cudaError_t set_smem(K kern, size_t bytes)
 static DecodeLayout cta_layout(const kivi_cache& c, int Hq, bool keys, bool values)
 {
     const int NQ = Hq / c.H, NQB = heads_per_pass(NQ);
-    return decode_layout(chunk_tokens(c, Hq), c.D, c.bits_k, c.bits_v, c.G, NQB, NQ > NQB, keys, values, 1);
+    const ChunkPlan cp = plan(c, Hq);
+    return decode_layout(cp.TC, cp.TC + cp.S, c.D, c.bits_k, c.bits_v, c.G, NQB, NQ > NQB, keys,
+                         values);
 }
 
 template <int BITS, int NQB>
@@ -327,7 +332,7 @@ static cudaError_t qk_launch(const kivi_cache& c, const uint16_t* q, int Hq, flo
     if (e != cudaSuccess)
         return e;
     kern<<<dim3(c.B * c.H, pv_chunks(c, Hq)), kDecodeThreads, smem, s>>>(c, q, Hq, sm, logits, ldl,
-                                                                        chunk_tokens(c, Hq), L);
+                                                                        plan(c, Hq).TC, plan(c, Hq).S, L);
     return cudaGetLastError();
 }
 
@@ -364,7 +369,7 @@ static cudaError_t pv_launch(const kivi_cache& c, const float* logits, int ldl, 
         return e;
     const int nch = pv_chunks(c, Hq);
     kern<<<dim3(c.B * c.H, nch), kDecodeThreads, smem, s>>>(c, logits, ldl, Hq, ws_o, ws_m, ws_l, nch,
-                                                           chunk_tokens(c, Hq), L);
+                                                           plan(c, Hq).TC, plan(c, Hq).S, L);
     return cudaGetLastError();
 }
 
@@ -405,7 +410,7 @@ static cudaError_t attn_launch(const kivi_cache& c, const uint16_t* q, int Hq, f
         return e;
     const int nch = pv_chunks(c, Hq);
     kern<<<dim3(c.B * c.H, nch), kDecodeThreads, smem, s>>>(c, q, Hq, sm, ws_o, ws_m, ws_l, nch,
-                                                           chunk_tokens(c, Hq), L);
+                                                           plan(c, Hq).TC, plan(c, Hq).S, L);
     return cudaGetLastError();
 }
 

@@ -154,30 +154,42 @@ __host__ __device__ constexpr size_t val_stage_words(int TC, int D, int bits_v, 
 {
     return (size_t)TC * (D / (32 / bits_v)) + 2 * (size_t)TC * (D / G);
 }
-// Probability rows [NQB][TC + 8] (the pad spreads heads over banks).
-__host__ __device__ constexpr int prob_stride(int TC) { return TC + 8; }
-// B fragments of p . V: [(D/G) NQB rows][TC/2] uint2 (hi pair, lo pair of
+// Probability rows [NQB][TX + 8] for chunks of up to TX tokens (the pad
+// spreads heads over banks).
+__host__ __device__ constexpr int prob_stride(int TX) { return TX + 8; }
+// B fragments of p . V: [(D/G) NQB rows][TX/2] uint2 (hi pair, lo pair of
 // tokens 2i, 2i+1), pair i of row r stored at i ^ bb_swz(r).
-__host__ __device__ constexpr int bb_stride(int TC) { return TC / 2; }
+__host__ __device__ constexpr int bb_stride(int TX) { return TX / 2; }
 __host__ __device__ constexpr int bb_swz(int r) { return (r & 3) << 2; }
-__host__ __device__ constexpr size_t bb_words(int TC, int D, int G, int NQB)
+__host__ __device__ constexpr size_t bb_words(int TX, int D, int G, int NQB)
 {
-    return 2 * (size_t)(D / G) * NQB * bb_stride(TC);
+    return 2 * (size_t)(D / G) * NQB * bb_stride(TX);
 }
 // Split partials [4][NQB][D]; per-warp zero terms [4][NQB][D/G].
 __host__ __device__ constexpr size_t part_words(int D, int NQB) { return (size_t)kDecodeWarps * NQB * D; }
 __host__ __device__ constexpr size_t zs_words(int D, int G, int NQB) { return (size_t)kDecodeWarps * NQB * (D / G); }
 
-// Word offsets into a decode kernel's dynamic shared memory.  `buffers` item
-// buffers (two for the persistent attention kernel, which fills one while it
-// computes from the other), each with the staged keys and / or values and the
-// fp16 q rows, then the probabilities, the B fragments and split partials
-// when they do not overlay a dead region of the buffer in use, and the zero
-// terms.
+// Largest slack S (tokens the last chunk of a sequence may hold beyond TC,
+// so that a short tail does not cost a CTA of its own).  A sequence keeps at
+// least R tokens in its fp16 residual (read from the ring, never staged), so
+// with S <= R the quantized tokens of any chunk still fit the TC staged ones:
+// the last chunk starts at c TC > n - TC - S and its quantized tokens end at
+// or before n - R.  A multiple of 16 (whole p . V slices).
+__host__ __device__ constexpr int max_chunk_slack(int TC, int R) { return cmin(R, TC / 4) & ~15; }
+// Chunks of a sequence of n tokens: all but the last hold TC tokens, the
+// last one at most TC + S.
+__host__ __device__ constexpr int decode_chunks(int n, int TC, int S)
+{
+    return n <= 0 ? 0 : cmax(1, (n - S + TC - 1) / TC);
+}
+
+// Word offsets into a decode kernel's dynamic shared memory: the staged keys
+// and / or values of TC tokens, then the probabilities and B fragments of up
+// to TX = TC + slack tokens, the split partials when they do not overlay a
+// dead region, and the zero terms.
 struct DecodeLayout {
-    size_t kw, ks, kz, vw, vs, vz, q16;  // within a buffer
-    size_t buf;                          // words per buffer
-    size_t p, bb, part, zs, total;       // bb / part: absolute, or within the buffer if overlaid
+    size_t kw, ks, kz, vw, vs, vz;
+    size_t p, bb, part, zs, total;
     bool bb_on_keys, part_on_vstats;
 };
 
@@ -185,9 +197,8 @@ struct DecodeLayout {
 // staged keys (dead once the logits exist), the split partials the value
 // statistics (dead once the B fragments exist) when one pass covers all query
 // heads of the staged chunk.
-__host__ __device__ inline DecodeLayout decode_layout(int TC, int D, int bits_k, int bits_v, int G,
-                                                      int NQB, bool multipass, bool keys, bool values,
-                                                      int buffers)
+__host__ __device__ inline DecodeLayout decode_layout(int TC, int TX, int D, int bits_k, int bits_v, int G,
+                                                      int NQB, bool multipass, bool keys, bool values)
 {
     DecodeLayout L{};
     size_t o = 0;
@@ -206,17 +217,9 @@ __host__ __device__ inline DecodeLayout decode_layout(int TC, int D, int bits_k,
         L.vs = o + vwn;
         L.vz = L.vs + vsn;
         o = L.vz + vsn;
-    }
-    if (buffers > 1) {  // q rows travel with the item
-        L.q16 = o;
-        o += ((size_t)NQB * D / 2 + 3) & ~(size_t)3;
-    }
-    L.buf = o;
-    o *= buffers;
-    if (values) {
         L.p = o;
-        o += (size_t)NQB * prob_stride(TC);
-        const size_t bbn = bb_words(TC, D, G, NQB);
+        o += (size_t)NQB * prob_stride(TX);
+        const size_t bbn = bb_words(TX, D, G, NQB);
         L.bb_on_keys = keys && bbn <= key_stage_words(TC, D, bits_k, G);
         if (L.bb_on_keys) {
             L.bb = L.kw;
@@ -238,28 +241,33 @@ __host__ __device__ inline DecodeLayout decode_layout(int TC, int D, int bits_k,
     return L;
 }
 
-// Tokens per decode chunk: the largest of 1024 ... 64 that is a multiple of
-// G and of the key warp tile and whose fused-kernel layout (staged keys and
-// values, probabilities, B fragments, partials) fits three CTAs per SM (else
-// two, else one); ctas_per_sm receives that count.
-__host__ __device__ inline int decode_chunk_tokens(int D, int bits_k, int bits_v, int G, int NQ,
-                                                   int* ctas_per_sm = nullptr)
+// Chunking of the decode kernels: TC tokens per chunk, the largest of 1024
+// ... 64 that is a multiple of G and of the key warp tile and whose
+// fused-kernel layout (staged keys and values, probabilities, B fragments,
+// partials) fits three CTAs per SM (else two, else one); then the slack S of
+// the last chunk, max_chunk_slack(TC, R) if the layout with it still fits the
+// same budget, else 0.
+struct ChunkPlan {
+    int TC, S, ctas_per_sm;
+};
+
+__host__ __device__ inline ChunkPlan decode_chunk_plan(int D, int bits_k, int bits_v, int G, int R, int NQ)
 {
     const int NQB = heads_per_pass(NQ);
     const int P = 32 / bits_k;
     const int tok = cmin(8, (8 / NQB) * 32 / P) * P;
     const int tc_min = cmax(cmax(tok, G), 64);
     const size_t budgets[3] = {74 * 1024, 110 * 1024, 220 * 1024};
+    auto bytes = [&](int TC, int S) {
+        return 4 * decode_layout(TC, TC + S, D, bits_k, bits_v, G, NQB, NQ > NQB, true, true).total;
+    };
     for (int bi = NQB >= 4 ? 1 : 0; bi < 3; ++bi)
         for (int TC = 1024; TC >= tc_min; TC >>= 1)
-            if (4 * decode_layout(TC, D, bits_k, bits_v, G, NQB, NQ > NQB, true, true, 1).total <= budgets[bi]) {
-                if (ctas_per_sm)
-                    *ctas_per_sm = 3 - bi;
-                return TC;
+            if (bytes(TC, 0) <= budgets[bi]) {
+                const int S = max_chunk_slack(TC, R);
+                return {TC, bytes(TC, S) <= budgets[bi] ? S : 0, 3 - bi};
             }
-    if (ctas_per_sm)
-        *ctas_per_sm = 1;
-    return tc_min;
+    return {tc_min, 0, 1};
 }
 
 // ------------------------------------------------------------- staging ---
@@ -852,7 +860,7 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
 // group, token split) and writes o_part[split] (splits of one segment group
 // are different warps).
 template <int BITS, int NQB>
-__device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TC, int t_begin,
+__device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TX, int t_begin,
                                          int tq_end, int t_end, const uint32_t* vw, const uint2* bb,
                                          float* o_part)
 {
@@ -862,7 +870,7 @@ __device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TC,
     const int nr_slices = (t_end - tq_end + 15) / 16;
     for (int unit = threadIdx.x >> 5; unit < NSP * NSPLIT; unit += kDecodeWarps) {
         const int sp = unit % NSP, split = unit / NSP;
-        pv_unit<BITS, NQB>(c, bh, t_begin, tq_end, t_end, vw, bb, bb_stride(TC), 0, sp, split, nq_slices,
+        pv_unit<BITS, NQB>(c, bh, t_begin, tq_end, t_end, vw, bb, bb_stride(TX), 0, sp, split, nq_slices,
                            split, nr_slices, NSPLIT, o_part + (size_t)split * NQB * c.D);
     }
 }
