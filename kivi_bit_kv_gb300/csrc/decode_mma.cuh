@@ -105,6 +105,14 @@ __device__ __forceinline__ void split_hi_lo(float a, float b, uint32_t& hi, uint
     lo = h2_bits(__floats2half2_rn(__fsub_rn(a, ah), __fsub_rn(b, bh)));
 }
 
+// One fp16 pair of the split: hi (part 0) or lo (part 1).
+__device__ __forceinline__ uint32_t split_part(float a, float b, int part)
+{
+    const float ah = __uint_as_float(__float_as_uint(a) & 0xFFFFE000u);
+    const float bh = __uint_as_float(__float_as_uint(b) & 0xFFFFE000u);
+    return h2_bits(__floats2half2_rn(part ? __fsub_rn(a, ah) : ah, part ? __fsub_rn(b, bh) : bh));
+}
+
 // -------------------------------------------------------------- shapes ---
 
 // Keys: the 8 lane groups g of a warp take WR word-rows (LPW = 8 / WR lane
@@ -124,6 +132,9 @@ struct KeyTile {
     __host__ __device__ static constexpr int pa(int j) { return BITS * ((2 * j) % CPB); }
     __host__ __device__ static constexpr int pb(int j) { return BITS * ((2 * j + 1) % CPB); }
     static_assert((2 * NT) % CPB == 0, "sub-lane positions must start on a byte");
+    // hi and lo weights as separate B columns (one MMA per tile) when the
+    // (group, head) units of a warp tile take at most four columns
+    static constexpr bool HL = NQB == 1 || (NQB == 2 && BITS >= 4);
 };
 
 // Values: a 16-byte segment of a token row holds 8 halves of HC codes; the
@@ -429,8 +440,11 @@ __device__ __forceinline__ void qk_quantized(int D, int G, int t_begin, int tq_e
     const int wr = g % T::WR, v = g / T::WR;
     const uint32_t soff = (uint32_t)(2 * v * T::NT / T::CPB) * 0x101u;  // byte offset of sub-lane v
     const int NGW = cmax(1, T::TOK >> lgG);         // statistic groups per warp tile
-    const int gi = cmin(g / NQB, NGW - 1);          // B column group (clamped; extra columns unused)
-    const int hq = g % NQB;
+    // B column g: unit (group gi, head hq) = g / 2 and weight part g & 1 with
+    // hi / lo columns, else unit g with hi and lo in two MMAs
+    const int unit = T::HL ? g >> 1 : g, part = g & 1;
+    const int gi = cmin(unit / NQB, NGW - 1);       // clamped; extra columns unused
+    const int hq = unit % NQB;
     const float* qrow = qs + hq * qstride + qpad(tg * 16);
     const int gi_row = (wr * T::P) >> lgG;          // group of this lane group's rows
 
@@ -461,8 +475,13 @@ __device__ __forceinline__ void qk_quantized(int D, int G, int t_begin, int tq_e
                 zacc = fmaf(qv.z, Z.z, zacc);
                 zacc = fmaf(qv.w, Z.w, zacc);
                 uint32_t bh0, bl0, bh1, bl1;
-                split_hi_lo(qv.x * S.x, qv.y * S.y, bh0, bl0);
-                split_hi_lo(qv.z * S.z, qv.w * S.w, bh1, bl1);
+                if constexpr (T::HL) {
+                    bh0 = split_part(qv.x * S.x, qv.y * S.y, part);
+                    bh1 = split_part(qv.z * S.z, qv.w * S.w, part);
+                } else {
+                    split_hi_lo(qv.x * S.x, qv.y * S.y, bh0, bl0);
+                    split_hi_lo(qv.z * S.z, qv.w * S.w, bh1, bl1);
+                }
 #pragma unroll
                 for (int j = 0; j < T::NT; ++j) {
                     const uint32_t sa = ((uint32_t)T::ya(j) | ((uint32_t)(4 + T::ya(j)) << 8)) + soff;
@@ -473,29 +492,45 @@ __device__ __forceinline__ void qk_quantized(int D, int G, int t_begin, int tq_e
                     const uint32_t a2 = __byte_perm(W.z, W.w, sa) & ma;
                     const uint32_t a3 = __byte_perm(W.z, W.w, sb) & mb;
                     mma_f16(acc[j], a0, a1, a2, a3, bh0, bh1);
-                    mma_f16(acc[j], a0, a1, a2, a3, bl0, bl1);
+                    if constexpr (!T::HL)
+                        mma_f16(acc[j], a0, a1, a2, a3, bl0, bl1);
                 }
             }
         }
-        // zero terms: column sums over the four lanes, then the lane's two columns
+        // zero terms: column sums over the four lanes, then the lane's columns
+        // (every lane shuffles, before any lane leaves the iteration).  With
+        // hi / lo columns, columns 2 tg and 2 tg + 1 both belong to unit tg.
         zacc += __shfl_xor_sync(0xffffffffu, zacc, 1);
         zacc += __shfl_xor_sync(0xffffffffu, zacc, 2);
         const float zc[2] = {__shfl_sync(0xffffffffu, zacc, 8 * tg),
                              __shfl_sync(0xffffffffu, zacc, 8 * tg + 4)};
         if (tok0 + wr * T::P >= tq_end)
             continue;
+        const int tbase = tok0 + wr * T::P + 2 * v * T::NT;
+        if constexpr (T::HL) {
+            const int h = tg % NQB;
+            if (tg / NQB == gi_row) {
+                const float f = fac[h];
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int u = 2 * tg + cc;
-            if (u / NQB != gi_row)
-                continue;
-            const int h = u % NQB;
-            const float f = fac[h];
-            const int tbase = tok0 + wr * T::P + 2 * v * T::NT;
+                for (int j = 0; j < T::NT; ++j) {
+                    sink(h, tbase + 2 * j, f * fmaf(code_unscale_bits(T::pa(j)), acc[j][0] + acc[j][1], zc[0]));
+                    sink(h, tbase + 2 * j + 1,
+                         f * fmaf(code_unscale_bits(T::pb(j)), acc[j][2] + acc[j][3], zc[0]));
+                }
+            }
+        } else {
 #pragma unroll
-            for (int j = 0; j < T::NT; ++j) {
-                sink(h, tbase + 2 * j, f * fmaf(code_unscale_bits(T::pa(j)), acc[j][cc], zc[cc]));
-                sink(h, tbase + 2 * j + 1, f * fmaf(code_unscale_bits(T::pb(j)), acc[j][2 + cc], zc[cc]));
+            for (int cc = 0; cc < 2; ++cc) {
+                const int u = 2 * tg + cc;
+                if (u / NQB != gi_row)
+                    continue;
+                const int h = u % NQB;
+                const float f = fac[h];
+#pragma unroll
+                for (int j = 0; j < T::NT; ++j) {
+                    sink(h, tbase + 2 * j, f * fmaf(code_unscale_bits(T::pa(j)), acc[j][cc], zc[cc]));
+                    sink(h, tbase + 2 * j + 1, f * fmaf(code_unscale_bits(T::pb(j)), acc[j][2 + cc], zc[cc]));
+                }
             }
         }
     }
@@ -720,10 +755,14 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
     const int D = c.D, G = c.G, lgG = ilog2(G), RG = c.R + c.G;
     const int DW = D / T::P, NSEG = DW / 4;
     const int SPL = pv_segs_per_load<BITS>(D);  // segments per ldmatrix (x4: 2, x2: 1)
-    const int NGS = cmax(1, T::CS >> lgG);      // groups per segment
+    const int NGS = cmax(1, T::CS >> lgG);      // groups per segment (1 or 2)
+    // hi and lo weights as separate B columns when the (group, head) units
+    // take at most four: B column g is unit g / 2, part g & 1
+    constexpr bool HL = NQB <= 2;
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tg = lane & 3;
-    const int gl = cmin(g / NQB, NGS - 1), hq = g % NQB;  // B column (clamped; extras unused)
+    const int unit = HL ? g >> 1 : g, part = g & 1;
+    const int gl = cmin(unit / NQB, NGS - 1), hq = unit % NQB;  // clamped; extra columns unused
     // ldmatrix row of this lane: matrix mi = lane / 8 = 2 s + (token half)
     const int mi = lane >> 3, lrow = (lane & 7) + 8 * (mi & 1), lseg = SPL == 2 ? mi >> 1 : 0;
     const int seg0 = sp * SPL;
@@ -759,8 +798,15 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
         for (int s = 0; s < 2; ++s) {
             if (s >= SPL)
                 break;
-            const uint2 b01 = bp[s][(k * 8 + tg - i_base) ^ bx[s]];
-            const uint2 b23 = bp[s][(k * 8 + 4 + tg - i_base) ^ bx[s]];
+            uint2 b01, b23;
+            if constexpr (HL) {
+                const uint32_t* b32 = reinterpret_cast<const uint32_t*>(bp[s]) + part;
+                b01.x = b32[2 * ((k * 8 + tg - i_base) ^ bx[s])];
+                b23.x = b32[2 * ((k * 8 + 4 + tg - i_base) ^ bx[s])];
+            } else {
+                b01 = bp[s][(k * 8 + tg - i_base) ^ bx[s]];
+                b23 = bp[s][(k * 8 + 4 + tg - i_base) ^ bx[s]];
+            }
             const uint32_t Rl = R[2 * s], Rh = R[2 * s + 1];
             const uint32_t Rls = Rl >> T::SHIFT, Rhs = Rh >> T::SHIFT;
 #pragma unroll
@@ -773,7 +819,8 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
                 const uint32_t x2 = (T::shifted(m0) ? Rhs : Rh) & mk0;
                 const uint32_t x3 = (T::shifted(m1) ? Rhs : Rh) & mk1;
                 mma_f16(acc[s][j], x0, x1, x2, x3, b01.x, b23.x);
-                mma_f16(acc[s][j], x0, x1, x2, x3, b01.y, b23.y);
+                if constexpr (!HL)
+                    mma_f16(acc[s][j], x0, x1, x2, x3, b01.y, b23.y);
             }
         }
     }
@@ -820,8 +867,15 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
                     X[i][0] = ok ? __ldg(reinterpret_cast<const uint32_t*>(vr)) : 0u;
                 }
             }
-            const uint2 b01 = bp[s][(nq2 + k * 8 + tg - i_base) ^ bx[s]];
-            const uint2 b23 = bp[s][(nq2 + k * 8 + 4 + tg - i_base) ^ bx[s]];
+            uint2 b01, b23;
+            if constexpr (HL) {
+                const uint32_t* b32 = reinterpret_cast<const uint32_t*>(bp[s]) + part;
+                b01.x = b32[2 * ((nq2 + k * 8 + tg - i_base) ^ bx[s])];
+                b23.x = b32[2 * ((nq2 + k * 8 + 4 + tg - i_base) ^ bx[s])];
+            } else {
+                b01 = bp[s][(nq2 + k * 8 + tg - i_base) ^ bx[s]];
+                b23 = bp[s][(nq2 + k * 8 + 4 + tg - i_base) ^ bx[s]];
+            }
 #pragma unroll
             for (int j = 0; j < T::NT; ++j) {
                 const uint32_t x0 = __byte_perm(X[0][j], X[1][j], 0x5410);
@@ -829,7 +883,8 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
                 const uint32_t x2 = __byte_perm(X[2][j], X[3][j], 0x5410);
                 const uint32_t x3 = __byte_perm(X[2][j], X[3][j], 0x7632);
                 mma_f16(acc[s][j], x0, x1, x2, x3, b01.x, b23.x);
-                mma_f16(acc[s][j], x0, x1, x2, x3, b01.y, b23.y);
+                if constexpr (!HL)
+                    mma_f16(acc[s][j], x0, x1, x2, x3, b01.y, b23.y);
             }
         }
     }
@@ -838,19 +893,29 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
     for (int s = 0; s < 2; ++s) {
         if (s >= SPL)
             break;
+        const int ch0 = (seg0 + s) * T::CS + g * T::HC;
+        if constexpr (HL) {
+            // columns 2 tg (hi) and 2 tg + 1 (lo) both belong to unit tg
+            const int ugl = tg / NQB, uh = tg % NQB;
+            if (ugl < NGS && grp_first[s] + ugl == (ch0 >> lgG)) {
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-            const int u = 2 * tg + cc;
-            const int ugl = u / NQB, uh = u % NQB;
-            if (ugl >= NGS)
-                continue;
-            const int ch0 = (seg0 + s) * T::CS + g * T::HC;
-            if (grp_first[s] + ugl != (ch0 >> lgG))
-                continue;
+                for (int j = 0; j < T::NT; ++j) {
+                    o_out[uh * D + ch0 + 2 * j] = acc[s][j][0] + acc[s][j][1];
+                    o_out[uh * D + ch0 + 2 * j + 1] = acc[s][j][2] + acc[s][j][3];
+                }
+            }
+        } else {
 #pragma unroll
-            for (int j = 0; j < T::NT; ++j) {
-                o_out[uh * D + ch0 + 2 * j] = acc[s][j][cc];
-                o_out[uh * D + ch0 + 2 * j + 1] = acc[s][j][2 + cc];
+            for (int cc = 0; cc < 2; ++cc) {
+                const int u = 2 * tg + cc;
+                const int ugl = u / NQB, uh = u % NQB;
+                if (ugl >= NGS || grp_first[s] + ugl != (ch0 >> lgG))
+                    continue;
+#pragma unroll
+                for (int j = 0; j < T::NT; ++j) {
+                    o_out[uh * D + ch0 + 2 * j] = acc[s][j][cc];
+                    o_out[uh * D + ch0 + 2 * j + 1] = acc[s][j][2 + cc];
+                }
             }
         }
     }
