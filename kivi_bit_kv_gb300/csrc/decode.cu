@@ -95,37 +95,37 @@ decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_
         __syncthreads();
         float* out = logits + ((size_t)r.b * Hq + hq0) * ldl;
         auto sink = [&](int h, int t, float s) { out[(size_t)h * ldl + t] = s; };
+        float lmax[2], rmax[NQB];  // unused here
         qk_quantized<BITS, NQB>(c.D, c.G, r.t_begin, r.tq_end, r.t_begin + warp * T::TOK, r.tq_end,
-                                kDecodeWarps * T::TOK, m.kw, m.ks, m.kz, qs, fac, sink);
-        qk_residual<NQB>(c, bh, r.tq_end + warp * rows, kDecodeWarps * rows, r.t_end, qs, fac, sink);
+                                kDecodeWarps * T::TOK, m.kw, m.ks, m.kz, qs, fac, sink, lmax);
+        qk_residual<NQB>(c, bh, r.tq_end + warp * rows, kDecodeWarps * rows, r.t_end, qs, fac, sink, rmax);
         (void)lane;
     }
 }
 
 // ---------------------------------------------------------------- p . V ---
 
-// Softmax statistics, B fragments and the weighted value sum of one pass
-// (p_sm holds the chunk's logits), then the chunk's partials.  Whole CTA.
+// B fragments (with the softmax numerators) and the weighted value sum of
+// one pass: p_sm holds the chunk's logits, mx their per-head maxima; then
+// the chunk's partials.  Whole CTA.
 template <int BITS, int NQB>
 __device__ __forceinline__ void pv_pass(const kivi_cache& c, size_t bh, int TX, const ChunkRange& r,
-                                        const DecodeSmem& m, float* red, size_t row0, int nchunks,
-                                        float* ws_o, float* ws_m, float* ws_l, bool first_pass)
+                                        const DecodeSmem& m, const float (&mx)[NQB], size_t row0,
+                                        int nchunks, float* ws_o, float* ws_m, float* ws_l, bool first_pass)
 {
     const int ps = prob_stride(TX), NGv = c.D >> ilog2(c.G);
     const int n = r.t_end - r.t_begin, nq = r.tq_end - r.t_begin;
-    float mx[NQB], l[NQB];
-    chunk_softmax<NQB>(m.p, ps, n, mx, l, red);
     if (first_pass) {
         cp_async_wait_all();  // the staged values
         __syncthreads();
     }
-    pv_weights<NQB>(n, nq, NGv, threadIdx.x, pv_pairs(n, nq), kDecodeThreads, 0, m.p, ps, m.vs, m.vz,
+    pv_weights<NQB>(n, nq, NGv, threadIdx.x, pv_pairs(n, nq), kDecodeThreads, 0, m.p, ps, mx, m.vs, m.vz,
                     m.bb, bb_stride(TX), m.zs);
     __syncthreads();
     pv_chunk<BITS, NQB>(c, bh, TX, r.t_begin, r.tq_end, r.t_end, m.vw, m.bb, m.part);
     __syncthreads();
-    write_partials<NQB>(c.D, c.G, pv_splits(pv_seg_groups<BITS>(c.D)), m.part, m.zs, mx, l, row0,
-                        nchunks, ws_o, ws_m, ws_l);
+    write_partials<NQB>(c.D, c.G, pv_splits(pv_seg_groups<BITS>(c.D)), m.part, m.zs, mx, row0, nchunks,
+                        ws_o, ws_m, ws_l);
 }
 
 template <int BITS, int NQB>
@@ -149,15 +149,20 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = r.h * NQ + pass * NQB;
         __syncthreads();
+        float mx[NQB];
 #pragma unroll
         for (int h = 0; h < NQB; ++h) {
             const float* lrow = logits + ((size_t)r.b * Hq + hq0 + h) * ldl + r.t_begin;
-            for (int t = threadIdx.x; t < n; t += kDecodeThreads)
-                m.p[h * ps + t] = lrow[t];
+            mx[h] = -INFINITY;
+            for (int t = threadIdx.x; t < n; t += kDecodeThreads) {
+                const float x = lrow[t];
+                m.p[h * ps + t] = x;
+                mx[h] = fmaxf(mx[h], x);
+            }
         }
-        __syncthreads();
-        pv_pass<BITS, NQB>(c, bh, TC + S, r, m, red, ((size_t)r.b * Hq + hq0) * nchunks + r.ci,
-                           nchunks, ws_o, ws_m, ws_l, pass == 0);
+        chunk_max<NQB>(mx, red);
+        pv_pass<BITS, NQB>(c, bh, TC + S, r, m, mx, ((size_t)r.b * Hq + hq0) * nchunks + r.ci, nchunks,
+                           ws_o, ws_m, ws_l, pass == 0);
     }
 }
 
@@ -207,12 +212,24 @@ decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, fl
             cp_async_wait_all();
         __syncthreads();
         auto sink = [&](int h, int t, float s) { m.p[h * ps + t - r.t_begin] = s; };
+        float lmax[2] = {-INFINITY, -INFINITY}, mx[NQB];
+#pragma unroll
+        for (int h = 0; h < NQB; ++h)
+            mx[h] = -INFINITY;
         qk_quantized<BITS, NQB>(c.D, c.G, r.t_begin, r.tq_end, r.t_begin + warp * T::TOK, r.tq_end,
-                                kDecodeWarps * T::TOK, m.kw, m.ks, m.kz, qs, fac, sink);
-        qk_residual<NQB>(c, bh, r.tq_end + warp * rows, kDecodeWarps * rows, r.t_end, qs, fac, sink);
-        __syncthreads();
-        pv_pass<BITS, NQB>(c, bh, TC + S, r, m, red, ((size_t)r.b * Hq + hq0) * nchunks + r.ci,
-                           nchunks, ws_o, ws_m, ws_l, pass == 0);
+                                kDecodeWarps * T::TOK, m.kw, m.ks, m.kz, qs, fac, sink, lmax);
+        qk_residual<NQB>(c, bh, r.tq_end + warp * rows, kDecodeWarps * rows, r.t_end, qs, fac, sink, mx);
+#pragma unroll
+        for (int slot = 0; slot < 2; ++slot) {
+            const int hs = qk_slot_head<BITS, NQB>(slot);
+#pragma unroll
+            for (int h = 0; h < NQB; ++h)
+                if (hs == h)
+                    mx[h] = fmaxf(mx[h], lmax[slot]);
+        }
+        chunk_max<NQB>(mx, red);  // also publishes the logits
+        pv_pass<BITS, NQB>(c, bh, TC + S, r, m, mx, ((size_t)r.b * Hq + hq0) * nchunks + r.ci, nchunks,
+                           ws_o, ws_m, ws_l, pass == 0);
     }
 }
 

@@ -176,9 +176,10 @@ __host__ __device__ constexpr size_t bb_words(int TX, int D, int G, int NQB)
 {
     return 2 * (size_t)(D / G) * NQB * bb_stride(TX);
 }
-// Split partials [4][NQB][D]; per-warp zero terms [4][NQB][D/G].
+// Split partials [4][NQB][D]; per-warp zero terms and exponential sums
+// [4][NQB][D/G + 1] (entry D/G of a row is the sum).
 __host__ __device__ constexpr size_t part_words(int D, int NQB) { return (size_t)kDecodeWarps * NQB * D; }
-__host__ __device__ constexpr size_t zs_words(int D, int G, int NQB) { return (size_t)kDecodeWarps * NQB * (D / G); }
+__host__ __device__ constexpr size_t zs_words(int D, int G, int NQB) { return (size_t)kDecodeWarps * NQB * (D / G + 1); }
 
 // Largest slack S (tokens the last chunk of a sequence may hold beyond TC,
 // so that a short tail does not cost a CTA of its own).  A sequence keeps at
@@ -420,16 +421,29 @@ __device__ __forceinline__ void stage_q(const uint16_t* __restrict__ q, int D, f
     }
 }
 
+// Query head whose logits land in running-maximum slot `slot` of the calling
+// lane in qk_quantized (-1: none).
+template <int BITS, int NQB>
+__device__ __forceinline__ int qk_slot_head(int slot)
+{
+    const int tg = threadIdx.x & 3;
+    if (KeyTile<BITS, NQB>::HL)
+        return slot == 0 ? tg % NQB : -1;
+    return (2 * tg + slot) % NQB;
+}
+
 // Logits of quantized tokens for NQB query heads from the staged keys of the
 // chunk starting at t_begin (zero-filled up to a whole warp tile); the calling
 // warp takes the warp tiles that start at tok_first, tok_first + tok_step, ...
 // below tok_end (<= tq_end, the end of the quantized tokens); sink(h, t, s)
-// receives each logit.
+// receives each logit.  lmax[slot] keeps the running maximum of the logits
+// the lane emits for head qk_slot_head<BITS, NQB>(slot) (two slots; the
+// caller initializes them).
 template <int BITS, int NQB, class Sink>
 __device__ __forceinline__ void qk_quantized(int D, int G, int t_begin, int tq_end, int tok_first,
                                              int tok_end, int tok_step, const uint32_t* kw,
                                              const float* ks, const float* kz, const float* qs,
-                                             const float* fac, Sink sink)
+                                             const float* fac, Sink sink, float (&lmax)[2])
 {
     using T = KeyTile<BITS, NQB>;
     const int qstride = qstride_of(D);
@@ -513,9 +527,11 @@ __device__ __forceinline__ void qk_quantized(int D, int G, int t_begin, int tq_e
                 const float f = fac[h];
 #pragma unroll
                 for (int j = 0; j < T::NT; ++j) {
-                    sink(h, tbase + 2 * j, f * fmaf(code_unscale_bits(T::pa(j)), acc[j][0] + acc[j][1], zc[0]));
-                    sink(h, tbase + 2 * j + 1,
-                         f * fmaf(code_unscale_bits(T::pb(j)), acc[j][2] + acc[j][3], zc[0]));
+                    const float s0 = f * fmaf(code_unscale_bits(T::pa(j)), acc[j][0] + acc[j][1], zc[0]);
+                    const float s1 = f * fmaf(code_unscale_bits(T::pb(j)), acc[j][2] + acc[j][3], zc[0]);
+                    sink(h, tbase + 2 * j, s0);
+                    sink(h, tbase + 2 * j + 1, s1);
+                    lmax[0] = fmaxf(lmax[0], fmaxf(s0, s1));
                 }
             }
         } else {
@@ -528,8 +544,11 @@ __device__ __forceinline__ void qk_quantized(int D, int G, int t_begin, int tq_e
                 const float f = fac[h];
 #pragma unroll
                 for (int j = 0; j < T::NT; ++j) {
-                    sink(h, tbase + 2 * j, f * fmaf(code_unscale_bits(T::pa(j)), acc[j][cc], zc[cc]));
-                    sink(h, tbase + 2 * j + 1, f * fmaf(code_unscale_bits(T::pb(j)), acc[j][2 + cc], zc[cc]));
+                    const float s0 = f * fmaf(code_unscale_bits(T::pa(j)), acc[j][cc], zc[cc]);
+                    const float s1 = f * fmaf(code_unscale_bits(T::pb(j)), acc[j][2 + cc], zc[cc]);
+                    sink(h, tbase + 2 * j, s0);
+                    sink(h, tbase + 2 * j + 1, s1);
+                    lmax[cc] = fmaxf(lmax[cc], fmaxf(s0, s1));
                 }
             }
         }
@@ -541,7 +560,7 @@ __device__ __forceinline__ void qk_quantized(int D, int G, int t_begin, int tq_e
 // takes 32 / (D/32) tokens from base0, then every `step` tokens, below t_end.
 template <int NQB, class Sink>
 __device__ __forceinline__ void qk_residual(const kivi_cache& c, size_t bh, int base0, int step, int t_end,
-                                            const float* qs, const float* fac, Sink sink)
+                                            const float* qs, const float* fac, Sink sink, float (&rmax)[NQB])
 {
     const int D = c.D, RG = c.R + c.G;
     const int qstride = qstride_of(D);
@@ -578,34 +597,31 @@ __device__ __forceinline__ void qk_residual(const kivi_cache& c, size_t bh, int 
                 acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], m);
         if (t < t_end && seg == 0)
 #pragma unroll
-            for (int h = 0; h < NQB; ++h)
-                sink(h, t, fac[h] * acc[h]);
+            for (int h = 0; h < NQB; ++h) {
+                const float sv = fac[h] * acc[h];
+                sink(h, t, sv);
+                rmax[h] = fmaxf(rmax[h], sv);
+            }
     }
 }
 
 // ---------------------------------------------------------------- values ---
 
-// Chunk softmax over p_sm[h][0 .. n) (row stride ps; logits on entry):
-// m_h = max, p = exp(s - m_h) in place, l_h = sum p.  Whole CTA; ends with a
-// barrier that publishes p_sm.
+// Per-head maximum over the CTA of the per-thread maxima m[h] (logits of
+// the chunk); every thread receives the result.  Whole CTA; its barrier also
+// publishes what the threads wrote to shared memory before the call.
 template <int NQB>
-__device__ __forceinline__ void chunk_softmax(float* p_sm, int ps, int n, float (&m)[NQB],
-                                              float (&l)[NQB], float* red)
+__device__ __forceinline__ void chunk_max(float (&m)[NQB], float* red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
 #pragma unroll
     for (int h = 0; h < NQB; ++h) {
-        float mx = -INFINITY;
-        for (int t = threadIdx.x; t < n; t += kDecodeThreads)
-            mx = fmaxf(mx, p_sm[h * ps + t]);
+        float mx = m[h];
         for (int k = 16; k > 0; k >>= 1)
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
-        m[h] = mx;
+        if (lane == 0)
+            red[warp * NQB + h] = mx;
     }
-    if (lane == 0)
-#pragma unroll
-        for (int h = 0; h < NQB; ++h)
-            red[warp * NQB + h] = m[h];
     __syncthreads();
 #pragma unroll
     for (int h = 0; h < NQB; ++h) {
@@ -615,71 +631,51 @@ __device__ __forceinline__ void chunk_softmax(float* p_sm, int ps, int n, float 
             r = fmaxf(r, red[w * NQB + h]);
         m[h] = r;
     }
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < NQB; ++h) {
-        float s = 0.0f;
-        for (int t = threadIdx.x; t < n; t += kDecodeThreads) {
-            const float e = expf(p_sm[h * ps + t] - m[h]);
-            p_sm[h * ps + t] = e;
-            s += e;
-        }
-        for (int k = 16; k > 0; k >>= 1)
-            s += __shfl_xor_sync(0xffffffffu, s, k);
-        l[h] = s;
-    }
-    if (lane == 0)
-#pragma unroll
-        for (int h = 0; h < NQB; ++h)
-            red[warp * NQB + h] = l[h];
-    __syncthreads();
-#pragma unroll
-    for (int h = 0; h < NQB; ++h) {
-        float r = red[h];
-#pragma unroll
-        for (int w = 1; w < kDecodeWarps; ++w)
-            r += red[w * NQB + h];
-        l[h] = r;
-    }
 }
 
-// B fragments of p . V for the chunk: bb row r = g NQB + h, pair i (stored at
-// i ^ bb_swz(r)) holds the (hi, lo) fp16 pairs of tokens 2i, 2i+1 of
+// B fragments of p . V for the chunk, from the logits in p_sm and the chunk
+// maxima mx: p_ht = exp(s_ht - mx_h); bb row r = g NQB + h, pair i (stored
+// at i ^ bb_swz(r)) holds the (hi, lo) fp16 pairs of tokens 2i, 2i+1 of
 // w = p_ht s_tg for quantized tokens (t < nq) and of w = p_ht for residual
 // tokens (nq <= t < n), zero up to the end of the last 16-token slice.
-// zw[warp][h][g] = the warp's share of sum over quantized t of p_ht z_tg.
-// One thread per token pair; whole CTA, the caller's barrier publishes both.
+// zw[warp][h][g] = the warp's share of sum over quantized t of p_ht z_tg,
+// zw[warp][h][NGV] its share of sum over t of p_ht.  One thread per token
+// pair; whole CTA, the caller's barrier publishes both.
 template <int NQB, int NGV>
 __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_end, int i_step, int i_base,
-                                             const float* p_sm, int ps, const float* vs,
-                                             const float* vz, uint2* bb, int bbs, float* zw)
+                                             const float* p_sm, int ps, const float (&mx)[NQB],
+                                             const float* vs, const float* vz, uint2* bb, int bbs, float* zw)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    float z[NQB][NGV];
+    float z[NQB][NGV], l[NQB];
 #pragma unroll
-    for (int h = 0; h < NQB; ++h)
+    for (int h = 0; h < NQB; ++h) {
+        l[h] = 0.0f;
 #pragma unroll
         for (int gg = 0; gg < NGV; ++gg)
             z[h][gg] = 0.0f;
+    }
     for (int i = i_first; i < i_end; i += i_step) {
         const int t = 2 * i;
+        float e0[NQB], e1[NQB];
+#pragma unroll
+        for (int h = 0; h < NQB; ++h) {
+            // p_sm rows are even-strided and t is even; entries past n are not read as weights
+            const float2 sv = *reinterpret_cast<const float2*>(p_sm + h * ps + t);
+            e0[h] = t < n ? expf(sv.x - mx[h]) : 0.0f;
+            e1[h] = t + 1 < n ? expf(sv.y - mx[h]) : 0.0f;
+            l[h] += e0[h] + e1[h];
+        }
         float s0[NGV], s1[NGV];
-        const bool quant = t < nq;  // nq is even: t + 1 is quantized too
-        if (quant) {
-            float z0[NGV], z1[NGV];
+        if (t < nq) {  // nq is even: t + 1 is quantized too
 #pragma unroll
             for (int gg = 0; gg < NGV; ++gg) {
                 s0[gg] = vs[t * NGV + gg];
                 s1[gg] = vs[(t + 1) * NGV + gg];
-                z0[gg] = vz[t * NGV + gg];
-                z1[gg] = vz[(t + 1) * NGV + gg];
-            }
+                const float z0 = vz[t * NGV + gg], z1 = vz[(t + 1) * NGV + gg];
 #pragma unroll
-            for (int h = 0; h < NQB; ++h) {
-                const float2 pp = *reinterpret_cast<const float2*>(p_sm + h * ps + t);
-#pragma unroll
-                for (int gg = 0; gg < NGV; ++gg)
-                    z[h][gg] = fmaf(pp.x, z0[gg], fmaf(pp.y, z1[gg], z[h][gg]));
+                for (int h = 0; h < NQB; ++h)
+                    z[h][gg] = fmaf(e0[h], z0, fmaf(e1[h], z1, z[h][gg]));
             }
         } else {
 #pragma unroll
@@ -687,28 +683,31 @@ __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_e
                 s0[gg] = s1[gg] = 1.0f;
         }
 #pragma unroll
-        for (int h = 0; h < NQB; ++h) {
-            const float p0 = t < n ? p_sm[h * ps + t] : 0.0f;
-            const float p1 = t + 1 < n ? p_sm[h * ps + t + 1] : 0.0f;
+        for (int h = 0; h < NQB; ++h)
 #pragma unroll
             for (int gg = 0; gg < NGV; ++gg) {
                 const int r = gg * NQB + h;
                 uint2 hl;
-                split_hi_lo(p0 * s0[gg], p1 * s1[gg], hl.x, hl.y);
+                split_hi_lo(e0[h] * s0[gg], e1[h] * s1[gg], hl.x, hl.y);
                 bb[r * bbs + ((i - i_base) ^ bb_swz(r))] = hl;
             }
-        }
     }
 #pragma unroll
-    for (int h = 0; h < NQB; ++h)
+    for (int h = 0; h < NQB; ++h) {
 #pragma unroll
         for (int gg = 0; gg < NGV; ++gg) {
             float v = z[h][gg];
             for (int k = 16; k > 0; k >>= 1)
                 v += __shfl_xor_sync(0xffffffffu, v, k);
             if (lane == 0)
-                zw[(warp * NQB + h) * NGV + gg] = v;
+                zw[(warp * NQB + h) * (NGV + 1) + gg] = v;
         }
+        float v = l[h];
+        for (int k = 16; k > 0; k >>= 1)
+            v += __shfl_xor_sync(0xffffffffu, v, k);
+        if (lane == 0)
+            zw[(warp * NQB + h) * (NGV + 1) + NGV] = v;
+    }
 }
 
 // Pairs i_first, i_first + i_step, ... below i_end; bb holds pairs from
@@ -717,14 +716,14 @@ __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_e
 // 16-token slice) get zero weights.
 template <int NQB>
 __device__ __forceinline__ void pv_weights(int n, int nq, int NGv, int i_first, int i_end, int i_step,
-                                           int i_base, const float* p_sm, int ps, const float* vs,
-                                           const float* vz, uint2* bb, int bbs, float* zw)
+                                           int i_base, const float* p_sm, int ps, const float (&mx)[NQB],
+                                           const float* vs, const float* vz, uint2* bb, int bbs, float* zw)
 {
     switch (NGv) {
-    case 1: pv_weights_g<NQB, 1>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, vs, vz, bb, bbs, zw); break;
-    case 2: pv_weights_g<NQB, 2>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, vs, vz, bb, bbs, zw); break;
-    case 4: pv_weights_g<NQB, 4>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, vs, vz, bb, bbs, zw); break;
-    default: pv_weights_g<NQB, 8>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, vs, vz, bb, bbs, zw); break;
+    case 1: pv_weights_g<NQB, 1>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw); break;
+    case 2: pv_weights_g<NQB, 2>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw); break;
+    case 4: pv_weights_g<NQB, 4>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw); break;
+    default: pv_weights_g<NQB, 8>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw); break;
     }
 }
 // Pairs a chunk of n tokens (nq quantized) needs: through the last residual slice.
@@ -942,22 +941,21 @@ __device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TX,
 
 // Writes the chunk's partial (o, m, l) for query heads hq0 .. hq0+NQB-1:
 // o[h][d] = sum over warps of zs[w][h][group of d] + sum over splits of
-// o_part (a fixed order: the result is deterministic).  Whole CTA, after
-// a barrier that follows pv_chunk.
+// o_part, l[h] = sum over warps of zs[w][h][D/G] (fixed orders: the result
+// is deterministic).  Whole CTA, after a barrier that follows pv_chunk.
 template <int NQB>
 __device__ __forceinline__ void write_partials(int D, int G, int nsplit, const float* o_part,
-                                               const float* zs, const float (&m)[NQB],
-                                               const float (&l)[NQB], size_t row0, int nchunks,
-                                               float* ws_o, float* ws_m, float* ws_l)
+                                               const float* zs, const float (&m)[NQB], size_t row0,
+                                               int nchunks, float* ws_o, float* ws_m, float* ws_l)
 {
-    const int lgD = ilog2(D), lgG = ilog2(G), NGv = D >> lgG;
+    const int lgD = ilog2(D), lgG = ilog2(G), NGv = D >> lgG, zr = NQB * (NGv + 1);
     for (int idx = threadIdx.x; idx < NQB * D; idx += kDecodeThreads) {
         const int h = idx >> lgD, d = idx & (D - 1);
-        const int zi = h * NGv + (d >> lgG);
+        const int zi = h * (NGv + 1) + (d >> lgG);
         float s = zs[zi];
 #pragma unroll
         for (int w = 1; w < kDecodeWarps; ++w)
-            s += zs[w * NQB * NGv + zi];
+            s += zs[w * zr + zi];
         for (int sp = 0; sp < nsplit; ++sp)
             s += o_part[(size_t)sp * NQB * D + idx];
         ws_o[(row0 + (size_t)h * nchunks) * D + d] = s;
@@ -965,8 +963,12 @@ __device__ __forceinline__ void write_partials(int D, int G, int nsplit, const f
 #pragma unroll
     for (int h = 0; h < NQB; ++h)
         if (threadIdx.x == h) {
+            float l = zs[h * (NGv + 1) + NGv];
+#pragma unroll
+            for (int w = 1; w < kDecodeWarps; ++w)
+                l += zs[w * zr + h * (NGv + 1) + NGv];
             ws_m[row0 + (size_t)h * nchunks] = m[h];
-            ws_l[row0 + (size_t)h * nchunks] = l[h];
+            ws_l[row0 + (size_t)h * nchunks] = l;
         }
 }
 
