@@ -282,6 +282,11 @@ __host__ __device__ inline ChunkPlan decode_chunk_plan(int D, int bits_k, int bi
     return {tc_min, 0, 1};
 }
 
+inline ChunkPlan chunk_plan(const kivi_cache& c, int Hq)
+{
+    return decode_chunk_plan(c.D, c.bits_k, c.bits_v, c.G, c.R, Hq / c.H);
+}
+
 // ------------------------------------------------------------- staging ---
 
 // Physical 16-byte chunk of logical chunk x in key row r (word-row or
@@ -307,18 +312,18 @@ __device__ __forceinline__ int val_swz(int t, int s, int NSEG)
 // thread's 16-byte chunks are kDecodeThreads apart, i.e. a fixed column of
 // every (kDecodeThreads / chunks-per-row)-th row, so its swizzled column is
 // fixed (the row step is even) and the loops only advance pointers.
-template <int BITS, int TOK>
+template <int BITS, int TOK, int D>
 __device__ __forceinline__ void stage_keys(const kivi_cache& c, size_t bh, int t_begin, int tq_end,
                                            uint32_t* kw, float* ks, float* kz)
 {
     constexpr int P = 32 / BITS;
-    const int D = c.D, lgG = ilog2(c.G);
-    const int lg = ilog2(D / 4);                    // 16-byte chunks per row: D / 4
-    const int step = kDecodeThreads >> lg;          // rows per sweep (even)
+    const int lgG = ilog2(c.G);
+    constexpr int lg = ilog2(D / 4);                // 16-byte chunks per row: D / 4
+    constexpr int step = kDecodeThreads >> lg;      // rows per sweep (even)
     const int x = threadIdx.x & (D / 4 - 1), r0 = threadIdx.x >> lg;
     const int xs = key_swz(r0, x);
     const int n = tq_end - t_begin, npad = (n + TOK - 1) / TOK * TOK;
-    const size_t adv = (size_t)step * D;            // words per sweep
+    constexpr size_t adv = (size_t)step * D;        // words per sweep
     {
         const int nw = n / P, nwp = npad / P;
         const int32_t* src = c.kq + (bh * (size_t)(c.Tmax / P) + t_begin / P) * D + (size_t)r0 * D + 4 * x;
@@ -352,17 +357,17 @@ __device__ __forceinline__ void stage_keys(const kivi_cache& c, size_t bh, int t
 // cp.async copies of the chunk's quantized values [t_begin, tq_end): token
 // rows into vw (val_swz layout), statistics into vs / vz [t - t_begin][D/G].
 // As for the keys, a thread's segment (and its swizzled place) is fixed.
-template <int BITS>
+template <int BITS, int D>
 __device__ __forceinline__ void stage_values(const kivi_cache& c, size_t bh, int t_begin, int tq_end,
                                              uint32_t* vw, float* vs, float* vz)
 {
-    constexpr int P = 32 / BITS;
-    const int D = c.D, DW = D / P, NSEG = DW / 4, NGv = D >> ilog2(c.G);
-    const int lg = ilog2(NSEG);
+    constexpr int P = 32 / BITS, DW = D / P, NSEG = DW / 4;
+    const int NGv = D >> ilog2(c.G);
+    constexpr int lg = ilog2(NSEG);
     const int n = tq_end - t_begin;
     const int seg = threadIdx.x & (NSEG - 1), t0 = threadIdx.x >> lg;
-    const int step = kDecodeThreads >> lg;          // tokens per sweep (a multiple of 8)
-    const size_t adv = (size_t)kDecodeThreads * 4;  // words per sweep
+    constexpr int step = kDecodeThreads >> lg;      // tokens per sweep (a multiple of 8)
+    constexpr size_t adv = (size_t)kDecodeThreads * 4;  // words per sweep
     {
         const int32_t* src = c.vq + (bh * (size_t)c.Tmax + t_begin) * DW + (size_t)threadIdx.x * 4;
         uint32_t* dst = vw + (size_t)t0 * DW + val_swz(t0, seg, NSEG) * 4;
@@ -395,12 +400,11 @@ __device__ __forceinline__ int qpad(int d) { return d + ((d >> 4) << 2); }
 // Stages query heads hq0 .. hq0+NQB-1 of sequence b: qs[h][qpad(d)] = q 2^-e_h
 // with 2^-e_h the power of two that brings max_d |q| into [1/2, 1), and
 // fac[h] = sm_scale 2^e_h.  Called by the whole CTA between barriers.
-template <int NQB>
-__device__ __forceinline__ void stage_q(const uint16_t* __restrict__ q, int D, float sm_scale,
-                                        float* qs, float* fac)
+template <int NQB, int D>
+__device__ __forceinline__ void stage_q(const uint16_t* __restrict__ q, float sm_scale, float* qs, float* fac)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int qstride = qstride_of(D);
+    constexpr int qstride = qstride_of(D);
     for (int h = warp; h < NQB; h += kDecodeWarps) {
         const uint16_t* row = q + (size_t)h * D;
         float mx = 0.0f;
@@ -439,15 +443,15 @@ __device__ __forceinline__ int qk_slot_head(int slot)
 // receives each logit.  lmax[slot] keeps the running maximum of the logits
 // the lane emits for head qk_slot_head<BITS, NQB>(slot) (two slots; the
 // caller initializes them).
-template <int BITS, int NQB, class Sink>
-__device__ __forceinline__ void qk_quantized(int D, int G, int t_begin, int tq_end, int tok_first,
+template <int BITS, int NQB, int D, class Sink>
+__device__ __forceinline__ void qk_quantized(int G, int t_begin, int tq_end, int tok_first,
                                              int tok_end, int tok_step, const uint32_t* kw,
                                              const float* ks, const float* kz, const float* qs,
                                              const float* fac, Sink sink, float (&lmax)[2])
 {
     using T = KeyTile<BITS, NQB>;
-    const int qstride = qstride_of(D);
-    const int cpr = D / 4;  // 16-byte chunks per staged row
+    constexpr int qstride = qstride_of(D);
+    constexpr int cpr = D / 4;  // 16-byte chunks per staged row
     const int lgG = ilog2(G);
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tg = lane & 3;
@@ -558,13 +562,13 @@ __device__ __forceinline__ void qk_quantized(int D, int G, int t_begin, int tq_e
 // Logits of fp16 residual tokens (read from the ring in global memory): D/32
 // lanes per token, each a 32-channel segment, fp32 FMA; the calling warp
 // takes 32 / (D/32) tokens from base0, then every `step` tokens, below t_end.
-template <int NQB, class Sink>
+template <int NQB, int D, class Sink>
 __device__ __forceinline__ void qk_residual(const kivi_cache& c, size_t bh, int base0, int step, int t_end,
                                             const float* qs, const float* fac, Sink sink, float (&rmax)[NQB])
 {
-    const int D = c.D, RG = c.R + c.G;
-    const int qstride = qstride_of(D);
-    const int LPR = D / 32;
+    const int RG = c.R + c.G;
+    constexpr int qstride = qstride_of(D);
+    constexpr int LPR = D / 32;
     const int lane = threadIdx.x & 31;
     const int seg = lane % LPR;
     for (int base = base0; base < t_end; base += step) {
@@ -744,16 +748,16 @@ __host__ __device__ constexpr int pv_seg_groups(int D) { return D / (32 / BITS) 
 // below kr_end (tokens tq_end + 16 kr ...) from the fp16 ring with the raw
 // values as A.  Writes o_out[h][d] (no zero terms) for the segment group's
 // channels, each entry by exactly one lane.
-template <int BITS, int NQB>
+template <int BITS, int NQB, int D>
 __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_begin, int tq_end,
                                         int t_end, const uint32_t* vw, const uint2* bb, int bbs,
                                         int i_base, int sp, int kq, int kq_end, int kr, int kr_end,
                                         int kstep, float* o_out)
 {
     using T = ValTile<BITS>;
-    const int D = c.D, G = c.G, lgG = ilog2(G), RG = c.R + c.G;
-    const int DW = D / T::P, NSEG = DW / 4;
-    const int SPL = pv_segs_per_load<BITS>(D);  // segments per ldmatrix (x4: 2, x2: 1)
+    const int G = c.G, lgG = ilog2(G), RG = c.R + c.G;
+    constexpr int DW = D / T::P, NSEG = DW / 4;
+    constexpr int SPL = pv_segs_per_load<BITS>(D);  // segments per ldmatrix (x4: 2, x2: 1)
     const int NGS = cmax(1, T::CS >> lgG);      // groups per segment (1 or 2)
     // hi and lo weights as separate B columns when the (group, head) units
     // take at most four: B column g is unit g / 2, part g & 1
@@ -923,19 +927,19 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
 // p . V_hat of the whole chunk by the CTA: each warp takes units (segment
 // group, token split) and writes o_part[split] (splits of one segment group
 // are different warps).
-template <int BITS, int NQB>
+template <int BITS, int NQB, int D>
 __device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TX, int t_begin,
                                          int tq_end, int t_end, const uint32_t* vw, const uint2* bb,
                                          float* o_part)
 {
-    const int NSP = pv_seg_groups<BITS>(c.D);
-    const int NSPLIT = pv_splits(NSP);
+    constexpr int NSP = pv_seg_groups<BITS>(D);
+    constexpr int NSPLIT = pv_splits(NSP);
     const int nq_slices = (tq_end - t_begin) / 16;
     const int nr_slices = (t_end - tq_end + 15) / 16;
     for (int unit = threadIdx.x >> 5; unit < NSP * NSPLIT; unit += kDecodeWarps) {
         const int sp = unit % NSP, split = unit / NSP;
-        pv_unit<BITS, NQB>(c, bh, t_begin, tq_end, t_end, vw, bb, bb_stride(TX), 0, sp, split, nq_slices,
-                           split, nr_slices, NSPLIT, o_part + (size_t)split * NQB * c.D);
+        pv_unit<BITS, NQB, D>(c, bh, t_begin, tq_end, t_end, vw, bb, bb_stride(TX), 0, sp, split, nq_slices,
+                              split, nr_slices, NSPLIT, o_part + (size_t)split * NQB * D);
     }
 }
 
@@ -943,12 +947,13 @@ __device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TX,
 // o[h][d] = sum over warps of zs[w][h][group of d] + sum over splits of
 // o_part, l[h] = sum over warps of zs[w][h][D/G] (fixed orders: the result
 // is deterministic).  Whole CTA, after a barrier that follows pv_chunk.
-template <int NQB>
-__device__ __forceinline__ void write_partials(int D, int G, int nsplit, const float* o_part,
+template <int NQB, int D>
+__device__ __forceinline__ void write_partials(int G, int nsplit, const float* o_part,
                                                const float* zs, const float (&m)[NQB], size_t row0,
                                                int nchunks, float* ws_o, float* ws_m, float* ws_l)
 {
-    const int lgD = ilog2(D), lgG = ilog2(G), NGv = D >> lgG, zr = NQB * (NGv + 1);
+    constexpr int lgD = ilog2(D);
+    const int lgG = ilog2(G), NGv = D >> lgG, zr = NQB * (NGv + 1);
     for (int idx = threadIdx.x; idx < NQB * D; idx += kDecodeThreads) {
         const int h = idx >> lgD, d = idx & (D - 1);
         const int zi = h * (NGv + 1) + (d >> lgG);

@@ -38,6 +38,18 @@ cudaError_t launch_decode_attention(const kivi_cache& c, const uint16_t* q, int 
                                     float* out, float* ws_o, float* ws_m, float* ws_l,
                                     cudaStream_t s);
 
+// The decode kernels of one head dimension D (64, 128, 256), without the
+// combine step; instantiated in decode_d<D>.cu.
+template <int D>
+cudaError_t launch_decode_qk_d(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale, float* logits,
+                               int ld_logits, cudaStream_t s);
+template <int D>
+cudaError_t launch_decode_pv_d(const kivi_cache& c, const float* logits, int ld_logits, int Hq, float* ws_o,
+                               float* ws_m, float* ws_l, cudaStream_t s);
+template <int D>
+cudaError_t launch_decode_attention_d(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale,
+                                      float* ws_o, float* ws_m, float* ws_l, cudaStream_t s);
+
 // Sets the message kivi_last_error() returns on this host thread; returns status.
 int32_t record_error(int32_t status, const char* message);
 
