@@ -29,6 +29,28 @@ __device__ __forceinline__ void flush_values(const kivi_cache& c, size_t bh, int
     }
 }
 
+// Keys of a flushed group: one G-token group per channel, lanes (s, j) with s
+// fastest (S = G/16 lanes per channel column).
+template <int BK, int S>
+__device__ __forceinline__ void flush_keys(const kivi_cache& c, size_t bh, int Tq)
+{
+    const int D = c.D, RG = c.R + c.G, NC = D / kLaneChans;
+    const int lane = threadIdx.x & 31;
+    const unsigned smask = (((1u << S) - 1u) << (lane & ~(S - 1)));
+    for (int task = threadIdx.x; task < S * NC; task += blockDim.x) {
+        const int s = task % S, j = task / S;
+        const int t0 = Tq + s * kLaneTokens;
+        uint4 raw[kLaneTokens];
+#pragma unroll
+        for (int i = 0; i < kLaneTokens; ++i)
+            raw[i] = *reinterpret_cast<const uint4*>(c.kres + (bh * RG + (t0 + i) % RG) * D +
+                                                      (size_t)j * kLaneChans);
+        // RG and t0 are multiples of 16: the lane's 16 ring rows never wrap
+        quant_store_key_lane<BK, S>(c, bh, t0, Tq / c.G, j, s, smask, raw,
+                                    c.kres + (bh * RG + t0 % RG) * D + (size_t)j * kLaneChans, D);
+    }
+}
+
 template <int BK, int BV>
 __global__ void __launch_bounds__(128)
 append_kernel(kivi_cache c, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
@@ -55,29 +77,20 @@ append_kernel(kivi_cache c, const uint16_t* __restrict__ k, const uint16_t* __re
         return;  // uniform over the CTA
     __syncthreads();  // the new token is visible to every thread of the CTA
 
-    const int lane = threadIdx.x & 31;
-    // keys: one G-token group per channel, lanes (s, j) with s fastest
-    {
-        const int S = G / kLaneTokens, NC = D / kLaneChans;
-        const unsigned smask = (((1u << S) - 1u) << (lane & ~(S - 1)));
-        for (int task = threadIdx.x; task < S * NC; task += blockDim.x) {
-            const int s = task % S, j = task / S;
-            const int t0 = Tq + s * kLaneTokens;
-            uint4 raw[kLaneTokens];
-#pragma unroll
-            for (int i = 0; i < kLaneTokens; ++i)
-                raw[i] = *reinterpret_cast<const uint4*>(
-                    c.kres + (bh * RG + (t0 + i) % RG) * D + (size_t)j * kLaneChans);
-            // RG and t0 are multiples of 16: the lane's 16 ring rows never wrap
-            quant_store_key_lane<BK>(c, bh, t0, Tq / G, j, s, S, smask, raw,
-                                     c.kres + (bh * RG + t0 % RG) * D + (size_t)j * kLaneChans, D);
-        }
-    }
-    // values: G token rows x D/G channel groups, one lane per group
+    // keys, then values: G token rows x D/G channel groups, one lane per group
     switch (G) {
-    case 32: flush_values<BV, 32>(c, bh, Tq); break;
-    case 64: flush_values<BV, 64>(c, bh, Tq); break;
-    default: flush_values<BV, 128>(c, bh, Tq); break;
+    case 32:
+        flush_keys<BK, 2>(c, bh, Tq);
+        flush_values<BV, 32>(c, bh, Tq);
+        break;
+    case 64:
+        flush_keys<BK, 4>(c, bh, Tq);
+        flush_values<BV, 64>(c, bh, Tq);
+        break;
+    default:
+        flush_keys<BK, 8>(c, bh, Tq);
+        flush_values<BV, 128>(c, bh, Tq);
+        break;
     }
 }
 

@@ -11,6 +11,7 @@
 #include <stdint.h>
 
 #include "kivi.h"
+#include "kivi_divm.h"
 
 namespace kivi {
 
@@ -100,6 +101,15 @@ __device__ __forceinline__ float add_h_f(uint16_t xh, float c)
     return r;
 }
 
+// RN(x / M) for a group range x (kivi_divm.h): one FMUL and one FFMA.  An
+// infinite range (non-finite input) keeps the IEEE quotient, infinity.
+template <int BITS>
+__device__ __forceinline__ float div_code_range(float x)
+{
+    const float q = __fmaf_rn(x, DivM<BITS>::hi, __fmul_rn(x, DivM<BITS>::lo));
+    return isinf(x) ? x : q;
+}
+
 // Group statistics from canonical fp32 min / max.
 template <int BITS>
 __device__ __forceinline__ void group_stats(float mn, float mx, float& scale,
@@ -107,8 +117,47 @@ __device__ __forceinline__ void group_stats(float mn, float mx, float& scale,
 {
     zero = __fadd_rn(mn, 0.0f);  // -0 -> +0
     mx = __fadd_rn(mx, 0.0f);
-    scale = __fdiv_rn(__fsub_rn(mx, zero), (float)Codec<BITS>::M);
+    scale = div_code_range<BITS>(__fsub_rn(mx, zero));
     inv = scale != 0.0f ? __frcp_rn(scale) : 0.0f;
+}
+
+// Scales, zeros and reciprocals of the eight channels of a key lane from the
+// min / max its tile column shares (mn, mx: channel pairs).  Lane s of the
+// column's S lanes computes channels k = S kk + s, 8/S of them with the same
+// instructions on every lane, and the lanes exchange the results.
+template <int BITS, int S>
+__device__ __forceinline__ void key_lane_stats(const __half2 (&mn)[4], const __half2 (&mx)[4], unsigned mask,
+                                               float (&scale)[8], float (&zero)[8], float (&inv)[8])
+{
+    const int lane = (int)(threadIdx.x & 31), s = lane & (S - 1), base = lane & ~(S - 1);
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+        zero[k] = __fadd_rn((k & 1) ? __high2float(mn[k >> 1]) : __low2float(mn[k >> 1]), 0.0f);
+    constexpr int NK = 8 / S;
+    float sc[NK], iv[NK];
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk) {
+        // channel k = S kk + s: pair (S kk) / 2 + s / 2, half s & 1 (S is even)
+        const int w = (S * kk) / 2 + (s >> 1);
+        __half2 a = mn[0], b = mx[0];
+#pragma unroll
+        for (int w2 = 1; w2 < 4; ++w2)
+            if (w == w2) {
+                a = mn[w2];
+                b = mx[w2];
+            }
+        const float lo = (s & 1) ? __high2float(a) : __low2float(a);
+        const float hi = (s & 1) ? __high2float(b) : __low2float(b);
+        float z;
+        group_stats<BITS>(lo, hi, sc[kk], z, iv[kk]);
+    }
+#pragma unroll
+    for (int kk = 0; kk < NK; ++kk)
+#pragma unroll
+        for (int s2 = 0; s2 < S; ++s2) {
+            scale[S * kk + s2] = __shfl_sync(mask, sc[kk], base + s2);
+            inv[S * kk + s2] = __shfl_sync(mask, iv[kk], base + s2);
+        }
 }
 
 // Exact code: round-half-even of the IEEE quotient a / scale (scale > 0).
@@ -190,8 +239,8 @@ __device__ __forceinline__ uint32_t dequant_h2(float f0, float f1, float s0, flo
 // aligned in the warp; `mask` names exactly them.  Produces the group's
 // per-channel scale/zero (identical on all S lanes) and this lane's packed
 // words: words[w][k] = word-row w (of Codec::kWordRows), channel k.
-template <int BITS>
-__device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens], int S,
+template <int BITS, int S>
+__device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens],
                                                unsigned mask, float (&scale)[8],
                                                float (&zero)[8], float (&inv)[8],
                                                uint32_t (&words)[Codec<BITS>::kWordRows][8],
@@ -210,37 +259,19 @@ __device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens], 
             mn[c] = __hmin2(mn[c], v);
             mx[c] = __hmax2(mx[c], v);
         }
+#pragma unroll
     for (int m = 1; m < S; m <<= 1)
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
             mn[c] = __hmin2(mn[c], as_h2(__shfl_xor_sync(mask, h2_bits(mn[c]), m)));
             mx[c] = __hmax2(mx[c], as_h2(__shfl_xor_sync(mask, h2_bits(mx[c]), m)));
         }
-    // Every lane of the tile column now holds the same min / max.  The S lanes
-    // split the eight divisions (lane s takes channels k with k % S == s) and
-    // exchange the results.
+    // every lane of the tile column now holds the same min / max
+    key_lane_stats<BITS, S>(mn, mx, mask, scale, zero, inv);
     float nzero[8];
-    const int s_lane = (int)(threadIdx.x & 31) & (S - 1);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float lo = (k & 1) ? __high2float(mn[k >> 1]) : __low2float(mn[k >> 1]);
-        const float hi = (k & 1) ? __high2float(mx[k >> 1]) : __low2float(mx[k >> 1]);
-        zero[k] = __fadd_rn(lo, 0.0f);
+    for (int k = 0; k < 8; ++k)
         nzero[k] = -zero[k];
-        scale[k] = 0.0f;
-        inv[k] = 0.0f;
-        if ((k & (S - 1)) == s_lane)  // S is a power of two <= 8
-            group_stats<BITS>(lo, hi, scale[k], zero[k], inv[k]);
-    }
-    if (S > 1) {
-        const int base = (int)(threadIdx.x & 31) & ~(S - 1);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int src = base + (k & (S - 1));
-            scale[k] = __shfl_sync(mask, scale[k], src);
-            inv[k] = __shfl_sync(mask, inv[k], src);
-        }
-    }
     // Pack t_bits * 2^sh (IMAD) and remove the constant bias once per word:
     // sum_i (bias + c_i) 2^(b i) - bias * sum_i 2^(b i) = sum_i c_i 2^(b i) (mod 2^32).
     constexpr uint32_t kWordBias = kCodeBias * (uint32_t)(((1ull << (Cd::P * BITS)) - 1) /
@@ -353,9 +384,9 @@ __device__ __forceinline__ void quant_value_group(const uint4 (&raw)[G / 8], flo
 // loaded by the caller) of slice bh, group g, and store its words and -- on
 // the first lane of the tile column (s == 0) -- the group statistics.  The S
 // lanes of the tile column (`smask`) must call this together.
-template <int BITS>
+template <int BITS, int S>
 __device__ __forceinline__ void quant_store_key_lane(const kivi_cache& c, size_t bh, int t0,
-                                                     int g, int j, int s, int S, unsigned smask,
+                                                     int g, int j, int s, unsigned smask,
                                                      const uint4 (&raw)[kLaneTokens],
                                                      const uint16_t* row0, size_t row_stride)
 {
@@ -364,7 +395,7 @@ __device__ __forceinline__ void quant_store_key_lane(const kivi_cache& c, size_t
     float scale[8], zero[8], inv[8];
     uint32_t words[Cd::kWordRows][8];
     unsigned flagged;
-    quant_key_lane<BITS>(raw, S, smask, scale, zero, inv, words, flagged);
+    quant_key_lane<BITS, S>(raw, smask, scale, zero, inv, words, flagged);
     if (__builtin_expect(flagged != 0u, 0))
         key_lane_fixup<BITS>(flagged, row0, row_stride, scale, inv, zero, words);
     int32_t* dst = c.kq + (bh * (size_t)(c.Tmax / Cd::P) + t0 / Cd::P) * D + (size_t)j * kLaneChans;

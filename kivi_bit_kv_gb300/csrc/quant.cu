@@ -25,13 +25,13 @@ __device__ __forceinline__ int log2_pow2(int x) { return __ffs(x) - 1; }
 // Keys.  One lane = 16 tokens x 8 channels of a (b, h, G-token group) tile;
 // the G/16 lanes of a tile column are adjacent.  A CTA covers 256 / (S*NC)
 // groups of one slice.  Tiles past Tq copy their tokens into the ring.
-template <int BITS>
+template <int BITS, int S>
 __global__ void __launch_bounds__(kEncodeThreads)
 quant_keys_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
                   const int32_t* __restrict__ seq_lens)
 {
     const int D = c.D;
-    const int S = c.G / kLaneTokens, lgS = log2_pow2(S);
+    constexpr int lgS = S == 2 ? 1 : S == 4 ? 2 : 3;
     const int NC = D / kLaneChans, lgNC = log2_pow2(NC);
     const int lane = threadIdx.x & 31;
     const unsigned smask = (((1u << S) - 1u) << (lane & ~(S - 1)));
@@ -55,7 +55,7 @@ quant_keys_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
 #pragma unroll
             for (int i = 0; i < kLaneTokens; ++i)
                 raw[i] = ld_stream(src + (size_t)(t0 + i) * D);
-            quant_store_key_lane<BITS>(c, bh, t0, g, j, s, S, smask, raw, src + (size_t)t0 * D, D);
+            quant_store_key_lane<BITS, S>(c, bh, t0, g, j, s, smask, raw, src + (size_t)t0 * D, D);
         } else {
             for (int i = 0; i < kLaneTokens; ++i) {
                 const int t = t0 + i;
@@ -87,9 +87,9 @@ __device__ __forceinline__ int key_stage_swz(int r, int x, int lgS)
 // shared memory at lrow[i * stride], i = 0..15: statistics as in
 // quant_key_lane, then the codes in short unrolled runs of four tokens, each
 // word-row stored (after its near-tie fix-up) as soon as it is complete.
-template <int BITS>
+template <int BITS, int S>
 __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, size_t bh, int t0, int g,
-                                                          int j, int s, int S, unsigned smask,
+                                                          int j, int s, unsigned smask,
                                                           const uint4* lrow, int stride)
 {
     using Cd = Codec<BITS>;
@@ -111,6 +111,7 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
             mx[k] = __hmax2(mx[k], v);
         }
     }
+#pragma unroll
     for (int m = 1; m < S; m <<= 1)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -118,27 +119,10 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
             mx[k] = __hmax2(mx[k], as_h2(__shfl_xor_sync(smask, h2_bits(mx[k]), m)));
         }
     float scale[8], zero[8], inv[8], nzero[8];
-    const int s_lane = (int)(threadIdx.x & 31) & (S - 1);
+    key_lane_stats<BITS, S>(mn, mx, smask, scale, zero, inv);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float lo = (k & 1) ? __high2float(mn[k >> 1]) : __low2float(mn[k >> 1]);
-        const float hi = (k & 1) ? __high2float(mx[k >> 1]) : __low2float(mx[k >> 1]);
-        zero[k] = __fadd_rn(lo, 0.0f);
+    for (int k = 0; k < 8; ++k)
         nzero[k] = -zero[k];
-        scale[k] = 0.0f;
-        inv[k] = 0.0f;
-        if ((k & (S - 1)) == s_lane)  // the S lanes of the column split the divisions
-            group_stats<BITS>(lo, hi, scale[k], zero[k], inv[k]);
-    }
-    if (S > 1) {
-        const int base = (int)(threadIdx.x & 31) & ~(S - 1);
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const int src = base + (k & (S - 1));
-            scale[k] = __shfl_sync(smask, scale[k], src);
-            inv[k] = __shfl_sync(smask, inv[k], src);
-        }
-    }
     if (s == 0) {
         const size_t so = (bh * (size_t)(c.Tmax / c.G) + g) * D + (size_t)j * kLaneChans;
         float4* sp = reinterpret_cast<float4*>(c.kscale + so);
@@ -196,14 +180,14 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
     }
 }
 
-template <int BITS>
+template <int BITS, int S>
 __global__ void __launch_bounds__(kKeyStageThreads, 3)
 quant_keys_staged_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
                          const int32_t* __restrict__ seq_lens, int tiles_per_seq)
 {
     extern __shared__ __align__(16) uint4 kst[];  // two buffers of kKeyStageBytes
     const int D = c.D;
-    const int S = c.G / kLaneTokens, lgS = log2_pow2(S);
+    constexpr int lgS = S == 2 ? 1 : S == 4 ? 2 : 3;
     const int NC = D / kLaneChans, lgNC = log2_pow2(NC);
     const int TT = (kKeyStageBytes / 2) / D;       // tokens per tile
     const int lane = threadIdx.x & 31;
@@ -257,7 +241,7 @@ quant_keys_staged_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
             // the lane's 16 rows share one swizzled column (r / 16 is fixed)
             const uint4* lrow = buf + lr * cpr + key_stage_swz(lr, j, lgS);
             if ((g + 1) * c.G <= Tq) {
-                quant_store_key_lane_smem<BITS>(c, bh, t0, g, j, s, S, smask, lrow, cpr);
+                quant_store_key_lane_smem<BITS, S>(c, bh, t0, g, j, s, smask, lrow, cpr);
             } else {
                 for (int i = 0; i < kLaneTokens; ++i) {
                     const int t = t0 + i;
@@ -275,7 +259,7 @@ quant_keys_staged_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
 // min/max, the division and the packing stay inside the lane.  A CTA covers
 // 256 / (D/G) * U rows of one slice.
 template <int BITS, int G>
-__global__ void __launch_bounds__(kEncodeThreads)
+__global__ void __launch_bounds__(kEncodeThreads, G == 128 ? 2 : 3)
 quant_values_kernel(kivi_cache c, const uint16_t* __restrict__ V, int T,
                     const int32_t* __restrict__ seq_lens)
 {
@@ -333,38 +317,46 @@ static dim3 encode_grid(const kivi_cache& c, int tiles)
     return dim3((unsigned)(tiles > 0 ? tiles : 1), (unsigned)(bh < 65535 ? bh : 65535));
 }
 
-cudaError_t launch_quant_keys(const kivi_cache& c, const uint16_t* K, int T,
-                              const int32_t* seq_lens, cudaStream_t s)
+template <int BITS, int S>
+static void key_launch(const kivi_cache& c, const uint16_t* K, int T, const int32_t* seq_lens, cudaStream_t s)
 {
-    const int lanes_per_group = (c.G / kLaneTokens) * (c.D / kLaneChans);
-    if (T > 0 && lanes_per_group <= kKeyStageThreads) {
+    const int lanes_per_group = S * (c.D / kLaneChans);
+    if (lanes_per_group <= kKeyStageThreads) {
         const int TT = (kKeyStageBytes / 2) / c.D;
         const int tiles_per_seq = (T + TT - 1) / TT;
         const long ntiles = (long)c.B * c.H * tiles_per_seq;
         const int grid = (int)std::min<long>(ntiles, (long)sm_count() * 3);
         const size_t smem = 2 * kKeyStageBytes;
-        switch (c.bits_k) {
-        case 2:
-            cudaFuncSetAttribute(quant_keys_staged_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            quant_keys_staged_kernel<2><<<grid, kKeyStageThreads, smem, s>>>(c, K, T, seq_lens, tiles_per_seq);
-            break;
-        case 4:
-            cudaFuncSetAttribute(quant_keys_staged_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            quant_keys_staged_kernel<4><<<grid, kKeyStageThreads, smem, s>>>(c, K, T, seq_lens, tiles_per_seq);
-            break;
-        default:
-            cudaFuncSetAttribute(quant_keys_staged_kernel<8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            quant_keys_staged_kernel<8><<<grid, kKeyStageThreads, smem, s>>>(c, K, T, seq_lens, tiles_per_seq);
-            break;
-        }
-    } else if (T > 0) {
+        cudaFuncSetAttribute(quant_keys_staged_kernel<BITS, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+        quant_keys_staged_kernel<BITS, S><<<grid, kKeyStageThreads, smem, s>>>(c, K, T, seq_lens, tiles_per_seq);
+    } else {
         const int groups_per_cta = kEncodeThreads / lanes_per_group;
         const int groups = (T + c.G - 1) / c.G;
         const dim3 grid = encode_grid(c, (groups + groups_per_cta - 1) / groups_per_cta);
+        quant_keys_kernel<BITS, S><<<grid, kEncodeThreads, 0, s>>>(c, K, T, seq_lens);
+    }
+}
+
+template <int BITS>
+static void key_launch_bits(const kivi_cache& c, const uint16_t* K, int T, const int32_t* seq_lens,
+                            cudaStream_t s)
+{
+    switch (c.G / kLaneTokens) {  // S lanes per group column
+    case 2: key_launch<BITS, 2>(c, K, T, seq_lens, s); break;
+    case 4: key_launch<BITS, 4>(c, K, T, seq_lens, s); break;
+    default: key_launch<BITS, 8>(c, K, T, seq_lens, s); break;
+    }
+}
+
+cudaError_t launch_quant_keys(const kivi_cache& c, const uint16_t* K, int T,
+                              const int32_t* seq_lens, cudaStream_t s)
+{
+    if (T > 0) {
         switch (c.bits_k) {
-        case 2: quant_keys_kernel<2><<<grid, kEncodeThreads, 0, s>>>(c, K, T, seq_lens); break;
-        case 4: quant_keys_kernel<4><<<grid, kEncodeThreads, 0, s>>>(c, K, T, seq_lens); break;
-        default: quant_keys_kernel<8><<<grid, kEncodeThreads, 0, s>>>(c, K, T, seq_lens); break;
+        case 2: key_launch_bits<2>(c, K, T, seq_lens, s); break;
+        case 4: key_launch_bits<4>(c, K, T, seq_lens, s); break;
+        default: key_launch_bits<8>(c, K, T, seq_lens, s); break;
         }
     } else {
         set_len_kernel<<<(c.B + 127) / 128, 128, 0, s>>>(c.len, c.B, T, seq_lens);
