@@ -213,7 +213,7 @@ int32_t kivi_decode_pv(const kivi_cache* c, const float* logits,
 /*
  * Decode attention in one pass over the cache: the logits of kivi_decode_qk,
  * the softmax and the weighted sum of kivi_decode_pv, fused per (KV head,
- * 1024-token chunk) so that the logits stay on chip:
+ * chunk of up to 1024 tokens) so that the logits stay on chip:
  *   out[b][hq][d] = sum_t softmax_t(sm_scale q . K_hat_t) V_hat[t][d]
  * over t < len[b] (CacheSeek PR #4: decode from the quantized KV).  q: fp16
  * [B][Hq][D]; out: fp32 [B][Hq][D]; ws as for kivi_decode_pv (>=
@@ -256,6 +256,76 @@ size_t kivi_workspace_bytes(const kivi_cache* c, int32_t Hq);
 int32_t kivi_decode_pv_noalloc(const kivi_cache* c, const float* logits,
                                int32_t ld_logits, int32_t Hq, float* out,
                                void* stream);
+
+/* ------------------------------------------------ compact payload (store) */
+
+/*
+ * The exact-prefix store of CacheSeek PR #4 keeps a quantized layer as a
+ * compact payload -- "qdata/scale/offset are moved back to CPU before being
+ * stored" -- and mixes a "quant fingerprint" into the prefix root hash, so a
+ * quantized entry never matches one stored under another codec.  These calls
+ * move a cache's payload between the device and caller-owned memory (pinned
+ * host memory: the copy kernels read and write it directly, over NVLink-C2C
+ * on a Grace-Blackwell node) in this format, all little-endian:
+ *
+ *   header, 64 bytes:
+ *     uint32 magic   KIVI_PAYLOAD_MAGIC ("KIVP")
+ *     uint32 format  KIVI_PAYLOAD_VERSION
+ *     uint64 kivi_codec_fingerprint(c)
+ *     int32  B, H, D, bits_k, bits_v, G, R;  int32 reserved[5] = 0
+ *   int32 len[B], zero-padded to a multiple of 4 entries
+ *   then for b = 0..B-1, h = 0..H-1 (n = len[b], Tq = Tq(n), res = n - Tq):
+ *     kq rows [0, Tq/Pk) of the slice     int32 [Tq/Pk][D]
+ *     kscale, kzero rows [0, Tq/G)        fp32  [Tq/G][D] each
+ *     vq rows [0, Tq)                     int32 [Tq][D/Pv]
+ *     vscale, vzero rows [0, Tq)          fp32  [Tq][D/G] each
+ *     key residual tokens Tq .. n-1       fp16  [res][D] (token order)
+ *     value residual tokens Tq .. n-1     fp16  [res][D]
+ *
+ * A slice takes kivi_cache_bytes(n, ..., 0) + kivi_cache_bytes(n, ..., 1)
+ * bytes, and every section starts 16-byte aligned.
+ */
+#define KIVI_PAYLOAD_MAGIC   0x5056494Bu /* bytes "KIVP" */
+#define KIVI_PAYLOAD_VERSION 1
+#define KIVI_PAYLOAD_HEADER_BYTES 64
+
+/*
+ * Codec fingerprint: FNV-1a 64 (offset basis 0xcbf29ce484222325, prime
+ * 0x100000001b3) of the 32 bytes "KIVI" followed by the int32 values
+ * {1 (layout version), D, bits_k, bits_v, G, R, 4 (bytes per statistic)},
+ * little-endian.  Equal fingerprints mean payloads that decode identically
+ * for any B, H and Tmax.  Host only; 0 for an invalid descriptor.
+ */
+uint64_t kivi_codec_fingerprint(const kivi_cache* c);
+
+/*
+ * Bytes of the payload of this descriptor when sequence b holds lens[b]
+ * tokens (lens: host int32 [B], 0 <= lens[b] <= Tmax).  Host only; 0 for
+ * invalid arguments.
+ */
+size_t kivi_payload_bytes(const kivi_cache* c, const int32_t* lens);
+
+/*
+ * Writes the payload of the cache (its current len[] on the device) to dst
+ * (dst_bytes bytes, 16-byte aligned, device memory or pinned host memory).
+ * If the payload would exceed dst_bytes, nothing is written and *status
+ * (device int32) is set to KIVI_EWORKSPACE; *status is otherwise not
+ * written.  One kernel on `stream`.
+ */
+int32_t kivi_export(const kivi_cache* c, void* dst, size_t dst_bytes,
+                    int32_t* status, void* stream);
+
+/*
+ * Reads a payload from src (src_bytes bytes, 16-byte aligned, device memory
+ * or pinned host memory) into the cache: codes, statistics, ring slots of the
+ * residual tokens, and len[b].  The header is checked on the device before
+ * anything is written: a wrong magic, format, fingerprint or B/H/D/bits/G/R
+ * sets *status to KIVI_EINVAL, a sequence longer than Tmax to
+ * KIVI_ECAPACITY, a payload longer than src_bytes to KIVI_EWORKSPACE; the
+ * cache is then left unchanged.  One kernel on `stream`.
+ */
+int32_t kivi_import(const kivi_cache* c, const void* src, size_t src_bytes,
+                    int32_t* status, void* stream);
 
 #ifdef __cplusplus
 }

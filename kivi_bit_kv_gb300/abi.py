@@ -32,7 +32,12 @@ EXPORTS = (
     "kivi_buffer_bytes", "kivi_cache_bytes", "kivi_quant_keys", "kivi_quant_values",
     "kivi_dequant", "kivi_append_token", "kivi_decode_qk", "kivi_decode_pv",
     "kivi_workspace_bytes", "kivi_decode_pv_noalloc", "kivi_decode_attention",
+    "kivi_codec_fingerprint", "kivi_payload_bytes", "kivi_export", "kivi_import",
 )
+
+KIVI_PAYLOAD_MAGIC = 0x5056494B
+KIVI_PAYLOAD_VERSION = 1
+KIVI_PAYLOAD_HEADER_BYTES = 64
 
 KIVI_NOALLOC_SCRATCH_BYTES = 16 * 1024 * 1024
 
@@ -86,6 +91,10 @@ def load(path: str | None = None):
         "kivi_workspace_bytes": ([cp, i32], sz),
         "kivi_decode_pv_noalloc": ([cp, vp, i32, i32, vp, vp], i32),
         "kivi_decode_attention": ([cp, vp, i32, f32, vp, vp, sz, vp], i32),
+        "kivi_codec_fingerprint": ([cp], C.c_uint64),
+        "kivi_payload_bytes": ([cp, vp], sz),
+        "kivi_export": ([cp, vp, sz, vp, vp], i32),
+        "kivi_import": ([cp, vp, sz, vp, vp], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -149,6 +158,17 @@ def kivi_buffer_bytes(desc: kivi_cache, buffer: int) -> int:
 
 def kivi_cache_bytes(T: int, D: int, bits: int, G: int, R: int, which: int) -> int:
     return int(load().kivi_cache_bytes(T, D, bits, G, R, which))
+
+
+def kivi_codec_fingerprint(desc: kivi_cache) -> int:
+    """FNV-1a 64 fingerprint of the codec (D, bits, G, R) of a descriptor."""
+    return int(load().kivi_codec_fingerprint(C.byref(desc)))
+
+
+def kivi_payload_bytes(desc: kivi_cache, lens) -> int:
+    """Bytes of the compact payload when sequence b holds lens[b] tokens."""
+    arr = (C.c_int32 * desc.B)(*[int(x) for x in lens])
+    return int(load().kivi_payload_bytes(C.byref(desc), C.cast(arr, C.c_void_p)))
 
 
 def kivi_workspace_bytes(cache, Hq: int) -> int:
@@ -262,3 +282,38 @@ def kivi_decode_attention(cache, q: torch.Tensor, out: torch.Tensor, ws: torch.T
                                         Hq, sm, _dev(out, torch.float32, "out", cache.device), wp,
                                         ws.numel() * ws.element_size(), _stream(stream, cache.device)),
            "kivi_decode_attention")
+
+
+def _payload_buf(t: torch.Tensor, name: str, device) -> int:
+    """A uint8 payload buffer: a CUDA tensor on the cache's device or a pinned
+    CPU tensor (read and written by the kernels over the CPU-GPU link)."""
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.uint8:
+        raise TypeError(f"{name} must be a torch.uint8 tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.is_cuda:
+        if t.device != device:
+            raise ValueError(f"{name} is on {t.device}, cache is on {device}")
+    elif not t.is_pinned():
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory (pin_memory=True)")
+    return t.data_ptr()
+
+
+def kivi_export(cache, dst: torch.Tensor, status: torch.Tensor, stream=None):
+    """Write the cache's compact payload (include/kivi.h) into dst (uint8,
+    CUDA or pinned host).  A payload larger than dst sets status[0] to
+    KIVI_EWORKSPACE on the device and writes nothing."""
+    _check(load().kivi_export(C.byref(cache.desc), _payload_buf(dst, "dst", cache.device), dst.numel(),
+                              _dev(status, torch.int32, "status", cache.device),
+                              _stream(stream, cache.device)), "kivi_export")
+
+
+def kivi_import(cache, src: torch.Tensor, status: torch.Tensor, stream=None):
+    """Read a compact payload from src (uint8, CUDA or pinned host) into the
+    cache.  A header that does not match the cache's codec sets status[0] to
+    KIVI_EINVAL on the device (KIVI_ECAPACITY for a sequence longer than
+    Tmax, KIVI_EWORKSPACE for a truncated payload) and the cache is left as
+    it was."""
+    _check(load().kivi_import(C.byref(cache.desc), _payload_buf(src, "src", cache.device), src.numel(),
+                              _dev(status, torch.int32, "status", cache.device),
+                              _stream(stream, cache.device)), "kivi_import")

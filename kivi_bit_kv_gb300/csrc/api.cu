@@ -296,6 +296,79 @@ int32_t kivi_decode_attention(const kivi_cache* c, const uint16_t* q, int32_t Hq
                                                   (cudaStream_t)stream));
 }
 
+// ------------------------------------------------------ compact payload ---
+
+uint64_t kivi_codec_fingerprint(const kivi_cache* c)
+{
+    if (check_sizes(c) != KIVI_OK)
+        return 0;
+    // FNV-1a 64 over "KIVI" + int32 {layout 1, D, bits_k, bits_v, G, R, 4}, little-endian
+    const int32_t f[7] = {1, c->D, c->bits_k, c->bits_v, c->G, c->R, 4};
+    uint8_t bytes[32] = {'K', 'I', 'V', 'I'};
+    for (int i = 0; i < 7; ++i)
+        for (int k = 0; k < 4; ++k)
+            bytes[4 + 4 * i + k] = (uint8_t)((uint32_t)f[i] >> (8 * k));
+    uint64_t hsh = 0xcbf29ce484222325ull;
+    for (int i = 0; i < 32; ++i) {
+        hsh ^= bytes[i];
+        hsh *= 0x100000001b3ull;
+    }
+    return hsh;
+}
+
+size_t kivi_payload_bytes(const kivi_cache* c, const int32_t* lens)
+{
+    if (check_sizes(c) != KIVI_OK || !lens)
+        return 0;
+    for (int b = 0; b < c->B; ++b)
+        if (lens[b] < 0 || lens[b] > c->Tmax)
+            return 0;
+    return kivi::payload_bytes(*c, lens);
+}
+
+static int32_t check_payload_buffer(const void* p, size_t bytes, const kivi_cache* c, const char* name)
+{
+    int32_t st = check_ptr(p, name);
+    if (st != KIVI_OK)
+        return st;
+    const size_t head = KIVI_PAYLOAD_HEADER_BYTES + (size_t)(c->B + 3) / 4 * 16;
+    if (bytes < head)
+        return fail(KIVI_EINVAL, "%s holds %zu bytes, fewer than the %zu of the header and lengths", name,
+                    bytes, head);
+    cudaPointerAttributes a;
+    if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return fail(KIVI_EINVAL, "%s: cudaPointerGetAttributes failed", name);
+    }
+    if (a.type != cudaMemoryTypeDevice && a.type != cudaMemoryTypeHost && a.type != cudaMemoryTypeManaged)
+        return fail(KIVI_EINVAL, "%s must be device memory or pinned (page-locked) host memory", name);
+    return KIVI_OK;
+}
+
+int32_t kivi_export(const kivi_cache* c, void* dst, size_t dst_bytes, int32_t* status, void* stream)
+{
+    int32_t st = check_cache(c);
+    if (st != KIVI_OK)
+        return st;
+    if ((st = check_payload_buffer(dst, dst_bytes, c, "dst")) != KIVI_OK ||
+        (st = check_ptr(status, "status", false)) != KIVI_OK)
+        return st;
+    return launched(kivi::launch_export(*c, dst, dst_bytes, kivi_codec_fingerprint(c), status,
+                                        (cudaStream_t)stream));
+}
+
+int32_t kivi_import(const kivi_cache* c, const void* src, size_t src_bytes, int32_t* status, void* stream)
+{
+    int32_t st = check_cache(c);
+    if (st != KIVI_OK)
+        return st;
+    if ((st = check_payload_buffer(src, src_bytes, c, "src")) != KIVI_OK ||
+        (st = check_ptr(status, "status", false)) != KIVI_OK)
+        return st;
+    return launched(kivi::launch_import(*c, src, src_bytes, kivi_codec_fingerprint(c), status,
+                                        (cudaStream_t)stream));
+}
+
 }  // extern "C"
 
 namespace kivi {

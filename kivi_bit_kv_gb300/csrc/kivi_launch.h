@@ -50,6 +50,14 @@ template <int D>
 cudaError_t launch_decode_attention_d(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale,
                                       float* ws_o, float* ws_m, float* ws_l, cudaStream_t s);
 
+// Compact payload (include/kivi.h): its size for host lengths lens[B], and
+// the export / import kernels (header checks and size limits on the device).
+size_t payload_bytes(const kivi_cache& c, const int32_t* lens);
+cudaError_t launch_export(const kivi_cache& c, void* dst, size_t dst_bytes, uint64_t fingerprint,
+                          int32_t* status, cudaStream_t s);
+cudaError_t launch_import(const kivi_cache& c, const void* src, size_t src_bytes, uint64_t fingerprint,
+                          int32_t* status, cudaStream_t s);
+
 // Sets the message kivi_last_error() returns on this host thread; returns status.
 int32_t record_error(int32_t status, const char* message);
 

@@ -393,3 +393,134 @@ size_t kref_cache_bytes(int T, int D, int bits, int G, int R, int which)
                               : Tq * (size_t)(D / G) * 8;
     return codes + stats + res * (size_t)D * 2;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Compact payload                                                           */
+/* ------------------------------------------------------------------------ */
+
+uint64_t kref_fnv1a64(const uint8_t* p, size_t n)
+{
+    uint64_t h = 14695981039346656037ull;
+    for (size_t i = 0; i < n; ++i) {
+        h ^= p[i];
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
+static void put_u32(uint8_t* out, uint32_t v)
+{
+    for (int k = 0; k < 4; ++k)
+        out[k] = (uint8_t)(v >> (8 * k));
+}
+
+static uint32_t get_u32(const uint8_t* in)
+{
+    uint32_t v = 0;
+    for (int k = 0; k < 4; ++k)
+        v |= (uint32_t)in[k] << (8 * k);
+    return v;
+}
+
+uint64_t kref_codec_fingerprint(int D, int bits_k, int bits_v, int G, int R)
+{
+    uint8_t b[32] = {'K', 'I', 'V', 'I'};
+    const int32_t f[7] = {1, D, bits_k, bits_v, G, R, 4};
+    for (int i = 0; i < 7; ++i)
+        put_u32(b + 4 + 4 * i, (uint32_t)f[i]);
+    return kref_fnv1a64(b, sizeof b);
+}
+
+size_t kref_payload_header(uint8_t* out, int B, int H, int D, int bits_k, int bits_v, int G, int R,
+                           const int32_t* lens)
+{
+    const uint64_t fp = kref_codec_fingerprint(D, bits_k, bits_v, G, R);
+    const int32_t f[7] = {B, H, D, bits_k, bits_v, G, R};
+    size_t o = 0;
+    put_u32(out + o, 0x5056494Bu); o += 4;  /* "KIVP" */
+    put_u32(out + o, 1u); o += 4;
+    put_u32(out + o, (uint32_t)fp); o += 4;
+    put_u32(out + o, (uint32_t)(fp >> 32)); o += 4;
+    for (int i = 0; i < 7; ++i) {
+        put_u32(out + o, (uint32_t)f[i]);
+        o += 4;
+    }
+    for (int i = 0; i < 5; ++i) {
+        put_u32(out + o, 0u);
+        o += 4;
+    }
+    const int nl = (B + 3) / 4 * 4;
+    for (int b = 0; b < nl; ++b) {
+        put_u32(out + o, b < B ? (uint32_t)lens[b] : 0u);
+        o += 4;
+    }
+    return o;
+}
+
+/* Copies n 32-bit elements (put: array -> bytes; get: bytes -> array). */
+static size_t words_io(uint8_t* bytes, void* words, size_t n, int put)
+{
+    uint8_t* w = (uint8_t*)words;
+    for (size_t i = 0; i < n; ++i) {
+        uint32_t v;
+        if (put) {
+            memcpy(&v, w + 4 * i, 4);
+            put_u32(bytes + 4 * i, v);
+        } else {
+            v = get_u32(bytes + 4 * i);
+            memcpy(w + 4 * i, &v, 4);
+        }
+    }
+    return 4 * n;
+}
+
+/* Residual tokens Tq .. n-1 of a ring (slot t mod RG), D halves each. */
+static size_t ring_io(uint8_t* bytes, uint16_t* ring, int Tq, int n, int D, int RG, int put)
+{
+    size_t o = 0;
+    for (int t = Tq; t < n; ++t) {
+        uint16_t* row = ring + (size_t)(t % RG) * D;
+        for (int d = 0; d < D; ++d, o += 2) {
+            if (put) {
+                bytes[o] = (uint8_t)(row[d] & 0xFFu);
+                bytes[o + 1] = (uint8_t)(row[d] >> 8);
+            } else {
+                row[d] = (uint16_t)(bytes[o] | (bytes[o + 1] << 8));
+            }
+        }
+    }
+    return o;
+}
+
+static size_t slice_io(uint8_t* io, int n, int D, int bits_k, int bits_v, int G, int R,
+                       int32_t* kq, float* ks, float* kz, uint16_t* kres,
+                       int32_t* vq, float* vs, float* vz, uint16_t* vres, int put)
+{
+    const int Tq = kref_quantized_tokens(n, G, R), RG = R + G;
+    const size_t Pk = (size_t)(32 / bits_k), Pv = (size_t)(32 / bits_v);
+    size_t o = 0;
+    o += words_io(io + o, kq, (size_t)Tq / Pk * D, put);
+    o += words_io(io + o, ks, (size_t)(Tq / G) * D, put);
+    o += words_io(io + o, kz, (size_t)(Tq / G) * D, put);
+    o += words_io(io + o, vq, (size_t)Tq * (D / Pv), put);
+    o += words_io(io + o, vs, (size_t)Tq * (D / G), put);
+    o += words_io(io + o, vz, (size_t)Tq * (D / G), put);
+    o += ring_io(io + o, kres, Tq, n, D, RG, put);
+    o += ring_io(io + o, vres, Tq, n, D, RG, put);
+    return o;
+}
+
+size_t kref_payload_put_slice(uint8_t* out, int n, int D, int bits_k, int bits_v, int G, int R,
+                              const int32_t* kq, const float* ks, const float* kz, const uint16_t* kres,
+                              const int32_t* vq, const float* vs, const float* vz, const uint16_t* vres)
+{
+    return slice_io(out, n, D, bits_k, bits_v, G, R, (int32_t*)kq, (float*)ks, (float*)kz,
+                    (uint16_t*)kres, (int32_t*)vq, (float*)vs, (float*)vz, (uint16_t*)vres, 1);
+}
+
+size_t kref_payload_get_slice(const uint8_t* in, int n, int D, int bits_k, int bits_v, int G, int R,
+                              int32_t* kq, float* ks, float* kz, uint16_t* kres,
+                              int32_t* vq, float* vs, float* vz, uint16_t* vres)
+{
+    return slice_io((uint8_t*)in, n, D, bits_k, bits_v, G, R, kq, ks, kz, kres, vq, vs, vz, vres, 0);
+}

@@ -96,6 +96,39 @@ void kref_attention(const uint16_t* q, int NQ, float sm_scale, int len, int D,
  * which = 0 keys, 1 values. */
 size_t kref_cache_bytes(int T, int D, int bits, int G, int R, int which);
 
+/* Compact payload (the store format of the CUDA library's kivi_export /
+ * kivi_import; CacheSeek PR #4: qdata/scale/offset moved to the CPU before
+ * being stored, and a quant fingerprint in the prefix root hash).  Written
+ * byte by byte, little-endian, independent of the host's byte order. */
+
+/* FNV-1a, 64-bit: h = 14695981039346656037; for each byte: h ^= byte,
+ * h *= 1099511628211 (mod 2^64). */
+uint64_t kref_fnv1a64(const uint8_t* p, size_t n);
+
+/* FNV-1a 64 of "KIVI" followed by the int32 values {1, D, bits_k, bits_v, G,
+ * R, 4}, little-endian (32 bytes). */
+uint64_t kref_codec_fingerprint(int D, int bits_k, int bits_v, int G, int R);
+
+/* Header (64 bytes: magic "KIVP", format 1, fingerprint, B, H, D, bits_k,
+ * bits_v, G, R, five zero words) and the len table (B int32, zero-padded to a
+ * multiple of 4 entries).  Returns the bytes written. */
+size_t kref_payload_header(uint8_t* out, int B, int H, int D, int bits_k, int bits_v, int G, int R,
+                           const int32_t* lens);
+
+/* One (b, h) slice of a sequence of n tokens: kq rows [0, Tq/Pk), ks and kz
+ * rows [0, Tq/G), vq rows [0, Tq), vs and vz rows [0, Tq), then key and
+ * value residual tokens Tq .. n-1 from their ring slots.  Returns the bytes
+ * written (kref_cache_bytes(n, .., 0) + kref_cache_bytes(n, .., 1)). */
+size_t kref_payload_put_slice(uint8_t* out, int n, int D, int bits_k, int bits_v, int G, int R,
+                              const int32_t* kq, const float* ks, const float* kz, const uint16_t* kres,
+                              const int32_t* vq, const float* vs, const float* vz, const uint16_t* vres);
+
+/* The inverse of kref_payload_put_slice: fills the slice's arrays (the same
+ * rows and ring slots) from `in`; returns the bytes read. */
+size_t kref_payload_get_slice(const uint8_t* in, int n, int D, int bits_k, int bits_v, int G, int R,
+                              int32_t* kq, float* ks, float* kz, uint16_t* kres,
+                              int32_t* vq, float* vs, float* vz, uint16_t* vres);
+
 #ifdef __cplusplus
 }
 #endif

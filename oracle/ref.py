@@ -65,6 +65,17 @@ def lib():
         L.kref_attention.restype = None
         L.kref_cache_bytes.argtypes = [C.c_int] * 6
         L.kref_cache_bytes.restype = C.c_size_t
+        L.kref_fnv1a64.argtypes = [_VP, C.c_size_t]
+        L.kref_fnv1a64.restype = C.c_uint64
+        L.kref_codec_fingerprint.argtypes = [C.c_int] * 5
+        L.kref_codec_fingerprint.restype = C.c_uint64
+        L.kref_payload_header.argtypes = [_VP] + [C.c_int] * 7 + [_VP]
+        L.kref_payload_header.restype = C.c_size_t
+        io = [_VP] + [C.c_int] * 6 + [_VP] * 8
+        L.kref_payload_put_slice.argtypes = io
+        L.kref_payload_put_slice.restype = C.c_size_t
+        L.kref_payload_get_slice.argtypes = io
+        L.kref_payload_get_slice.restype = C.c_size_t
         _LIB = L
     return _LIB
 
@@ -259,6 +270,73 @@ class RefCache:
         items = slices if slices is not None else [(b, h) for b in range(B) for h in range(self.H)]
         _pool_map(one, items, threads)
         return logits, out
+
+
+def fnv1a64(data: bytes) -> int:
+    """FNV-1a 64 of a byte string (the C oracle's kref_fnv1a64)."""
+    buf = np.frombuffer(bytes(data) or b"\0", np.uint8).copy()
+    return int(lib().kref_fnv1a64(_p(buf), len(data)))
+
+
+def codec_fingerprint(D: int, bits_k: int, bits_v: int, G: int, R: int) -> int:
+    return int(lib().kref_codec_fingerprint(D, bits_k, bits_v, G, R))
+
+
+def payload_bytes(B, H, D, bits_k, bits_v, G, R, lens) -> int:
+    """Size of the compact payload: header, padded len table, slices."""
+    L = lib()
+    n = 64 + (B + 3) // 4 * 16
+    for b in range(B):
+        t = int(lens[b])
+        n += H * (L.kref_cache_bytes(t, D, bits_k, G, R, 0) + L.kref_cache_bytes(t, D, bits_v, G, R, 1))
+    return n
+
+
+def _payload(self) -> np.ndarray:
+    """The cache's compact payload (kref_payload_header, then the slices in
+    (b, h) order through kref_payload_put_slice) as a uint8 array."""
+    L = lib()
+    B, H = self.B, self.H
+    total = payload_bytes(B, H, self.D, self.bits_k, self.bits_v, self.G, self.R, self.lens)
+    out = np.zeros(total, np.uint8)
+    lens = np.ascontiguousarray(self.lens, np.int32)
+    o = L.kref_payload_header(_p(out), B, H, self.D, self.bits_k, self.bits_v, self.G, self.R, _p(lens))
+    for b in range(B):
+        for h in range(H):
+            o += L.kref_payload_put_slice(
+                out.ctypes.data + o, int(lens[b]), self.D, self.bits_k, self.bits_v, self.G, self.R,
+                _p(self.kq[b, h]), _p(self.kscale[b, h]), _p(self.kzero[b, h]), _p(self.kres[b, h]),
+                _p(self.vq[b, h]), _p(self.vscale[b, h]), _p(self.vzero[b, h]), _p(self.vres[b, h]))
+    assert o == total
+    return out
+
+
+def _from_payload(cls, buf, Tmax: int) -> "RefCache":
+    """A RefCache of capacity Tmax holding the payload `buf` (header fields
+    unpacked here; the slices through kref_payload_get_slice)."""
+    import struct
+    buf = np.ascontiguousarray(np.frombuffer(bytes(buf), np.uint8))
+    magic, fmt, fp = struct.unpack_from("<IIQ", buf, 0)
+    B, H, D, bits_k, bits_v, G, R = struct.unpack_from("<7i", buf, 16)
+    assert magic == 0x5056494B and fmt == 1, (hex(magic), fmt)
+    assert fp == codec_fingerprint(D, bits_k, bits_v, G, R)
+    lens = np.frombuffer(buf[64:64 + 4 * B].tobytes(), "<i4").astype(np.int32)
+    rc = cls(B, H, D, bits_k, bits_v, G, R, Tmax)
+    rc.lens[:] = lens
+    L = lib()
+    o = 64 + (B + 3) // 4 * 16
+    for b in range(B):
+        for h in range(H):
+            o += L.kref_payload_get_slice(
+                buf.ctypes.data + o, int(lens[b]), D, bits_k, bits_v, G, R,
+                _p(rc.kq[b, h]), _p(rc.kscale[b, h]), _p(rc.kzero[b, h]), _p(rc.kres[b, h]),
+                _p(rc.vq[b, h]), _p(rc.vscale[b, h]), _p(rc.vzero[b, h]), _p(rc.vres[b, h]))
+    assert o == len(buf), (o, len(buf))
+    return rc
+
+
+RefCache.payload = _payload
+RefCache.from_payload = classmethod(_from_payload)
 
 
 def host_threads() -> int:
