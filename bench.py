@@ -50,6 +50,7 @@ def parse():
     p.add_argument("--workload", default="llama2_7b_layer")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-c2c", action="store_true")
     p.add_argument("--decode", default="fused", choices=["fused", "split"],
                    help="decode through kivi_decode_attention (fused) or kivi_decode_qk + kivi_decode_pv")
     return p.parse_args()
@@ -376,11 +377,44 @@ def run_kivi(args, rank, world, local):
     }
     if kind == "full" and not args.no_e2e:
         line["e2e"] = run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq, calls)
+    if kind == "full" and not args.no_c2c:
+        line["c2c"] = run_c2c(cache, dev)
     if rank == 0 and world == 1 and kind == "full" and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(w, K, V, qs[0], kn[0], vn[0])
     if world > 1:
         torch.distributed.destroy_process_group()
     return line if rank == 0 else None
+
+
+def run_c2c(cache, dev, reps: int = 5) -> dict:
+    """Compact-payload round trip through pinned host memory (kivi_export,
+    kivi_import): payload bytes over the CUDA-event time of each call.  The
+    kernels load and store host memory directly, so this is the CPU-GPU link's
+    rate, reported apart from the HBM roofline."""
+    import torch
+    from kivi_bit_kv_gb300 import abi
+    lens = cache.lens.cpu().tolist()
+    n = abi.kivi_payload_bytes(cache.desc, lens)
+    host = torch.empty(n, dtype=torch.uint8, pin_memory=True)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    res = {}
+    for name, fn in (("export", lambda: abi.kivi_export(cache, host, status)),
+                     ("import", lambda: abi.kivi_import(cache, host, status))):
+        fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(reps):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        res[name] = e0.elapsed_time(e1) / reps
+    assert int(status.item()) == 0
+    return {"payload_bytes": n, "export_ms": round(res["export"], 4), "import_ms": round(res["import"], 4),
+            "export_gbs": round(n / (res["export"] * 1e-3) / 1e9, 1),
+            "import_gbs": round(n / (res["import"] * 1e-3) / 1e9, 1),
+            "memory": "pinned host (kernel loads / stores over the CPU-GPU link)"}
 
 
 def run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq, calls):
