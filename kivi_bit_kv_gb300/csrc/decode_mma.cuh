@@ -196,9 +196,9 @@ __host__ __device__ constexpr int decode_chunks(int n, int TC, int S)
 }
 
 // Word offsets into a decode kernel's dynamic shared memory: the staged keys
-// and / or values of TC tokens, then the probabilities and B fragments of up
-// to TX = TC + slack tokens, the split partials when they do not overlay a
-// dead region, and the zero terms.
+// and / or values of TC tokens, then the probabilities (logits) and B
+// fragments of up to TX = TC + slack tokens, the split partials when they do
+// not overlay a dead region; the zero terms overlay the logits.
 struct DecodeLayout {
     size_t kw, ks, kz, vw, vs, vz;
     size_t p, bb, part, zs, total;
@@ -246,8 +246,9 @@ __host__ __device__ inline DecodeLayout decode_layout(int TC, int TX, int D, int
             L.part = o;
             o += part_words(D, NQB);
         }
-        L.zs = o;
-        o += zs_words(D, G, NQB);
+        // the zero terms overlay the logits, dead once the B fragments exist
+        // (pv_weights writes them after a barrier)
+        L.zs = L.p;
     }
     L.total = o;
     return L;
@@ -263,22 +264,38 @@ struct ChunkPlan {
     int TC, S, ctas_per_sm;
 };
 
+// fp32 q row in shared memory: channel d at qpad(d) (4 floats of padding per
+// 16 channels spread the LDS.128 of the four lanes of a lane group over banks)
+// and rows D + D/4 (+16) floats apart, 16 (mod 32), so that two heads read by
+// one quarter-warp use the other half of the banks.
+__host__ __device__ constexpr int qstride_of(int D) { return D + D / 4 + ((D + D / 4) % 32 == 0 ? 16 : 0); }
+
+// Shared memory per SM, and what each resident CTA also takes besides the
+// dynamic layout: the runtime's reserve and the static q rows / reductions.
+constexpr size_t kSmemPerSM = 228 * 1024;
+constexpr size_t kSmemReservedPerCTA = 1024;
+__host__ __device__ constexpr size_t decode_static_smem(int D, int NQB)
+{
+    return 4 * ((size_t)NQB * qstride_of(D) + NQB + (size_t)kDecodeWarps * NQB);
+}
+
 __host__ __device__ inline ChunkPlan decode_chunk_plan(int D, int bits_k, int bits_v, int G, int R, int NQ)
 {
     const int NQB = heads_per_pass(NQ);
     const int P = 32 / bits_k;
     const int tok = cmin(8, (8 / NQB) * 32 / P) * P;
     const int tc_min = cmax(cmax(tok, G), 64);
-    const size_t budgets[3] = {74 * 1024, 110 * 1024, 220 * 1024};
     auto bytes = [&](int TC, int S) {
         return 4 * decode_layout(TC, TC + S, D, bits_k, bits_v, G, NQB, NQ > NQB, true, true).total;
     };
-    for (int bi = NQB >= 4 ? 1 : 0; bi < 3; ++bi)
+    for (int ctas = 3; ctas >= 1; --ctas) {
+        const size_t budget = kSmemPerSM / ctas - kSmemReservedPerCTA - decode_static_smem(D, NQB);
         for (int TC = 1024; TC >= tc_min; TC >>= 1)
-            if (bytes(TC, 0) <= budgets[bi]) {
+            if (bytes(TC, 0) <= budget) {
                 const int S = max_chunk_slack(TC, R);
-                return {TC, bytes(TC, S) <= budgets[bi] ? S : 0, 3 - bi};
+                return {TC, bytes(TC, S) <= budget ? S : 0, ctas};
             }
+    }
     return {tc_min, 0, 1};
 }
 
@@ -390,11 +407,6 @@ __device__ __forceinline__ void stage_values(const kivi_cache& c, size_t bh, int
 
 // ------------------------------------------------------------------ keys ---
 
-// fp32 q row in shared memory: channel d at qpad(d) (4 floats of padding per
-// 16 channels spread the LDS.128 of the four lanes of a lane group over banks)
-// and rows D + D/4 (+16) floats apart, 16 (mod 32), so that two heads read by
-// one quarter-warp use the other half of the banks.
-__host__ __device__ constexpr int qstride_of(int D) { return D + D / 4 + ((D + D / 4) % 32 == 0 ? 16 : 0); }
 __device__ __forceinline__ int qpad(int d) { return d + ((d >> 4) << 2); }
 
 // Stages query heads hq0 .. hq0+NQB-1 of sequence b: qs[h][qpad(d)] = q 2^-e_h
@@ -643,8 +655,9 @@ __device__ __forceinline__ void chunk_max(float (&m)[NQB], float* red)
 // w = p_ht s_tg for quantized tokens (t < nq) and of w = p_ht for residual
 // tokens (nq <= t < n), zero up to the end of the last 16-token slice.
 // zw[warp][h][g] = the warp's share of sum over quantized t of p_ht z_tg,
-// zw[warp][h][NGV] its share of sum over t of p_ht.  One thread per token
-// pair; whole CTA, the caller's barrier publishes both.
+// zw[warp][h][NGV] its share of sum over t of p_ht (zw may overlay p_sm: it
+// is written after a barrier).  One thread per token pair; whole CTA, the
+// caller's barrier publishes both.
 template <int NQB, int NGV>
 __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_end, int i_step, int i_base,
                                              const float* p_sm, int ps, const float (&mx)[NQB],
@@ -699,19 +712,21 @@ __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_e
 #pragma unroll
     for (int h = 0; h < NQB; ++h) {
 #pragma unroll
-        for (int gg = 0; gg < NGV; ++gg) {
-            float v = z[h][gg];
+        for (int gg = 0; gg < NGV; ++gg)
             for (int k = 16; k > 0; k >>= 1)
-                v += __shfl_xor_sync(0xffffffffu, v, k);
-            if (lane == 0)
-                zw[(warp * NQB + h) * (NGV + 1) + gg] = v;
-        }
-        float v = l[h];
+                z[h][gg] += __shfl_xor_sync(0xffffffffu, z[h][gg], k);
         for (int k = 16; k > 0; k >>= 1)
-            v += __shfl_xor_sync(0xffffffffu, v, k);
-        if (lane == 0)
-            zw[(warp * NQB + h) * (NGV + 1) + NGV] = v;
+            l[h] += __shfl_xor_sync(0xffffffffu, l[h], k);
     }
+    __syncthreads();  // zw overlays p_sm: every thread has read its logits
+    if (lane == 0)
+#pragma unroll
+        for (int h = 0; h < NQB; ++h) {
+#pragma unroll
+            for (int gg = 0; gg < NGV; ++gg)
+                zw[(warp * NQB + h) * (NGV + 1) + gg] = z[h][gg];
+            zw[(warp * NQB + h) * (NGV + 1) + NGV] = l[h];
+        }
 }
 
 // Pairs i_first, i_first + i_step, ... below i_end; bb holds pairs from
