@@ -10,65 +10,78 @@
 namespace kivi {
 
 // out[b][hq][d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M), M = max m_c
-// over the chunks c that hold tokens of sequence b.  One CTA per (b, hq): the
-// chunk weights go to shared memory, each warp sums a quarter of the chunks
-// with 16-byte loads, and the four warp sums are added in a fixed order.
+// over the chunks c that hold tokens of sequence b.  CTA (b hq, y) writes
+// channels [y C, y C + C), C = D / gridDim.y: one merge of the (m, l) pairs
+// (each thread folds its chunks with the usual rescaling, then warps and
+// warps' results in a fixed order), the chunk weights to shared memory, and
+// the weighted sum with one 16-byte load per (chunk, column) and thread.
 constexpr int kCombineThreads = 128;
+
+__device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2)
+{
+    if (m2 > m) {
+        l = fmaf(l, expf(m - m2), l2);
+        m = m2;
+    } else if (m2 > -INFINITY) {
+        l = fmaf(l2, expf(m2 - m), l);
+    }
+}
 
 __global__ void __launch_bounds__(kCombineThreads)
 decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunks, int TC, int S,
                       const float* __restrict__ ws_o, const float* __restrict__ ws_m,
                       const float* __restrict__ ws_l, float* __restrict__ out)
 {
-    extern __shared__ __align__(16) float cmb[];  // e[nchunks], then [4][D] warp sums
-    __shared__ float red[kDecodeWarps];
+    extern __shared__ __align__(16) float cmb[];  // e[nchunks], then [rows][C] partial sums
+    __shared__ float red_m[kDecodeWarps], red_l[kDecodeWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t bhq = blockIdx.x;
+    const int C = D / gridDim.y, c0 = blockIdx.y * C;
     const int n = len[bhq / Hq];
     const int nv = decode_chunks(n, TC, S);
     const float* mrow = ws_m + bhq * nchunks;
     const float* lrow = ws_l + bhq * nchunks;
-    float mx = -INFINITY;
+    float m = -INFINITY, l = 0.0f;
     for (int k = threadIdx.x; k < nv; k += kCombineThreads)
-        mx = fmaxf(mx, mrow[k]);
-    for (int m = 16; m > 0; m >>= 1)
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
-    if (lane == 0)
-        red[warp] = mx;
-    __syncthreads();
-    const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
-    __syncthreads();
-    float L = 0.0f;
-    for (int k = threadIdx.x; k < nv; k += kCombineThreads) {
-        const float e = expf(mrow[k] - M);
-        cmb[k] = e;
-        L = fmaf(lrow[k], e, L);
+        merge_ml(m, l, mrow[k], lrow[k]);
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, l, o);
+        merge_ml(m, l, m2, l2);
     }
-    for (int m = 16; m > 0; m >>= 1)
-        L += __shfl_xor_sync(0xffffffffu, L, m);
-    if (lane == 0)
-        red[warp] = L;
-    __syncthreads();  // also publishes cmb[0 .. nv)
-    L = (red[0] + red[1]) + (red[2] + red[3]);
-    float* wsum = cmb + ((nchunks + 3) & ~3);
-    const float4* o4 = reinterpret_cast<const float4*>(ws_o + bhq * nchunks * D);
-    for (int d4 = lane; d4 < D / 4; d4 += 32) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (lane == 0) {
+        red_m[warp] = m;
+        red_l[warp] = l;
+    }
+    __syncthreads();
+    float M = red_m[0], L = red_l[0];
+#pragma unroll
+    for (int w = 1; w < kDecodeWarps; ++w)
+        merge_ml(M, L, red_m[w], red_l[w]);
+    for (int k = threadIdx.x; k < nv; k += kCombineThreads)
+        cmb[k] = expf(mrow[k] - M);
+    __syncthreads();
+    const int V = C / 4, rows = kCombineThreads / V;  // float4 columns; chunks in flight per round
+    const int v = threadIdx.x % V, r0 = threadIdx.x / V;
+    const float4* o4 = reinterpret_cast<const float4*>(ws_o + bhq * nchunks * D + c0);
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-        for (int k = warp; k < nv; k += kDecodeWarps) {
-            const float4 o = o4[(size_t)k * (D / 4) + d4];
-            const float e = cmb[k];
-            acc.x = fmaf(o.x, e, acc.x);
-            acc.y = fmaf(o.y, e, acc.y);
-            acc.z = fmaf(o.z, e, acc.z);
-            acc.w = fmaf(o.w, e, acc.w);
-        }
-        reinterpret_cast<float4*>(wsum + warp * D)[d4] = acc;
+    for (int k = r0; k < nv; k += rows) {
+        const float4 o = o4[(size_t)k * (D / 4) + v];
+        const float e = cmb[k];
+        acc.x = fmaf(o.x, e, acc.x);
+        acc.y = fmaf(o.y, e, acc.y);
+        acc.z = fmaf(o.z, e, acc.z);
+        acc.w = fmaf(o.w, e, acc.w);
     }
+    float4* part = reinterpret_cast<float4*>(cmb + ((nchunks + 3) & ~3));
+    part[r0 * V + v] = acc;
     __syncthreads();
-    for (int d = threadIdx.x; d < D; d += kCombineThreads) {
-        const float o = (wsum[d] + wsum[D + d]) + (wsum[2 * D + d] + wsum[3 * D + d]);
-        out[bhq * D + d] = nv > 0 ? o / L : 0.0f;
+    for (int d = threadIdx.x; d < C; d += kCombineThreads) {
+        const float* pf = reinterpret_cast<const float*>(part);
+        float o = 0.0f;
+        for (int r = 0; r < rows; ++r)
+            o += pf[r * C + d];
+        out[bhq * D + c0 + d] = nv > 0 ? o / L : 0.0f;
     }
 }
 
@@ -85,14 +98,20 @@ static cudaError_t combine(const kivi_cache& c, int Hq, const float* ws_o, const
                            const float* ws_l, float* out, cudaStream_t s)
 {
     const int nch = pv_chunks(c, Hq);
-    const size_t smem = (((size_t)nch + 3) / 4 * 4 + (size_t)kDecodeWarps * c.D) * sizeof(float);
+    // channel slices per (b, hq): at least two CTAs per SM in all, 32 channels or more each
+    const int rows = c.B * Hq;
+    int ds = 1;
+    while (ds < c.D / 32 && rows * ds < 2 * sm_count())
+        ds *= 2;
+    const int C = c.D / ds;
+    const size_t smem = (((size_t)nch + 3) / 4 * 4 + (size_t)(kCombineThreads / (C / 4)) * C) * sizeof(float);
     cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess)
         return e;
     const ChunkPlan cp = chunk_plan(c, Hq);
-    decode_combine_kernel<<<c.B * Hq, kCombineThreads, smem, s>>>(c.len, Hq, c.D, nch, cp.TC, cp.S,
-                                                                  ws_o, ws_m, ws_l, out);
+    decode_combine_kernel<<<dim3(rows, ds), kCombineThreads, smem, s>>>(c.len, Hq, c.D, nch, cp.TC, cp.S, ws_o,
+                                                                       ws_m, ws_l, out);
     return cudaGetLastError();
 }
 
