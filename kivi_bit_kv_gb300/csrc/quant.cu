@@ -85,8 +85,9 @@ __device__ __forceinline__ int key_stage_swz(int r, int x, int lgS)
 
 // Encode one key lane (16 tokens x 8 channels) whose rows are staged in
 // shared memory at lrow[i * stride], i = 0..15: statistics as in
-// quant_key_lane, then the codes in short unrolled runs of four tokens, each
-// word-row stored (after its near-tie fix-up) as soon as it is complete.
+// quant_key_lane, then the codes, fully unrolled over the P tokens of a word
+// (constant shifts), each word-row stored (after its near-tie fix-up) as soon
+// as it is complete.
 template <int BITS, int S>
 __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, size_t bh, int t0, int g,
                                                           int j, int s, unsigned smask,
@@ -101,7 +102,7 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
         for (int k = 0; k < 4; ++k)
             mn[k] = mx[k] = as_h2(u4_word(r0, k));
     }
-#pragma unroll 5
+#pragma unroll
     for (int i = 1; i < kLaneTokens; ++i) {
         const uint4 r = lrow[i * stride];
 #pragma unroll
@@ -143,21 +144,16 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
         for (int k = 0; k < 8; ++k)
             words[k] = 0u - kWordBias;
         unsigned flagged = 0u;
-        uint32_t mul = 1u;
-#pragma unroll 1
-        for (int i0 = 0; i0 < Cd::P; i0 += 4) {
 #pragma unroll
-            for (int ii = 0; ii < 4; ++ii) {
-                const uint4 r = lrow[(w * Cd::P + i0 + ii) * stride];
-                float worst = 0.0f;
+        for (int i = 0; i < Cd::P; ++i) {
+            const uint4 r = lrow[(w * Cd::P + i) * stride];
+            float worst = 0.0f;
 #pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    const float a = add_h_f(u4_half(r, k), nzero[k]);
-                    words[k] += fast_code_bits(a, inv[k], worst) * mul;
-                }
-                flagged |= (worst >= near_tie<BITS>() ? 1u : 0u) << (i0 + ii);
-                mul <<= BITS;
+            for (int k = 0; k < 8; ++k) {
+                const float a = add_h_f(u4_half(r, k), nzero[k]);
+                words[k] += fast_code_bits(a, inv[k], worst) * (1u << (i * BITS));
             }
+            flagged |= (worst >= near_tie<BITS>() ? 1u : 0u) << i;
         }
         if (__builtin_expect(flagged != 0u, 0)) {
 #pragma unroll 1
