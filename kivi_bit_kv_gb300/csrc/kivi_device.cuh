@@ -167,43 +167,45 @@ static __device__ __noinline__ uint32_t exact_code(float a, float scale)
     return (uint32_t)__float2int_rn(__fdiv_rn(a, scale));
 }
 
-// Fast code for a = x - zero >= 0, without branches.  With inv = rn(1/scale)
-// the exact product p = a * inv equals y = a / scale up to a factor
-// (1 + d1), |d1| <= 2^-24, and y <= M (1 + 2^-23).
-//   t = rn(p + C), C = 1.5 * 2^23 (ulp 1): t - C = r, the nearest integer to
-//   p, ties to even (one FFMA, the product is not rounded first);
-//   dlt = rn(p - r) = fma(a, inv, C - t) (C - t is exact), so
-//   |dlt - (p - r)| <= 2^-26.
-// The IEEE quotient rn(y) = y (1 + d2), |d2| <= 2^-24, so
-// |rn(y) - p| <= 2^-23 y <= 2^-23 M (1 + 2^-23), and
-// |rn(y) - r| <= |dlt| + 2^-23 M + 2^-23 2^-23 M + 2^-26 < |dlt| + 2^(b-23).
-// Hence when |dlt| < 1/2 - 2^(b-23) (near_tie<b>) rn(y) lies strictly within
-// 1/2 of r and rounds to r; the caller resolves the other case (about 2^(b-21)
-// of the codes) with exact_code().  The code never exceeds M:
-// p <= M (1 + 2^-24)^2 / (1 - 2^-24) < M + 1/2.  Returns the bits of t:
-// code = t_bits - 0x4B400000.  scale == 0 gives inv == 0, p == 0 and code 0.
-__device__ __forceinline__ uint32_t fast_code_bits(float a, float inv, float& worst)
+// Code of a = x - zero >= 0 with its own exactness test, without a division.
+// With inv = rn(1/scale), the bracket inv_lo = rn(inv (1 - 2^-21)) and
+// inv_hi = rn(inv (1 + 2^-21)) satisfies
+//   inv_lo <= (1/scale)(1 - 2^-24),   inv_hi >= (1/scale)(1 + 2^-24)
+// (inv is within 2^-24 of 1/scale, each product rounding within 2^-24 more),
+// and the IEEE quotient q = rn(a / scale) is within 2^-24 of a / scale, so,
+// as a >= 0,
+//   a inv_lo <= q <= a inv_hi.
+// t_lo = rn(a inv_lo + C) and t_hi = rn(a inv_hi + C), C = 1.5 * 2^23 (ulp 1,
+// even): each FFMA rounds the exact product to the nearest integer, ties to
+// even, and that rounding is monotone, so t_lo == t_hi means every value in
+// [a inv_lo, a inv_hi] -- q included -- rounds to the same integer: the code
+// is t_lo - C.  Otherwise (a half-integer inside the bracket: about 2^(b-20)
+// of the codes) the caller takes exact_code().  No code exceeds M:
+// a inv_lo <= q <= M (1 + 2^-23).  scale == 0 gives inv == 0, both brackets 0
+// and code 0.  Returns the bits of t_lo; `diff` collects t_lo ^ t_hi.
+struct InvBracket {
+    float lo, hi;
+};
+__device__ __forceinline__ InvBracket inv_bracket(float inv)
 {
-    const float t = __fmaf_rn(a, inv, 12582912.0f);
-    const float dlt = __fmaf_rn(a, inv, __fsub_rn(12582912.0f, t));
-    worst = fmaxf(worst, fabsf(dlt));  // flags are tested once per batch of codes
-    return __float_as_uint(t);
+    return {__fmul_rn(inv, 1.0f - 0x1p-21f), __fmul_rn(inv, 1.0f + 0x1p-21f)};
 }
-// |dlt| at or above this: use exact_code (see fast_code_bits).
-template <int BITS>
-__host__ __device__ constexpr float near_tie() { return 0.5f - (float)(1u << BITS) * 0x1p-23f; }
+__device__ __forceinline__ uint32_t bracket_code_bits(float a, InvBracket ib, uint32_t& diff)
+{
+    const uint32_t tl = __float_as_uint(__fmaf_rn(a, ib.lo, 12582912.0f));
+    const uint32_t th = __float_as_uint(__fmaf_rn(a, ib.hi, 12582912.0f));
+    diff |= tl ^ th;
+    return tl;
+}
 constexpr uint32_t kCodeBias = 0x4B400000u;
 
 // code = clamp(rne(a / scale), 0, M), bit-identical to rounding the IEEE
-// quotient (see fast_code_bits).
-template <int BITS>
+// quotient (see bracket_code_bits).
 __device__ __forceinline__ uint32_t quant_code(float a, float scale, float inv)
 {
-    float worst = 0.0f;
-    uint32_t c = fast_code_bits(a, inv, worst) - kCodeBias;
-    if (worst >= near_tie<BITS>())
-        c = exact_code(a, scale);
-    return c;
+    uint32_t diff = 0u;
+    const uint32_t c = bracket_code_bits(a, inv_bracket(inv), diff) - kCodeBias;
+    return diff != 0u ? exact_code(a, scale) : c;
 }
 
 // 2^23 as an opaque register value (see one_bits).
@@ -269,9 +271,12 @@ __device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens],
     // every lane of the tile column now holds the same min / max
     key_lane_stats<BITS, S>(mn, mx, mask, scale, zero, inv);
     float nzero[8];
+    InvBracket ib[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
+    for (int k = 0; k < 8; ++k) {
         nzero[k] = -zero[k];
+        ib[k] = inv_bracket(inv[k]);
+    }
     // Pack t_bits * 2^sh (IMAD) and remove the constant bias once per word:
     // sum_i (bias + c_i) 2^(b i) - bias * sum_i 2^(b i) = sum_i c_i 2^(b i) (mod 2^32).
     constexpr uint32_t kWordBias = kCodeBias * (uint32_t)(((1ull << (Cd::P * BITS)) - 1) /
@@ -284,14 +289,13 @@ __device__ __forceinline__ void quant_key_lane(const uint4 (&raw)[kLaneTokens],
     flagged = 0u;
 #pragma unroll
     for (int i = 0; i < kLaneTokens; ++i) {
-        float worst = 0.0f;
+        uint32_t diff = 0u;
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const float a = add_h_f(u4_half(raw[i], k), nzero[k]);
-            const uint32_t tb = fast_code_bits(a, inv[k], worst);
-            words[i / Cd::P][k] += tb * (1u << ((i % Cd::P) * BITS));
+            words[i / Cd::P][k] += bracket_code_bits(a, ib[k], diff) * (1u << ((i % Cd::P) * BITS));
         }
-        flagged |= (worst >= near_tie<BITS>() ? 1u : 0u) << i;
+        flagged |= (diff != 0u ? 1u : 0u) << i;
     }
 }
 
@@ -314,9 +318,9 @@ __device__ __forceinline__ void key_lane_fixup(unsigned flagged, const uint16_t*
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
             const float a = add_h_f(u4_half(r, k), -zero[k]);
-            float w1 = 0.0f;
-            const uint32_t fast = fast_code_bits(a, inv[k], w1) - kCodeBias;
-            if (w1 >= near_tie<BITS>()) {
+            uint32_t diff = 0u;
+            const uint32_t fast = bracket_code_bits(a, inv_bracket(inv[k]), diff) - kCodeBias;
+            if (diff != 0u) {
                 const uint32_t fix = (exact_code(a, scale[k]) - fast) << sh;
 #pragma unroll
                 for (int w = 0; w < Cd::kWordRows; ++w)
@@ -352,6 +356,7 @@ __device__ __forceinline__ void quant_value_group(const uint4 (&raw)[G / 8], flo
     float inv;
     group_stats<BITS>(lo, hi, scale, zero, inv);
     const float nz = -zero;
+    const InvBracket ib = inv_bracket(inv);
     constexpr uint32_t kWordBias = kCodeBias * (uint32_t)(((1ull << (Cd::P * BITS)) - 1) /
                                                           ((1ull << BITS) - 1));
 #pragma unroll
@@ -359,19 +364,19 @@ __device__ __forceinline__ void quant_value_group(const uint4 (&raw)[G / 8], flo
         words[w] = 0u - kWordBias;
 #pragma unroll
     for (int e0 = 0; e0 < G; e0 += 8) {
-        float worst = 0.0f;
+        uint32_t diff = 0u;
 #pragma unroll
         for (int e = e0; e < e0 + 8; ++e) {
-            const uint32_t tb = fast_code_bits(add_h_f(u4_half(raw[e / 8], e % 8), nz), inv, worst);
+            const uint32_t tb = bracket_code_bits(add_h_f(u4_half(raw[e / 8], e % 8), nz), ib, diff);
             words[e / Cd::P] += tb * (1u << ((e % Cd::P) * BITS));
         }
-        if (__builtin_expect(worst >= near_tie<BITS>(), 0)) {
+        if (__builtin_expect(diff != 0u, 0)) {
 #pragma unroll
             for (int e = e0; e < e0 + 8; ++e) {
                 const float a = add_h_f(u4_half(raw[e / 8], e % 8), nz);
-                float w1 = 0.0f;
-                const uint32_t fast = fast_code_bits(a, inv, w1) - kCodeBias;
-                if (w1 >= near_tie<BITS>())
+                uint32_t d1 = 0u;
+                const uint32_t fast = bracket_code_bits(a, ib, d1) - kCodeBias;
+                if (d1 != 0u)
                     words[e / Cd::P] += (exact_code(a, scale) - fast) << ((e % Cd::P) * BITS);
             }
         }

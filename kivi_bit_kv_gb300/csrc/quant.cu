@@ -121,9 +121,12 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
         }
     float scale[8], zero[8], inv[8], nzero[8];
     key_lane_stats<BITS, S>(mn, mx, smask, scale, zero, inv);
+    InvBracket ib[8];
 #pragma unroll
-    for (int k = 0; k < 8; ++k)
+    for (int k = 0; k < 8; ++k) {
         nzero[k] = -zero[k];
+        ib[k] = inv_bracket(inv[k]);
+    }
     if (s == 0) {
         const size_t so = (bh * (size_t)(c.Tmax / c.G) + g) * D + (size_t)j * kLaneChans;
         float4* sp = reinterpret_cast<float4*>(c.kscale + so);
@@ -147,13 +150,13 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
 #pragma unroll
         for (int i = 0; i < Cd::P; ++i) {
             const uint4 r = lrow[(w * Cd::P + i) * stride];
-            float worst = 0.0f;
+            uint32_t diff = 0u;
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const float a = add_h_f(u4_half(r, k), nzero[k]);
-                words[k] += fast_code_bits(a, inv[k], worst) * (1u << (i * BITS));
+                words[k] += bracket_code_bits(a, ib[k], diff) * (1u << (i * BITS));
             }
-            flagged |= (worst >= near_tie<BITS>() ? 1u : 0u) << i;
+            flagged |= (diff != 0u ? 1u : 0u) << i;
         }
         if (__builtin_expect(flagged != 0u, 0)) {
 #pragma unroll 1
@@ -164,9 +167,9 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const float a = add_h_f(u4_half(r, k), nzero[k]);
-                    float w1 = 0.0f;
-                    const uint32_t fast = fast_code_bits(a, inv[k], w1) - kCodeBias;
-                    if (w1 >= near_tie<BITS>())
+                    uint32_t d1 = 0u;
+                    const uint32_t fast = bracket_code_bits(a, ib[k], d1) - kCodeBias;
+                    if (d1 != 0u)
                         words[k] += (exact_code(a, scale[k]) - fast) << (i * BITS);
                 }
             }
