@@ -190,6 +190,17 @@ __device__ __forceinline__ InvBracket inv_bracket(float inv)
 {
     return {__fmul_rn(inv, 1.0f - 0x1p-21f), __fmul_rn(inv, 1.0f + 0x1p-21f)};
 }
+// bracket_code_bits with the collection pinned to one 3-input LOP3 (the
+// compiler otherwise turns the OR of XORs into compare-and-select chains).
+__device__ __forceinline__ uint32_t bracket_code_bits_lop3(float a, InvBracket ib, uint32_t& diff)
+{
+    const uint32_t tl = __float_as_uint(__fmaf_rn(a, ib.lo, 12582912.0f));
+    const uint32_t th = __float_as_uint(__fmaf_rn(a, ib.hi, 12582912.0f));
+    uint32_t d;
+    asm("lop3.b32 %0, %1, %2, %3, 0xBE;" : "=r"(d) : "r"(tl), "r"(th), "r"(diff));  // (tl ^ th) | diff
+    diff = d;
+    return tl;
+}
 __device__ __forceinline__ uint32_t bracket_code_bits(float a, InvBracket ib, uint32_t& diff)
 {
     const uint32_t tl = __float_as_uint(__fmaf_rn(a, ib.lo, 12582912.0f));

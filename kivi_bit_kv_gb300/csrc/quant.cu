@@ -154,7 +154,7 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
                 const float a = add_h_f(u4_half(r, k), nzero[k]);
-                words[k] += bracket_code_bits(a, ib[k], diff) * (1u << (i * BITS));
+                words[k] += bracket_code_bits_lop3(a, ib[k], diff) * (1u << (i * BITS));
             }
             flagged |= (diff != 0u ? 1u : 0u) << i;
         }
