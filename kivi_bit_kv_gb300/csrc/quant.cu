@@ -88,13 +88,12 @@ __device__ __forceinline__ int key_stage_swz(int r, int x, int lgS)
 // quant_key_lane, then the codes, fully unrolled over the P tokens of a word
 // (constant shifts), each word-row stored (after its near-tie fix-up) as soon
 // as it is complete.
-template <int BITS, int S>
+template <int BITS, int S, int D>
 __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, size_t bh, int t0, int g,
-                                                          int j, int s, unsigned smask,
-                                                          const uint4* lrow, int stride)
+                                                          int j, int s, unsigned smask, const uint4* lrow)
 {
     using Cd = Codec<BITS>;
-    const int D = c.D;
+    constexpr int stride = D / kLaneChans;  // 16-byte chunks per staged row
     __half2 mn[4], mx[4];
     {
         const uint4 r0 = lrow[0];
@@ -179,16 +178,15 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
     }
 }
 
-template <int BITS, int S>
+template <int BITS, int S, int D>
 __global__ void __launch_bounds__(kKeyStageThreads, 3)
 quant_keys_staged_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
                          const int32_t* __restrict__ seq_lens, int tiles_per_seq)
 {
     extern __shared__ __align__(16) uint4 kst[];  // two buffers of kKeyStageBytes
-    const int D = c.D;
     constexpr int lgS = S == 2 ? 1 : S == 4 ? 2 : 3;
-    const int NC = D / kLaneChans, lgNC = log2_pow2(NC);
-    const int TT = (kKeyStageBytes / 2) / D;       // tokens per tile
+    constexpr int NC = D / kLaneChans, lgNC = NC == 8 ? 3 : NC == 16 ? 4 : 5;
+    constexpr int TT = (kKeyStageBytes / 2) / D;   // tokens per tile
     const int lane = threadIdx.x & 31;
     const unsigned smask = (((1u << S) - 1u) << (lane & ~(S - 1)));
     const int s = threadIdx.x & (S - 1);
@@ -196,8 +194,8 @@ quant_keys_staged_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
     const int gl = threadIdx.x >> (lgS + lgNC);   // group within the tile
     const int RG = c.R + c.G;
     const int ntiles = c.B * c.H * tiles_per_seq;
-    const int cpr = NC;                            // 16-byte chunks per row
-    const int rsweep = kKeyStageThreads / cpr;    // rows per copy sweep
+    constexpr int cpr = NC;                        // 16-byte chunks per row
+    constexpr int rsweep = kKeyStageThreads / cpr; // rows per copy sweep
     const int cx = threadIdx.x & (cpr - 1), cr = threadIdx.x / cpr;
 
     auto tile_of = [&](int tile, int& bh, int& tt0, int& n) {
@@ -240,7 +238,7 @@ quant_keys_staged_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
             // the lane's 16 rows share one swizzled column (r / 16 is fixed)
             const uint4* lrow = buf + lr * cpr + key_stage_swz(lr, j, lgS);
             if ((g + 1) * c.G <= Tq) {
-                quant_store_key_lane_smem<BITS, S>(c, bh, t0, g, j, s, smask, lrow, cpr);
+                quant_store_key_lane_smem<BITS, S, D>(c, bh, t0, g, j, s, smask, lrow);
             } else {
                 for (int i = 0; i < kLaneTokens; ++i) {
                     const int t = t0 + i;
@@ -316,20 +314,31 @@ static dim3 encode_grid(const kivi_cache& c, int tiles)
     return dim3((unsigned)(tiles > 0 ? tiles : 1), (unsigned)(bh < 65535 ? bh : 65535));
 }
 
+template <int BITS, int S, int D>
+static void staged_launch(const kivi_cache& c, const uint16_t* K, int T, const int32_t* seq_lens, cudaStream_t s)
+{
+    constexpr int TT = (kKeyStageBytes / 2) / D;
+    const int tiles_per_seq = (T + TT - 1) / TT;
+    const long ntiles = (long)c.B * c.H * tiles_per_seq;
+    const int grid = (int)std::min<long>(ntiles, (long)sm_count() * 3);
+    const size_t smem = 2 * kKeyStageBytes;
+    cudaFuncSetAttribute(quant_keys_staged_kernel<BITS, S, D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         (int)smem);
+    quant_keys_staged_kernel<BITS, S, D><<<grid, kKeyStageThreads, smem, s>>>(c, K, T, seq_lens, tiles_per_seq);
+}
+
 template <int BITS, int S>
 static void key_launch(const kivi_cache& c, const uint16_t* K, int T, const int32_t* seq_lens, cudaStream_t s)
 {
-    const int lanes_per_group = S * (c.D / kLaneChans);
-    if (lanes_per_group <= kKeyStageThreads) {
-        const int TT = (kKeyStageBytes / 2) / c.D;
-        const int tiles_per_seq = (T + TT - 1) / TT;
-        const long ntiles = (long)c.B * c.H * tiles_per_seq;
-        const int grid = (int)std::min<long>(ntiles, (long)sm_count() * 3);
-        const size_t smem = 2 * kKeyStageBytes;
-        cudaFuncSetAttribute(quant_keys_staged_kernel<BITS, S>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem);
-        quant_keys_staged_kernel<BITS, S><<<grid, kKeyStageThreads, smem, s>>>(c, K, T, seq_lens, tiles_per_seq);
+    // staged when a group column takes at most 128 lanes: S * D / 8 <= 128
+    if (c.D == 64) {
+        staged_launch<BITS, S, 64>(c, K, T, seq_lens, s);
+    } else if (c.D == 128 && S <= 8) {
+        staged_launch<BITS, S, 128>(c, K, T, seq_lens, s);
+    } else if constexpr (S <= 4) {
+        staged_launch<BITS, S, 256>(c, K, T, seq_lens, s);
     } else {
+        const int lanes_per_group = S * (c.D / kLaneChans);
         const int groups_per_cta = kEncodeThreads / lanes_per_group;
         const int groups = (T + c.G - 1) / c.G;
         const dim3 grid = encode_grid(c, (groups + groups_per_cta - 1) / groups_per_cta);
