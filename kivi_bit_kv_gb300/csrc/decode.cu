@@ -87,7 +87,6 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
 
 // ---------------------------------------------------------------- launch ---
 
-int chunk_tokens(const kivi_cache& c, int Hq) { return chunk_plan(c, Hq).TC; }
 int pv_chunks(const kivi_cache& c, int Hq)
 {
     const ChunkPlan cp = chunk_plan(c, Hq);

@@ -12,9 +12,7 @@ namespace kivi {
 // Streaming multiprocessors of the current device (cached per device).
 int sm_count();
 
-// Tokens per decode chunk (one CTA per KV head and chunk) and the number of
-// chunks that cover Tmax.
-int chunk_tokens(const kivi_cache& c, int Hq);
+// Number of decode chunks (one CTA per KV head and chunk) that cover Tmax.
 int pv_chunks(const kivi_cache& c, int Hq);
 
 cudaError_t launch_quant_keys(const kivi_cache& c, const uint16_t* K, int T,
