@@ -52,6 +52,7 @@ struct DecodeSmem {
     uint32_t *kw, *vw;
     float *ks, *kz, *vs, *vz, *p, *part, *zs;
     uint2* bb;
+    bool zs_on_p;  // the zero terms overlay the logits
 };
 
 __device__ __forceinline__ DecodeSmem carve(float* base, const DecodeLayout& L)
@@ -67,6 +68,7 @@ __device__ __forceinline__ DecodeSmem carve(float* base, const DecodeLayout& L)
     m.bb = reinterpret_cast<uint2*>(base + L.bb);
     m.part = base + L.part;
     m.zs = base + L.zs;
+    m.zs_on_p = L.zs_on_p;
     return m;
 }
 
@@ -125,7 +127,7 @@ __device__ __forceinline__ void pv_pass(const kivi_cache& c, size_t bh, int TX, 
         __syncthreads();
     }
     pv_weights<NQB>(n, nq, NGv, threadIdx.x, pv_pairs(n, nq), kDecodeThreads, 0, m.p, ps, mx, m.vs, m.vz,
-                    m.bb, bb_stride(TX), m.zs);
+                    m.bb, bb_stride(TX), m.zs, m.zs_on_p);
     __syncthreads();
     pv_chunk<BITS, NQB, D>(c, bh, TX, r.t_begin, r.tq_end, r.t_end, m.vw, m.bb, m.part);
     __syncthreads();
@@ -244,7 +246,8 @@ inline DecodeLayout cta_layout(const kivi_cache& c, int Hq, bool keys, bool valu
 {
     const int NQ = Hq / c.H, NQB = heads_per_pass(NQ);
     const ChunkPlan cp = chunk_plan(c, Hq);
-    return decode_layout(cp.TC, cp.TC + cp.S, c.D, c.bits_k, c.bits_v, c.G, NQB, NQ > NQB, keys, values);
+    return decode_layout(cp.TC, cp.TC + cp.S, c.D, c.bits_k, c.bits_v, c.G, NQB, NQ > NQB, keys, values,
+                         cp.zs_on_p);
 }
 
 template <class K>

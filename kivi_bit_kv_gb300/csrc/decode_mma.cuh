@@ -198,11 +198,11 @@ __host__ __device__ constexpr int decode_chunks(int n, int TC, int S)
 // Word offsets into a decode kernel's dynamic shared memory: the staged keys
 // and / or values of TC tokens, then the probabilities (logits) and B
 // fragments of up to TX = TC + slack tokens, the split partials when they do
-// not overlay a dead region; the zero terms overlay the logits.
+// not overlay a dead region, and the zero terms (or these on the logits).
 struct DecodeLayout {
     size_t kw, ks, kz, vw, vs, vz;
     size_t p, bb, part, zs, total;
-    bool bb_on_keys, part_on_vstats;
+    bool bb_on_keys, part_on_vstats, zs_on_p;
 };
 
 // keys / values: whether the kernel stages them.  The B fragments overlay the
@@ -210,7 +210,8 @@ struct DecodeLayout {
 // statistics (dead once the B fragments exist) when one pass covers all query
 // heads of the staged chunk.
 __host__ __device__ inline DecodeLayout decode_layout(int TC, int TX, int D, int bits_k, int bits_v, int G,
-                                                      int NQB, bool multipass, bool keys, bool values)
+                                                      int NQB, bool multipass, bool keys, bool values,
+                                                      bool zs_on_p = false)
 {
     DecodeLayout L{};
     size_t o = 0;
@@ -246,9 +247,16 @@ __host__ __device__ inline DecodeLayout decode_layout(int TC, int TX, int D, int
             L.part = o;
             o += part_words(D, NQB);
         }
-        // the zero terms overlay the logits, dead once the B fragments exist
-        // (pv_weights writes them after a barrier)
-        L.zs = L.p;
+        // the zero terms get their own words, or (zs_on_p, when shared memory
+        // is tight) overlay the logits, dead once the B fragments exist:
+        // pv_weights then writes them after a barrier
+        L.zs_on_p = zs_on_p;
+        if (zs_on_p) {
+            L.zs = L.p;
+        } else {
+            L.zs = o;
+            o += zs_words(D, G, NQB);
+        }
     }
     L.total = o;
     return L;
@@ -262,6 +270,7 @@ __host__ __device__ inline DecodeLayout decode_layout(int TC, int TX, int D, int
 // same budget, else 0.
 struct ChunkPlan {
     int TC, S, ctas_per_sm;
+    bool zs_on_p;
 };
 
 // fp32 q row in shared memory: channel d at qpad(d) (4 floats of padding per
@@ -285,18 +294,19 @@ __host__ __device__ inline ChunkPlan decode_chunk_plan(int D, int bits_k, int bi
     const int P = 32 / bits_k;
     const int tok = cmin(8, (8 / NQB) * 32 / P) * P;
     const int tc_min = cmax(cmax(tok, G), 64);
-    auto bytes = [&](int TC, int S) {
-        return 4 * decode_layout(TC, TC + S, D, bits_k, bits_v, G, NQB, NQ > NQB, true, true).total;
+    auto bytes = [&](int TC, int S, bool zp) {
+        return 4 * decode_layout(TC, TC + S, D, bits_k, bits_v, G, NQB, NQ > NQB, true, true, zp).total;
     };
     for (int ctas = 3; ctas >= 1; --ctas) {
         const size_t budget = kSmemPerSM / ctas - kSmemReservedPerCTA - decode_static_smem(D, NQB);
         for (int TC = 1024; TC >= tc_min; TC >>= 1)
-            if (bytes(TC, 0) <= budget) {
-                const int S = max_chunk_slack(TC, R);
-                return {TC, bytes(TC, S) <= budget ? S : 0, ctas};
-            }
+            for (int zp = 0; zp < 2; ++zp)  // the zero terms on the logits only if that makes it fit
+                if (bytes(TC, 0, zp) <= budget) {
+                    const int S = max_chunk_slack(TC, R);
+                    return {TC, bytes(TC, S, zp) <= budget ? S : 0, ctas, zp != 0};
+                }
     }
-    return {tc_min, 0, 1};
+    return {tc_min, 0, 1, true};
 }
 
 inline ChunkPlan chunk_plan(const kivi_cache& c, int Hq)
@@ -655,13 +665,14 @@ __device__ __forceinline__ void chunk_max(float (&m)[NQB], float* red)
 // w = p_ht s_tg for quantized tokens (t < nq) and of w = p_ht for residual
 // tokens (nq <= t < n), zero up to the end of the last 16-token slice.
 // zw[warp][h][g] = the warp's share of sum over quantized t of p_ht z_tg,
-// zw[warp][h][NGV] its share of sum over t of p_ht (zw may overlay p_sm: it
-// is written after a barrier).  One thread per token pair; whole CTA, the
+// zw[warp][h][NGV] its share of sum over t of p_ht (when zw_on_p, zw
+// overlays p_sm and is written after a barrier).  One thread per token pair; whole CTA, the
 // caller's barrier publishes both.
 template <int NQB, int NGV>
 __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_end, int i_step, int i_base,
                                              const float* p_sm, int ps, const float (&mx)[NQB],
-                                             const float* vs, const float* vz, uint2* bb, int bbs, float* zw)
+                                             const float* vs, const float* vz, uint2* bb, int bbs, float* zw,
+                                             bool zw_on_p)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float z[NQB][NGV], l[NQB];
@@ -718,7 +729,8 @@ __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_e
         for (int k = 16; k > 0; k >>= 1)
             l[h] += __shfl_xor_sync(0xffffffffu, l[h], k);
     }
-    __syncthreads();  // zw overlays p_sm: every thread has read its logits
+    if (zw_on_p)
+        __syncthreads();  // zw overlays p_sm: every thread has read its logits
     if (lane == 0)
 #pragma unroll
         for (int h = 0; h < NQB; ++h) {
@@ -736,13 +748,14 @@ __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_e
 template <int NQB>
 __device__ __forceinline__ void pv_weights(int n, int nq, int NGv, int i_first, int i_end, int i_step,
                                            int i_base, const float* p_sm, int ps, const float (&mx)[NQB],
-                                           const float* vs, const float* vz, uint2* bb, int bbs, float* zw)
+                                           const float* vs, const float* vz, uint2* bb, int bbs, float* zw,
+                                           bool zw_on_p)
 {
     switch (NGv) {
-    case 1: pv_weights_g<NQB, 1>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw); break;
-    case 2: pv_weights_g<NQB, 2>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw); break;
-    case 4: pv_weights_g<NQB, 4>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw); break;
-    default: pv_weights_g<NQB, 8>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw); break;
+    case 1: pv_weights_g<NQB, 1>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
+    case 2: pv_weights_g<NQB, 2>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
+    case 4: pv_weights_g<NQB, 4>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
+    default: pv_weights_g<NQB, 8>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
     }
 }
 // Pairs a chunk of n tokens (nq quantized) needs: through the last residual slice.
