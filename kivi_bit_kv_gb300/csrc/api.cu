@@ -224,6 +224,10 @@ static int32_t check_heads(const kivi_cache* c, int32_t Hq)
 {
     if (Hq < c->H || Hq % c->H != 0 || Hq / c->H > 16)
         return fail(KIVI_EINVAL, "Hq=%d must be a multiple of H=%d with Hq/H <= 16", Hq, c->H);
+    // one CTA per (b, h, chunk) in a 1-D grid
+    const long long ctas = (long long)c->B * c->H * kivi::pv_chunks(*c, Hq);
+    if (ctas >= (1ll << 31))
+        return fail(KIVI_EINVAL, "B*H*chunks = %lld decode CTAs; the grid holds fewer than 2^31", ctas);
     return KIVI_OK;
 }
 

@@ -27,12 +27,14 @@ __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2)
     }
 }
 
+// With cache_e false (more chunks than shared memory holds weights for), the
+// weights are recomputed where they are used instead of cached.
 __global__ void __launch_bounds__(kCombineThreads)
 decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunks, int TC, int S,
-                      const float* __restrict__ ws_o, const float* __restrict__ ws_m,
+                      bool cache_e, const float* __restrict__ ws_o, const float* __restrict__ ws_m,
                       const float* __restrict__ ws_l, float* __restrict__ out)
 {
-    extern __shared__ __align__(16) float cmb[];  // e[nchunks], then [rows][C] partial sums
+    extern __shared__ __align__(16) float cmb[];  // e[nchunks] (if cached), then [rows][C] partial sums
     __shared__ float red_m[kDecodeWarps], red_l[kDecodeWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t bhq = blockIdx.x;
@@ -57,8 +59,9 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
 #pragma unroll
     for (int w = 1; w < kDecodeWarps; ++w)
         merge_ml(M, L, red_m[w], red_l[w]);
-    for (int k = threadIdx.x; k < nv; k += kCombineThreads)
-        cmb[k] = expf(mrow[k] - M);
+    if (cache_e)
+        for (int k = threadIdx.x; k < nv; k += kCombineThreads)
+            cmb[k] = expf(mrow[k] - M);
     __syncthreads();
     const int V = C / 4, rows = kCombineThreads / V;  // float4 columns; chunks in flight per round
     const int v = threadIdx.x % V, r0 = threadIdx.x / V;
@@ -67,13 +70,13 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
 #pragma unroll 4
     for (int k = r0; k < nv; k += rows) {
         const float4 o = o4[(size_t)k * (D / 4) + v];
-        const float e = cmb[k];
+        const float e = cache_e ? cmb[k] : expf(mrow[k] - M);
         acc.x = fmaf(o.x, e, acc.x);
         acc.y = fmaf(o.y, e, acc.y);
         acc.z = fmaf(o.z, e, acc.z);
         acc.w = fmaf(o.w, e, acc.w);
     }
-    float4* part = reinterpret_cast<float4*>(cmb + ((nchunks + 3) & ~3));
+    float4* part = reinterpret_cast<float4*>(cmb + (cache_e ? (nchunks + 3) & ~3 : 0));
     part[r0 * V + v] = acc;
     __syncthreads();
     for (int d = threadIdx.x; d < C; d += kCombineThreads) {
@@ -103,14 +106,16 @@ static cudaError_t combine(const kivi_cache& c, int Hq, const float* ws_o, const
     while (ds < c.D / 32 && rows * ds < 2 * sm_count())
         ds *= 2;
     const int C = c.D / ds;
-    const size_t smem = (((size_t)nch + 3) / 4 * 4 + (size_t)(kCombineThreads / (C / 4)) * C) * sizeof(float);
+    const size_t part = (size_t)(kCombineThreads / (C / 4)) * C * sizeof(float);
+    const bool cache_e = ((size_t)nch + 3) / 4 * 4 * sizeof(float) + part <= 160 * 1024;
+    const size_t smem = (cache_e ? ((size_t)nch + 3) / 4 * 4 * sizeof(float) : 0) + part;
     cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
     if (e != cudaSuccess)
         return e;
     const ChunkPlan cp = chunk_plan(c, Hq);
-    decode_combine_kernel<<<dim3(rows, ds), kCombineThreads, smem, s>>>(c.len, Hq, c.D, nch, cp.TC, cp.S, ws_o,
-                                                                       ws_m, ws_l, out);
+    decode_combine_kernel<<<dim3(rows, ds), kCombineThreads, smem, s>>>(c.len, Hq, c.D, nch, cp.TC, cp.S,
+                                                                       cache_e, ws_o, ws_m, ws_l, out);
     return cudaGetLastError();
 }
 

@@ -22,22 +22,26 @@
 
 namespace kivi {
 
-// Per-CTA coordinates of decode chunk ci: TC tokens, or up to TC + S for the
-// last chunk of a sequence (decode_chunks).  Chunks run in reverse order of
-// blockIdx.y, so the last chunks of the sequences, which also carry the
-// residual tokens, are dispatched first and full chunks fill the tail.
+// Per-CTA coordinates of decode chunk ci of slice bh: TC tokens, or up to
+// TC + S for the last chunk of a sequence (decode_chunks).  The 1-D grid holds
+// B H nchunks CTAs, slice fastest; chunks run in reverse order, so the last
+// chunks of the sequences, which also carry the residual tokens, are
+// dispatched first and full chunks fill the tail.
 struct ChunkRange {
-    int b, h, n, ci, t_begin, t_end, Tq, tq_end;
+    int bh, b, h, n, ci, t_begin, t_end, Tq, tq_end;
 };
 
 __device__ __forceinline__ bool chunk_range(const kivi_cache& c, int TC, int S, ChunkRange& r)
 {
-    const int bh = (int)blockIdx.x;
+    const int BH = c.B * c.H;
+    const int y = (int)(blockIdx.x / BH);
+    const int bh = (int)blockIdx.x - y * BH;
+    r.bh = bh;
     r.b = bh / c.H;
     r.h = bh - r.b * c.H;
     r.n = c.len[r.b];
     const int nch = decode_chunks(r.n, TC, S);
-    r.ci = (int)(gridDim.y - 1 - blockIdx.y);
+    r.ci = (int)(gridDim.x / BH) - 1 - y;
     if (r.ci >= nch)
         return false;
     r.t_begin = r.ci * TC;
@@ -87,7 +91,7 @@ decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_
     ChunkRange r;
     if (!chunk_range(c, TC, S, r))
         return;
-    const size_t bh = blockIdx.x;
+    const size_t bh = r.bh;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const DecodeSmem m = carve(dsm, L);
     stage_keys<BITS, T::TOK, D>(c, bh, r.t_begin, r.tq_end, m.kw, m.ks, m.kz);
@@ -146,7 +150,7 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
     ChunkRange r;
     if (!chunk_range(c, TC, S, r))
         return;
-    const size_t bh = blockIdx.x;
+    const size_t bh = r.bh;
     const DecodeSmem m = carve(dsm, L);
     stage_values<BITS, D>(c, bh, r.t_begin, r.tq_end, m.vw, m.vs, m.vz);
     cp_async_commit();
@@ -194,7 +198,7 @@ decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, fl
     ChunkRange r;
     if (!chunk_range(c, TC, S, r))
         return;
-    const size_t bh = blockIdx.x;
+    const size_t bh = r.bh;
     const int warp = threadIdx.x >> 5;
     const int NQ = Hq / c.H;
     const DecodeSmem m = carve(dsm, L);
@@ -256,8 +260,9 @@ inline cudaError_t set_smem(K kern, size_t bytes)
     return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
 }
 
-// Grid of the decode kernels: one CTA per (KV head, chunk).
-inline dim3 decode_grid(const kivi_cache& c, int Hq) { return dim3(c.B * c.H, pv_chunks(c, Hq)); }
+// Grid of the decode kernels: one CTA per (KV head, chunk), 1-D (the host
+// keeps B H nchunks below 2^31).
+inline dim3 decode_grid(const kivi_cache& c, int Hq) { return dim3((unsigned)(c.B * c.H * pv_chunks(c, Hq))); }
 
 template <int D, int BITS, int NQB>
 cudaError_t qk_launch(const kivi_cache& c, const uint16_t* q, int Hq, float sm, float* logits, int ldl,

@@ -81,6 +81,24 @@ def test_encode_dequant_decode_small(cuda, case):
     compare_attention(lg, o, rlg, ro, lens, fused=fo)
 
 
+def test_decode_many_chunks(cuda):
+    """A capacity of 2^24 tokens in 256-token chunks: 65536 chunk partials per
+    row, more weights than the combine kernel keeps in shared memory, so it
+    recomputes them where it uses them.  Results as for any other shape."""
+    B, H, Hq, D, bits, G, Rr, T = 1, 1, 2, 64, 8, 32, 0, 3000
+    K = f16_host((B, H, T, D), 21, 2.0)
+    V = f16_host((B, H, T, D), 22)
+    q = f16_host((B, Hq, D), 23)
+    cache = new_cache(B, H, D, bits, bits, G, Rr, 1 << 24, cuda)
+    gpu_encode(cache, K, V)
+    rc = R.RefCache(B, H, D, bits, bits, G, Rr, roundup(T, G)).encode(np16(K), np16(V))
+    lg, o, fo = gpu_decode(cache, q)
+    rlg, ro = rc.attention(np16(q))
+    compare_attention(lg[:, :, :T], o, rlg, ro, rc.lens, fused=fo)
+    del cache
+    torch.cuda.empty_cache()
+
+
 def test_decode_is_deterministic(cuda):
     B, H, Hq, D, T = 2, 2, 4, 128, 3000
     K, V = f16_host((B, H, T, D), 5, 2.0), f16_host((B, H, T, D), 6)
