@@ -130,7 +130,7 @@ __device__ __forceinline__ void pv_pass(const kivi_cache& c, size_t bh, int TX, 
         cp_async_wait_all();  // the staged values
         __syncthreads();
     }
-    pv_weights<NQB>(n, nq, NGv, threadIdx.x, pv_pairs(n, nq), kDecodeThreads, 0, m.p, ps, mx, m.vs, m.vz,
+    pv_weights<NQB>(n, nq, NGv, threadIdx.x, pv_pairs(n, nq), kDecodeThreads, m.p, ps, mx, m.vs, m.vz,
                     m.bb, bb_stride(TX), m.zs, m.zs_on_p);
     __syncthreads();
     pv_chunk<BITS, NQB, D>(c, bh, TX, r.t_begin, r.tq_end, r.t_end, m.vw, m.bb, m.part);

@@ -669,7 +669,7 @@ __device__ __forceinline__ void chunk_max(float (&m)[NQB], float* red)
 // overlays p_sm and is written after a barrier).  One thread per token pair; whole CTA, the
 // caller's barrier publishes both.
 template <int NQB, int NGV>
-__device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_end, int i_step, int i_base,
+__device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_end, int i_step,
                                              const float* p_sm, int ps, const float (&mx)[NQB],
                                              const float* vs, const float* vz, uint2* bb, int bbs, float* zw,
                                              bool zw_on_p)
@@ -717,7 +717,7 @@ __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_e
                 const int r = gg * NQB + h;
                 uint2 hl;
                 split_hi_lo(e0[h] * s0[gg], e1[h] * s1[gg], hl.x, hl.y);
-                bb[r * bbs + ((i - i_base) ^ bb_swz(r))] = hl;
+                bb[r * bbs + (i ^ bb_swz(r))] = hl;
             }
     }
 #pragma unroll
@@ -741,21 +741,19 @@ __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_e
         }
 }
 
-// Pairs i_first, i_first + i_step, ... below i_end; bb holds pairs from
-// i_base on (i_base = 0 for a whole-chunk array, the warp's first pair for a
-// warp-private one).  Pairs past the last token (up to the end of the last
-// 16-token slice) get zero weights.
+// Pairs i_first, i_first + i_step, ... below i_end of the chunk.  Pairs past
+// the last token (up to the end of the last 16-token slice) get zero weights.
 template <int NQB>
 __device__ __forceinline__ void pv_weights(int n, int nq, int NGv, int i_first, int i_end, int i_step,
-                                           int i_base, const float* p_sm, int ps, const float (&mx)[NQB],
+                                           const float* p_sm, int ps, const float (&mx)[NQB],
                                            const float* vs, const float* vz, uint2* bb, int bbs, float* zw,
                                            bool zw_on_p)
 {
     switch (NGv) {
-    case 1: pv_weights_g<NQB, 1>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
-    case 2: pv_weights_g<NQB, 2>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
-    case 4: pv_weights_g<NQB, 4>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
-    default: pv_weights_g<NQB, 8>(n, nq, i_first, i_end, i_step, i_base, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
+    case 1: pv_weights_g<NQB, 1>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
+    case 2: pv_weights_g<NQB, 2>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
+    case 4: pv_weights_g<NQB, 4>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
+    default: pv_weights_g<NQB, 8>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
     }
 }
 // Pairs a chunk of n tokens (nq quantized) needs: through the last residual slice.
@@ -771,7 +769,7 @@ __host__ __device__ constexpr int pv_seg_groups(int D) { return D / (32 / BITS) 
 // p . V_hat for NQB query heads and the channels of segment group sp (SPL
 // segments of 8 halves each) with the staged values of the chunk at t_begin
 // (vw, val_swz layout) and B fragments of pv_weights (pair i of the chunk at
-// bb pair i - i_base).  Quantized 16-token slices k = kq, kq + kstep, ...
+// bb pair i).  Quantized 16-token slices k = kq, kq + kstep, ...
 // below kq_end through ldmatrix.trans; residual slices kr, kr + kstep, ...
 // below kr_end (tokens tq_end + 16 kr ...) from the fp16 ring with the raw
 // values as A.  Writes o_out[h][d] (no zero terms) for the segment group's
@@ -779,7 +777,7 @@ __host__ __device__ constexpr int pv_seg_groups(int D) { return D / (32 / BITS) 
 template <int BITS, int NQB, int D>
 __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_begin, int tq_end,
                                         int t_end, const uint32_t* vw, const uint2* bb, int bbs,
-                                        int i_base, int sp, int kq, int kq_end, int kr, int kr_end,
+                                        int sp, int kq, int kq_end, int kr, int kr_end,
                                         int kstep, float* o_out)
 {
     using T = ValTile<BITS>;
@@ -832,11 +830,11 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
             uint2 b01, b23;
             if constexpr (HL) {
                 const uint32_t* b32 = reinterpret_cast<const uint32_t*>(bp[s]) + part;
-                b01.x = b32[2 * ((k * 8 + tg - i_base) ^ bx[s])];
-                b23.x = b32[2 * ((k * 8 + 4 + tg - i_base) ^ bx[s])];
+                b01.x = b32[2 * ((k * 8 + tg) ^ bx[s])];
+                b23.x = b32[2 * ((k * 8 + 4 + tg) ^ bx[s])];
             } else {
-                b01 = bp[s][(k * 8 + tg - i_base) ^ bx[s]];
-                b23 = bp[s][(k * 8 + 4 + tg - i_base) ^ bx[s]];
+                b01 = bp[s][(k * 8 + tg) ^ bx[s]];
+                b23 = bp[s][(k * 8 + 4 + tg) ^ bx[s]];
             }
             const uint32_t Rl = R[2 * s], Rh = R[2 * s + 1];
             const uint32_t Rls = Rl >> T::SHIFT, Rhs = Rh >> T::SHIFT;
@@ -901,11 +899,11 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
             uint2 b01, b23;
             if constexpr (HL) {
                 const uint32_t* b32 = reinterpret_cast<const uint32_t*>(bp[s]) + part;
-                b01.x = b32[2 * ((nq2 + k * 8 + tg - i_base) ^ bx[s])];
-                b23.x = b32[2 * ((nq2 + k * 8 + 4 + tg - i_base) ^ bx[s])];
+                b01.x = b32[2 * ((nq2 + k * 8 + tg) ^ bx[s])];
+                b23.x = b32[2 * ((nq2 + k * 8 + 4 + tg) ^ bx[s])];
             } else {
-                b01 = bp[s][(nq2 + k * 8 + tg - i_base) ^ bx[s]];
-                b23 = bp[s][(nq2 + k * 8 + 4 + tg - i_base) ^ bx[s]];
+                b01 = bp[s][(nq2 + k * 8 + tg) ^ bx[s]];
+                b23 = bp[s][(nq2 + k * 8 + 4 + tg) ^ bx[s]];
             }
 #pragma unroll
             for (int j = 0; j < T::NT; ++j) {
@@ -966,7 +964,7 @@ __device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TX,
     const int nr_slices = (t_end - tq_end + 15) / 16;
     for (int unit = threadIdx.x >> 5; unit < NSP * NSPLIT; unit += kDecodeWarps) {
         const int sp = unit % NSP, split = unit / NSP;
-        pv_unit<BITS, NQB, D>(c, bh, t_begin, tq_end, t_end, vw, bb, bb_stride(TX), 0, sp, split, nq_slices,
+        pv_unit<BITS, NQB, D>(c, bh, t_begin, tq_end, t_end, vw, bb, bb_stride(TX), sp, split, nq_slices,
                               split, nr_slices, NSPLIT, o_part + (size_t)split * NQB * D);
     }
 }
