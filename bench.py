@@ -419,22 +419,38 @@ def run_c2c(cache, dev, reps: int = 5) -> dict:
 
 def run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq, calls):
     """Same step through the public API from pinned host buffers: H2D of the
-    step's K, V, q and new token, the step, D2H of the attention output."""
+    step's K, V, q and new token, the step, D2H of the attention output.
+    Double-buffered the way a serving loop would run it: a copy stream moves
+    step i+1's inputs into the other pair of device buffers while step i
+    computes, so every step's copy is inside the timed region and the compute
+    hides behind it."""
     import torch
     from kivi_bit_kv_gb300 import abi
     from kivi_bit_kv_gb300 import workloads as W
     Kh, Vh = (t.pin_memory() for t in W.make_kv(w, device="cpu"))
     qh = W.make_q(w, "cpu").pin_memory()
     knh, vnh = (t[0].contiguous().pin_memory() for t in W.make_step_tokens(w, 1, "cpu"))
-    Kd, Vd = torch.empty_like(Kh, device=dev), torch.empty_like(Vh, device=dev)
-    qd, knd, vnd = (torch.empty_like(t, device=dev) for t in (qh, knh, vnh))
+    hosts = (Kh, Vh, qh, knh, vnh)
+    bufs = [tuple(torch.empty_like(h, device=dev) for h in hosts) for _ in range(2)]
     outh = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     stream = torch.cuda.current_stream(dev)
+    copy = torch.cuda.Stream(dev)
+    ready = [torch.cuda.Event() for _ in range(2)]  # inputs of the buffer copied
+    free = [torch.cuda.Event() for _ in range(2)]   # the buffer's last step done
     n = max(3, args.steps // 20)
 
-    def step():
-        for d, h in ((Kd, Kh), (Vd, Vh), (qd, qh), (knd, knh), (vnd, vnh)):
-            d.copy_(h, non_blocking=True)
+    def issue_copy(i):
+        b = i % 2
+        copy.wait_event(free[b])
+        with torch.cuda.stream(copy):
+            for d, h in zip(bufs[b], hosts):
+                d.copy_(h, non_blocking=True)
+        ready[b].record(copy)
+
+    def compute(i):
+        b = i % 2
+        stream.wait_event(ready[b])
+        Kd, Vd, qd, knd, vnd = bufs[b]
         abi.kivi_quant_keys(cache, Kd)
         abi.kivi_quant_values(cache, Vd)
         abi.kivi_dequant(cache, 0, kh)
@@ -445,24 +461,33 @@ def run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq, cal
         else:
             abi.kivi_decode_qk(cache, qd, logits)
             abi.kivi_decode_pv(cache, logits, out, ws)
+        free[b].record(stream)
         outh.copy_(out, non_blocking=True)
 
-    for _ in range(2):
-        step()
+    def run(steps, start=None):
+        if start is not None:
+            copy.wait_event(start)
+        issue_copy(0)
+        for i in range(steps):
+            if i + 1 < steps:
+                issue_copy(i + 1)
+            compute(i)
+
+    run(2)
     torch.cuda.synchronize(dev)
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
     t0.record(stream)
-    for _ in range(n):
-        step()
+    run(n, start=t0)
     t1.record(stream)
     torch.cuda.synchronize(dev)
     ms = reduce_max(t0.elapsed_time(t1), dev)
-    bi = sum(t.numel() * t.element_size() for t in (Kh, Vh, qh, knh, vnh))
+    bi = sum(t.numel() * t.element_size() for t in hosts)
     bo = outh.numel() * outh.element_size()
     return {"value": round(whole_job_value(eq, world, ms / n), 1), "unit": UNIT,
-            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n}
+            "h2d_bytes_per_step": bi, "d2h_bytes_per_step": bo, "steps": n,
+            "pipeline": "inputs of step i+1 copied on a second stream while step i computes"}
 
 
 # ------------------------------------------------------ CPU oracle legs --
