@@ -39,6 +39,9 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t bhq = blockIdx.x;
     const int C = D / gridDim.y, c0 = blockIdx.y * C;
+    // launched as a programmatic dependent of the chunk kernel: wait for its
+    // partials (a no-op for an ordinary launch)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int n = len[bhq / Hq];
     const int nv = decode_chunks(n, TC, S);
     const float* mrow = ws_m + bhq * nchunks;
@@ -114,8 +117,25 @@ static cudaError_t combine(const kivi_cache& c, int Hq, const float* ws_o, const
     if (e != cudaSuccess)
         return e;
     const ChunkPlan cp = chunk_plan(c, Hq);
-    decode_combine_kernel<<<dim3(rows, ds), kCombineThreads, smem, s>>>(c.len, Hq, c.D, nch, cp.TC, cp.S,
-                                                                       cache_e, ws_o, ws_m, ws_l, out);
+    // programmatic dependent launch: the combine CTAs are scheduled while the
+    // chunk kernel drains and wait in griddepcontrol.wait for its results
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(rows, ds);
+    cfg.blockDim = dim3(kCombineThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel, c.len, Hq, c.D, nch, cp.TC, cp.S, cache_e,
+                           (const float*)ws_o, (const float*)ws_m, (const float*)ws_l, out);
+    if (e != cudaSuccess) {  // attribute not supported: an ordinary launch
+        (void)cudaGetLastError();
+        decode_combine_kernel<<<dim3(rows, ds), kCombineThreads, smem, s>>>(c.len, Hq, c.D, nch, cp.TC, cp.S,
+                                                                           cache_e, ws_o, ws_m, ws_l, out);
+    }
     return cudaGetLastError();
 }
 

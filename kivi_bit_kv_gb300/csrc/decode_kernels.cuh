@@ -147,6 +147,9 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
 {
     extern __shared__ __align__(16) float dsm[];
     __shared__ float red[kDecodeWarps * NQB];
+    // the combine kernel may launch once every chunk CTA has started: it waits
+    // for this grid's results in griddepcontrol.wait
+    asm volatile("griddepcontrol.launch_dependents;");
     ChunkRange r;
     if (!chunk_range(c, TC, S, r))
         return;
@@ -195,6 +198,9 @@ decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, fl
     __shared__ float fac[NQB];
     __shared__ float red[kDecodeWarps * NQB];
     using T = KeyTile<BITS, NQB>;
+    // the combine kernel may launch once every chunk CTA has started: it waits
+    // for this grid's results in griddepcontrol.wait
+    asm volatile("griddepcontrol.launch_dependents;");
     ChunkRange r;
     if (!chunk_range(c, TC, S, r))
         return;
