@@ -70,8 +70,8 @@ def load(path: str | None = None):
         return _LIB
     p = path or LIB_PATH
     if not os.path.exists(p):
-        raise ImportError(f"{p} is missing: build it with kivi_bit_kv_gb300.build.build() "
-                          "(or __graft_entry__.build()); there is no fallback path")
+        raise ImportError(f"{p} is missing: build it with kivi_bit_kv_gb300.build.build(); "
+                          "there is no fallback path")
     L = C.CDLL(p)
     vp, i32, f32, sz = C.c_void_p, C.c_int32, C.c_float, C.c_size_t
     cp = C.POINTER(kivi_cache)
