@@ -99,6 +99,33 @@ def test_decode_many_chunks(cuda):
     torch.cuda.empty_cache()
 
 
+def test_more_slices_than_a_grid_dimension(cuda):
+    """66000 (b, h) slices, more than one grid dimension holds (65535): the
+    encode and materialize kernels loop over slices, decode runs on a 1-D
+    grid.  Sampled batch rows are compared with the oracle run on those rows
+    alone (slices are independent)."""
+    B, H, Hq, D, bits, G, Rr, T = 33000, 2, 4, 64, 4, 32, 0, 70
+    Tmax = roundup(T + 8, G)
+    K = f16_host((B, H, T, D), 31, 2.0)
+    V = f16_host((B, H, T, D), 32)
+    q = f16_host((B, Hq, D), 33)
+    cache = new_cache(B, H, D, bits, bits, G, Rr, Tmax, cuda)
+    gpu_encode(cache, K, V)
+    rows = [0, 1, 16383, 32767, 32768, B - 1]
+    rc = R.RefCache(len(rows), H, D, bits, bits, G, Rr, Tmax).encode(np16(K[rows]), np16(V[rows]))
+    compare_state(state(cache, rows), rc)
+    out = torch.zeros((B, H, T, D), dtype=torch.float16, device=cuda)
+    abi.kivi_dequant(cache, 1, out)
+    torch.cuda.synchronize()
+    ex, tot = compare_dequant(np16(out[rows]).view(np.uint16), rc.decode(1, T_out=T), rc.lens)
+    assert ex == tot
+    lg, o, fo = gpu_decode(cache, q)
+    rlg, ro = rc.attention(np16(q[rows]))
+    compare_attention(lg[rows][:, :, :T], o[rows], rlg, ro, rc.lens, fused=fo[rows])
+    del cache, out
+    torch.cuda.empty_cache()
+
+
 def test_decode_is_deterministic(cuda):
     B, H, Hq, D, T = 2, 2, 4, 128, 3000
     K, V = f16_host((B, H, T, D), 5, 2.0), f16_host((B, H, T, D), 6)
