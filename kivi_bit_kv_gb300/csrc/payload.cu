@@ -7,9 +7,11 @@
 // CPU-GPU link without a staging copy), and one kernel scatters a payload
 // back into a cache.
 //
-// Every CTA recomputes the payload geometry from len[] (the slice offsets are
-// prefix sums of kivi_cache_bytes over the sequences), so the kernels need no
-// scratch memory and no second launch; the copies move 16-byte units.
+// Each row of CTAs takes a contiguous range of slices and computes the first
+// slice's offset from len[] (a prefix sum of kivi_cache_bytes over the
+// sequences, one block-wide scan), the others by adding slice sizes, so the
+// kernels need no scratch memory and no second launch; the copies move
+// 16-byte units.
 #include <algorithm>
 
 #include "kivi_device.cuh"
@@ -137,42 +139,56 @@ __device__ __forceinline__ int section_of(const SliceGeom& g, uint32_t u, uint32
     return s;
 }
 
+// Slices of CTA row blockIdx.y: a contiguous range [bh0, bh1) of the B H
+// slices, so one prefix scan gives the first offset and the others follow.
+__device__ __forceinline__ bool slice_range(const kivi_cache& c, int& bh0, int& bh1)
+{
+    const int BH = c.B * c.H;
+    const int per = (BH + gridDim.y - 1) / gridDim.y;
+    bh0 = blockIdx.y * per;
+    bh1 = min(BH, bh0 + per);
+    return bh0 < bh1;
+}
+
 __global__ void __launch_bounds__(kPayloadThreads)
 export_kernel(kivi_cache c, uint4* __restrict__ dst, size_t dst_units, uint64_t fingerprint, int32_t* status)
 {
-    const int BH = c.B * c.H;
-    for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
-        const int b = bh / c.H, h = bh - b * c.H;
-        const PayloadScan ps = payload_scan(c, c.len, b);
-        if (ps.bad)
-            return;  // len[] is the library's own state: cannot happen
-        if (ps.total > dst_units) {
-            if (blockIdx.x == 0 && bh == 0 && threadIdx.x == 0)
-                *status = KIVI_EWORKSPACE;
-            return;
+    int bh0, bh1;
+    if (!slice_range(c, bh0, bh1))
+        return;
+    const PayloadScan ps = payload_scan(c, c.len, bh0 / c.H);
+    if (ps.bad)
+        return;  // len[] is the library's own state: cannot happen
+    if (ps.total > dst_units) {
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+            *status = KIVI_EWORKSPACE;
+        return;
+    }
+    if (blockIdx.x == 0 && blockIdx.y == 0) {
+        uint32_t* hd = reinterpret_cast<uint32_t*>(dst);
+        const int32_t fields[7] = {c.B, c.H, c.D, c.bits_k, c.bits_v, c.G, c.R};
+        for (int i = threadIdx.x; i < 16 + 4 * (int)(head_units(c.B) - 4); i += kPayloadThreads) {
+            uint32_t w = 0;
+            if (i == 0) w = KIVI_PAYLOAD_MAGIC;
+            else if (i == 1) w = KIVI_PAYLOAD_VERSION;
+            else if (i == 2) w = (uint32_t)fingerprint;
+            else if (i == 3) w = (uint32_t)(fingerprint >> 32);
+            else if (i < 11) w = (uint32_t)fields[i - 4];
+            else if (i >= 16 && i - 16 < c.B) w = (uint32_t)c.len[i - 16];
+            hd[i] = w;
         }
-        if (blockIdx.x == 0 && bh == 0) {
-            uint32_t* hd = reinterpret_cast<uint32_t*>(dst);
-            const int32_t fields[7] = {c.B, c.H, c.D, c.bits_k, c.bits_v, c.G, c.R};
-            for (int i = threadIdx.x; i < 16 + 4 * (int)(head_units(c.B) - 4); i += kPayloadThreads) {
-                uint32_t w = 0;
-                if (i == 0) w = KIVI_PAYLOAD_MAGIC;
-                else if (i == 1) w = KIVI_PAYLOAD_VERSION;
-                else if (i == 2) w = (uint32_t)fingerprint;
-                else if (i == 3) w = (uint32_t)(fingerprint >> 32);
-                else if (i < 11) w = (uint32_t)fields[i - 4];
-                else if (i >= 16 && i - 16 < c.B) w = (uint32_t)c.len[i - 16];
-                hd[i] = w;
-            }
-        }
-        const SliceGeom g = slice_geom(c.len[b], c.D, c.bits_k, c.bits_v, c.G, c.R);
-        const size_t off = ps.base + (size_t)h * slice_units(g);
+    }
+    size_t off = ps.base;  // offset of slice (bh0 / H, 0)
+    for (int bh = bh0 - bh0 % c.H; bh < bh1; ++bh) {
+        const SliceGeom g = slice_geom(c.len[bh / c.H], c.D, c.bits_k, c.bits_v, c.G, c.R);
         const uint32_t U = (uint32_t)slice_units(g);
-        for (uint32_t u = blockIdx.x * kPayloadThreads + threadIdx.x; u < U; u += gridDim.x * kPayloadThreads) {
-            uint32_t r;
-            const int s = section_of(g, u, r);
-            dst[off + u] = ld_nc(reinterpret_cast<const uint16_t*>(cache_unit(c, bh, g, s, r)));
-        }
+        if (bh >= bh0)
+            for (uint32_t u = blockIdx.x * kPayloadThreads + threadIdx.x; u < U; u += gridDim.x * kPayloadThreads) {
+                uint32_t r;
+                const int s = section_of(g, u, r);
+                dst[off + u] = ld_nc(reinterpret_cast<const uint16_t*>(cache_unit(c, bh, g, s, r)));
+            }
+        off += U;
     }
 }
 
@@ -193,34 +209,41 @@ import_kernel(kivi_cache c, const uint4* __restrict__ src, size_t src_units, uin
         return;
     }
     const int32_t* lens = reinterpret_cast<const int32_t*>(hd + 16);
-    const int BH = c.B * c.H;
-    for (int bh = blockIdx.y; bh < BH; bh += gridDim.y) {
-        const int b = bh / c.H, h = bh - b * c.H;
-        const PayloadScan ps = payload_scan(c, lens, b);
-        if (ps.bad || ps.total > src_units) {
-            if (blockIdx.x == 0 && bh == 0 && threadIdx.x == 0)
-                *status = ps.bad ? KIVI_ECAPACITY : KIVI_EWORKSPACE;
-            return;
-        }
-        const int n = lens[b];
+    int bh0, bh1;
+    if (!slice_range(c, bh0, bh1))
+        return;
+    const PayloadScan ps = payload_scan(c, lens, bh0 / c.H);
+    if (ps.bad || ps.total > src_units) {
+        if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+            *status = ps.bad ? KIVI_ECAPACITY : KIVI_EWORKSPACE;
+        return;
+    }
+    size_t off = ps.base;  // offset of slice (bh0 / H, 0)
+    for (int bh = bh0 - bh0 % c.H; bh < bh1; ++bh) {
+        const int b = bh / c.H, n = lens[b];
         const SliceGeom g = slice_geom(n, c.D, c.bits_k, c.bits_v, c.G, c.R);
-        const size_t off = ps.base + (size_t)h * slice_units(g);
         const uint32_t U = (uint32_t)slice_units(g);
-        for (uint32_t u = blockIdx.x * kPayloadThreads + threadIdx.x; u < U; u += gridDim.x * kPayloadThreads) {
-            uint32_t r;
-            const int s = section_of(g, u, r);
-            *cache_unit(c, bh, g, s, r) = src[off + u];
+        if (bh >= bh0) {
+            for (uint32_t u = blockIdx.x * kPayloadThreads + threadIdx.x; u < U; u += gridDim.x * kPayloadThreads) {
+                uint32_t r;
+                const int s = section_of(g, u, r);
+                *cache_unit(c, bh, g, s, r) = src[off + u];
+            }
+            if (bh % c.H == 0 && blockIdx.x == 0 && threadIdx.x == 0)
+                c.len[b] = n;
         }
-        if (h == 0 && blockIdx.x == 0 && threadIdx.x == 0)
-            c.len[b] = n;
+        off += U;
     }
 }
 
+// Rows of CTAs over contiguous slice ranges (at most four rows per SM), and
+// CTAs per row splitting each slice's units when there are few slices.
 static dim3 payload_grid(const kivi_cache& c)
 {
     const int BH = c.B * c.H;
+    const int y = std::min(BH, 4 * sm_count());
     const int x = std::max(1, std::min(64, (4 * sm_count() + BH - 1) / BH));
-    return dim3((unsigned)x, (unsigned)std::min(BH, 65535));
+    return dim3((unsigned)x, (unsigned)y);
 }
 
 size_t payload_bytes(const kivi_cache& c, const int32_t* lens)

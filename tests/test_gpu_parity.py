@@ -122,7 +122,22 @@ def test_more_slices_than_a_grid_dimension(cuda):
     lg, o, fo = gpu_decode(cache, q)
     rlg, ro = rc.attention(np16(q[rows]))
     compare_attention(lg[rows][:, :, :T], o[rows], rlg, ro, rc.lens, fused=fo[rows])
-    del cache, out
+    # compact payload round trip on the device: every slice's offset
+    n = abi.kivi_payload_bytes(cache.desc, cache.lens.cpu().tolist())
+    buf = torch.empty(n, dtype=torch.uint8, device=cuda)
+    status = torch.zeros(1, dtype=torch.int32, device=cuda)
+    abi.kivi_export(cache, buf, status)
+    fresh = new_cache(B, H, D, bits, bits, G, Rr, Tmax, cuda)
+    abi.kivi_import(fresh, buf, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    Tq = R.quantized_tokens(T, G, Rr)
+    for name, used in (("kq", Tq * bits // 32), ("kscale", Tq // G), ("kzero", Tq // G), ("vq", Tq),
+                       ("vscale", Tq), ("vzero", Tq)):
+        assert torch.equal(getattr(fresh, name)[:, :, :used], getattr(cache, name)[:, :, :used]), name
+    assert torch.equal(fresh.lens, cache.lens)
+    compare_state(state(fresh, rows), rc)
+    del cache, out, fresh, buf
     torch.cuda.empty_cache()
 
 
