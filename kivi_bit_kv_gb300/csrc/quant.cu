@@ -212,8 +212,21 @@ quant_keys_staged_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
             if (rows > 0) {
                 const uint16_t* src = K + ((size_t)bh * T + tt0) * D + cx * 8;
                 uint4* dst = kst + (size_t)buf * (kKeyStageBytes / 16);
-                for (int r = cr; r < rows; r += rsweep)
-                    cp_async16(dst + r * cpr + key_stage_swz(r, cx, lgS), src + (size_t)r * D);
+                if (rows == TT) {
+                    // a full tile: TT / rsweep copies per thread; row r = cr + rsweep k with
+                    // cr < rsweep <= 16, so the swizzle term (r / 16) mod S is a constant per k
+                    static_assert(rsweep <= 16 && 16 % rsweep == 0, "row sweep");
+#pragma unroll
+                    for (int k = 0; k < TT / rsweep; ++k) {
+                        constexpr int sh = 3 - lgS;
+                        const int v = ((rsweep * k) >> 4) & (S - 1);
+                        cp_async16(dst + (cr + rsweep * k) * cpr + (cx ^ (v << sh)),
+                                   src + (size_t)(cr + rsweep * k) * D);
+                    }
+                } else {
+                    for (int r = cr; r < rows; r += rsweep)
+                        cp_async16(dst + r * cpr + key_stage_swz(r, cx, lgS), src + (size_t)r * D);
+                }
             }
         }
         cp_async_commit();
