@@ -45,7 +45,6 @@ __host__ __device__ __forceinline__ SliceGeom slice_geom(int n, int D, int bits_
 __host__ __device__ __forceinline__ size_t slice_units(const SliceGeom& g)
 {
     size_t s = 0;
-#pragma unroll
     for (int i = 0; i < 8; ++i)
         s += g.u[i];
     return s;
