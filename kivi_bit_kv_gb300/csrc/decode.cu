@@ -13,8 +13,10 @@ namespace kivi {
 // over the chunks c that hold tokens of sequence b.  CTA (b hq, y) writes
 // channels [y C, y C + C), C = D / gridDim.y: one merge of the (m, l) pairs
 // (each thread folds its chunks with the usual rescaling, then warps and
-// warps' results in a fixed order), the chunk weights to shared memory, and
-// the weighted sum with one 16-byte load per (chunk, column) and thread.
+// warps' results in a fixed order) and the weighted sum with one 16-byte load
+// per (chunk, column) and thread.  The first rows of o and their maxima are
+// loaded together with the (m, l) pairs, so the merge costs one round trip to
+// L2 after the chunk kernel's results become visible.
 constexpr int kCombineThreads = 128;
 
 __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2)
@@ -27,25 +29,35 @@ __device__ __forceinline__ void merge_ml(float& m, float& l, float m2, float l2)
     }
 }
 
-// With cache_e false (more chunks than shared memory holds weights for), the
-// weights are recomputed where they are used instead of cached.
 __global__ void __launch_bounds__(kCombineThreads)
 decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunks, int TC, int S,
-                      bool cache_e, const float* __restrict__ ws_o, const float* __restrict__ ws_m,
+                      const float* __restrict__ ws_o, const float* __restrict__ ws_m,
                       const float* __restrict__ ws_l, float* __restrict__ out)
 {
-    extern __shared__ __align__(16) float cmb[];  // e[nchunks] (if cached), then [rows][C] partial sums
+    __shared__ __align__(16) float4 part[kCombineThreads];  // [rows][V] column sums
     __shared__ float red_m[kDecodeWarps], red_l[kDecodeWarps];
+    constexpr int KP = 4;  // rows of o each thread loads before the merge
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const size_t bhq = blockIdx.x;
     const int C = D / gridDim.y, c0 = blockIdx.y * C;
-    // launched as a programmatic dependent of the chunk kernel: wait for its
-    // partials (a no-op for an ordinary launch)
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int n = len[bhq / Hq];
+    const int V = C / 4, rows = kCombineThreads / V;
+    const int v = threadIdx.x % V, r0 = threadIdx.x / V;
+    const int n = len[bhq / Hq];  // not written by the chunk kernel: read before the wait
     const int nv = decode_chunks(n, TC, S);
     const float* mrow = ws_m + bhq * nchunks;
     const float* lrow = ws_l + bhq * nchunks;
+    const float4* o4 = reinterpret_cast<const float4*>(ws_o + bhq * nchunks * D + c0);
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    float4 op[KP];
+    float mp[KP];
+#pragma unroll
+    for (int i = 0; i < KP; ++i) {
+        const int k = r0 + i * rows;
+        if (k < nv) {
+            op[i] = o4[(size_t)k * (D / 4) + v];
+            mp[i] = mrow[k];
+        }
+    }
     float m = -INFINITY, l = 0.0f;
     for (int k = threadIdx.x; k < nv; k += kCombineThreads)
         merge_ml(m, l, mrow[k], lrow[k]);
@@ -62,24 +74,26 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
 #pragma unroll
     for (int w = 1; w < kDecodeWarps; ++w)
         merge_ml(M, L, red_m[w], red_l[w]);
-    if (cache_e)
-        for (int k = threadIdx.x; k < nv; k += kCombineThreads)
-            cmb[k] = expf(mrow[k] - M);
-    __syncthreads();
-    const int V = C / 4, rows = kCombineThreads / V;  // float4 columns; chunks in flight per round
-    const int v = threadIdx.x % V, r0 = threadIdx.x / V;
-    const float4* o4 = reinterpret_cast<const float4*>(ws_o + bhq * nchunks * D + c0);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < KP; ++i) {
+        if (r0 + i * rows < nv) {
+            const float e = expf(mp[i] - M);
+            acc.x = fmaf(op[i].x, e, acc.x);
+            acc.y = fmaf(op[i].y, e, acc.y);
+            acc.z = fmaf(op[i].z, e, acc.z);
+            acc.w = fmaf(op[i].w, e, acc.w);
+        }
+    }
 #pragma unroll 4
-    for (int k = r0; k < nv; k += rows) {
+    for (int k = r0 + KP * rows; k < nv; k += rows) {
         const float4 o = o4[(size_t)k * (D / 4) + v];
-        const float e = cache_e ? cmb[k] : expf(mrow[k] - M);
+        const float e = expf(mrow[k] - M);
         acc.x = fmaf(o.x, e, acc.x);
         acc.y = fmaf(o.y, e, acc.y);
         acc.z = fmaf(o.z, e, acc.z);
         acc.w = fmaf(o.w, e, acc.w);
     }
-    float4* part = reinterpret_cast<float4*>(cmb + (cache_e ? (nchunks + 3) & ~3 : 0));
     part[r0 * V + v] = acc;
     __syncthreads();
     for (int d = threadIdx.x; d < C; d += kCombineThreads) {
@@ -108,33 +122,25 @@ static cudaError_t combine(const kivi_cache& c, int Hq, const float* ws_o, const
     int ds = 1;
     while (ds < c.D / 32 && rows * ds < 2 * sm_count())
         ds *= 2;
-    const int C = c.D / ds;
-    const size_t part = (size_t)(kCombineThreads / (C / 4)) * C * sizeof(float);
-    const bool cache_e = ((size_t)nch + 3) / 4 * 4 * sizeof(float) + part <= 160 * 1024;
-    const size_t smem = (cache_e ? ((size_t)nch + 3) / 4 * 4 * sizeof(float) : 0) + part;
-    cudaError_t e = cudaFuncSetAttribute(decode_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess)
-        return e;
     const ChunkPlan cp = chunk_plan(c, Hq);
     // programmatic dependent launch: the combine CTAs are scheduled while the
     // chunk kernel drains and wait in griddepcontrol.wait for its results
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(rows, ds);
     cfg.blockDim = dim3(kCombineThreads);
-    cfg.dynamicSmemBytes = smem;
+    cfg.dynamicSmemBytes = 0;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_combine_kernel, c.len, Hq, c.D, nch, cp.TC, cp.S, cache_e,
-                           (const float*)ws_o, (const float*)ws_m, (const float*)ws_l, out);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, decode_combine_kernel, c.len, Hq, c.D, nch, cp.TC, cp.S,
+                                       (const float*)ws_o, (const float*)ws_m, (const float*)ws_l, out);
     if (e != cudaSuccess) {  // attribute not supported: an ordinary launch
         (void)cudaGetLastError();
-        decode_combine_kernel<<<dim3(rows, ds), kCombineThreads, smem, s>>>(c.len, Hq, c.D, nch, cp.TC, cp.S,
-                                                                           cache_e, ws_o, ws_m, ws_l, out);
+        decode_combine_kernel<<<dim3(rows, ds), kCombineThreads, 0, s>>>(c.len, Hq, c.D, nch, cp.TC, cp.S, ws_o,
+                                                                        ws_m, ws_l, out);
     }
     return cudaGetLastError();
 }
