@@ -160,11 +160,6 @@ __host__ __device__ constexpr size_t key_stage_words(int TC, int D, int bits_k, 
 {
     return (size_t)(TC / (32 / bits_k)) * D + 2 * (size_t)(TC / G) * D;
 }
-// Staged values: token rows [TC][D/P] then scales and zeros [TC][D/G].
-__host__ __device__ constexpr size_t val_stage_words(int TC, int D, int bits_v, int G)
-{
-    return (size_t)TC * (D / (32 / bits_v)) + 2 * (size_t)TC * (D / G);
-}
 // Probability rows [NQB][TX + 8] for chunks of up to TX tokens (the pad
 // spreads heads over banks).
 __host__ __device__ constexpr int prob_stride(int TX) { return TX + 8; }

@@ -15,10 +15,8 @@
 
 namespace kivi {
 
-// Tokens one lane covers in a key tile (one int2 word; two int4 / four int8)
-// and in a decode_qk row.
+// Tokens one lane covers in a key tile (one int2 word; two int4 / four int8).
 constexpr int kLaneTokens = 16;
-constexpr int kRowTokens = kLaneTokens;
 // Channels one lane covers in an encode / materialize tile (one 16-byte vector).
 constexpr int kLaneChans = 8;
 
@@ -210,16 +208,8 @@ __device__ __forceinline__ uint32_t bracket_code_bits(float a, InvBracket ib, ui
 }
 constexpr uint32_t kCodeBias = 0x4B400000u;
 
-// code = clamp(rne(a / scale), 0, M), bit-identical to rounding the IEEE
-// quotient (see bracket_code_bits).
-__device__ __forceinline__ uint32_t quant_code(float a, float scale, float inv)
-{
-    uint32_t diff = 0u;
-    const uint32_t c = bracket_code_bits(a, inv_bracket(inv), diff) - kCodeBias;
-    return diff != 0u ? exact_code(a, scale) : c;
-}
-
-// 2^23 as an opaque register value (see one_bits).
+// 2^23 as an opaque register value: keeps the operand of the per-code LOP3 in
+// a register instead of being rematerialized per use.
 __device__ __forceinline__ uint32_t two23_bits()
 {
     uint32_t v = 0x4B000000u;
@@ -454,92 +444,6 @@ __device__ __forceinline__ void quant_store_value_group(const kivi_cache& c, siz
     const size_t so = row * (c.D / G) + gi;
     c.vscale[so] = scale;
     c.vzero[so] = zero;
-}
-
-// ------------------------------------------------- fused-dequant windows ---
-//
-// The decode kernels never materialize x_hat.  A code c is turned into the
-// fp32 value f = 1 + c * 2^(pos-23) by masking it into mantissa bits
-// [pos, pos+b) of 1.0f (one LOP3 after a shared shift), and the multiplier
-// carries 2^(23-pos): mult * f = mult + c.  The constant `mult` is removed
-// once per group through the sum of the multipliers.  `pos` is chosen per
-// code position so that one shift serves several codes ("windows").
-
-template <int BITS>
-struct Window;
-
-// int2: code i of a word at bits [2i, 2i+2).  Codes go in threes to mantissa
-// bits 17/19/21 after one shift each: shift(i) = 19 - 6*floor((i+1)/3)
-// (i = 0,1: <<19; 2-4: <<13; 5-7: <<7; 8-10: <<1; 11-13: >>5; 14,15: >>11),
-// pos(i) = 2i + shift(i), pos_index(i) = (i+1) % 3, mult = 64, 16, 4.
-template <>
-struct Window<2> {
-    static constexpr int kNumPos = 3;
-    __host__ __device__ static constexpr int shift(int i) { return 19 - 6 * ((i + 1) / 3); }
-    __host__ __device__ static constexpr int pos(int i) { return 2 * i + shift(i); }
-    __host__ __device__ static constexpr int pos_index(int i) { return (i + 1) % 3; }
-    __host__ __device__ static constexpr float mult_of_index(int k) { return (float)(64 >> (2 * k)); }
-};
-
-// int4: code i at bits [4i, 4i+4); pairs go to mantissa bits 15/19 after
-// shift(i) = 15 - 8*floor(i/2) (<<15, <<7, >>1, >>9); pos_index = i & 1;
-// mult = 256, 16.
-template <>
-struct Window<4> {
-    static constexpr int kNumPos = 2;
-    __host__ __device__ static constexpr int shift(int i) { return 15 - 8 * (i / 2); }
-    __host__ __device__ static constexpr int pos(int i) { return 4 * i + shift(i); }
-    __host__ __device__ static constexpr int pos_index(int i) { return i & 1; }
-    __host__ __device__ static constexpr float mult_of_index(int k) { return (float)(256 >> (4 * k)); }
-};
-
-// int8: code i at bits [8i, 8i+8); each goes to mantissa bits 15..22 after
-// shift(i) = 15 - 8i (<<15, <<7, >>1, >>9); mult = 256.
-template <>
-struct Window<8> {
-    static constexpr int kNumPos = 1;
-    __host__ __device__ static constexpr int shift(int i) { return 15 - 8 * i; }
-    __host__ __device__ static constexpr int pos(int i) { return 8 * i + shift(i); }
-    __host__ __device__ static constexpr int pos_index(int) { return 0; }
-    __host__ __device__ static constexpr float mult_of_index(int) { return 256.0f; }
-};
-
-static_assert(Window<2>::pos(0) == 19 && Window<2>::pos(1) == 21 && Window<2>::pos(2) == 17 &&
-                  Window<2>::pos(10) == 21 && Window<2>::pos(11) == 17 && Window<2>::pos(15) == 19,
-              "int2 windows");
-static_assert(Window<4>::pos(0) == 15 && Window<4>::pos(1) == 19 && Window<4>::pos(6) == 15 &&
-                  Window<4>::pos(7) == 19, "int4 windows");
-static_assert(Window<8>::pos(3) == 15, "int8 windows");
-
-// 1.0f as an opaque register value: keeps the exponent operand of the
-// per-code mask in a register instead of being rematerialized per use.
-__device__ __forceinline__ uint32_t one_bits()
-{
-    uint32_t v = 0x3F800000u;
-    asm volatile("" : "+r"(v));
-    return v;
-}
-
-// (a & mask) | one in a single LOP3.
-__device__ __forceinline__ float mask_or(uint32_t a, uint32_t mask, uint32_t one)
-{
-    uint32_t r;
-    asm("lop3.b32 %0, %1, %2, %3, 0xEA;" : "=r"(r) : "r"(a), "r"(mask), "r"(one));
-    return __uint_as_float(r);
-}
-
-// All P window values of one word: f[i] = 1 + c_i * 2^(pos(i)-23).  Each
-// distinct shift is formed once; every code then costs one LOP3.
-template <int BITS>
-__device__ __forceinline__ void window_values(uint32_t word, uint32_t one,
-                                              float (&f)[32 / BITS])
-{
-#pragma unroll
-    for (int i = 0; i < 32 / BITS; ++i) {
-        const int sh = Window<BITS>::shift(i);
-        const uint32_t sw = sh >= 0 ? (word << sh) : (word >> (-sh));
-        f[i] = mask_or(sw, ((1u << BITS) - 1u) << Window<BITS>::pos(i), one);
-    }
 }
 
 }  // namespace kivi
