@@ -33,10 +33,14 @@ _VP = C.c_void_p
 
 
 def lib():
-    """Load the oracle library, building it first if it is missing or stale."""
+    """Load the oracle library, building it first if it is missing or stale.
+
+    KIVI_REF_LIB, when set, names another build of kivi_ref.c to load instead:
+    the planted-mistake tests point it at deliberately broken copies to show
+    that the pins reject them."""
     global _LIB
     if _LIB is None:
-        path = _build.build()
+        path = os.environ.get("KIVI_REF_LIB") or _build.build()
         L = C.CDLL(path)
         L.kref_half_to_float.argtypes = [C.c_uint16]
         L.kref_half_to_float.restype = C.c_float
