@@ -7,11 +7,15 @@ flags, and the pin suite (test_oracle_pins.py and the oracle payload tests)
 runs against it in a child process, with KIVI_REF_LIB pointing the oracle at
 that build.  A mutant passes this test only if some pin fails on it.  The
 unmodified source, compiled the same way, must pass every pin; that control
-shows that the mutants fail for their mistake and not for the harness.
+shows that the mutants fail for their mistake and not for the harness.  The
+same is done for the oracle's Python front end (oracle/ref.py): each mutant
+there runs the pins from a copy of oracle/ and tests/ whose ref.py carries
+the mistake.
 
 Nothing here touches a GPU or the CUDA library.
 """
 import os
+import shutil
 import subprocess
 import sys
 from concurrent.futures import ThreadPoolExecutor
@@ -78,6 +82,30 @@ MUTANTS = {
 }
 
 
+# Mistakes in the Python front end of the oracle (oracle/ref.py), which maps
+# query heads to KV heads, applies the default softmax scale, honours ragged
+# lengths and keeps the append bookkeeping.
+PY_MUTANTS = {
+    "gqa_heads_interleaved": ("qs = np.ascontiguousarray(q[b, h * NQ:(h + 1) * NQ])",
+                              "qs = np.ascontiguousarray(q[b, h::self.H])"),
+    "default_scale_1_over_D": ("sm = float(1.0 / np.sqrt(D)) if sm_scale is None else float(sm_scale)",
+                               "sm = float(1.0 / D) if sm_scale is None else float(sm_scale)"),
+    "encode_ignores_lengths": ("Tb = int(lens[b])\n", "Tb = T\n"),
+    "append_keeps_the_length": ("                self.lens[b] = new", "                self.lens[b] = n"),
+    "append_ignores_overflow": ("            if new < 0:\n                overflow[b] = True",
+                                "            if False:\n                overflow[b] = True"),
+}
+
+
+def _copy_tree(dst: str, ref_text: str):
+    """The oracle and the tests under dst, with ref.py replaced by ref_text."""
+    ignore = shutil.ignore_patterns("__pycache__", "*.so", "*.so.tmp*")
+    shutil.copytree(os.path.join(ROOT, "oracle"), os.path.join(dst, "oracle"), ignore=ignore)
+    shutil.copytree(os.path.join(ROOT, "tests"), os.path.join(dst, "tests"), ignore=ignore)
+    with open(os.path.join(dst, "oracle", "ref.py"), "w") as f:
+        f.write(ref_text)
+
+
 def _compile(src_text: str, out: str):
     src = out[:-3] + ".c"
     with open(src, "w") as f:
@@ -86,10 +114,13 @@ def _compile(src_text: str, out: str):
     subprocess.run(cmd, check=True, capture_output=True)
 
 
-def _run_pins(lib: str) -> subprocess.CompletedProcess:
-    env = dict(os.environ, KIVI_REF_LIB=lib)
+def _run_pins(lib: str | None, root: str = ROOT) -> subprocess.CompletedProcess:
+    env = dict(os.environ)
+    env.pop("KIVI_REF_LIB", None)
+    if lib:
+        env["KIVI_REF_LIB"] = lib
     cmd = [sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider", "-m", "not gpu", *PINS]
-    return subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
+    return subprocess.run(cmd, cwd=root, env=env, capture_output=True, text=True, timeout=600)
 
 
 def test_mutant_texts_are_unique():
@@ -97,6 +128,26 @@ def test_mutant_texts_are_unique():
     for name, (old, new) in MUTANTS.items():
         assert src.count(old) == 1, name
         assert old != new, name
+    py = open(os.path.join(ROOT, "oracle", "ref.py")).read()
+    for name, (old, new) in PY_MUTANTS.items():
+        assert py.count(old) == 1, name
+        assert old != new, name
+
+
+def test_every_planted_mistake_in_the_front_end_fails_a_pin(tmp_path):
+    py = open(os.path.join(ROOT, "oracle", "ref.py")).read()
+    texts = {"control": py}
+    texts.update({name: py.replace(old, new) for name, (old, new) in PY_MUTANTS.items()})
+    for name, text in texts.items():
+        _copy_tree(str(tmp_path / name), text)
+    with ThreadPoolExecutor(max(2, min(8, os.cpu_count() or 2))) as ex:
+        results = dict(zip(texts, ex.map(lambda n: _run_pins(None, str(tmp_path / n)), texts)))
+    control = results.pop("control")
+    assert control.returncode == 0, "unmodified front end failed its pins:\n" + control.stdout[-2000:]
+    survivors = [n for n, r in results.items() if r.returncode == 0]
+    assert not survivors, f"planted mistakes that no pin catches: {survivors}"
+    crashed = [n for n, r in results.items() if r.returncode not in (0, 1)]
+    assert not crashed, {n: results[n].stdout[-500:] for n in crashed}
 
 
 def test_every_planted_mistake_fails_a_pin(tmp_path):

@@ -353,6 +353,43 @@ def test_attention_reduces_to_textbook(ref, NQ):
     o = torch.einsum("bhnt,bhtd->bhnd", torch.softmax(s, dim=-1), Vt)
     assert np.allclose(logits, s.reshape(B, H * NQ, T).numpy(), rtol=1e-6, atol=1e-6)
     assert np.allclose(out, o.reshape(B, H * NQ, D).numpy(), rtol=1e-6, atol=1e-6)
+    # default scale: torch's scaled_dot_product_attention, whose own default
+    # is 1/sqrt(D), with the KV head repeated for each of its query heads
+    Kr = Kt.repeat_interleave(NQ, dim=1)
+    Vr = Vt.repeat_interleave(NQ, dim=1)
+    o_sdpa = torch.nn.functional.scaled_dot_product_attention(qt.reshape(B, H * NQ, 1, D), Kr, Vr)
+    assert np.allclose(rc.attention(q)[1], o_sdpa.reshape(B, H * NQ, D).numpy(), rtol=1e-6, atol=1e-6)
+
+
+def test_ragged_lengths_equal_truncated_prefixes(ref):
+    """Encoding a batch with seq_lens keeps, for each sequence b, what encoding
+    its first seq_lens[b] tokens on their own gives: the codes and statistics
+    of its quantized groups, the residual tokens in their ring slots, and the
+    same materialized rows and attention (groups and sequences are
+    independent)."""
+    rng = np.random.default_rng(77)
+    B, H, D, G, R, T, bk, bv = 4, 2, 64, 32, 32, 200, 4, 2
+    lens = [200, 77, 5, 0]
+    Pk, Pv, RG = 32 // bk, 32 // bv, R + G
+    K = f16(rng.standard_normal((B, H, T, D)))
+    V = f16(rng.standard_normal((B, H, T, D)))
+    q = f16(rng.standard_normal((B, H, D)))
+    rc = ref.RefCache(B, H, D, bk, bv, G, R, 224).encode(K, V, seq_lens=lens)
+    dk, dv = rc.decode(0, T_out=T), rc.decode(1, T_out=T)
+    lg, out = rc.attention(q)
+    for b, n in enumerate(lens):
+        one = ref.RefCache(1, H, D, bk, bv, G, R, 224).encode(K[b:b + 1, :, :n], V[b:b + 1, :, :n])
+        Tq = ref.quantized_tokens(n, G, R)
+        for name, rows in (("kq", Tq // Pk), ("kscale", Tq // G), ("kzero", Tq // G),
+                           ("vq", Tq), ("vscale", Tq), ("vzero", Tq)):
+            assert np.array_equal(getattr(rc, name)[b, :, :rows], getattr(one, name)[0, :, :rows]), (b, name)
+        slots = [t % RG for t in range(Tq, n)]
+        assert np.array_equal(rc.kres[b][:, slots], one.kres[0][:, slots]), b
+        assert np.array_equal(rc.vres[b][:, slots], one.vres[0][:, slots]), b
+        assert np.array_equal(dk[b, :, :n], one.decode(0, T_out=n)[0]), b
+        assert np.array_equal(dv[b, :, :n], one.decode(1, T_out=n)[0]), b
+        lg1, o1 = one.attention(q[b:b + 1])
+        assert np.array_equal(lg[b, :, :n], lg1[0, :, :n]) and np.array_equal(out[b], o1[0]), b
 
 
 def test_attention_gqa_mapping(ref):
