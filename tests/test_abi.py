@@ -134,3 +134,45 @@ def test_missing_library_fails_loudly(tmp_path):
     from kivi_bit_kv_gb300 import abi
     with pytest.raises(ImportError):
         abi.load(str(tmp_path / "libkivi.so"))
+
+
+C_CLIENT = r"""
+#include <stdio.h>
+#include <string.h>
+#include "kivi.h"
+
+int main(void)
+{
+    kivi_cache c;
+    memset(&c, 0, sizeof c);
+    c.B = 1; c.H = 1; c.D = 100; c.bits_k = 2; c.bits_v = 2; c.G = 32; c.R = 32; c.Tmax = 64;
+    const int32_t st = kivi_cache_validate(&c);
+    printf("%d %d %zu %d %s|%s\n", kivi_abi_version(), st, kivi_cache_bytes(100, 64, 2, 32, 32, 0),
+           st == KIVI_EINVAL, kivi_status_string(st), kivi_last_error());
+    return 0;
+}
+"""
+
+
+def test_plain_c_client_links_and_calls(kivi_lib, tmp_path):
+    """The boundary is usable from C99 with nothing but include/kivi.h and
+    libkivi.so: a strict C program compiles, links and calls host-side entry
+    points (no CUDA call is reached)."""
+    import shutil
+    import subprocess
+    from kivi_bit_kv_gb300 import abi
+    if shutil.which("gcc") is None:
+        pytest.skip("gcc not found")
+    src, exe = tmp_path / "client.c", tmp_path / "client"
+    src.write_text(C_CLIENT)
+    libdir = os.path.dirname(abi.LIB_PATH)
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    f"-I{os.path.join(ROOT, 'include')}", str(src), "-o", str(exe),
+                    f"-L{libdir}", "-lkivi", f"-Wl,-rpath,{libdir}"], check=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.strip()
+    head, err = out.split("|", 1)
+    version, status, nbytes, is_einval, text = head.split(" ", 4)
+    assert int(version) == abi.kivi_abi_version()
+    assert int(status) == abi.KIVI_EINVAL and is_einval == "1" and text == "invalid argument"
+    assert int(nbytes) == abi.kivi_cache_bytes(100, 64, 2, 32, 32, 0)
+    assert "D=100" in err
