@@ -50,6 +50,8 @@ SMALL = [
     ("T1", 1, 1, 1, 64, 2, 2, 32, 0, 1, None),
     ("multi_chunk", 1, 1, 2, 128, 2, 2, 32, 128, 5000, None),
     ("int8_gqa4_multi", 1, 2, 8, 128, 8, 8, 32, 64, 3000, None),
+    # the largest grouped-query ratio, 16 query heads per KV head: four passes
+    ("gqa16_4pass", 1, 2, 32, 128, 2, 2, 32, 128, 1200, None),
     # a sequence's last chunk absorbs a tail of up to min(R, TC/4) tokens
     ("slack_tail", 4, 1, 1, 128, 2, 2, 32, 128, 1160, [1025, 1152, 1153, 640]),
     ("slack_R32", 4, 1, 2, 128, 4, 4, 32, 32, 1100, [512, 543, 544, 1056]),
