@@ -90,3 +90,33 @@ def test_fp16_equivalent_bytes_per_kind():
     assert bench.fp16_equiv_bytes(w, "store", lens, lens) == 2 * kv
     assert bench.fp16_equiv_bytes(w, "decode", lens, lens) == kv + 2 * w.B * w.H * w.D * 2
     assert bench.fp16_equiv_bytes(w, "full", lens, lens) == 3 * kv + 2 * w.B * w.H * w.D * 2
+
+
+def test_reference_arm_prints_the_contract_line():
+    """`bench.py --impl reference` (the CPU oracle) prints one JSON line with
+    the keys the benchmark contract asks for, on the host cores."""
+    import json
+    import subprocess
+    r = subprocess.run([sys.executable, "bench.py", "--impl", "reference", "--workload", "tiny",
+                        "--steps", "1", "--warmup", "1"], cwd=ROOT, capture_output=True, text=True,
+                       timeout=300, check=True)
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+                "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+                "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["n_gpus"] == 1
+    assert (line["steps"], line["warmup"]) == (1, 1) and line["higher_is_better"] is True
+    assert line["config"]["workload"] == "tiny"
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"] == {"value": line["value"], "unit": line["unit"], "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}
+
+
+def test_reference_arm_runs_on_rank_0_only():
+    from types import SimpleNamespace
+    args = SimpleNamespace(workload="tiny", steps=1, warmup=1)
+    assert bench.run_reference(args, rank=1, world=2) is None
