@@ -66,6 +66,10 @@ MUTANTS = {
     "softmax_not_normalized": ("acc += (s[t] / sum) *", "acc += s[t] *"),
     "softmax_scale_dropped": ("s[t] = (double)sm_scale * acc;", "s[t] = acc;"),
     "every_head_uses_head_0": ("const uint16_t* qh = q + (size_t)h * D;", "const uint16_t* qh = q;"),
+    "key_hat_stats_of_next_channel": ("        size_t si = (size_t)(t / G) * D + d;\n        return (double)key_code",
+                                      "        size_t si = ((size_t)(t / G) * D + d) ^ 1;\n"
+                                      "        return (double)key_code"),
+    "value_hat_stats_of_group_0": ("size_t si = (size_t)t * (D / G) + d / G;", "size_t si = (size_t)t * (D / G);"),
     # storage accounting and payload
     "key_stats_counted_once": ("size_t stats = which == 0 ? (Tq / (size_t)G) * (size_t)D * 8",
                                "size_t stats = which == 0 ? (Tq / (size_t)G) * (size_t)D * 4"),

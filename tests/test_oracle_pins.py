@@ -361,6 +361,64 @@ def test_attention_reduces_to_textbook(ref, NQ):
     assert np.allclose(rc.attention(q)[1], o_sdpa.reshape(B, H * NQ, D).numpy(), rtol=1e-6, atol=1e-6)
 
 
+def _exact_groups_tensor(rng, shape, axis, G, bits):
+    """fp16 values z + c 2^e whose groups along `axis` (G elements) each have
+    their own exponent e in {-8, -7, -6} and offset z (a multiple of 2^-8 in
+    [-2, 2]), with codes c in [0, 2^b - 1] and both ends present.  Every value
+    is exact in fp16 (|x| < 8, a multiple of 2^-8), the group's scale is
+    exactly 2^e and its zero exactly z, so the b-bit codes reproduce the
+    tensor exactly while the statistics differ from group to group."""
+    M = (1 << bits) - 1
+    x = np.moveaxis(np.empty(shape), axis, -1).copy()
+    ng = x.shape[-1] // G
+    lead = x.shape[:-1]
+    e = rng.integers(-8, -5, lead + (ng,))
+    z = rng.integers(-512, 513, lead + (ng,)) / 256.0
+    c = rng.integers(0, M + 1, lead + (ng, G))
+    c[..., 0] = 0
+    c[..., 1] = M
+    vals = z[..., None] + c * np.exp2(e)[..., None]
+    x[...] = rng.integers(-512, 513, x.shape) / 256.0  # a ragged tail stays fp16
+    x[..., :ng * G] = vals.reshape(lead + (ng * G,))
+    out = f16(np.moveaxis(x, -1, axis))
+    assert np.array_equal(out.astype(np.float64), np.moveaxis(x, -1, axis))
+    return out
+
+
+@pytest.mark.parametrize("bk,bv,NQ", [(8, 4, 1), (4, 8, 2), (2, 2, 3)])
+def test_attention_with_per_group_statistics(ref, bk, bv, NQ):
+    """Decode attention over a cache whose every key group (channel d, G
+    tokens) and value group (token t, G channels) has its own exact scale and
+    zero, at mixed widths: K_hat == K and V_hat == V exactly, so the result is
+    textbook softmax attention in float64 -- but only if the dequantization
+    inside the attention reads each element's own group statistics
+    (CacheForge README, "How it works": per-channel key groups, per-token
+    value groups)."""
+    import torch
+    rng = np.random.default_rng(40 + bk + 3 * bv + NQ)
+    B, H, D, G, R, T = 2, 2, 64, 32, 32, 150
+    K = _exact_groups_tensor(rng, (B, H, T, D), axis=2, G=G, bits=bk)
+    V = _exact_groups_tensor(rng, (B, H, T, D), axis=3, G=G, bits=bv)
+    q = f16(rng.standard_normal((B, H * NQ, D)))
+    rc = ref.RefCache(B, H, D, bk, bv, G, R, 192).encode(K, V)
+    Tq = ref.quantized_tokens(T, G, R)
+    # the statistics really differ between neighbouring channels and groups
+    assert not np.array_equal(rc.kscale[:, :, :Tq // G, 0::2], rc.kscale[:, :, :Tq // G, 1::2])
+    assert not np.array_equal(rc.kzero[:, :, :Tq // G, 0::2], rc.kzero[:, :, :Tq // G, 1::2])
+    assert not np.array_equal(rc.vscale[:, :, :Tq, 0], rc.vscale[:, :, :Tq, 1])
+    assert np.array_equal(rc.decode(0), K.view(np.uint16))
+    assert np.array_equal(rc.decode(1), V.view(np.uint16))
+    sm = 0.125
+    logits, out = rc.attention(q, sm_scale=sm)
+    Kt = torch.from_numpy(K.astype(np.float64))
+    Vt = torch.from_numpy(V.astype(np.float64))
+    qt = torch.from_numpy(q.astype(np.float64)).view(B, H, NQ, D)
+    s = torch.einsum("bhnd,bhtd->bhnt", qt, Kt) * sm
+    o = torch.einsum("bhnt,bhtd->bhnd", torch.softmax(s, dim=-1), Vt)
+    assert np.allclose(logits, s.reshape(B, H * NQ, T).numpy(), rtol=1e-6, atol=1e-6)
+    assert np.allclose(out, o.reshape(B, H * NQ, D).numpy(), rtol=1e-6, atol=1e-6)
+
+
 def test_ragged_lengths_equal_truncated_prefixes(ref):
     """Encoding a batch with seq_lens keeps, for each sequence b, what encoding
     its first seq_lens[b] tokens on their own gives: the codes and statistics
