@@ -2,9 +2,9 @@
  * kivi.h -- C ABI of libkivi: KIVI grouped asymmetric KV-cache quantization
  * on one NVIDIA GB300 (sm_103a).
  *
- * The method (KIVI, "A Tuning-Free Asymmetric 2bit Quantization for KV
- * Cache", as described on the CacheForge README, section "How it works", and
- * in CacheSeek PR #4 "add KIVI KV-cache quantization for exact-prefix reuse"):
+ * The method (KIVI, Liu et al., ICML 2024, as the CacheForge README describes
+ * it in its section "How it works", and as the CacheSeek PR #4 change notes
+ * use it for exact-prefix reuse):
  * keys are quantized per channel over groups of G tokens, values per token
  * over groups of G channels, each group with its own min/max statistics; the
  * most recent tokens stay in fp16.  The pages print no formula; this library
@@ -13,7 +13,8 @@
  *   M     = 2^b - 1, b in {2, 4, 8}            (CacheForge "Example": k_bits,
  *                                               v_bits; CacheSeek: int4/int8)
  *   scale = (max - min) / M     fp32 subtraction, IEEE fp32 division
- *   zero  = min                 (the "offset" of CacheSeek's qdata/scale/offset)
+ *   zero  = min                 (CacheSeek PR #4 change notes: the payload's
+ *                                offset field)
  *   code  = clamp(rne((x - zero) / scale), 0, M)   fp32, IEEE division,
  *           round half to even; code = 0 when scale == 0
  *   x_hat = fp16_rne(fmaf(code, scale, zero))
@@ -25,14 +26,15 @@
  * (16 x int2, 8 x int4, 4 x int8; code i occupies bits [i*b, i*b+b)), along
  * the grouping axis: key words run along tokens, value words along channels.
  *
- * Residual (CacheForge "Example": residual_length = number of recent fp16
- * tokens).  A sequence of T tokens keeps its first
+ * Residual (CacheForge README, "Example": the residual_length setting, the
+ * count of recent tokens kept in fp16).  A sequence of T tokens keeps its first
  *     Tq = max(0, floor((T - R) / G) * G)
  * tokens quantized and the remaining T - Tq tokens (R <= T - Tq < R + G once
  * T >= R) in fp16, in a ring of R + G slots: token t lives in slot t mod (R+G).
  * Appending a token that makes the residual reach R + G quantizes its oldest
- * G tokens as one group and drops them from the ring ("quantization flow
- * during prefill and decoding", CacheForge README, "How it works").
+ * G tokens as one group and drops them from the ring (CacheForge README,
+ * "How it works": the figure of how tokens move from fp16 into groups during
+ * prefill and decoding).
  *
  * Conventions for every call:
  *   - All tensors are caller-allocated device memory (the library never
@@ -131,9 +133,9 @@ size_t kivi_buffer_bytes(const kivi_cache* c, int32_t buffer);
 
 /*
  * Bytes a sequence of T tokens occupies in the cache for one (batch, head)
- * slice -- codes + fp32 scale/zero + fp16 residual (CacheSeek PR #4:
- * "manager-side accounting so stored payload sizes reflect optional
- * quantization"):
+ * slice -- codes + fp32 scale/zero + fp16 residual (CacheSeek PR #4 change
+ * notes: the store's size accounting counts a payload at its quantized
+ * size):
  *   keys   (which = 0): Tq*D*b/8 + (Tq/G)*D*8 + (T-Tq)*D*2
  *   values (which = 1): Tq*D*b/8 + Tq*(D/G)*8 + (T-Tq)*D*2
  * Host only.  Returns 0 for invalid arguments.
@@ -162,7 +164,8 @@ int32_t kivi_quant_values(const kivi_cache* c, const uint16_t* V, int32_t T,
                           const int32_t* seq_lens, void* stream);
 
 /*
- * Materialize (CacheSeek PR #4: "decode after materialize"): unpack and
+ * Materialize (CacheSeek PR #4 change notes: a stored layer is dequantized
+ * on the device once it has been brought back there): unpack and
  * dequantize keys (which = 0) or values (which = 1) into out, fp16
  * [B][H][T_out][D].  Rows t < len[b] are written (quantized rows as x_hat,
  * residual rows copied from the ring); rows t >= len[b] are not touched.
@@ -185,7 +188,12 @@ int32_t kivi_append_token(const kivi_cache* c, const uint16_t* k,
                           const uint16_t* v, int32_t* status, void* stream);
 
 /*
- * Decode logits with dequantization fused into the load:
+ * Decode logits with dequantization fused into the load.  The decode-time
+ * consumer of the cache: CacheForge README, "How it works" (the cache is
+ * quantized during prefill and read back at every decoding step) and
+ * "Example" (generation with the quantized cache).  The pages print no
+ * attention formula; this is standard scaled dot-product attention of one
+ * query token over the dequantized keys:
  *   logits[b][hq][t] = sm_scale * sum_d q[b][hq][d] * K_hat[b][h][t][d]
  * for t < len[b], where h = hq / (Hq / H) (grouped-query attention) and
  * K_hat = code*scale + zero evaluated in fp32 (quantized tokens) or the fp16
@@ -198,7 +206,8 @@ int32_t kivi_decode_qk(const kivi_cache* c, const uint16_t* q, int32_t Hq,
                        void* stream);
 
 /*
- * Decode output with dequantization fused into the load:
+ * Decode output with dequantization fused into the load (the second half of
+ * the decode-time consumer, same passages as kivi_decode_qk):
  *   p = softmax over t < len[b] of logits[b][hq][t]     (fp32, max-subtracted)
  *   out[b][hq][d] = sum_t p_t * V_hat[b][h][t][d]
  * out: fp32 [B][Hq][D].  The token range is split into chunks processed in
@@ -215,7 +224,8 @@ int32_t kivi_decode_pv(const kivi_cache* c, const float* logits,
  * the softmax and the weighted sum of kivi_decode_pv, fused per (KV head,
  * chunk of up to 1024 tokens) so that the logits stay on chip:
  *   out[b][hq][d] = sum_t softmax_t(sm_scale q . K_hat_t) V_hat[t][d]
- * over t < len[b] (CacheSeek PR #4: decode from the quantized KV).  q: fp16
+ * over t < len[b] (the decode-time consumer: CacheForge README, "How it
+ * works" and "Example", as for kivi_decode_qk).  q: fp16
  * [B][Hq][D]; out: fp32 [B][Hq][D]; ws as for kivi_decode_pv (>=
  * kivi_workspace_bytes(c, Hq) bytes, 16-byte aligned).  Requires
  * bits_k == bits_v (KIVI_EINVAL otherwise: use kivi_decode_qk followed by
@@ -226,7 +236,12 @@ int32_t kivi_decode_attention(const kivi_cache* c, const uint16_t* q,
                               int32_t Hq, float sm_scale, float* out,
                               void* ws, size_t ws_bytes, void* stream);
 
-/* Workspace bytes kivi_decode_pv needs for this descriptor and Hq. */
+/*
+ * Workspace bytes kivi_decode_pv and kivi_decode_attention need for this
+ * descriptor and Hq: room for the per-chunk partial results of the split
+ * token range.  An implementation detail of the decode-time consumer (the
+ * pages have no counterpart).  Host only; 0 for invalid sizes.
+ */
 size_t kivi_workspace_bytes(const kivi_cache* c, int32_t Hq);
 
 /* Size of the fixed device scratch behind kivi_decode_pv_noalloc. */
@@ -245,9 +260,14 @@ size_t kivi_workspace_bytes(const kivi_cache* c, int32_t Hq);
  * until the process exits.  The call allocates nothing.
  *   - Shapes with kivi_workspace_bytes(c, Hq) > KIVI_NOALLOC_SCRATCH_BYTES are
  *     rejected with KIVI_EWORKSPACE before anything is launched.
+ *   - The arguments are checked as kivi_decode_pv checks them (KIVI_EINVAL
+ *     for a bad cache, Hq, logits or out) before the size test.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress, with that device current); make that first call
- *     before any stream capture.
+ *     (cudaGetSymbolAddress, with that device current) and caches it for the
+ *     rest of the process; make that first call before any stream capture.
+ *     A device reset (cudaDeviceReset, or anything else that destroys the
+ *     device's primary context) frees the array and leaves the cached address
+ *     stale: do not call this entry point on a device after resetting it.
  *   - Every call on a device shares the one array and it keeps the last
  *     call's contents.  Calls whose kernels may overlap on the GPU (unordered
  *     streams) race and corrupt each other's results: order them.  No part
@@ -260,10 +280,11 @@ int32_t kivi_decode_pv_noalloc(const kivi_cache* c, const float* logits,
 /* ------------------------------------------------ compact payload (store) */
 
 /*
- * The exact-prefix store of CacheSeek PR #4 keeps a quantized layer as a
- * compact payload -- "qdata/scale/offset are moved back to CPU before being
- * stored" -- and mixes a "quant fingerprint" into the prefix root hash, so a
- * quantized entry never matches one stored under another codec.  These calls
+ * The exact-prefix store of CacheSeek PR #4 (change notes) keeps a quantized
+ * layer as a compact payload of codes, scales and offsets that is copied to
+ * host memory for storage, and folds a fingerprint of the quantization
+ * settings into the prefix root hash, so that a quantized entry never matches
+ * one stored under another codec.  These calls
  * move a cache's payload between the device and caller-owned memory (pinned
  * host memory: the copy kernels read and write it directly, over NVLink-C2C
  * on a Grace-Blackwell node) in this format, all little-endian:

@@ -242,6 +242,26 @@ static int32_t check_logits(const kivi_cache* c, const float* logits, int32_t ld
     return KIVI_OK;
 }
 
+}  // extern "C"
+
+namespace kivi {
+
+// The argument checks of kivi_decode_pv other than the workspace's, for
+// entry points that bring their own workspace.
+int32_t check_decode_pv_args(const kivi_cache* c, const float* logits, int32_t ld_logits, int32_t Hq,
+                             const float* out)
+{
+    int32_t st = check_cache(c);
+    if (st != KIVI_OK || (st = check_heads(c, Hq)) != KIVI_OK ||
+        (st = check_logits(c, logits, ld_logits)) != KIVI_OK || (st = check_ptr(out, "out")) != KIVI_OK)
+        return st;
+    return KIVI_OK;
+}
+
+}  // namespace kivi
+
+extern "C" {
+
 int32_t kivi_decode_qk(const kivi_cache* c, const uint16_t* q, int32_t Hq, float sm_scale,
                        float* logits, int32_t ld_logits, void* stream)
 {

@@ -34,7 +34,10 @@ void* g_scratch_addr[kMaxDevices] = {};
 
 // Device address of g_decode_scratch on the current device.  In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device, with that device current, and cached.
+// per device, with that device current, and cached for the life of the
+// process.  A device reset (cudaDeviceReset, or anything else that destroys
+// the device's primary context) frees the array and leaves the cached address
+// dangling: this entry point must not be used on a device after such a reset.
 int32_t scratch_address(void** addr)
 {
     int dev = -1;
@@ -58,6 +61,11 @@ int32_t scratch_address(void** addr)
 extern "C" int32_t kivi_decode_pv_noalloc(const kivi_cache* c, const float* logits,
                                           int32_t ld_logits, int32_t Hq, float* out, void* stream)
 {
+    // the same argument checks as kivi_decode_pv first, so that a bad cache or
+    // Hq is reported as such and not as a size problem
+    const int32_t valid = kivi::check_decode_pv_args(c, logits, ld_logits, Hq, out);
+    if (valid != KIVI_OK)
+        return valid;
     const size_t need = kivi_workspace_bytes(c, Hq);
     if (need > (size_t)KIVI_NOALLOC_SCRATCH_BYTES)
         return kivi::record_error(

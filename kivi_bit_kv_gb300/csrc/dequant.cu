@@ -1,7 +1,7 @@
 // dequant.cu -- materialize: unpack codes and dequantize to fp16
 // (x_hat = fp16_rne(fmaf(code, scale, zero))), residual rows copied from the
-// ring.  CacheSeek PR #4 change notes: "decode after materialize" moves only
-// the compact qdata/scale/offset to the device and dequantizes there.
+// ring.  CacheSeek PR #4 change notes: only the compact codes, scales and
+// offsets travel back to the device, and dequantization happens there.
 //
 // HBM-bound: reads b/8 bytes of code plus the statistics per element and
 // writes 2 bytes per element with 16-byte stores.  2-D grids (x: token tiles,

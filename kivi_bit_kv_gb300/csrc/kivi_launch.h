@@ -56,6 +56,11 @@ cudaError_t launch_export(const kivi_cache& c, void* dst, size_t dst_bytes, uint
 cudaError_t launch_import(const kivi_cache& c, const void* src, size_t src_bytes, uint64_t fingerprint,
                           int32_t* status, cudaStream_t s);
 
+// The argument checks kivi_decode_pv makes before it looks at its workspace
+// (cache, Hq, logits, out); KIVI_OK or the status it would return.
+int32_t check_decode_pv_args(const kivi_cache* c, const float* logits, int32_t ld_logits, int32_t Hq,
+                             const float* out);
+
 // Sets the message kivi_last_error() returns on this host thread; returns status.
 int32_t record_error(int32_t status, const char* message);
 

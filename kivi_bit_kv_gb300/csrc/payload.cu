@@ -1,7 +1,7 @@
 // payload.cu -- the compact payload of a cache (include/kivi.h, "compact
 // payload"): export to and import from caller memory, in the format the
-// header documents.  CacheSeek PR #4 stores a quantized layer as its qdata,
-// scale and offset moved "back to CPU before being stored"; here one kernel
+// header documents.  CacheSeek PR #4 (change notes) stores a quantized layer
+// as its codes, scales and offsets, copied to host memory; here one kernel
 // gathers the packed codes, statistics and fp16 residual of every slice
 // straight into the destination (pinned host memory is written over the
 // CPU-GPU link without a staging copy), and one kernel scatters a payload

@@ -11,13 +11,12 @@
  *  - CacheForge README, "How it works": keys are quantized per channel and
  *    values per token; recent tokens stay at higher precision.
  *  - CacheForge README, "Example": k_bits, v_bits, group_size and
- *    residual_length ("number of recent fp16 tokens").
- *  - CacheSeek PR #4 "add KIVI KV-cache quantization for exact-prefix reuse",
- *    change notes: KIVI int4/int8 encode/decode with grouped statistics, codes
- *    packed into int32 words, payload = qdata + scale + offset.
- *  - KIVI (Liu et al., ICML 2024, "A Tuning-Free Asymmetric 2bit Quantization
- *    for KV Cache"), cited by the CacheForge README: asymmetric min/max
- *    quantization.
+ *    residual_length (how many recent tokens stay in fp16).
+ *  - CacheSeek PR #4, change notes: KIVI int4/int8 encode/decode with grouped
+ *    statistics, codes packed into int32 words, a payload of codes, scales
+ *    and offsets.
+ *  - KIVI (Liu et al., ICML 2024), cited by the CacheForge README: asymmetric
+ *    min/max quantization.
  * The arithmetic the pages leave open is fixed as follows (the same contract
  * the CUDA library documents in include/kivi.h):
  *    scale = (max - min) / (2^b - 1)   fp32 subtraction, IEEE fp32 division
@@ -97,8 +96,9 @@ void kref_attention(const uint16_t* q, int NQ, float sm_scale, int len, int D,
 size_t kref_cache_bytes(int T, int D, int bits, int G, int R, int which);
 
 /* Compact payload (the store format of the CUDA library's kivi_export /
- * kivi_import; CacheSeek PR #4: qdata/scale/offset moved to the CPU before
- * being stored, and a quant fingerprint in the prefix root hash).  Written
+ * kivi_import; CacheSeek PR #4 change notes: codes, scales and offsets are
+ * copied to host memory for storage, and a fingerprint of the quantization
+ * settings enters the prefix root hash).  Written
  * byte by byte, little-endian, independent of the host's byte order. */
 
 /* FNV-1a, 64-bit: h = 14695981039346656037; for each byte: h ^= byte,

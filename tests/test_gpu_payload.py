@@ -3,8 +3,8 @@ oracle's payload byte for byte (to pinned host memory and to device memory),
 kivi_import of the oracle's payload reproduces the oracle's cache state and
 decode output, and every header / capacity / size error is reported through
 the status word with the cache or the destination left as it was.  (CacheSeek
-PR #4: the store keeps qdata/scale/offset on the CPU; the root hash includes
-a quant fingerprint.)"""
+PR #4 change notes: the store keeps the codes, scales and offsets in host
+memory, and its root hash covers a fingerprint of the quantization settings.)"""
 import numpy as np
 import pytest
 import torch

@@ -2,8 +2,9 @@
 against the specification's test vectors, the library's fingerprint and
 payload size against the oracle's, the oracle's payload layout and its round
 trip, and the export / import argument checks that return before any CUDA
-call.  (CacheSeek PR #4 stores a quantized layer as qdata/scale/offset moved
-to the CPU and mixes a quant fingerprint into the prefix root hash.)"""
+call.  (CacheSeek PR #4 change notes: a quantized layer is stored in host
+memory as its codes, scales and offsets, and a fingerprint of the quantization
+settings enters the prefix root hash.)"""
 import ctypes as C
 import struct
 
