@@ -87,6 +87,7 @@ decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_
     extern __shared__ __align__(16) float dsm[];
     __shared__ __align__(16) float qs[NQB * qstride_of(D)];
     __shared__ float fac[NQB];
+    __shared__ float red[kDecodeWarps];
     using T = KeyTile<BITS, NQB>;
     ChunkRange r;
     if (!chunk_range(c, TC, S, r))
@@ -96,13 +97,15 @@ decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_
     const DecodeSmem m = carve(dsm, L);
     stage_keys<BITS, T::TOK, D>(c, bh, r.t_begin, r.tq_end, m.kw, m.ks, m.kz);
     cp_async_commit();
+    cp_async_wait_all();
+    __syncthreads();
+    const float fk = weight_scale_pow2(cta_max_stat(m.ks, ((r.tq_end - r.t_begin) / c.G) * D, red));
     const int NQ = Hq / c.H;
     constexpr int rows = 32 / (D / 32);  // residual tokens per warp step
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = r.h * NQ + pass * NQB;
         __syncthreads();
-        stage_q<NQB, D>(q + ((size_t)r.b * Hq + hq0) * D, sm_scale, qs, fac);
-        cp_async_wait_all();
+        stage_q<NQB, D>(q + ((size_t)r.b * Hq + hq0) * D, sm_scale, fk, qs, fac);
         __syncthreads();
         float* out = logits + ((size_t)r.b * Hq + hq0) * ldl;
         auto sink = [&](int h, int t, float s) { out[(size_t)h * ldl + t] = s; };
@@ -119,21 +122,25 @@ decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_
 // B fragments (with the softmax numerators) and the weighted value sum of
 // one pass: p_sm holds the chunk's logits, mx their per-head maxima; then
 // the chunk's partials.  Whole CTA.
+// fv: the chunk's value weight scale, set on the first pass (red:
+// kDecodeWarps floats of shared memory).
 template <int BITS, int NQB, int D>
 __device__ __forceinline__ void pv_pass(const kivi_cache& c, size_t bh, int TX, const ChunkRange& r,
                                         const DecodeSmem& m, const float (&mx)[NQB], size_t row0,
-                                        int nchunks, float* ws_o, float* ws_m, float* ws_l, bool first_pass)
+                                        int nchunks, float* ws_o, float* ws_m, float* ws_l, bool first_pass,
+                                        float& fv, float* red)
 {
     const int ps = prob_stride(TX), NGv = D >> ilog2(c.G);
     const int n = r.t_end - r.t_begin, nq = r.tq_end - r.t_begin;
     if (first_pass) {
         cp_async_wait_all();  // the staged values
         __syncthreads();
+        fv = weight_scale_pow2(cta_max_stat(m.vs, nq * NGv, red));
     }
-    pv_weights<NQB>(n, nq, NGv, threadIdx.x, pv_pairs(n, nq), kDecodeThreads, m.p, ps, mx, m.vs, m.vz,
+    pv_weights<NQB>(n, nq, NGv, threadIdx.x, pv_pairs(n, nq), kDecodeThreads, m.p, ps, mx, m.vs, m.vz, fv,
                     m.bb, bb_stride(TX), m.zs, m.zs_on_p);
     __syncthreads();
-    pv_chunk<BITS, NQB, D>(c, bh, TX, r.t_begin, r.tq_end, r.t_end, m.vw, m.bb, m.part);
+    pv_chunk<BITS, NQB, D>(c, bh, TX, r.t_begin, r.tq_end, r.t_end, m.vw, m.bb, __frcp_rn(fv), m.part);
     __syncthreads();
     write_partials<NQB, D>(c.G, pv_splits(pv_seg_groups<BITS>(D)), m.part, m.zs, mx, row0, nchunks, ws_o,
                            ws_m, ws_l);
@@ -160,6 +167,7 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
     const int NQ = Hq / c.H;
     const int n = r.t_end - r.t_begin;
     const int ps = prob_stride(TC + S);
+    float fv = 1.0f;
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = r.h * NQ + pass * NQB;
         __syncthreads();
@@ -176,7 +184,7 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
         }
         chunk_max<NQB>(mx, red);
         pv_pass<BITS, NQB, D>(c, bh, TC + S, r, m, mx, ((size_t)r.b * Hq + hq0) * nchunks + r.ci, nchunks,
-                           ws_o, ws_m, ws_l, pass == 0);
+                           ws_o, ws_m, ws_l, pass == 0, fv, red);
     }
 }
 
@@ -214,6 +222,7 @@ decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, fl
     cp_async_commit();
     const int ps = prob_stride(TC + S);
     constexpr int rows = 32 / (D / 32);  // residual tokens per warp step
+    float fk = 1.0f, fv = 1.0f;
     for (int pass = 0; pass < NQ / NQB; ++pass) {
         const int hq0 = r.h * NQ + pass * NQB;
         __syncthreads();
@@ -222,11 +231,14 @@ decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, fl
             stage_keys<BITS, T::TOK, D>(c, bh, r.t_begin, r.tq_end, m.kw, m.ks, m.kz);
             cp_async_commit();
         }
-        stage_q<NQB, D>(q + ((size_t)r.b * Hq + hq0) * D, sm_scale, qs, fac);
         if (pass == 0)
             cp_async_wait_prior();  // the keys have landed; the values may still be in flight
         else
             cp_async_wait_all();
+        __syncthreads();
+        if (pass == 0)
+            fk = weight_scale_pow2(cta_max_stat(m.ks, ((r.tq_end - r.t_begin) / c.G) * D, red));
+        stage_q<NQB, D>(q + ((size_t)r.b * Hq + hq0) * D, sm_scale, fk, qs, fac);
         __syncthreads();
         auto sink = [&](int h, int t, float s) { m.p[h * ps + t - r.t_begin] = s; };
         float lmax[2] = {-INFINITY, -INFINITY}, mx[NQB];
@@ -246,7 +258,7 @@ decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, fl
         }
         chunk_max<NQB>(mx, red);  // also publishes the logits
         pv_pass<BITS, NQB, D>(c, bh, TC + S, r, m, mx, ((size_t)r.b * Hq + hq0) * nchunks + r.ci, nchunks,
-                           ws_o, ws_m, ws_l, pass == 0);
+                           ws_o, ws_m, ws_l, pass == 0, fv, red);
     }
 }
 

@@ -113,6 +113,42 @@ __device__ __forceinline__ uint32_t split_part(float a, float b, int part)
     return h2_bits(__floats2half2_rn(part ? __fsub_rn(a, ah) : ah, part ? __fsub_rn(b, bh) : bh));
 }
 
+// Power of two f with mx f in [2^13, 2^14) for the largest statistic mx >= 0
+// of a chunk (1 when mx == 0): the decode weights q s f (|q| < 1) and p s f
+// (p <= 1) then lie below 2^14, and every weight within 2^-27 of the largest
+// keeps its hi part a normal fp16 number, so the hi / lo split holds its 22
+// bits relative to the chunk's largest weight however small the statistics
+// are.  f and 1 / f are exact.
+__device__ __forceinline__ float weight_scale_pow2(float mx)
+{
+    if (!(mx > 0.0f))
+        return 1.0f;
+    const int E = min(max((int)(__float_as_uint(mx) >> 23), 127 - 40), 254);
+    return __uint_as_float((uint32_t)(267 - E) << 23);  // 2^(140 - E)
+}
+
+// Largest of n non-negative staged statistics, over the whole CTA; every
+// thread receives it.  red: kDecodeWarps floats of shared memory.  Contains
+// barriers: call from every thread, after the statistics are visible.
+__device__ __forceinline__ float cta_max_stat(const float* s, int n, float* red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    float mx = 0.0f;
+    for (int i = threadIdx.x; i < n; i += kDecodeThreads)
+        mx = fmaxf(mx, s[i]);
+    for (int k = 16; k > 0; k >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
+    __syncthreads();  // red may still be read by a previous reduction
+    if (lane == 0)
+        red[warp] = mx;
+    __syncthreads();
+    mx = red[0];
+#pragma unroll
+    for (int w = 1; w < kDecodeWarps; ++w)
+        mx = fmaxf(mx, red[w]);
+    return mx;
+}
+
 // -------------------------------------------------------------- shapes ---
 
 // Keys: the 8 lane groups g of a warp take WR word-rows (LPW = 8 / WR lane
@@ -414,11 +450,13 @@ __device__ __forceinline__ void stage_values(const kivi_cache& c, size_t bh, int
 
 __device__ __forceinline__ int qpad(int d) { return d + ((d >> 4) << 2); }
 
-// Stages query heads hq0 .. hq0+NQB-1 of sequence b: qs[h][qpad(d)] = q 2^-e_h
-// with 2^-e_h the power of two that brings max_d |q| into [1/2, 1), and
-// fac[h] = sm_scale 2^e_h.  Called by the whole CTA between barriers.
+// Stages query heads hq0 .. hq0+NQB-1 of sequence b: qs[h][qpad(d)] = q 2^-e_h fk
+// with 2^-e_h the power of two that brings max_d |q| into [1/2, 1) and fk the
+// chunk's key weight scale (weight_scale_pow2 of its largest key scale), and
+// fac[h] = sm_scale 2^e_h / fk.  Called by the whole CTA between barriers.
 template <int NQB, int D>
-__device__ __forceinline__ void stage_q(const uint16_t* __restrict__ q, float sm_scale, float* qs, float* fac)
+__device__ __forceinline__ void stage_q(const uint16_t* __restrict__ q, float sm_scale, float fk, float* qs,
+                                        float* fac)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     constexpr int qstride = qstride_of(D);
@@ -435,6 +473,8 @@ __device__ __forceinline__ void stage_q(const uint16_t* __restrict__ q, float sm
             inv = __uint_as_float((253u - E) << 23);        // 2^(126 - E)
             f = __uint_as_float((E + 1u) << 23);            // 2^(E - 126)
         }
+        inv *= fk;
+        f *= __frcp_rn(fk);  // exact: fk is a power of two
         for (int d = lane; d < D; d += 32)
             qs[h * qstride + qpad(d)] = __half2float(__ushort_as_half(row[d])) * inv;
         if (lane == 0)
@@ -666,8 +706,8 @@ __device__ __forceinline__ void chunk_max(float (&m)[NQB], float* red)
 template <int NQB, int NGV>
 __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_end, int i_step,
                                              const float* p_sm, int ps, const float (&mx)[NQB],
-                                             const float* vs, const float* vz, uint2* bb, int bbs, float* zw,
-                                             bool zw_on_p)
+                                             const float* vs, const float* vz, float fv, uint2* bb, int bbs,
+                                             float* zw, bool zw_on_p)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     float z[NQB][NGV], l[NQB];
@@ -693,8 +733,8 @@ __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_e
         if (t < nq) {  // nq is even: t + 1 is quantized too
 #pragma unroll
             for (int gg = 0; gg < NGV; ++gg) {
-                s0[gg] = vs[t * NGV + gg];
-                s1[gg] = vs[(t + 1) * NGV + gg];
+                s0[gg] = vs[t * NGV + gg] * fv;
+                s1[gg] = vs[(t + 1) * NGV + gg] * fv;
                 const float z0 = vz[t * NGV + gg], z1 = vz[(t + 1) * NGV + gg];
 #pragma unroll
                 for (int h = 0; h < NQB; ++h)
@@ -738,17 +778,19 @@ __device__ __forceinline__ void pv_weights_g(int n, int nq, int i_first, int i_e
 
 // Pairs i_first, i_first + i_step, ... below i_end of the chunk.  Pairs past
 // the last token (up to the end of the last 16-token slice) get zero weights.
+// Quantized tokens' weights carry the chunk's value weight scale fv
+// (weight_scale_pow2 of its largest value scale); pv_unit takes it out again.
 template <int NQB>
 __device__ __forceinline__ void pv_weights(int n, int nq, int NGv, int i_first, int i_end, int i_step,
                                            const float* p_sm, int ps, const float (&mx)[NQB],
-                                           const float* vs, const float* vz, uint2* bb, int bbs, float* zw,
-                                           bool zw_on_p)
+                                           const float* vs, const float* vz, float fv, uint2* bb, int bbs,
+                                           float* zw, bool zw_on_p)
 {
     switch (NGv) {
-    case 1: pv_weights_g<NQB, 1>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
-    case 2: pv_weights_g<NQB, 2>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
-    case 4: pv_weights_g<NQB, 4>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
-    default: pv_weights_g<NQB, 8>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, bb, bbs, zw, zw_on_p); break;
+    case 1: pv_weights_g<NQB, 1>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, fv, bb, bbs, zw, zw_on_p); break;
+    case 2: pv_weights_g<NQB, 2>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, fv, bb, bbs, zw, zw_on_p); break;
+    case 4: pv_weights_g<NQB, 4>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, fv, bb, bbs, zw, zw_on_p); break;
+    default: pv_weights_g<NQB, 8>(n, nq, i_first, i_end, i_step, p_sm, ps, mx, vs, vz, fv, bb, bbs, zw, zw_on_p); break;
     }
 }
 // Pairs a chunk of n tokens (nq quantized) needs: through the last residual slice.
@@ -773,7 +815,7 @@ template <int BITS, int NQB, int D>
 __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_begin, int tq_end,
                                         int t_end, const uint32_t* vw, const uint2* bb, int bbs,
                                         int sp, int kq, int kq_end, int kr, int kr_end,
-                                        int kstep, float* o_out)
+                                        int kstep, float inv_fv, float* o_out)
 {
     using T = ValTile<BITS>;
     const int G = c.G, lgG = ilog2(G), RG = c.R + c.G;
@@ -848,12 +890,14 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
             }
         }
     }
-    // undo the code scaling before the residual tokens join the sums
+    // undo the code scaling and the weight scale before the residual tokens
+    // join the sums
 #pragma unroll
     for (int s = 0; s < 2; ++s)
 #pragma unroll
         for (int j = 0; j < T::NT; ++j) {
-            const float f0 = code_unscale_bits(T::bitpos(2 * j)), f1 = code_unscale_bits(T::bitpos(2 * j + 1));
+            const float f0 = code_unscale_bits(T::bitpos(2 * j)) * inv_fv;
+            const float f1 = code_unscale_bits(T::bitpos(2 * j + 1)) * inv_fv;
             acc[s][j][0] *= f0;
             acc[s][j][1] *= f0;
             acc[s][j][2] *= f1;
@@ -951,7 +995,7 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
 template <int BITS, int NQB, int D>
 __device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TX, int t_begin,
                                          int tq_end, int t_end, const uint32_t* vw, const uint2* bb,
-                                         float* o_part)
+                                         float inv_fv, float* o_part)
 {
     constexpr int NSP = pv_seg_groups<BITS>(D);
     constexpr int NSPLIT = pv_splits(NSP);
@@ -960,7 +1004,7 @@ __device__ __forceinline__ void pv_chunk(const kivi_cache& c, size_t bh, int TX,
     for (int unit = threadIdx.x >> 5; unit < NSP * NSPLIT; unit += kDecodeWarps) {
         const int sp = unit % NSP, split = unit / NSP;
         pv_unit<BITS, NQB, D>(c, bh, t_begin, tq_end, t_end, vw, bb, bb_stride(TX), sp, split, nq_slices,
-                              split, nr_slices, NSPLIT, o_part + (size_t)split * NQB * D);
+                              split, nr_slices, NSPLIT, inv_fv, o_part + (size_t)split * NQB * D);
     }
 }
 
