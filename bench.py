@@ -165,15 +165,14 @@ STEP_CALLS = {
     "stream": ["append", "decode"],
 }
 # "decode" is the fused kivi_decode_attention (--decode fused, the default) or
-# kivi_decode_qk followed by kivi_decode_pv (--decode split, and always when
-# bits_k != bits_v).
+# kivi_decode_qk followed by kivi_decode_pv (--decode split).
 DECODE_CALLS = {"fused": ["decode_attn"], "split": ["decode_qk", "decode_pv"]}
 LAUNCHES = {"quant_keys": 1, "quant_values": 1, "dequant_keys": 1, "dequant_values": 1,
             "append": 2, "decode_qk": 1, "decode_pv": 2, "decode_attn": 2}  # + combine kernels
 
 
 def step_calls(w, kind: str, decode: str) -> list:
-    mode = decode if w.bits_k == w.bits_v else "split"
+    mode = decode
     out = []
     for c in STEP_CALLS[kind]:
         out += DECODE_CALLS[mode] if c == "decode" else [c]

@@ -277,7 +277,8 @@ size_t kivi_workspace_bytes(const kivi_cache* c, int32_t Hq)
 {
     if (check_sizes(c) != KIVI_OK || Hq < 1)
         return 0;
-    return ws_bytes(*c, Hq);
+    const size_t pv = ws_bytes(*c, Hq), fused = kivi::stream_ws_bytes(*c, Hq);
+    return pv > fused ? pv : fused;
 }
 
 int32_t kivi_decode_pv(const kivi_cache* c, const float* logits, int32_t ld_logits, int32_t Hq,
@@ -306,17 +307,10 @@ int32_t kivi_decode_attention(const kivi_cache* c, const uint16_t* q, int32_t Hq
     if (st != KIVI_OK || (st = check_heads(c, Hq)) != KIVI_OK || (st = check_ptr(q, "q")) != KIVI_OK ||
         (st = check_ptr(out, "out")) != KIVI_OK || (st = check_ptr(ws, "ws")) != KIVI_OK)
         return st;
-    if (c->bits_k != c->bits_v)
-        return fail(KIVI_EINVAL, "kivi_decode_attention needs bits_k == bits_v (got %d, %d); "
-                    "use kivi_decode_qk + kivi_decode_pv", c->bits_k, c->bits_v);
-    const size_t need = ws_bytes(*c, Hq);
+    const size_t need = kivi::stream_ws_bytes(*c, Hq);
     if (ws_bytes_given < need)
         return fail(KIVI_EWORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes_given, need);
-    const size_t rows = (size_t)c->B * Hq * kivi::pv_chunks(*c, Hq);
-    float* ws_o = static_cast<float*>(ws);
-    float* ws_m = ws_o + rows * c->D;
-    float* ws_l = ws_m + rows;
-    return launched(kivi::launch_decode_attention(*c, q, Hq, sm_scale, out, ws_o, ws_m, ws_l,
+    return launched(kivi::launch_decode_attention(*c, q, Hq, sm_scale, out, static_cast<float*>(ws),
                                                   (cudaStream_t)stream));
 }
 

@@ -5,9 +5,25 @@
 #include <math.h>
 
 #include "decode_mma.cuh"
+#include "decode_stream.cuh"
 #include "kivi_launch.h"
 
 namespace kivi {
+
+// The streamed decode is instantiated in decode_stream_d<D>_k<BK>.cu, not here.
+#define KIVI_STREAM_EXTERN(DIM, BK)                                                                              \
+    extern template cudaError_t launch_decode_stream<DIM, BK>(const kivi_cache&, const uint16_t*, int, float, \
+                                                              float*, float*, cudaStream_t);
+KIVI_STREAM_EXTERN(64, 2)
+KIVI_STREAM_EXTERN(64, 4)
+KIVI_STREAM_EXTERN(64, 8)
+KIVI_STREAM_EXTERN(128, 2)
+KIVI_STREAM_EXTERN(128, 4)
+KIVI_STREAM_EXTERN(128, 8)
+KIVI_STREAM_EXTERN(256, 2)
+KIVI_STREAM_EXTERN(256, 4)
+KIVI_STREAM_EXTERN(256, 8)
+#undef KIVI_STREAM_EXTERN
 
 // out[b][hq][d] = sum_c o_c[d] e^(m_c - M) / sum_c l_c e^(m_c - M), M = max m_c
 // over the chunks c that hold tokens of sequence b.  CTA (b hq, y) writes
@@ -170,19 +186,26 @@ cudaError_t launch_decode_pv(const kivi_cache& c, const float* logits, int ld_lo
 }
 
 cudaError_t launch_decode_attention(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale,
-                                    float* out, float* ws_o, float* ws_m, float* ws_l,
-                                    cudaStream_t s)
+                                    float* out, float* ws, cudaStream_t s)
 {
-    // the fused kernel needs bits_k == bits_v (checked by the caller)
-    cudaError_t e;
-    switch (c.D) {
-    case 64: e = launch_decode_attention_d<64>(c, q, Hq, sm_scale, ws_o, ws_m, ws_l, s); break;
-    case 128: e = launch_decode_attention_d<128>(c, q, Hq, sm_scale, ws_o, ws_m, ws_l, s); break;
-    default: e = launch_decode_attention_d<256>(c, q, Hq, sm_scale, ws_o, ws_m, ws_l, s); break;
+#define KIVI_STREAM_BK(DIM)                                                                  \
+    switch (c.bits_k) {                                                                      \
+    case 2: return launch_decode_stream<DIM, 2>(c, q, Hq, sm_scale, out, ws, s);            \
+    case 4: return launch_decode_stream<DIM, 4>(c, q, Hq, sm_scale, out, ws, s);            \
+    default: return launch_decode_stream<DIM, 8>(c, q, Hq, sm_scale, out, ws, s);           \
     }
-    if (e != cudaSuccess)
-        return e;
-    return combine(c, Hq, ws_o, ws_m, ws_l, out, s);
+    switch (c.D) {
+    case 64: KIVI_STREAM_BK(64)
+    case 128: KIVI_STREAM_BK(128)
+    default: KIVI_STREAM_BK(256)
+    }
+#undef KIVI_STREAM_BK
+}
+
+size_t stream_ws_bytes(const kivi_cache& c, int Hq)
+{
+    const int NQ = Hq / c.H;
+    return stream_ws_floats(c.D, heads_per_pass(NQ), kMaxStreamCTAs) * sizeof(float);
 }
 
 }  // namespace kivi

@@ -5,14 +5,13 @@
 // tile's index arithmetic is resolved at compile time).  decode_d64.cu,
 // decode_d128.cu and decode_d256.cu instantiate them; decode.cu dispatches.
 //
-// Three entry kernels share the tiles of decode_mma.cuh:
+// Two entry kernels share the tiles of decode_mma.cuh:
 //   decode_qk_kernel         logits to global memory (kivi_decode_qk)
 //   decode_pv_kernel         softmax + p . V from given logits (kivi_decode_pv)
-//   decode_attention_kernel  both, logits kept in shared memory
-//                            (kivi_decode_attention)
 // Each CTA owns one KV head and one chunk of tokens (decode_chunk_plan),
-// staged into shared memory at launch; the pv and fused kernels leave
-// per-chunk (o, m, l) partials that decode_combine_kernel (decode.cu) merges.
+// staged into shared memory at launch; the pv kernel leaves per-chunk
+// (o, m, l) partials that decode_combine_kernel (decode.cu) merges.  The fused
+// kivi_decode_attention runs the streamed kernel of decode_stream.cuh.
 #pragma once
 
 #include <math.h>
@@ -188,80 +187,6 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
     }
 }
 
-// ------------------------------------------------------------ attention ---
-
-// One CTA per (KV head, chunk): the chunk's keys and values are staged at
-// launch (two cp.async groups, keys first); q . K_hat^T runs as soon as the
-// keys have landed and leaves the logits in shared memory, then the softmax,
-// the B fragments and p . V_hat run as in decode_pv_kernel.  The logits never
-// reach HBM.
-template <int BITS, int NQB, int D>
-__global__ void __launch_bounds__(kDecodeThreads, 3)
-decode_attention_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_scale,
-                        float* __restrict__ ws_o, float* __restrict__ ws_m,
-                        float* __restrict__ ws_l, int nchunks, int TC, int S, const DecodeLayout L)
-{
-    extern __shared__ __align__(16) float dsm[];
-    __shared__ __align__(16) float qs[NQB * qstride_of(D)];
-    __shared__ float fac[NQB];
-    __shared__ float red[kDecodeWarps * NQB];
-    using T = KeyTile<BITS, NQB>;
-    // the combine kernel may launch once every chunk CTA has started: it waits
-    // for this grid's results in griddepcontrol.wait
-    asm volatile("griddepcontrol.launch_dependents;");
-    ChunkRange r;
-    if (!chunk_range(c, TC, S, r))
-        return;
-    const size_t bh = r.bh;
-    const int warp = threadIdx.x >> 5;
-    const int NQ = Hq / c.H;
-    const DecodeSmem m = carve(dsm, L);
-    stage_keys<BITS, T::TOK, D>(c, bh, r.t_begin, r.tq_end, m.kw, m.ks, m.kz);
-    cp_async_commit();
-    stage_values<BITS, D>(c, bh, r.t_begin, r.tq_end, m.vw, m.vs, m.vz);
-    cp_async_commit();
-    const int ps = prob_stride(TC + S);
-    constexpr int rows = 32 / (D / 32);  // residual tokens per warp step
-    float fk = 1.0f, fv = 1.0f;
-    for (int pass = 0; pass < NQ / NQB; ++pass) {
-        const int hq0 = r.h * NQ + pass * NQB;
-        __syncthreads();
-        if (pass > 0 && L.bb_on_keys) {
-            // the previous pass's B fragments overwrote the staged keys
-            stage_keys<BITS, T::TOK, D>(c, bh, r.t_begin, r.tq_end, m.kw, m.ks, m.kz);
-            cp_async_commit();
-        }
-        if (pass == 0)
-            cp_async_wait_prior();  // the keys have landed; the values may still be in flight
-        else
-            cp_async_wait_all();
-        __syncthreads();
-        if (pass == 0)
-            fk = weight_scale_pow2(cta_max_stat(m.ks, ((r.tq_end - r.t_begin) / c.G) * D, red));
-        stage_q<NQB, D>(q + ((size_t)r.b * Hq + hq0) * D, sm_scale, fk, qs, fac);
-        __syncthreads();
-        auto sink = [&](int h, int t, float s) { m.p[h * ps + t - r.t_begin] = s; };
-        float lmax[2] = {-INFINITY, -INFINITY}, mx[NQB];
-#pragma unroll
-        for (int h = 0; h < NQB; ++h)
-            mx[h] = -INFINITY;
-        qk_quantized<BITS, NQB, D>(c.G, r.t_begin, r.tq_end, r.t_begin + warp * T::TOK, r.tq_end,
-                                kDecodeWarps * T::TOK, m.kw, m.ks, m.kz, qs, fac, sink, lmax);
-        qk_residual<NQB, D>(c, bh, r.tq_end + warp * rows, kDecodeWarps * rows, r.t_end, qs, fac, sink, mx);
-#pragma unroll
-        for (int slot = 0; slot < 2; ++slot) {
-            const int hs = qk_slot_head<BITS, NQB>(slot);
-#pragma unroll
-            for (int h = 0; h < NQB; ++h)
-                if (hs == h)
-                    mx[h] = fmaxf(mx[h], lmax[slot]);
-        }
-        chunk_max<NQB>(mx, red);  // also publishes the logits
-        pv_pass<BITS, NQB, D>(c, bh, TC + S, r, m, mx, ((size_t)r.b * Hq + hq0) * nchunks + r.ci, nchunks,
-                           ws_o, ws_m, ws_l, pass == 0, fv, red);
-    }
-}
-
 // ---------------------------------------------------------------- launch ---
 
 inline DecodeLayout cta_layout(const kivi_cache& c, int Hq, bool keys, bool values)
@@ -311,21 +236,6 @@ cudaError_t pv_launch(const kivi_cache& c, const float* logits, int ldl, int Hq,
     return cudaGetLastError();
 }
 
-template <int D, int BITS, int NQB>
-cudaError_t attn_launch(const kivi_cache& c, const uint16_t* q, int Hq, float sm, float* ws_o, float* ws_m,
-                        float* ws_l, cudaStream_t s)
-{
-    auto kern = decode_attention_kernel<BITS, NQB, D>;
-    const DecodeLayout L = cta_layout(c, Hq, true, true);
-    const ChunkPlan cp = chunk_plan(c, Hq);
-    cudaError_t e = set_smem(kern, 4 * L.total);
-    if (e != cudaSuccess)
-        return e;
-    kern<<<decode_grid(c, Hq), kDecodeThreads, 4 * L.total, s>>>(c, q, Hq, sm, ws_o, ws_m, ws_l,
-                                                                pv_chunks(c, Hq), cp.TC, cp.S, L);
-    return cudaGetLastError();
-}
-
 // Dispatch of the code width (bits) and the query heads per pass (NQB) for
 // head dimension D; `launch` is one of the launchers above.
 #define KIVI_DECODE_DISPATCH(bits, NQ, launch, ...)                              \
@@ -364,22 +274,13 @@ cudaError_t launch_decode_pv_d(const kivi_cache& c, const float* logits, int ld_
     KIVI_DECODE_DISPATCH(c.bits_v, Hq / c.H, pv_launch, c, logits, ld_logits, Hq, ws_o, ws_m, ws_l, s)
 }
 
-template <int D>
-cudaError_t launch_decode_attention_d(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale,
-                                      float* ws_o, float* ws_m, float* ws_l, cudaStream_t s)
-{
-    KIVI_DECODE_DISPATCH(c.bits_k, Hq / c.H, attn_launch, c, q, Hq, sm_scale, ws_o, ws_m, ws_l, s)
-}
-
 #undef KIVI_DECODE_DISPATCH
 
-// Instantiates the three launchers for one head dimension.
+// Instantiates the two launchers for one head dimension.
 #define KIVI_DECODE_INSTANTIATE(DIM)                                                                      \
     template cudaError_t launch_decode_qk_d<DIM>(const kivi_cache&, const uint16_t*, int, float, float*, \
                                                  int, cudaStream_t);                                      \
     template cudaError_t launch_decode_pv_d<DIM>(const kivi_cache&, const float*, int, int, float*,      \
-                                                 float*, float*, cudaStream_t);                           \
-    template cudaError_t launch_decode_attention_d<DIM>(const kivi_cache&, const uint16_t*, int, float,  \
-                                                        float*, float*, float*, cudaStream_t);
+                                                 float*, float*, cudaStream_t);
 
 }  // namespace kivi

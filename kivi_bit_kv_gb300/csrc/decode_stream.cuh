@@ -1,0 +1,1307 @@
+// decode_stream.cuh -- kivi_decode_attention as one persistent, pipelined
+// kernel: the decode-time consumer of the KIVI cache (q . K_hat^T, softmax,
+// p . V_hat over the packed cache plus the fp16 residual, dequantization
+// fused into the operand build; CacheForge README, "How it works").
+//
+// Work.  The rows of the problem are (sequence b, KV head h, pass) -- one pass
+// covers NQB query heads of h's grouped-query set -- and a row of n tokens is
+// cut into tiles: ceil(Tq/TS) quantized tiles of TS tokens (the last one
+// shorter), then ceil((n - Tq)/RT) residual tiles of RT fp16 tokens.  Both
+// kinds move about the same number of bytes.  One CTA runs per SM; CTA i takes
+// the contiguous range [i NT / N, (i+1) NT / N) of the NT tiles of all rows in
+// order, so the load is balanced whatever the (device-side, ragged) lengths.
+// A row that lies wholly inside one CTA's range is finished there and its
+// output written; a row cut by a range boundary leaves one partial (o, m, l)
+// per CTA, merged by decode_stream_combine_kernel.
+//
+// Pipeline.  Warp NC of the CTA is the producer: for every tile of the range
+// one of its threads waits for a free stage, announces the stage's byte count
+// on the stage's mbarrier and issues 1-D bulk copies (cp.async.bulk, the TMA
+// engine), global to shared: seven per quantized tile (the row's query, the
+// packed key word-rows, key scales, key zeros, packed value rows, value
+// scales, value zeros; each a contiguous range of its buffer) and three or
+// five per residual tile (query, key and value ring slots, which wrap at most
+// once).  Warps 0 .. NC-1 are consumers: consumer w takes tiles w,
+// w + NC, ... of the range, waits for its stage, computes the whole tile and
+// releases the stage.  Each consumer keeps its own online-softmax state
+// (running maximum m, sums l, the weighted value sums); at the end of every
+// row segment the consumers merge their states through shared memory.
+//
+// A quantized tile, per consumer warp:
+//   1. q . K_hat on the warp-level tensor cores (decode_mma.cuh: codes as
+//      fp16 subnormals in the A operand, weights q s as hi / lo fp16 pairs in
+//      B, one MMA per 16 x 16 codes), zero terms sum_d q_d z_gd in fp32;
+//      the logits go to a per-warp row in shared memory.  The weights carry a
+//      power of two f (weight_scale_pow2 of max|q| times the tile's largest
+//      key scale) that keeps them normal fp16 numbers, and the logits divide
+//      it out.
+//   2. the online softmax over the tile's logits: new maximum, rescaling of
+//      the state, p = exp(s - m).
+//   3. the value weights u = p s f_v (f_v from the tile's largest value
+//      scale) as hi / lo fp16 pairs in B-fragment order, and the zero terms
+//      sum_t p_t z_tg, then p . V_hat with the codes from ldmatrix.trans.
+// A residual tile: q . K on the tensor cores with the fp16 keys as A and the
+// fp16 query as B (both exact, fp32 accumulation), the softmax as above, and
+// p . V in fp32 FMA over the fp16 values.
+//
+// Every wait on an mbarrier gives up after two seconds (which only a fault
+// elsewhere could cause): it records KIVI_ETIMEOUT in the workspace's status
+// word, the outputs of the affected rows are then meaningless, and the CTA
+// leaves once the copies it issued have landed (a bounded wait as well).
+#pragma once
+
+#include <math.h>
+
+#include "decode_mma.cuh"
+#include "kivi_launch.h"
+
+namespace kivi {
+
+// ------------------------------------------------------------------ PTX ---
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t* b, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{ .reg .pred p; mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2; selp.u32 %0, 1, 0, p; }"
+        : "=r"(done)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+// 1-D bulk copy global -> shared, completing `bytes` on the mbarrier.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* b)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     smem_addr(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_addr(b))
+                 : "memory");
+}
+constexpr uint64_t kStreamWaitNs = 2000000000ull;  // a wait on a stage gives up after 2 s
+
+// Nanoseconds of the global timer.
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Waits for the phase of parity `parity` of mbarrier b; false if it has not
+// completed within kStreamWaitNs or *abort became set.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity, const volatile int* abort);
+// 2^x (ex2.approx: relative error below 2^-22; 2^-inf = 0).  The streamed
+// decode keeps its logits in log2 units (the softmax scale times log2 e), so
+// every exponential of the softmax is one ex2.
+__device__ __forceinline__ float ex2(float x)
+{
+    float y;
+    asm("ex2.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void named_bar(int id, int threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* b, uint32_t parity, const volatile int* abort)
+{
+    if (mbar_try_wait(b, parity))
+        return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t it = 1;; ++it) {
+        if (mbar_try_wait(b, parity))
+            return true;
+        if ((it & 63u) == 0 && (*abort || global_ns() - t0 > kStreamWaitNs))
+            return false;
+    }
+}
+
+// ---------------------------------------------------------------- shape ---
+
+__host__ __device__ constexpr int pow2floor(int x) { return x <= 1 ? 1 : 2 * pow2floor(x / 2); }
+__host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
+
+constexpr int kMaxStreamCTAs = 1024;          // workspace sizing bound on the grid
+constexpr int kStreamLocInts = 8;             // ints per CTA range record in the workspace
+constexpr int kStreamHeaderFloats = 4;        // workspace header (status word)
+
+// Compile-time shape of the streamed decode for key / value widths BK / BV,
+// NQB query heads per pass, head dimension D and NC consumer warps.  Sizes
+// that depend on the group size G (32, 64 or 128) are taken at G = 32, the
+// largest.
+template <int BK, int BV, int NQB, int D, int NC>
+struct StreamCfg {
+    using KT = KeyTile<BK, NQB>;
+    using VT = ValTile<BV>;
+    static constexpr int PK = 32 / BK, PV = 32 / BV;
+    static constexpr int TOK = KT::TOK;                // tokens per key warp tile
+    static constexpr int DW = D / PV;                  // value words per token
+    static constexpr int NSEG = DW / 4;                // 16-byte value segments per token
+    static constexpr int SPL = NSEG >= 2 ? 2 : 1;      // segments per ldmatrix
+    static constexpr int NTV = VT::NT;                 // value MMA tiles per segment
+    static constexpr int NGM = D / 32;                 // statistic groups per row (G = 32)
+    static constexpr int CPL = D / 32;                 // residual channels per lane
+    // bytes per quantized token (codes and fp32 statistics at G = 32); a
+    // quantized stage holds about 16 KB, a residual stage as much
+    static constexpr int BPT = D * (BK + BV) / 8 + D / 2;
+    static constexpr int TS = cmax(cmax(TOK, 32), pow2floor(16384 / BPT));
+    static constexpr int RT = cmax(16, cmin(64, pow2floor(TS * BPT / (4 * D))));
+    // stage slot (bytes from the slot start, each region 16-byte aligned)
+    static constexpr int QB = NQB * D * 2;             // the row's query heads, fp16
+    static constexpr int KROW = D * 4;                 // key word-row
+    static constexpr int KSR = cmax(1, TS / 32);       // key statistic rows
+    static constexpr int O_KW = round_up(QB, 128);
+    static constexpr int O_KS = O_KW + (TS / PK) * KROW;
+    static constexpr int O_KZ = O_KS + KSR * D * 4;
+    static constexpr int O_VW = O_KZ + KSR * D * 4;
+    static constexpr int O_VS = O_VW + TS * DW * 4;
+    static constexpr int O_VZ = O_VS + TS * NGM * 4;
+    static constexpr int Q_END = O_VZ + TS * NGM * 4;
+    static constexpr int RROW = D * 2;                 // residual row
+    static constexpr int O_KR = O_KW;
+    static constexpr int O_VR = O_KR + RT * RROW;
+    static constexpr int R_END = O_VR + RT * RROW;
+    static constexpr int SLOT = round_up(cmax(Q_END, R_END), 128);
+    // per-consumer scratch (floats): logits / probabilities [NQB][LS]
+    // (two floats of padding per 16 tokens), the scaled query [NQB][QWS],
+    // the value weights [2 parts][UNITS][UTS] fp16 for UB tokens at a time
+    static constexpr int LS = TS + TS / 8;
+    static constexpr int QWS = D + 4;
+    static constexpr int UNITS = NGM * NQB;            // value weight units (group, head)
+    static constexpr bool HLV = NQB <= 2;              // value hi / lo in separate B columns
+    static constexpr int UF = HLV ? 4 : 8;             // units per B fragment
+    static constexpr int UB = UNITS <= 8 ? TS : cmin(TS, 64);
+    static constexpr int UTS = UB + 8;                 // halves per weight row
+    static constexpr int W_LG = 0;
+    static constexpr int W_QW = W_LG + NQB * LS;
+    static constexpr int W_UB = W_QW + NQB * QWS;
+    static constexpr int WARP_FLOATS = round_up(W_UB + UNITS * UTS, 4);
+    // merge area (floats): o [NC][NQB][D], m, l [NC][NQB], z [NC][NQB][NGM]
+    static constexpr int M_O = 0;
+    static constexpr int M_M = M_O + NC * NQB * D;
+    static constexpr int M_L = M_M + NC * NQB;
+    static constexpr int M_Z = M_L + NC * NQB;
+    static constexpr int M_END = round_up(M_Z + NC * NQB * NGM, 4);
+    static constexpr int FIXED_BYTES = 4 * (NC * WARP_FLOATS + M_END) + 256;
+    static constexpr int THREADS = 32 * (NC + 1);
+    static_assert(TS % TOK == 0 && TS % 16 == 0 && RT % 16 == 0 && RT <= TS, "tile shape");
+    static_assert(UB % 16 == 0 && TS % UB == 0, "weight batches");
+    static_assert(UF % NQB == 0, "a fragment holds whole groups");
+};
+
+// Stages that fit the shared memory of one SM next to the fixed areas.
+constexpr int kStreamSmemBytes = 227 * 1024;  // dynamic + static shared memory of one CTA
+template <class C>
+__host__ __device__ constexpr int stream_stages()
+{
+    return (kStreamSmemBytes - C::FIXED_BYTES) / (C::SLOT + 16);
+}
+
+// Consumer warps of the streamed decode for a shape: up to seven (eight warps
+// with the producer, two per SM sub-partition, so each thread may hold up to
+// 255 registers), fewer when the shared memory would otherwise hold no more
+// stages than consumers -- every consumer then has a stage and at least one
+// more is in flight.
+constexpr int kStreamMaxConsumers = 7;
+template <int BK, int BV, int NQB, int D, int NC = kStreamMaxConsumers>
+__host__ __device__ constexpr int stream_consumers()
+{
+    if constexpr (NC <= 1)
+        return 1;
+    else
+        return stream_stages<StreamCfg<BK, BV, NQB, D, NC>>() >= NC + 1 ? NC
+                                                                          : stream_consumers<BK, BV, NQB, D, NC - 1>();
+}
+
+// Workspace of the streamed decode: header, the CTA range records and two
+// partial (o, m, l) slots per CTA.
+inline size_t stream_ws_floats(int D, int NQB, int ctas)
+{
+    return (size_t)kStreamHeaderFloats + (size_t)(ctas + 1) * kStreamLocInts +
+           (size_t)ctas * 2 * NQB * (D + 2);
+}
+
+// ---------------------------------------------------------- tile walker ---
+
+// Position in the row-major sequence of tiles: sequence b, row rr = h NP +
+// pass of b, tile j of the row; the rest describes sequence b.
+struct Walk {
+    int b, rr, j;
+    int len, Tq, nq, nt;
+};
+
+__device__ __forceinline__ void walk_load(Walk& w, const kivi_cache& c, int TS, int RT)
+{
+    w.len = c.len[w.b];
+    w.Tq = quantized_tokens(w.len, c.G, c.R);
+    w.nq = (w.Tq + TS - 1) / TS;
+    w.nt = w.nq + (w.len - w.Tq + RT - 1) / RT;
+}
+
+__device__ __forceinline__ void walk_next(Walk& w, const kivi_cache& c, int RB, int TS, int RT)
+{
+    if (++w.j < w.nt)
+        return;
+    w.j = 0;
+    if (++w.rr < RB)
+        return;
+    w.rr = 0;
+    for (++w.b; w.b < c.B; ++w.b) {
+        walk_load(w, c, TS, RT);
+        if (w.nt > 0)
+            return;
+    }
+}
+
+// Tokens of the current tile: [t0, t0 + n), quantized or residual.
+__device__ __forceinline__ bool walk_quant(const Walk& w) { return w.j < w.nq; }
+__device__ __forceinline__ int walk_t0(const Walk& w, int TS, int RT)
+{
+    return w.j < w.nq ? w.j * TS : w.Tq + (w.j - w.nq) * RT;
+}
+__device__ __forceinline__ int walk_n(const Walk& w, int TS, int RT)
+{
+    const int t0 = walk_t0(w, TS, RT);
+    return w.j < w.nq ? min(TS, w.Tq - t0) : min(RT, w.len - t0);
+}
+
+// Tiles of sequence b's rows (each of the RB rows of b holds nt tiles).
+__device__ __forceinline__ int row_tiles(int len, const kivi_cache& c, int TS, int RT)
+{
+    const int Tq = quantized_tokens(len, c.G, c.R);
+    return (Tq + TS - 1) / TS + (len - Tq + RT - 1) / RT;
+}
+
+// Exclusive prefix sum of v over the CTA (THREADS threads) and its total.
+template <int THREADS>
+__device__ __forceinline__ long long cta_exscan(long long v, long long& total, long long* red)
+{
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    long long x = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o)
+            x += y;
+    }
+    if (lane == 31)
+        red[warp] = x;
+    __syncthreads();
+    long long off = 0, tot = 0;
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) {
+        const long long r = red[w];
+        off += w < warp ? r : 0;
+        tot += r;
+    }
+    __syncthreads();
+    total = tot;
+    return off + x - v;
+}
+
+// CTA range record: first tile (global index) and its position.
+struct RangeStart {
+    long long g;
+    int b, rr, j;
+};
+
+// Start of CTA k's range and of CTA k+1's (the end), from the device-side
+// lengths: two passes over the sequences (total, then location).
+template <int THREADS>
+__device__ __forceinline__ void locate_range(const kivi_cache& c, int RB, int TS, int RT, int k, int N,
+                                             RangeStart& r0, RangeStart& r1, long long* red, RangeStart* sh)
+{
+    long long NT = 0;
+    for (int base = 0; base < c.B; base += THREADS) {
+        const int b = base + (int)threadIdx.x;
+        const long long v = b < c.B ? (long long)RB * row_tiles(c.len[b], c, TS, RT) : 0;
+        long long tot;
+        cta_exscan<THREADS>(v, tot, red);
+        NT += tot;
+    }
+    const long long X[2] = {NT * k / N, NT * (k + 1) / N};
+    if (threadIdx.x < 2)
+        sh[threadIdx.x] = RangeStart{X[threadIdx.x], c.B, 0, 0};
+    __syncthreads();
+    long long ex0 = 0;
+    for (int base = 0; base < c.B; base += THREADS) {
+        const int b = base + (int)threadIdx.x;
+        const int nt = b < c.B ? row_tiles(c.len[b], c, TS, RT) : 0;
+        const long long v = (long long)RB * nt;
+        long long tot;
+        const long long ex = ex0 + cta_exscan<THREADS>(v, tot, red);
+#pragma unroll
+        for (int i = 0; i < 2; ++i)
+            if (v > 0 && ex <= X[i] && X[i] < ex + v) {
+                const long long w = X[i] - ex;
+                sh[i] = RangeStart{X[i], b, (int)(w / nt), (int)(w % nt)};
+            }
+        ex0 += tot;
+    }
+    __syncthreads();
+    r0 = sh[0];
+    r1 = sh[1];
+}
+
+// ------------------------------------------------------- consumer state ---
+
+template <class C, int NQB>
+struct ConsumerState {
+    float m[NQB];                    // running maxima (of the logits)
+    float l[NQB];                    // lane partial sums of exp(s - m)
+    float z[NQB][C::NGM];            // lane partial zero terms sum_t p_t z_tg
+    float o[C::NSEG][C::NTV][4];     // weighted value sums, MMA layout, in units 1 / fv
+    float r[NQB][C::CPL];            // residual weighted sums, channels lane*CPL + i
+    float qmax[NQB];                 // max |q| of the row's heads (< 0: not yet known)
+    float fv;                        // current value weight scale of o
+};
+
+template <class C, int NQB>
+__device__ __forceinline__ void state_reset(ConsumerState<C, NQB>& s)
+{
+#pragma unroll
+    for (int h = 0; h < NQB; ++h) {
+        s.m[h] = -INFINITY;
+        s.l[h] = 0.0f;
+        s.qmax[h] = -1.0f;
+#pragma unroll
+        for (int g = 0; g < C::NGM; ++g)
+            s.z[h][g] = 0.0f;
+#pragma unroll
+        for (int i = 0; i < C::CPL; ++i)
+            s.r[h][i] = 0.0f;
+    }
+#pragma unroll
+    for (int sg = 0; sg < C::NSEG; ++sg)
+#pragma unroll
+        for (int j = 0; j < C::NTV; ++j)
+            s.o[sg][j][0] = s.o[sg][j][1] = s.o[sg][j][2] = s.o[sg][j][3] = 0.0f;
+    s.fv = 1.0f;
+}
+
+__device__ __forceinline__ int lg_phys(int t) { return t + 2 * (t >> 4); }
+
+__device__ __forceinline__ float sel4(const float (&a)[4], int i)
+{
+    return i == 0 ? a[0] : i == 1 ? a[1] : i == 2 ? a[2] : a[3];
+}
+template <int N>
+__device__ __forceinline__ float seln(const float (&a)[N], int i)
+{
+    float r = a[0];
+#pragma unroll
+    for (int k = 1; k < N; ++k)
+        r = i == k ? a[k] : r;
+    return r;
+}
+
+// Value head of the lane's MMA output column pair cc (0, 1) for fragment-
+// local units (2 tg + cc without hi / lo columns, tg with them).
+template <class C, int NQB>
+__device__ __forceinline__ int pv_col_head(int tg, int cc)
+{
+    return C::HLV ? tg % NQB : (2 * tg + cc) % NQB;
+}
+
+// ----------------------------------------------------------- quantized ---
+
+// Largest statistic of the first n floats at p (a multiple of 4), per warp.
+__device__ __forceinline__ float warp_max_stat(const float* p, int n)
+{
+    const int lane = threadIdx.x & 31;
+    float mx = 0.0f;
+    for (int i = 4 * lane; i < n; i += 128) {
+        const float4 v = *reinterpret_cast<const float4*>(p + i);
+        mx = fmaxf(fmaxf(mx, v.x), fmaxf(fmaxf(v.y, v.z), v.w));
+    }
+#pragma unroll
+    for (int k = 16; k > 0; k >>= 1)
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
+    return mx;
+}
+
+// q . K_hat of one key warp tile (tokens tok0 .. tok0 + TOK of the stage,
+// valid below n) into the logit rows lg[h][lg_phys(t)] for valid tokens.
+// kst0: the stage's first key statistic row is group kst0; t0: first token
+// of the stage in its sequence; fac[h] = sm_scale log2(e) / f_h.
+template <int BK, int NQB, int D, class C>
+__device__ __forceinline__ void qk_warp_tile(int lgG, int t0, int tok0, int n, const uint8_t* slot,
+                                             const float* qw, const float (&fac)[NQB], float* lg)
+{
+    using T = KeyTile<BK, NQB>;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tg = lane & 3;
+    const int wr = g % T::WR, v = g / T::WR;
+    const uint32_t soff = (uint32_t)(2 * v * T::NT / T::CPB) * 0x101u;
+    const int NGW = cmax(1, T::TOK >> lgG);
+    const int unit = T::HL ? g >> 1 : g, part = g & 1;
+    const int gi = cmin(unit / NQB, NGW - 1);
+    const int hq = unit % NQB;
+    const int gi_row = (wr * T::P) >> lgG;
+    const int krow = ((t0 + tok0) >> lgG) + gi - (t0 >> lgG);  // stage statistics row of the B column
+    const uint4* wrow = reinterpret_cast<const uint4*>(slot + C::O_KW + (tok0 / T::P + wr) * C::KROW);
+    const float4* srow = reinterpret_cast<const float4*>(slot + C::O_KS) + krow * (D / 4);
+    const float4* zrow = reinterpret_cast<const float4*>(slot + C::O_KZ) + krow * (D / 4);
+    const float4* qrow = reinterpret_cast<const float4*>(qw + hq * C::QWS);
+
+    float acc[T::NT][4];
+#pragma unroll
+    for (int j = 0; j < T::NT; ++j)
+        acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+    float zacc = 0.0f;
+#pragma unroll
+    for (int s = 0; s < D / 16; ++s) {
+        const int cidx = 2 * tg + (s & 1) + 8 * (s >> 1);  // 16-byte chunk: channels 4 cidx .. 4 cidx + 3
+        const uint4 W = wrow[cidx];
+        const float4 S = srow[cidx];
+        const float4 Z = zrow[cidx];
+        const float4 Q = qrow[cidx];
+        zacc = fmaf(Q.x, Z.x, zacc);
+        zacc = fmaf(Q.y, Z.y, zacc);
+        zacc = fmaf(Q.z, Z.z, zacc);
+        zacc = fmaf(Q.w, Z.w, zacc);
+        uint32_t bh0, bl0, bh1, bl1;
+        if constexpr (T::HL) {
+            bh0 = split_part(Q.x * S.x, Q.y * S.y, part);
+            bh1 = split_part(Q.z * S.z, Q.w * S.w, part);
+        } else {
+            split_hi_lo(Q.x * S.x, Q.y * S.y, bh0, bl0);
+            split_hi_lo(Q.z * S.z, Q.w * S.w, bh1, bl1);
+        }
+#pragma unroll
+        for (int j = 0; j < T::NT; ++j) {
+            const uint32_t sa = ((uint32_t)T::ya(j) | ((uint32_t)(4 + T::ya(j)) << 8)) + soff;
+            const uint32_t sb = ((uint32_t)T::yb(j) | ((uint32_t)(4 + T::yb(j)) << 8)) + soff;
+            const uint32_t ma = half_pair_mask<BK>(T::pa(j)), mb = half_pair_mask<BK>(T::pb(j));
+            const uint32_t a0 = __byte_perm(W.x, W.y, sa) & ma;
+            const uint32_t a1 = __byte_perm(W.x, W.y, sb) & mb;
+            const uint32_t a2 = __byte_perm(W.z, W.w, sa) & ma;
+            const uint32_t a3 = __byte_perm(W.z, W.w, sb) & mb;
+            mma_f16(acc[j], a0, a1, a2, a3, bh0, bh1);
+            if constexpr (!T::HL)
+                mma_f16(acc[j], a0, a1, a2, a3, bl0, bl1);
+        }
+    }
+    zacc += __shfl_xor_sync(0xffffffffu, zacc, 1);
+    zacc += __shfl_xor_sync(0xffffffffu, zacc, 2);
+    const float zc0 = __shfl_sync(0xffffffffu, zacc, 8 * tg);
+    const float zc1 = __shfl_sync(0xffffffffu, zacc, 8 * tg + 4);
+    if (tok0 + wr * T::P >= n)
+        return;
+    const int tbase = tok0 + wr * T::P + 2 * v * T::NT;
+    if constexpr (T::HL) {
+        const int h = tg % NQB;
+        if (tg / NQB == gi_row) {
+            const float f = seln<NQB>(fac, h);
+            float* row = lg + h * C::LS;
+#pragma unroll
+            for (int j = 0; j < T::NT; ++j) {
+                const float s0 = f * fmaf(code_unscale_bits(T::pa(j)), acc[j][0] + acc[j][1], zc0);
+                const float s1 = f * fmaf(code_unscale_bits(T::pb(j)), acc[j][2] + acc[j][3], zc0);
+                *reinterpret_cast<float2*>(row + lg_phys(tbase + 2 * j)) = make_float2(s0, s1);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int u = 2 * tg + cc;
+            if (u / NQB != gi_row)
+                continue;
+            const int h = u % NQB;
+            const float f = seln<NQB>(fac, h);
+            const float zc = cc ? zc1 : zc0;
+            float* row = lg + h * C::LS;
+#pragma unroll
+            for (int j = 0; j < T::NT; ++j) {
+                const float s0 = f * fmaf(code_unscale_bits(T::pa(j)), acc[j][cc], zc);
+                const float s1 = f * fmaf(code_unscale_bits(T::pb(j)), acc[j][2 + cc], zc);
+                *reinterpret_cast<float2*>(row + lg_phys(tbase + 2 * j)) = make_float2(s0, s1);
+            }
+        }
+    }
+}
+
+// Online softmax over the n logits of the stage in lg: new maxima, the
+// state's rescaling (alpha for the sums, alpha * fv_new / fv for o), and
+// p = exp(s - m) written over the logits.  Whole warp; lg is published by the
+// caller's __syncwarp and published again here.
+template <class C, int NQB>
+__device__ __forceinline__ void softmax_stage(ConsumerState<C, NQB>& st, float* lg, int n, float fv_new)
+{
+    const int lane = threadIdx.x & 31;
+    float mt[NQB];
+#pragma unroll
+    for (int h = 0; h < NQB; ++h)
+        mt[h] = -INFINITY;
+#pragma unroll
+    for (int u = 0; u < (C::TS + 63) / 64; ++u) {
+        const int t = 2 * (lane + 32 * u);
+        if (t < n) {
+#pragma unroll
+            for (int h = 0; h < NQB; ++h) {
+                const float2 x = *reinterpret_cast<const float2*>(lg + h * C::LS + lg_phys(t));
+                mt[h] = fmaxf(mt[h], t + 1 < n ? fmaxf(x.x, x.y) : x.x);
+            }
+        }
+    }
+    float alpha[NQB];
+#pragma unroll
+    for (int h = 0; h < NQB; ++h) {
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1)
+            mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], k));
+        const float mn = fmaxf(st.m[h], mt[h]);
+        alpha[h] = ex2(st.m[h] - mn);  // 0 while the state is empty
+        st.m[h] = mn;
+        st.l[h] *= alpha[h];
+#pragma unroll
+        for (int g = 0; g < C::NGM; ++g)
+            st.z[h][g] *= alpha[h];
+#pragma unroll
+        for (int i = 0; i < C::CPL; ++i)
+            st.r[h][i] *= alpha[h];
+    }
+    // o is kept in units of 1 / fv: rescale to the new value weight scale
+    const float ratio = fv_new * __frcp_rn(st.fv);  // exact: powers of two
+    st.fv = fv_new;
+    const int tg = lane & 3;
+    const float ro0 = seln<NQB>(alpha, pv_col_head<C, NQB>(tg, 0)) * ratio;
+    const float ro1 = seln<NQB>(alpha, pv_col_head<C, NQB>(tg, 1)) * ratio;
+#pragma unroll
+    for (int sg = 0; sg < C::NSEG; ++sg)
+#pragma unroll
+        for (int j = 0; j < C::NTV; ++j) {
+            st.o[sg][j][0] *= ro0;
+            st.o[sg][j][1] *= ro1;
+            st.o[sg][j][2] *= ro0;
+            st.o[sg][j][3] *= ro1;
+        }
+#pragma unroll
+    for (int u = 0; u < (C::TS + 63) / 64; ++u) {
+        const int t = 2 * (lane + 32 * u);
+        if (t < n) {
+#pragma unroll
+            for (int h = 0; h < NQB; ++h) {
+                float2* px = reinterpret_cast<float2*>(lg + h * C::LS + lg_phys(t));
+                const float2 x = *px;
+                const float p0 = ex2(x.x - st.m[h]);
+                const float p1 = t + 1 < n ? ex2(x.y - st.m[h]) : 0.0f;
+                st.l[h] += p0 + p1;
+                *px = make_float2(p0, p1);
+            }
+        }
+    }
+    __syncwarp();
+}
+
+// Value weights of the stage's tokens [tb, tb + UB) below n: for unit
+// (group gg, head h) = gg NQB + h, ub[part][unit][t - tb] holds the hi
+// (part 0) and lo (part 1) fp16 terms of u = p_ht s_tg fv, and the lane's
+// zero terms gather p_ht z_tg.  Token pairs per lane.
+template <class C, int NQB, int NG>
+__device__ __forceinline__ void value_weights(ConsumerState<C, NQB>& st, const float* lg, const uint8_t* slot,
+                                              int tb, int n, float fv, uint16_t* ub)
+{
+    const int lane = threadIdx.x & 31;
+    const float* vs = reinterpret_cast<const float*>(slot + C::O_VS);
+    const float* vz = reinterpret_cast<const float*>(slot + C::O_VZ);
+    uint32_t* ub32 = reinterpret_cast<uint32_t*>(ub);
+#pragma unroll
+    for (int u = 0; u < (C::UB + 63) / 64; ++u) {
+        const int i = lane + 32 * u;  // pair within the batch
+        const int t = tb + 2 * i;
+        if (2 * i >= C::UB || t >= n)
+            continue;
+        float s0[NG], s1[NG], z0[NG], z1[NG];
+#pragma unroll
+        for (int gg = 0; gg < NG; ++gg) {
+            s0[gg] = vs[t * NG + gg] * fv;
+            s1[gg] = vs[(t + 1) * NG + gg] * fv;
+            z0[gg] = vz[t * NG + gg];
+            z1[gg] = vz[(t + 1) * NG + gg];
+        }
+#pragma unroll
+        for (int h = 0; h < NQB; ++h) {
+            const float2 p = *reinterpret_cast<const float2*>(lg + h * C::LS + lg_phys(t));
+#pragma unroll
+            for (int gg = 0; gg < NG; ++gg) {
+                st.z[h][gg] = fmaf(p.x, z0[gg], fmaf(p.y, z1[gg], st.z[h][gg]));
+                uint32_t hi, lo;
+                split_hi_lo(p.x * s0[gg], p.y * s1[gg], hi, lo);
+                const int unit = gg * NQB + h;
+                ub32[(unit * C::UTS) / 2 + i] = hi;
+                ub32[((C::UNITS + unit) * C::UTS) / 2 + i] = lo;
+            }
+        }
+    }
+}
+
+// p . V_hat of the 16-token slices k0 .. k1 of the stage (weights of the
+// batch at tb in ub), accumulated into st.o.
+template <int BV, int NQB, int D, class C>
+__device__ __forceinline__ void pv_slices(ConsumerState<C, NQB>& st, int lgG, const uint8_t* slot,
+                                          const uint16_t* ub, int tb, int k0, int k1)
+{
+    using VT = ValTile<BV>;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tg = lane & 3;
+    const int mi = lane >> 3, lrow = (lane & 7) + 8 * (mi & 1), lseg = C::SPL == 2 ? mi >> 1 : 0;
+    const uint32_t vbase = smem_addr(slot + C::O_VW) + (uint32_t)(lrow * C::DW * 4 + lseg * 16);
+    const uint32_t* ub32 = reinterpret_cast<const uint32_t*>(ub);
+    // B column of this lane: unit within a fragment and weight part
+    const int ucol = C::HLV ? g >> 1 : g, part = g & 1;
+#pragma unroll 2
+    for (int k = k0; k < k1; ++k) {
+        const int pi = (16 * k - tb) / 2 + tg;  // pair index of tokens 2 tg, 2 tg + 1 of the slice
+#pragma unroll
+        for (int sp = 0; sp < C::NSEG / C::SPL; ++sp) {
+            uint32_t R[4];
+            const uint32_t addr = vbase + (uint32_t)(16 * k * C::DW * 4 + sp * C::SPL * 16);
+            if constexpr (C::SPL == 2)
+                ldsm_x4_t(R, addr);
+            else
+                ldsm_x2_t(R, addr);
+#pragma unroll
+            for (int s2 = 0; s2 < C::SPL; ++s2) {
+                const int sg = sp * C::SPL + s2;
+                // first unit of the segment's fragment: its first group times NQB, rounded to a fragment
+                const int gfirst = (sg * VT::CS) >> lgG;
+                const int frag0 = (gfirst * NQB) / C::UF * C::UF;
+                const int unit = frag0 + ucol;
+                uint32_t b0, b1, c0 = 0, c1 = 0;
+                if constexpr (C::HLV) {
+                    const int row = (part * C::UNITS + unit) * C::UTS / 2;
+                    b0 = ub32[row + pi];
+                    b1 = ub32[row + pi + 4];
+                } else {
+                    const int rh = unit * C::UTS / 2, rl = (C::UNITS + unit) * C::UTS / 2;
+                    b0 = ub32[rh + pi];
+                    b1 = ub32[rh + pi + 4];
+                    c0 = ub32[rl + pi];
+                    c1 = ub32[rl + pi + 4];
+                }
+                const uint32_t Rl = R[2 * s2], Rh = R[2 * s2 + 1];
+                const uint32_t Rls = Rl >> VT::SHIFT, Rhs = Rh >> VT::SHIFT;
+#pragma unroll
+                for (int j = 0; j < VT::NT; ++j) {
+                    const int m0 = 2 * j, m1 = 2 * j + 1;
+                    const uint32_t mk0 = half_pair_mask<BV>(VT::bitpos(m0));
+                    const uint32_t mk1 = half_pair_mask<BV>(VT::bitpos(m1));
+                    const uint32_t x0 = (VT::shifted(m0) ? Rls : Rl) & mk0;
+                    const uint32_t x1 = (VT::shifted(m1) ? Rls : Rl) & mk1;
+                    const uint32_t x2 = (VT::shifted(m0) ? Rhs : Rh) & mk0;
+                    const uint32_t x3 = (VT::shifted(m1) ? Rhs : Rh) & mk1;
+                    mma_f16(st.o[sg][j], x0, x1, x2, x3, b0, b1);
+                    if constexpr (!C::HLV)
+                        mma_f16(st.o[sg][j], x0, x1, x2, x3, c0, c1);
+                }
+            }
+        }
+    }
+    (void)D;
+}
+
+// --------------------------------------------------------------- residual ---
+
+// q . K of a residual stage (n fp16 tokens, padded rows) on the tensor cores:
+// A = the keys (ldmatrix), B = the row's fp16 query (column h = head h),
+// logits sl2 q . k into lg (sl2 = sm_scale log2 e).
+template <int NQB, int D, class C>
+__device__ __forceinline__ void qk_residual_stage(const uint8_t* slot, int n, float sl2, float* lg)
+{
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tg = lane & 3;
+    const int mi = lane >> 3, lrow = (lane & 7) + 8 * (mi & 1), lch = mi >> 1;
+    const uint32_t kb = smem_addr(slot + C::O_KR) + (uint32_t)(lrow * C::RROW + lch * 16);
+    const uint16_t* qh = reinterpret_cast<const uint16_t*>(slot) + (g < NQB ? g : 0) * D;
+#pragma unroll 1
+    for (int mt = 0; mt < (n + 15) / 16; ++mt) {
+        float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+#pragma unroll 4
+        for (int ks = 0; ks < D / 16; ++ks) {
+            uint32_t A[4];
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(A[0]), "=r"(A[1]), "=r"(A[2]), "=r"(A[3])
+                         : "r"(kb + (uint32_t)(mt * 16 * C::RROW + ks * 32)));
+            const uint32_t b0 = *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 2 * tg);
+            const uint32_t b1 = *reinterpret_cast<const uint32_t*>(qh + 16 * ks + 8 + 2 * tg);
+            mma_f16(acc, A[0], A[1], A[2], A[3], b0, b1);
+        }
+        // rows g, g + 8 (tokens), columns 2 tg, 2 tg + 1 (heads)
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+            const int h = 2 * tg + cc;
+            if (h < NQB) {
+                const int t0 = 16 * mt + g, t1 = t0 + 8;
+                if (t0 < n)
+                    lg[h * C::LS + lg_phys(t0)] = sl2 * acc[cc];
+                if (t1 < n)
+                    lg[h * C::LS + lg_phys(t1)] = sl2 * acc[2 + cc];
+            }
+        }
+    }
+}
+
+// p . V of a residual stage in fp32: the lane's channels lane*CPL .. +CPL-1.
+template <int NQB, int D, class C>
+__device__ __forceinline__ void pv_residual_stage(ConsumerState<C, NQB>& st, const uint8_t* slot, int n,
+                                                  const float* lg)
+{
+    const int lane = threadIdx.x & 31;
+    const uint8_t* vr = slot + C::O_VR + lane * C::CPL * 2;
+#pragma unroll 2
+    for (int t = 0; t < n; ++t) {
+        uint16_t v[C::CPL];
+        if constexpr (C::CPL == 4) {
+            const uint2 x = *reinterpret_cast<const uint2*>(vr + t * C::RROW);
+            v[0] = (uint16_t)x.x;
+            v[1] = (uint16_t)(x.x >> 16);
+            v[2] = (uint16_t)x.y;
+            v[3] = (uint16_t)(x.y >> 16);
+        } else {
+#pragma unroll
+            for (int i = 0; i < C::CPL; ++i)
+                v[i] = reinterpret_cast<const uint16_t*>(vr + t * C::RROW)[i];
+        }
+#pragma unroll
+        for (int h = 0; h < NQB; ++h) {
+            const float p = lg[h * C::LS + lg_phys(t)];
+#pragma unroll
+            for (int i = 0; i < C::CPL; ++i)
+                st.r[h][i] = fmaf(p, __half2float(__ushort_as_half(v[i])), st.r[h][i]);
+        }
+    }
+}
+
+// ------------------------------------------------------------------ merge ---
+
+// Publishes the warp's state for the row segment in the merge area: o (the
+// MMA-layout sums times their code and value scales, plus the residual sums),
+// the zero terms per (head, group), m and the warp's l.
+template <int BV, int NQB, int D, class C>
+__device__ __forceinline__ void state_publish(const ConsumerState<C, NQB>& st, int lgG, int cw, float* mb)
+{
+    using VT = ValTile<BV>;
+    const int lane = threadIdx.x & 31;
+    const int g = lane >> 2, tg = lane & 3;
+    float* mo = mb + C::M_O + cw * NQB * D;
+    const float invfv = __frcp_rn(st.fv);
+    // each (head, channel) of the MMA layout is held by exactly one lane
+#pragma unroll
+    for (int sg = 0; sg < C::NSEG; ++sg) {
+        const int ch0 = sg * VT::CS + g * VT::HC;
+        const int grp = ch0 >> lgG;
+        const int gfirst = (sg * VT::CS) >> lgG;
+        const int frag0 = (gfirst * NQB) / C::UF * C::UF;
+#pragma unroll
+        for (int cc = 0; cc < (C::HLV ? 1 : 2); ++cc) {
+            const int unit = frag0 + (C::HLV ? tg : 2 * tg + cc);
+            if (unit / NQB != grp)
+                continue;
+            const int h = unit % NQB;
+#pragma unroll
+            for (int j = 0; j < VT::NT; ++j) {
+                const float f0 = code_unscale_bits(VT::bitpos(2 * j)) * invfv;
+                const float f1 = code_unscale_bits(VT::bitpos(2 * j + 1)) * invfv;
+                float a, b;
+                if constexpr (C::HLV) {
+                    a = st.o[sg][j][0] + st.o[sg][j][1];
+                    b = st.o[sg][j][2] + st.o[sg][j][3];
+                } else {
+                    a = st.o[sg][j][cc];
+                    b = st.o[sg][j][2 + cc];
+                }
+                mo[h * D + ch0 + 2 * j] = a * f0;
+                mo[h * D + ch0 + 2 * j + 1] = b * f1;
+            }
+        }
+    }
+    __syncwarp();
+#pragma unroll
+    for (int h = 0; h < NQB; ++h)
+#pragma unroll
+        for (int i = 0; i < C::CPL; ++i)
+            mo[h * D + lane * C::CPL + i] += st.r[h][i];
+    float* mz = mb + C::M_Z + cw * NQB * C::NGM;
+#pragma unroll
+    for (int h = 0; h < NQB; ++h) {
+        float l = st.l[h];
+#pragma unroll
+        for (int k = 16; k > 0; k >>= 1)
+            l += __shfl_xor_sync(0xffffffffu, l, k);
+#pragma unroll
+        for (int gg = 0; gg < C::NGM; ++gg) {
+            float z = st.z[h][gg];
+#pragma unroll
+            for (int k = 16; k > 0; k >>= 1)
+                z += __shfl_xor_sync(0xffffffffu, z, k);
+            if (lane == 0)
+                mz[h * C::NGM + gg] = z;
+        }
+        if (lane == 0) {
+            mb[C::M_M + cw * NQB + h] = st.m[h];
+            mb[C::M_L + cw * NQB + h] = l;
+        }
+    }
+}
+
+// ------------------------------------------------------- one quantized stage ---
+
+// Tokens [t0, t0 + n) of a quantized stage, by one consumer warp: weight
+// scales (keys from max|q| and the largest key scale, values from the largest
+// value scale, valid rows only), q . K_hat into the logit rows, the online
+// softmax, then the value weights and p . V_hat in batches of UB tokens.
+// FULL: n == TS, so that every loop bound and mask is a constant.
+template <int BK, int BV, int NQB, int D, class C, bool FULL>
+__device__ __forceinline__ void consume_quant(ConsumerState<C, NQB>& st, const uint8_t* sl, int t0, int n_rt,
+                                              int lgG, float sl2, float* lg, float* qw, uint16_t* ub)
+{
+    const int lane = threadIdx.x & 31;
+    const int n = FULL ? C::TS : n_rt;
+    const int NG = D >> lgG;
+    const int ngr = ((t0 + n - 1) >> lgG) - (t0 >> lgG) + 1;
+    const float smax_k = warp_max_stat(reinterpret_cast<const float*>(sl + C::O_KS), ngr * D);
+    const float smax_v = warp_max_stat(reinterpret_cast<const float*>(sl + C::O_VS), n * NG);
+    const uint16_t* qh = reinterpret_cast<const uint16_t*>(sl);
+    float fac[NQB];
+#pragma unroll
+    for (int hh = 0; hh < NQB; ++hh) {
+        if (st.qmax[hh] < 0.0f) {
+            float mx = 0.0f;
+#pragma unroll
+            for (int d = lane; d < D; d += 32)
+                mx = fmaxf(mx, fabsf(__half2float(__ushort_as_half(qh[hh * D + d]))));
+#pragma unroll
+            for (int kk = 16; kk > 0; kk >>= 1)
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, kk));
+            st.qmax[hh] = mx;
+        }
+        const float fk = weight_scale_pow2(st.qmax[hh] * smax_k);
+        fac[hh] = sl2 * __frcp_rn(fk);
+#pragma unroll
+        for (int d = lane; d < D; d += 32)
+            qw[hh * C::QWS + d] = __half2float(__ushort_as_half(qh[hh * D + d])) * fk;
+    }
+    __syncwarp();
+#pragma unroll 1
+    for (int tok0 = 0; tok0 < n; tok0 += C::TOK)
+        qk_warp_tile<BK, NQB, D, C>(lgG, t0, tok0, n, sl, qw, fac, lg);
+    __syncwarp();
+    softmax_stage<C, NQB>(st, lg, n, weight_scale_pow2(smax_v));
+#pragma unroll 1
+    for (int tb = 0; tb < n; tb += C::UB) {
+        switch (NG) {
+        case 1: value_weights<C, NQB, 1>(st, lg, sl, tb, n, st.fv, ub); break;
+        case 2: value_weights<C, NQB, 2>(st, lg, sl, tb, n, st.fv, ub); break;
+        case 4: value_weights<C, NQB, cmin(4, C::NGM)>(st, lg, sl, tb, n, st.fv, ub); break;
+        default: value_weights<C, NQB, C::NGM>(st, lg, sl, tb, n, st.fv, ub); break;
+        }
+        __syncwarp();
+        pv_slices<BV, NQB, D, C>(st, lgG, sl, ub, tb, tb / 16, min(n, tb + C::UB) / 16);
+        __syncwarp();
+    }
+}
+
+// ---------------------------------------------------------------- kernel ---
+
+template <int BK, int BV, int NQB, int D, int NC>
+__global__ void __launch_bounds__(32 * (NC + 1), 1)
+decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_scale,
+                     float* __restrict__ out, float* __restrict__ ws, int ns)
+{
+    using C = StreamCfg<BK, BV, NQB, D, NC>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ long long red[C::THREADS / 32];
+    __shared__ RangeStart sh_range[2];
+    __shared__ int abort_flag;
+
+    // the combine kernel may start once every CTA is running; it waits for
+    // this grid's results in griddepcontrol.wait
+    asm volatile("griddepcontrol.launch_dependents;");
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NQ = Hq / c.H, NP = NQ / NQB, RB = c.H * NP;
+    const float sl2 = sm_scale * 1.44269504088896341f;  // logits in log2 units
+    const int lgG = ilog2(c.G);
+    uint8_t* slots = smem;
+    float* wscr = reinterpret_cast<float*>(smem + (size_t)ns * C::SLOT);
+    float* mbuf = wscr + NC * C::WARP_FLOATS;
+    uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + C::M_END);
+    uint64_t* empty = full + ns;
+    int* wsi = reinterpret_cast<int*>(ws);
+
+    RangeStart r0, r1;
+    locate_range<C::THREADS>(c, RB, C::TS, C::RT, blockIdx.x, gridDim.x, r0, r1, red, sh_range);
+    if (threadIdx.x == 0) {
+        int* rec = wsi + kStreamHeaderFloats + blockIdx.x * kStreamLocInts;
+        rec[0] = (int)(r0.g & 0xffffffff);
+        rec[1] = (int)(r0.g >> 32);
+        rec[2] = r0.b;
+        rec[3] = r0.rr;
+        rec[4] = r0.j;
+        if (blockIdx.x == gridDim.x - 1) {
+            int* e = rec + kStreamLocInts;
+            e[0] = (int)(r1.g & 0xffffffff);
+            e[1] = (int)(r1.g >> 32);
+            e[2] = r1.b;
+            e[3] = r1.rr;
+            e[4] = r1.j;
+        }
+        for (int s = 0; s < ns; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_fence_init();
+        abort_flag = 0;
+        if (blockIdx.x == 0)
+            wsi[0] = KIVI_OK;  // status word: KIVI_ETIMEOUT if a bounded wait gives up
+    }
+    __syncthreads();
+    const long long ntiles = r1.g - r0.g;
+    if (ntiles <= 0)
+        return;
+    Walk w0{r0.b, r0.rr, r0.j, 0, 0, 0, 0};
+    walk_load(w0, c, C::TS, C::RT);
+
+    if (warp == NC) {
+        // ------------------------------------------------------ producer
+        // lane 0 issues every copy: a handful of large bulk copies per stage
+        if (lane != 0)
+            return;
+        Walk w = w0;
+        int slot = 0;
+        uint32_t round = 0;
+        long long issued = 0;
+        for (long long k = 0; k < ntiles; ++k) {
+            if (k >= ns && !mbar_wait_bounded(&empty[slot], (round & 1u) ^ 1u, &abort_flag)) {
+                atomicExch(&abort_flag, 1);
+                atomicExch(wsi, KIVI_ETIMEOUT);
+                break;
+            }
+            const int h = w.rr / NP, pass = w.rr - h * NP;
+            const size_t bh = (size_t)w.b * c.H + h;
+            const int hq0 = h * NQ + pass * NQB;
+            const int t0 = walk_t0(w, C::TS, C::RT), n = walk_n(w, C::TS, C::RT);
+            uint8_t* sl = slots + (size_t)slot * C::SLOT;
+            uint64_t* bar = &full[slot];
+            const uint16_t* qsrc = q + ((size_t)w.b * Hq + hq0) * D;
+            if (walk_quant(w)) {
+                const int nw = n / C::PK;
+                const int g0 = t0 >> lgG, ngr = ((t0 + n - 1) >> lgG) - g0 + 1;
+                const int NG = D >> lgG;
+                const size_t so = (bh * (size_t)(c.Tmax >> lgG) + g0) * D;
+                const size_t vo = bh * (size_t)c.Tmax + t0;
+                mbar_arrive_tx(bar, C::QB + nw * D * 4 + 2 * ngr * D * 4 + n * C::DW * 4 + 2 * n * NG * 4);
+                bulk_g2s(sl, qsrc, C::QB, bar);
+                bulk_g2s(sl + C::O_KW, c.kq + (bh * (size_t)(c.Tmax / C::PK) + t0 / C::PK) * D, nw * D * 4, bar);
+                bulk_g2s(sl + C::O_KS, c.kscale + so, ngr * D * 4, bar);
+                bulk_g2s(sl + C::O_KZ, c.kzero + so, ngr * D * 4, bar);
+                bulk_g2s(sl + C::O_VW, c.vq + vo * C::DW, n * C::DW * 4, bar);
+                bulk_g2s(sl + C::O_VS, c.vscale + vo * NG, n * NG * 4, bar);
+                bulk_g2s(sl + C::O_VZ, c.vzero + vo * NG, n * NG * 4, bar);
+            } else {
+                // ring slots of tokens t0 .. t0+n-1: contiguous up to the ring's end
+                const int RG = c.R + c.G;
+                const int s0 = t0 % RG, n1 = min(n, RG - s0);
+                const size_t ring = bh * RG * D;
+                mbar_arrive_tx(bar, C::QB + 2 * n * D * 2);
+                bulk_g2s(sl, qsrc, C::QB, bar);
+                bulk_g2s(sl + C::O_KR, c.kres + ring + (size_t)s0 * D, n1 * D * 2, bar);
+                bulk_g2s(sl + C::O_VR, c.vres + ring + (size_t)s0 * D, n1 * D * 2, bar);
+                if (n1 < n) {
+                    bulk_g2s(sl + C::O_KR + n1 * C::RROW, c.kres + ring, (n - n1) * D * 2, bar);
+                    bulk_g2s(sl + C::O_VR + n1 * C::RROW, c.vres + ring, (n - n1) * D * 2, bar);
+                }
+            }
+            ++issued;
+            walk_next(w, c, RB, C::TS, C::RT);
+            if (++slot == ns) {
+                slot = 0;
+                ++round;
+            }
+        }
+        // leave only once the copies issued have landed (the consumers
+        // normally wait for every one of them already)
+        if (*(volatile int*)&abort_flag) {
+            const volatile int never = 0;
+            for (long long k = issued - 1; k >= 0 && k >= issued - ns; --k)
+                (void)mbar_wait_bounded(&full[(int)(k % ns)], (uint32_t)((k / ns) & 1), &never);
+        }
+        return;
+    }
+
+    // ------------------------------------------------------------ consumer
+    using CS = ConsumerState<C, NQB>;
+    CS st;
+    state_reset<C, NQB>(st);
+    float* lg = wscr + warp * C::WARP_FLOATS + C::W_LG;
+    float* qw = wscr + warp * C::WARP_FLOATS + C::W_QW;
+    uint16_t* ub = reinterpret_cast<uint16_t*>(wscr + warp * C::WARP_FLOATS + C::W_UB);
+    Walk w = w0;
+    int slot = 0;
+    uint32_t round = 0;
+    int mine = 0;           // k mod NC
+    bool first_seg = true;  // the CTA's first row segment
+    int seg_j0 = w.j;       // first tile of the current segment in its row
+    for (long long k = 0; k < ntiles; ++k) {
+        const int h = w.rr / NP, pass = w.rr - h * NP;
+        const int hq0 = h * NQ + pass * NQB;
+        const bool aborted = __shfl_sync(0xffffffffu, *(volatile int*)&abort_flag, 0) != 0;
+        if (mine == warp && !aborted) {
+            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], round & 1u, &abort_flag));
+            if (!ok && lane == 0) {
+                atomicExch(&abort_flag, 1);
+                atomicExch(wsi, KIVI_ETIMEOUT);
+            }
+            if (ok) {
+                const uint8_t* sl = slots + (size_t)slot * C::SLOT;
+                const int t0 = walk_t0(w, C::TS, C::RT), n = walk_n(w, C::TS, C::RT);
+                if (walk_quant(w)) {
+                    if (n == C::TS)
+                        consume_quant<BK, BV, NQB, D, C, true>(st, sl, t0, n, lgG, sl2, lg, qw, ub);
+                    else
+                        consume_quant<BK, BV, NQB, D, C, false>(st, sl, t0, n, lgG, sl2, lg, qw, ub);
+                } else {
+                    qk_residual_stage<NQB, D, C>(sl, n, sl2, lg);
+                    __syncwarp();
+                    softmax_stage<C, NQB>(st, lg, n, st.fv);
+                    pv_residual_stage<NQB, D, C>(st, sl, n, lg);
+                    __syncwarp();
+                }
+                if (lane == 0)
+                    mbar_arrive(&empty[slot]);
+            }
+        }
+        const bool seg_end = (w.j == w.nt - 1) || (k == ntiles - 1);
+        if (seg_end) {
+            // ---------------------------------------------- row segment merge
+            state_publish<BV, NQB, D, C>(st, lgG, warp, mbuf);
+            named_bar(1, 32 * NC);
+            const bool whole = seg_j0 == 0 && w.j == w.nt - 1;
+            float* dst_o;
+            float* dst_ml = nullptr;
+            if (whole) {
+                dst_o = out + ((size_t)w.b * Hq + hq0) * D;
+            } else {
+                const int slot_id = first_seg ? 0 : 1;
+                dst_o = ws + kStreamHeaderFloats + (size_t)(gridDim.x + 1) * kStreamLocInts +
+                        ((size_t)blockIdx.x * 2 + slot_id) * NQB * (D + 2);
+                dst_ml = dst_o + NQB * D;
+            }
+            for (int idx = threadIdx.x; idx < NQB * D; idx += 32 * NC) {
+                const int hh = idx / D, d = idx - hh * D;
+                float M = -INFINITY;
+#pragma unroll
+                for (int cw = 0; cw < NC; ++cw)
+                    M = fmaxf(M, mbuf[C::M_M + cw * NQB + hh]);
+                float o = 0.0f, L = 0.0f;
+                const int gg = d >> lgG;
+#pragma unroll
+                for (int cw = 0; cw < NC; ++cw) {
+                    const float mw = mbuf[C::M_M + cw * NQB + hh];
+                    const float e = mw > -INFINITY ? ex2(mw - M) : 0.0f;
+                    o = fmaf(e, mbuf[C::M_O + (cw * NQB + hh) * D + d] +
+                                    mbuf[C::M_Z + (cw * NQB + hh) * C::NGM + gg], o);
+                    L = fmaf(e, mbuf[C::M_L + cw * NQB + hh], L);
+                }
+                if (whole) {
+                    dst_o[hh * D + d] = o / L;
+                } else {
+                    dst_o[hh * D + d] = o;
+                    if (d == 0) {
+                        dst_ml[hh] = M;
+                        dst_ml[NQB + hh] = L;
+                    }
+                }
+            }
+            named_bar(1, 32 * NC);
+            state_reset<C, NQB>(st);
+            first_seg = false;
+        }
+        walk_next(w, c, RB, C::TS, C::RT);
+        if (seg_end)
+            seg_j0 = w.j;
+        if (++slot == ns) {
+            slot = 0;
+            ++round;
+        }
+        if (++mine == NC)
+            mine = 0;
+    }
+}
+
+// --------------------------------------------------------------- combine ---
+
+// Merges the partials of the rows that CTA ranges cut: CTA i of this grid
+// takes the row in which range i ends, if range i is not empty, ends inside
+// a row, and holds that row's first tile; the ranges after it that start
+// inside the row hold its other pieces (their first row segment, slot 0).
+// Also writes zero outputs for sequences of length 0.
+template <int NQB, int D>
+__global__ void __launch_bounds__(128)
+decode_stream_combine_kernel(const int32_t* __restrict__ len, int B, int Hq, int H, int NP,
+                             const float* __restrict__ ws, float* __restrict__ out)
+{
+    const int N = gridDim.x, i = blockIdx.x;
+    const int NQ = Hq / H;
+    // zero rows of empty sequences (len is not written by the decode kernel)
+    for (int b = i; b < B; b += N)
+        if (len[b] == 0)
+            for (int x = threadIdx.x; x < Hq * D; x += blockDim.x)
+                out[(size_t)b * Hq * D + x] = 0.0f;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int* rec = reinterpret_cast<const int*>(ws) + kStreamHeaderFloats;
+    auto gidx = [&](int k) {
+        return (long long)(unsigned)rec[k * kStreamLocInts] | ((long long)rec[k * kStreamLocInts + 1] << 32);
+    };
+    const long long g0 = gidx(i), g1 = gidx(i + 1);
+    const int* nx = rec + (i + 1) * kStreamLocInts;  // where range i ends
+    if (g1 <= g0 || nx[4] == 0 || nx[2] >= B)
+        return;
+    const int b = nx[2], rr = nx[3], jn = nx[4];
+    const long long row_first = g1 - jn;
+    if (row_first < g0)
+        return;  // an earlier range holds the row's first tile
+    const float* part = ws + kStreamHeaderFloats + (size_t)(N + 1) * kStreamLocInts;
+    const size_t pstride = (size_t)NQB * (D + 2);
+    const int h = rr / NP, pass = rr - h * NP;
+    const int hq0 = h * NQ + pass * NQB;
+    float* dst = out + ((size_t)b * Hq + hq0) * D;
+    __shared__ int s_last;
+    if (threadIdx.x == 0) {
+        // ranges that start inside the row (their record points into it at j > 0)
+        int k = i + 1;
+        while (k < N) {
+            const int* rk = rec + k * kStreamLocInts;
+            if (!(rk[2] == b && rk[3] == rr && rk[4] > 0))
+                break;
+            ++k;
+        }
+        s_last = k - 1;
+    }
+    __syncthreads();
+    const int last = s_last;
+    const int slot_i = row_first == g0 ? 0 : 1;
+    for (int idx = threadIdx.x; idx < NQB * D; idx += blockDim.x) {
+        const int hh = idx / D;
+        float M = -INFINITY;
+        for (int k = i; k <= last; ++k) {
+            if (k > i && gidx(k + 1) <= gidx(k))
+                continue;  // an empty range holds no piece
+            const float* p = part + ((size_t)k * 2 + (k == i ? slot_i : 0)) * pstride;
+            M = fmaxf(M, p[NQB * D + hh]);
+        }
+        float o = 0.0f, L = 0.0f;
+        for (int k = i; k <= last; ++k) {
+            if (k > i && gidx(k + 1) <= gidx(k))
+                continue;
+            const float* p = part + ((size_t)k * 2 + (k == i ? slot_i : 0)) * pstride;
+            const float m = p[NQB * D + hh];
+            const float e = m > -INFINITY ? ex2(m - M) : 0.0f;
+            o = fmaf(e, p[idx], o);
+            L = fmaf(e, p[NQB * D + NQB + hh], L);
+        }
+        dst[idx] = o / L;
+    }
+}
+
+// ---------------------------------------------------------------- launch ---
+
+template <int D, int BK, int BV, int NQB, int NC>
+cudaError_t stream_launch(const kivi_cache& c, const uint16_t* q, int Hq, float sm, float* out, float* ws,
+                          cudaStream_t s)
+{
+    using C = StreamCfg<BK, BV, NQB, D, NC>;
+    auto kern = decode_stream_kernel<BK, BV, NQB, D, NC>;
+    constexpr int ns = stream_stages<C>();
+    static_assert(ns >= 2, "the shared memory holds at least two stages");
+    const size_t smem = (size_t)ns * C::SLOT + C::FIXED_BYTES - 256 + 2 * (size_t)ns * 8;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    const int N = cmin(sm_count(), kMaxStreamCTAs);
+    kern<<<N, C::THREADS, smem, s>>>(c, q, Hq, sm, out, ws, ns);
+    e = cudaGetLastError();
+    if (e != cudaSuccess)
+        return e;
+    const int NP = (Hq / c.H) / NQB;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(N);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, decode_stream_combine_kernel<NQB, D>, (const int32_t*)c.len, c.B, Hq, c.H, NP,
+                           (const float*)ws, out);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        decode_stream_combine_kernel<NQB, D><<<N, 128, 0, s>>>(c.len, c.B, Hq, c.H, NP, ws, out);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace kivi
+
+namespace kivi {
+
+
+
+// Dispatch of the key and value widths and the query heads per pass for head
+// dimension D.
+template <int D, int BK, int BV>
+cudaError_t stream_launch_nq(const kivi_cache& c, const uint16_t* q, int Hq, float sm, float* out, float* ws,
+                             cudaStream_t s)
+{
+    switch (heads_per_pass(Hq / c.H)) {
+    case 4: return stream_launch<D, BK, BV, 4, stream_consumers<BK, BV, 4, D>()>(c, q, Hq, sm, out, ws, s);
+    case 2: return stream_launch<D, BK, BV, 2, stream_consumers<BK, BV, 2, D>()>(c, q, Hq, sm, out, ws, s);
+    default: return stream_launch<D, BK, BV, 1, stream_consumers<BK, BV, 1, D>()>(c, q, Hq, sm, out, ws, s);
+    }
+}
+
+template <int D, int BK>
+cudaError_t stream_launch_bv(const kivi_cache& c, const uint16_t* q, int Hq, float sm, float* out, float* ws,
+                             cudaStream_t s)
+{
+    switch (c.bits_v) {
+    case 2: return stream_launch_nq<D, BK, 2>(c, q, Hq, sm, out, ws, s);
+    case 4: return stream_launch_nq<D, BK, 4>(c, q, Hq, sm, out, ws, s);
+    default: return stream_launch_nq<D, BK, 8>(c, q, Hq, sm, out, ws, s);
+    }
+}
+
+template <int D, int BK>
+cudaError_t launch_decode_stream(const kivi_cache& c, const uint16_t* q, int Hq, float sm, float* out, float* ws,
+                                 cudaStream_t s)
+{
+    return stream_launch_bv<D, BK>(c, q, Hq, sm, out, ws, s);
+}
+
+// Instantiates the streamed decode for one head dimension and key width (one
+// translation unit each, so that they compile in parallel).
+#define KIVI_STREAM_INSTANTIATE(DIM, BK)                                                                      \
+    template cudaError_t launch_decode_stream<DIM, BK>(const kivi_cache&, const uint16_t*, int, float, float*, \
+                                                       float*, cudaStream_t);
+
+}  // namespace kivi

@@ -1,0 +1,7 @@
+// decode_stream_d64_k4.cu -- the streamed fused decode attention for head
+// dimension 64 and 4-bit keys (every value width, 1, 2 or 4 query heads per pass).
+#include "decode_stream.cuh"
+
+namespace kivi {
+KIVI_STREAM_INSTANTIATE(64, 4)
+}  // namespace kivi

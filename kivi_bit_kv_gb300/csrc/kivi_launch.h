@@ -30,11 +30,13 @@ cudaError_t launch_decode_pv(const kivi_cache& c, const float* logits, int ld_lo
                              float* out, float* ws_o, float* ws_m, float* ws_l,
                              cudaStream_t s);
 
-// q . K, softmax and p . V in one kernel per (KV head, chunk) plus the combine
-// kernel; requires c.bits_k == c.bits_v.  Workspace as for launch_decode_pv.
+// q . K, softmax and p . V in one persistent pipelined kernel (one CTA per
+// SM) plus a combine kernel for rows that CTA ranges cut; any bits_k, bits_v.
+// ws: stream_ws_bytes(c, Hq) bytes.
 cudaError_t launch_decode_attention(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale,
-                                    float* out, float* ws_o, float* ws_m, float* ws_l,
-                                    cudaStream_t s);
+                                    float* out, float* ws, cudaStream_t s);
+// Workspace bytes of launch_decode_attention (grid bounded by kMaxStreamCTAs).
+size_t stream_ws_bytes(const kivi_cache& c, int Hq);
 
 // The decode kernels of one head dimension D (64, 128, 256), without the
 // combine step; instantiated in decode_d<D>.cu.
@@ -44,9 +46,12 @@ cudaError_t launch_decode_qk_d(const kivi_cache& c, const uint16_t* q, int Hq, f
 template <int D>
 cudaError_t launch_decode_pv_d(const kivi_cache& c, const float* logits, int ld_logits, int Hq, float* ws_o,
                                float* ws_m, float* ws_l, cudaStream_t s);
-template <int D>
-cudaError_t launch_decode_attention_d(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale,
-                                      float* ws_o, float* ws_m, float* ws_l, cudaStream_t s);
+// The streamed fused decode of one head dimension D and key width BK (all
+// value widths and query heads per pass), instantiated in
+// decode_stream_d<D>_k<BK>.cu.
+template <int D, int BK>
+cudaError_t launch_decode_stream(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale, float* out,
+                                 float* ws, cudaStream_t s);
 
 // Compact payload (include/kivi.h): its size for host lengths lens[B], and
 // the export / import kernels (header checks and size limits on the device).

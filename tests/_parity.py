@@ -40,8 +40,8 @@ def gpu_encode(cache: KiviCache, K: torch.Tensor, V: torch.Tensor, seq_lens=None
 
 
 def gpu_decode(cache: KiviCache, q: torch.Tensor, sm_scale=None):
-    """Two-kernel decode (logits, out) and, when bits_k == bits_v, the fused
-    kivi_decode_attention output (else None)."""
+    """Two-kernel decode (logits, out) and the fused kivi_decode_attention
+    output."""
     B, Hq, D = q.shape
     ld = roundup(cache.Tmax, 4)
     logits = torch.zeros((B, Hq, ld), dtype=torch.float32, device=cache.device)
@@ -50,12 +50,10 @@ def gpu_decode(cache: KiviCache, q: torch.Tensor, sm_scale=None):
     qd = q.to(cache.device)
     abi.kivi_decode_qk(cache, qd, logits, sm_scale)
     abi.kivi_decode_pv(cache, logits, out, ws)
-    fused = None
-    if cache.bits_k == cache.bits_v:
-        fused = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=cache.device)
-        abi.kivi_decode_attention(cache, qd, fused, cache.workspace(Hq), sm_scale)
+    fused = torch.full((B, Hq, D), float("nan"), dtype=torch.float32, device=cache.device)
+    abi.kivi_decode_attention(cache, qd, fused, cache.workspace(Hq), sm_scale)
     torch.cuda.synchronize(cache.device)
-    return logits.cpu().numpy(), out.cpu().numpy(), None if fused is None else fused.cpu().numpy()
+    return logits.cpu().numpy(), out.cpu().numpy(), fused.cpu().numpy()
 
 
 def state(cache: KiviCache, rows=None) -> dict:
