@@ -65,7 +65,7 @@ extern "C" {
 #define KIVI_EINVAL     1 /* bad descriptor, shape, pointer or alignment       */
 #define KIVI_ECAPACITY  2 /* a sequence would exceed Tmax tokens (device flag) */
 #define KIVI_ECUDA      3 /* the CUDA launch reported an error                  */
-#define KIVI_ETIMEOUT   4 /* reserved: a bounded device wait gave up            */
+#define KIVI_ETIMEOUT   4 /* a bounded device wait gave up (workspace status)  */
 #define KIVI_EWORKSPACE 5 /* workspace smaller than kivi_workspace_bytes()      */
 
 /*
@@ -221,16 +221,20 @@ int32_t kivi_decode_pv(const kivi_cache* c, const float* logits,
 
 /*
  * Decode attention in one pass over the cache: the logits of kivi_decode_qk,
- * the softmax and the weighted sum of kivi_decode_pv, fused per (KV head,
- * chunk of up to 1024 tokens) so that the logits stay on chip:
+ * the softmax and the weighted sum of kivi_decode_pv, fused so that the
+ * logits stay on chip:
  *   out[b][hq][d] = sum_t softmax_t(sm_scale q . K_hat_t) V_hat[t][d]
  * over t < len[b] (the decode-time consumer: CacheForge README, "How it
- * works" and "Example", as for kivi_decode_qk).  q: fp16
- * [B][Hq][D]; out: fp32 [B][Hq][D]; ws as for kivi_decode_pv (>=
- * kivi_workspace_bytes(c, Hq) bytes, 16-byte aligned).  Requires
- * bits_k == bits_v (KIVI_EINVAL otherwise: use kivi_decode_qk followed by
- * kivi_decode_pv).  A sequence with len[b] == 0 gets out = 0.  Two kernels on
- * `stream`.
+ * works" and "Example", as for kivi_decode_qk).  Any bits_k, bits_v.
+ * q: fp16 [B][Hq][D]; out: fp32 [B][Hq][D]; ws: device, >=
+ * kivi_workspace_bytes(c, Hq) bytes, 16-byte aligned, contents need not be
+ * initialized.  One persistent kernel (one CTA per SM, each taking a
+ * contiguous share of all rows' tiles) and a combine kernel for the rows that
+ * two CTAs share: two kernels on `stream`.  A sequence with len[b] == 0 gets
+ * out = 0.  The first 4 bytes of ws receive a status word: KIVI_OK, or
+ * KIVI_ETIMEOUT if a bounded wait inside the kernel gave up (after two
+ * seconds; the outputs are then invalid).  Calls that share a workspace must
+ * not overlap on the GPU.
  */
 int32_t kivi_decode_attention(const kivi_cache* c, const uint16_t* q,
                               int32_t Hq, float sm_scale, float* out,
