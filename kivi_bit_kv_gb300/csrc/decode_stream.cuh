@@ -139,8 +139,10 @@ __host__ __device__ constexpr int pow2floor(int x) { return x <= 1 ? 1 : 2 * pow
 __host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / m * m; }
 
 constexpr int kMaxStreamCTAs = 1024;          // workspace sizing bound on the grid
+constexpr int kStreamStaticSmem = 512;        // room left for the kernel's static shared arrays
 constexpr int kStreamLocInts = 8;             // ints per CTA range record in the workspace
 constexpr int kStreamHeaderFloats = 4;        // workspace header (status word)
+constexpr int kStreamMaxStages = 32;          // stages of the ring (the consumed counters are static)
 
 // Compile-time shape of the streamed decode for key / value widths BK / BV,
 // NQB query heads per pass, head dimension D and NC consumer warps.  Sizes
@@ -164,10 +166,9 @@ struct StreamCfg {
     static constexpr int TS = cmax(cmax(TOK, 32), pow2floor(16384 / BPT));
     static constexpr int RT = cmax(16, cmin(64, pow2floor(TS * BPT / (4 * D))));
     // stage slot (bytes from the slot start, each region 16-byte aligned)
-    static constexpr int QB = NQB * D * 2;             // the row's query heads, fp16
     static constexpr int KROW = D * 4;                 // key word-row
     static constexpr int KSR = cmax(1, TS / 32);       // key statistic rows
-    static constexpr int O_KW = round_up(QB, 128);
+    static constexpr int O_KW = 0;
     static constexpr int O_KS = O_KW + (TS / PK) * KROW;
     static constexpr int O_KZ = O_KS + KSR * D * 4;
     static constexpr int O_VW = O_KZ + KSR * D * 4;
@@ -181,7 +182,8 @@ struct StreamCfg {
     static constexpr int SLOT = round_up(cmax(Q_END, R_END), 128);
     // per-consumer scratch (floats): logits / probabilities [NQB][LS]
     // (two floats of padding per 16 tokens), the scaled query [NQB][QWS],
-    // the value weights [2 parts][UNITS][UTS] fp16 for UB tokens at a time
+    // the value weights [2 parts][UNITS][UTS] fp16 for UB tokens at a time,
+    // the row's query heads [NQB][D] fp16
     static constexpr int LS = TS + TS / 8;
     static constexpr int QWS = D + 4;
     static constexpr int UNITS = NGM * NQB;            // value weight units (group, head)
@@ -192,14 +194,18 @@ struct StreamCfg {
     static constexpr int W_LG = 0;
     static constexpr int W_QW = W_LG + NQB * LS;
     static constexpr int W_UB = W_QW + NQB * QWS;
-    static constexpr int WARP_FLOATS = round_up(W_UB + UNITS * UTS, 4);
-    // merge area (floats): o [NC][NQB][D], m, l [NC][NQB], z [NC][NQB][NGM]
+    static constexpr int W_Q = round_up(W_UB + UNITS * UTS, 4);  // the row's query heads, fp16
+    static constexpr int QPIECES = NQB * D / 8;                  // 16-byte pieces of them
+    static constexpr int WARP_FLOATS = W_Q + NQB * D / 2;
+    // merge buffer (floats): o [NC][NQB][D], m, l [NC][NQB], z [NC][NQB][NGM];
+    // NMB of them, used by row segments in turn
     static constexpr int M_O = 0;
     static constexpr int M_M = M_O + NC * NQB * D;
     static constexpr int M_L = M_M + NC * NQB;
     static constexpr int M_Z = M_L + NC * NQB;
     static constexpr int M_END = round_up(M_Z + NC * NQB * NGM, 4);
-    static constexpr int FIXED_BYTES = 4 * (NC * WARP_FLOATS + M_END) + 256;
+    static constexpr int NMB = NC * NQB * D <= 2048 ? 4 : 2;
+    static constexpr int FIXED_BYTES = 4 * (NC * WARP_FLOATS + NMB * M_END) + kStreamStaticSmem;
     static constexpr int THREADS = 32 * (NC + 1);
     static_assert(TS % TOK == 0 && TS % 16 == 0 && RT % 16 == 0 && RT <= TS, "tile shape");
     static_assert(UB % 16 == 0 && TS % UB == 0, "weight batches");
@@ -211,7 +217,7 @@ constexpr int kStreamSmemBytes = 227 * 1024;  // dynamic + static shared memory 
 template <class C>
 __host__ __device__ constexpr int stream_stages()
 {
-    return (kStreamSmemBytes - C::FIXED_BYTES) / (C::SLOT + 16);
+    return cmin((kStreamSmemBytes - C::FIXED_BYTES) / (C::SLOT + 16), kStreamMaxStages);
 }
 
 // Consumer warps of the streamed decode for a shape: up to seven (eight warps
@@ -268,6 +274,27 @@ __device__ __forceinline__ void walk_next(Walk& w, const kivi_cache& c, int RB, 
         if (w.nt > 0)
             return;
     }
+}
+
+// Advances the walker by n tiles; returns the number of rows it left (each
+// starts a new row segment).  Stops at the end of the sequences.
+__device__ __forceinline__ int walk_skip(Walk& w, const kivi_cache& c, int RB, int TS, int RT, int n)
+{
+    int crossed = 0;
+    w.j += n;
+    while (w.j >= w.nt && w.b < c.B) {
+        w.j -= w.nt;
+        ++crossed;
+        if (++w.rr < RB)
+            continue;
+        w.rr = 0;
+        for (++w.b; w.b < c.B; ++w.b) {
+            walk_load(w, c, TS, RT);
+            if (w.nt > 0)
+                break;
+        }
+    }
+    return crossed;
 }
 
 // Tokens of the current tile: [t0, t0 + n), quantized or residual.
@@ -422,6 +449,22 @@ __device__ __forceinline__ int pv_col_head(int tg, int cc)
 
 // ----------------------------------------------------------- quantized ---
 
+// Warp maximum of non-negative floats: their bit patterns order like
+// unsigned integers, so one integer reduction gives it.
+__device__ __forceinline__ float warp_max_nonneg(float x)
+{
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(x)));
+}
+// Warp maximum of any floats (NaN excluded): a monotone map to signed
+// integers, one integer reduction, and the map back.
+__device__ __forceinline__ float warp_max(float x)
+{
+    const int b = __float_as_int(x);
+    const int key = b >= 0 ? b : b ^ 0x7fffffff;
+    const int m = __reduce_max_sync(0xffffffffu, key);
+    return __int_as_float(m >= 0 ? m : m ^ 0x7fffffff);
+}
+
 // Largest statistic of the first n floats at p (a multiple of 4), per warp.
 __device__ __forceinline__ float warp_max_stat(const float* p, int n)
 {
@@ -431,10 +474,7 @@ __device__ __forceinline__ float warp_max_stat(const float* p, int n)
         const float4 v = *reinterpret_cast<const float4*>(p + i);
         mx = fmaxf(fmaxf(mx, v.x), fmaxf(fmaxf(v.y, v.z), v.w));
     }
-#pragma unroll
-    for (int k = 16; k > 0; k >>= 1)
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, k));
-    return mx;
+    return warp_max_nonneg(mx);
 }
 
 // q . K_hat of one key warp tile (tokens tok0 .. tok0 + TOK of the stage,
@@ -466,7 +506,9 @@ __device__ __forceinline__ void qk_warp_tile(int lgG, int t0, int tok0, int n, c
     for (int j = 0; j < T::NT; ++j)
         acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
     float zacc = 0.0f;
-#pragma unroll
+    // two channel blocks per iteration: a fully unrolled loop overflows the
+    // instruction cache next to the other phases
+#pragma unroll 2
     for (int s = 0; s < D / 16; ++s) {
         const int cidx = 2 * tg + (s & 1) + 8 * (s >> 1);  // 16-byte chunk: channels 4 cidx .. 4 cidx + 3
         const uint4 W = wrow[cidx];
@@ -564,9 +606,7 @@ __device__ __forceinline__ void softmax_stage(ConsumerState<C, NQB>& st, float* 
     float alpha[NQB];
 #pragma unroll
     for (int h = 0; h < NQB; ++h) {
-#pragma unroll
-        for (int k = 16; k > 0; k >>= 1)
-            mt[h] = fmaxf(mt[h], __shfl_xor_sync(0xffffffffu, mt[h], k));
+        mt[h] = warp_max(mt[h]);
         const float mn = fmaxf(st.m[h], mt[h]);
         alpha[h] = ex2(st.m[h] - mn);  // 0 while the state is empty
         st.m[h] = mn;
@@ -611,6 +651,31 @@ __device__ __forceinline__ void softmax_stage(ConsumerState<C, NQB>& st, float* 
     __syncwarp();
 }
 
+// N consecutive floats from shared memory at p (aligned to 4 N bytes, up to
+// 16), in 16-byte pieces where N allows.
+template <int N>
+__device__ __forceinline__ void load_vec(float (&v)[N], const float* p)
+{
+    if constexpr (N % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < N; i += 4) {
+            const float4 x = *reinterpret_cast<const float4*>(p + i);
+            v[i] = x.x;
+            v[i + 1] = x.y;
+            v[i + 2] = x.z;
+            v[i + 3] = x.w;
+        }
+    } else if constexpr (N == 2) {
+        const float2 x = *reinterpret_cast<const float2*>(p);
+        v[0] = x.x;
+        v[1] = x.y;
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            v[i] = p[i];
+    }
+}
+
 // Value weights of the stage's tokens [tb, tb + UB) below n: for unit
 // (group gg, head h) = gg NQB + h, ub[part][unit][t - tb] holds the hi
 // (part 0) and lo (part 1) fp16 terms of u = p_ht s_tg fv, and the lane's
@@ -629,13 +694,18 @@ __device__ __forceinline__ void value_weights(ConsumerState<C, NQB>& st, const f
         const int t = tb + 2 * i;
         if (2 * i >= C::UB || t >= n)
             continue;
+        // statistics of tokens t, t + 1: 2 NG consecutive floats, read as
+        // vectors (scalar reads at a stride of 2 NG floats conflict on banks)
+        float s01[2 * NG], z01[2 * NG];
+        load_vec<2 * NG>(s01, vs + t * NG);
+        load_vec<2 * NG>(z01, vz + t * NG);
         float s0[NG], s1[NG], z0[NG], z1[NG];
 #pragma unroll
         for (int gg = 0; gg < NG; ++gg) {
-            s0[gg] = vs[t * NG + gg] * fv;
-            s1[gg] = vs[(t + 1) * NG + gg] * fv;
-            z0[gg] = vz[t * NG + gg];
-            z1[gg] = vz[(t + 1) * NG + gg];
+            s0[gg] = s01[gg] * fv;
+            s1[gg] = s01[NG + gg] * fv;
+            z0[gg] = z01[gg];
+            z1[gg] = z01[NG + gg];
         }
 #pragma unroll
         for (int h = 0; h < NQB; ++h) {
@@ -721,16 +791,18 @@ __device__ __forceinline__ void pv_slices(ConsumerState<C, NQB>& st, int lgG, co
 // --------------------------------------------------------------- residual ---
 
 // q . K of a residual stage (n fp16 tokens, padded rows) on the tensor cores:
-// A = the keys (ldmatrix), B = the row's fp16 query (column h = head h),
+// A = the keys (ldmatrix), B = the row's fp16 query heads (column h = head
+// h, qrow in the warp's scratch),
 // logits sl2 q . k into lg (sl2 = sm_scale log2 e).
 template <int NQB, int D, class C>
-__device__ __forceinline__ void qk_residual_stage(const uint8_t* slot, int n, float sl2, float* lg)
+__device__ __forceinline__ void qk_residual_stage(const uint8_t* slot, const uint16_t* qrow, int n, float sl2,
+                                                  float* lg)
 {
     const int lane = threadIdx.x & 31;
     const int g = lane >> 2, tg = lane & 3;
     const int mi = lane >> 3, lrow = (lane & 7) + 8 * (mi & 1), lch = mi >> 1;
     const uint32_t kb = smem_addr(slot + C::O_KR) + (uint32_t)(lrow * C::RROW + lch * 16);
-    const uint16_t* qh = reinterpret_cast<const uint16_t*>(slot) + (g < NQB ? g : 0) * D;
+    const uint16_t* qh = qrow + (g < NQB ? g : 0) * D;
 #pragma unroll 1
     for (int mt = 0; mt < (n + 15) / 16; ++mt) {
         float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
@@ -864,14 +936,16 @@ __device__ __forceinline__ void state_publish(const ConsumerState<C, NQB>& st, i
 
 // ------------------------------------------------------- one quantized stage ---
 
-// Tokens [t0, t0 + n) of a quantized stage, by one consumer warp: weight
+// Tokens [t0, t0 + n) of a quantized stage, by one consumer warp (qh: the
+// row's NQB query heads, fp16, in the warp's scratch): weight
 // scales (keys from max|q| and the largest key scale, values from the largest
 // value scale, valid rows only), q . K_hat into the logit rows, the online
 // softmax, then the value weights and p . V_hat in batches of UB tokens.
 // FULL: n == TS, so that every loop bound and mask is a constant.
 template <int BK, int BV, int NQB, int D, class C, bool FULL>
-__device__ __forceinline__ void consume_quant(ConsumerState<C, NQB>& st, const uint8_t* sl, int t0, int n_rt,
-                                              int lgG, float sl2, float* lg, float* qw, uint16_t* ub)
+__device__ __forceinline__ void consume_quant(ConsumerState<C, NQB>& st, const uint8_t* sl, const uint16_t* qh,
+                                              int t0, int n_rt, int lgG, float sl2, float* lg, float* qw,
+                                              uint16_t* ub)
 {
     const int lane = threadIdx.x & 31;
     const int n = FULL ? C::TS : n_rt;
@@ -879,7 +953,6 @@ __device__ __forceinline__ void consume_quant(ConsumerState<C, NQB>& st, const u
     const int ngr = ((t0 + n - 1) >> lgG) - (t0 >> lgG) + 1;
     const float smax_k = warp_max_stat(reinterpret_cast<const float*>(sl + C::O_KS), ngr * D);
     const float smax_v = warp_max_stat(reinterpret_cast<const float*>(sl + C::O_VS), n * NG);
-    const uint16_t* qh = reinterpret_cast<const uint16_t*>(sl);
     float fac[NQB];
 #pragma unroll
     for (int hh = 0; hh < NQB; ++hh) {
@@ -888,10 +961,7 @@ __device__ __forceinline__ void consume_quant(ConsumerState<C, NQB>& st, const u
 #pragma unroll
             for (int d = lane; d < D; d += 32)
                 mx = fmaxf(mx, fabsf(__half2float(__ushort_as_half(qh[hh * D + d]))));
-#pragma unroll
-            for (int kk = 16; kk > 0; kk >>= 1)
-                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, kk));
-            st.qmax[hh] = mx;
+            st.qmax[hh] = warp_max_nonneg(mx);
         }
         const float fk = weight_scale_pow2(st.qmax[hh] * smax_k);
         fac[hh] = sl2 * __frcp_rn(fk);
@@ -924,13 +994,18 @@ __device__ __forceinline__ void consume_quant(ConsumerState<C, NQB>& st, const u
 template <int BK, int BV, int NQB, int D, int NC>
 __global__ void __launch_bounds__(32 * (NC + 1), 1)
 decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_scale,
-                     float* __restrict__ out, float* __restrict__ ws, int ns)
+                     float* __restrict__ out, float* __restrict__ ws)
 {
     using C = StreamCfg<BK, BV, NQB, D, NC>;
+    constexpr int ns = stream_stages<C>();  // stages of the ring
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ long long red[C::THREADS / 32];
     __shared__ RangeStart sh_range[2];
     __shared__ int abort_flag;
+    // per merge buffer: warps published (bit mask), tiles published, last segment merged
+    __shared__ int pmask[C::NMB], ptiles[C::NMB], merged[C::NMB];
+    __shared__ unsigned long long next_tile;  // the consumers' tile counter
+    __shared__ int consumed[kStreamMaxStages];  // tiles finished per slot
 
     // the combine kernel may start once every CTA is running; it waits for
     // this grid's results in griddepcontrol.wait
@@ -943,7 +1018,7 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     uint8_t* slots = smem;
     float* wscr = reinterpret_cast<float*>(smem + (size_t)ns * C::SLOT);
     float* mbuf = wscr + NC * C::WARP_FLOATS;
-    uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + C::M_END);
+    uint64_t* full = reinterpret_cast<uint64_t*>(mbuf + C::NMB * C::M_END);
     uint64_t* empty = full + ns;
     int* wsi = reinterpret_cast<int*>(ws);
 
@@ -967,9 +1042,16 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
         for (int s = 0; s < ns; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
+            consumed[s] = 0;
         }
         mbar_fence_init();
         abort_flag = 0;
+        for (int i = 0; i < C::NMB; ++i) {
+            pmask[i] = 0;
+            ptiles[i] = 0;
+            merged[i] = i - C::NMB;
+        }
+        next_tile = 0ull;
         if (blockIdx.x == 0)
             wsi[0] = KIVI_OK;  // status word: KIVI_ETIMEOUT if a bounded wait gives up
     }
@@ -982,7 +1064,7 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
 
     if (warp == NC) {
         // ------------------------------------------------------ producer
-        // lane 0 issues every copy: a handful of large bulk copies per stage
+        // lane 0 issues every copy: six bulk copies per quantized stage
         if (lane != 0)
             return;
         Walk w = w0;
@@ -990,26 +1072,25 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
         uint32_t round = 0;
         long long issued = 0;
         for (long long k = 0; k < ntiles; ++k) {
+            // the empty barrier of a slot completes once per tile taken from
+            // it, in order, so its phase never runs more than one ahead
             if (k >= ns && !mbar_wait_bounded(&empty[slot], (round & 1u) ^ 1u, &abort_flag)) {
                 atomicExch(&abort_flag, 1);
                 atomicExch(wsi, KIVI_ETIMEOUT);
                 break;
             }
-            const int h = w.rr / NP, pass = w.rr - h * NP;
+            const int h = w.rr / NP;
             const size_t bh = (size_t)w.b * c.H + h;
-            const int hq0 = h * NQ + pass * NQB;
             const int t0 = walk_t0(w, C::TS, C::RT), n = walk_n(w, C::TS, C::RT);
             uint8_t* sl = slots + (size_t)slot * C::SLOT;
             uint64_t* bar = &full[slot];
-            const uint16_t* qsrc = q + ((size_t)w.b * Hq + hq0) * D;
             if (walk_quant(w)) {
                 const int nw = n / C::PK;
                 const int g0 = t0 >> lgG, ngr = ((t0 + n - 1) >> lgG) - g0 + 1;
                 const int NG = D >> lgG;
                 const size_t so = (bh * (size_t)(c.Tmax >> lgG) + g0) * D;
                 const size_t vo = bh * (size_t)c.Tmax + t0;
-                mbar_arrive_tx(bar, C::QB + nw * D * 4 + 2 * ngr * D * 4 + n * C::DW * 4 + 2 * n * NG * 4);
-                bulk_g2s(sl, qsrc, C::QB, bar);
+                mbar_arrive_tx(bar, nw * D * 4 + 2 * ngr * D * 4 + n * C::DW * 4 + 2 * n * NG * 4);
                 bulk_g2s(sl + C::O_KW, c.kq + (bh * (size_t)(c.Tmax / C::PK) + t0 / C::PK) * D, nw * D * 4, bar);
                 bulk_g2s(sl + C::O_KS, c.kscale + so, ngr * D * 4, bar);
                 bulk_g2s(sl + C::O_KZ, c.kzero + so, ngr * D * 4, bar);
@@ -1021,8 +1102,7 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
                 const int RG = c.R + c.G;
                 const int s0 = t0 % RG, n1 = min(n, RG - s0);
                 const size_t ring = bh * RG * D;
-                mbar_arrive_tx(bar, C::QB + 2 * n * D * 2);
-                bulk_g2s(sl, qsrc, C::QB, bar);
+                mbar_arrive_tx(bar, 2 * n * D * 2);
                 bulk_g2s(sl + C::O_KR, c.kres + ring + (size_t)s0 * D, n1 * D * 2, bar);
                 bulk_g2s(sl + C::O_VR, c.vres + ring + (size_t)s0 * D, n1 * D * 2, bar);
                 if (n1 < n) {
@@ -1048,103 +1128,206 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     }
 
     // ------------------------------------------------------------ consumer
+    // The consumers take the range's tiles in order from a shared counter, so
+    // a warp that falls behind (a merge, a slow tile) takes fewer of them and
+    // holds up no one.  A row segment is the range's tiles of one row; a warp
+    // keeps one open segment and, when its next tile lies in another one (or
+    // the range is done), publishes its state for it in merge buffer
+    // (segment mod NMB) with the number of the segment's tiles it took.  The
+    // publisher that completes the segment's count merges the states and
+    // writes the segment's output or partial.  Which warp takes which tile
+    // varies from run to run, so the merged results agree to rounding order.
     using CS = ConsumerState<C, NQB>;
     CS st;
     state_reset<C, NQB>(st);
     float* lg = wscr + warp * C::WARP_FLOATS + C::W_LG;
     float* qw = wscr + warp * C::WARP_FLOATS + C::W_QW;
     uint16_t* ub = reinterpret_cast<uint16_t*>(wscr + warp * C::WARP_FLOATS + C::W_UB);
+    uint4* wq = reinterpret_cast<uint4*>(wscr + warp * C::WARP_FLOATS + C::W_Q);
+    constexpr int QPL = (C::QPIECES + 31) / 32;  // query pieces per lane
     Walk w = w0;
-    int slot = 0;
-    uint32_t round = 0;
-    int mine = 0;           // k mod NC
-    bool first_seg = true;  // the CTA's first row segment
-    int seg_j0 = w.j;       // first tile of the current segment in its row
-    for (long long k = 0; k < ntiles; ++k) {
+    long long kw = 0;            // tile of the walker
+    int seg = 0;                 // segment of the walker's tile
+    long long seg_start = 0;     // its first tile
+    // the open segment
+    int o_seg = -1, o_tiles = 0, o_b = 0, o_hq0 = 0;
+    long long o_start = 0, o_rowend = 0;
+    auto publish = [&]() {
+        const long long seg_end = o_rowend < ntiles ? o_rowend : ntiles - 1;
+        const int seg_len = (int)(seg_end - o_start + 1);
+        const int buf = o_seg % C::NMB;
+        const bool whole = (o_seg > 0 || r0.j == 0) && o_rowend < ntiles;
+        float* mb = mbuf + buf * C::M_END;
+        // the buffer's previous segment must have been merged
+        {
+            const uint64_t t0 = global_ns();
+            for (uint32_t it = 0; *(volatile int*)&merged[buf] != o_seg - C::NMB; ++it)
+                if ((it & 63u) == 0 && global_ns() - t0 > kStreamWaitNs) {
+                    if (lane == 0) {
+                        atomicExch(&abort_flag, 1);
+                        atomicExch(wsi, KIVI_ETIMEOUT);
+                    }
+                    break;
+                }
+            __syncwarp();
+            __threadfence_block();
+        }
+        state_publish<BV, NQB, D, C>(st, lgG, warp, mb);
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) {
+            __threadfence_block();  // this warp's published state before its count
+            atomicOr(&pmask[buf], 1 << warp);
+            __threadfence_block();
+            last = atomicAdd(&ptiles[buf], o_tiles) + o_tiles == seg_len;
+            __threadfence_block();  // the others' states after the completing count
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        __syncwarp();
+        if (last) {
+            const unsigned mask = (unsigned)*(volatile int*)&pmask[buf];
+            float* dst_o;
+            float* dst_ml = nullptr;
+            if (whole) {
+                dst_o = out + ((size_t)o_b * Hq + o_hq0) * D;
+            } else {
+                dst_o = ws + kStreamHeaderFloats + (size_t)(gridDim.x + 1) * kStreamLocInts +
+                        ((size_t)blockIdx.x * 2 + (o_seg == 0 ? 0 : 1)) * NQB * (D + 2);
+                dst_ml = dst_o + NQB * D;
+            }
+#pragma unroll
+            for (int hh = 0; hh < NQB; ++hh) {
+                float M = -INFINITY;
+#pragma unroll
+                for (int cw = 0; cw < NC; ++cw)
+                    if (mask >> cw & 1u)
+                        M = fmaxf(M, mb[C::M_M + cw * NQB + hh]);
+                float e[NC], L = 0.0f;
+#pragma unroll
+                for (int cw = 0; cw < NC; ++cw) {
+                    const float mw = mb[C::M_M + cw * NQB + hh];
+                    e[cw] = (mask >> cw & 1u) && mw > -INFINITY ? ex2(mw - M) : 0.0f;
+                    L = fmaf(e[cw], (mask >> cw & 1u) ? mb[C::M_L + cw * NQB + hh] : 0.0f, L);
+                }
+                const float inv_l = whole ? 1.0f / L : 1.0f;
+                for (int d = lane; d < D; d += 32) {
+                    const int gg = d >> lgG;
+                    float o = 0.0f;
+#pragma unroll
+                    for (int cw = 0; cw < NC; ++cw)
+                        if (e[cw] != 0.0f)
+                            o = fmaf(e[cw],
+                                     mb[C::M_O + (cw * NQB + hh) * D + d] + mb[C::M_Z + (cw * NQB + hh) * C::NGM + gg],
+                                     o);
+                    dst_o[hh * D + d] = o * inv_l;
+                }
+                if (!whole && lane == 0) {
+                    dst_ml[hh] = M;
+                    dst_ml[NQB + hh] = L;
+                }
+            }
+            __syncwarp();
+            if (lane == 0) {
+                pmask[buf] = 0;
+                ptiles[buf] = 0;
+                __threadfence_block();
+                atomicExch(&merged[buf], o_seg);
+            }
+        }
+        state_reset<C, NQB>(st);
+        o_seg = -1;
+        o_tiles = 0;
+    };
+    for (;;) {
+        unsigned long long kk = 0;
+        if (lane == 0)
+            kk = atomicAdd(&next_tile, 1ull);
+        const long long k = (long long)__shfl_sync(0xffffffffu, kk, 0);
+        if (k >= ntiles)
+            break;
+        const int crossed = walk_skip(w, c, RB, C::TS, C::RT, (int)(k - kw));
+        kw = k;
+        if (crossed) {
+            seg += crossed;
+            seg_start = k - w.j;
+        }
+        if (o_seg >= 0 && o_seg != seg)
+            publish();
         const int h = w.rr / NP, pass = w.rr - h * NP;
         const int hq0 = h * NQ + pass * NQB;
+        // a new segment (a new row): its query heads go to the warp's scratch
+        // once the tile's wait is over; the loads start now
+        const bool newq = o_seg < 0;
+        uint4 qv[QPL];
+        if (newq) {
+            o_seg = seg;
+            o_start = seg_start;
+            o_rowend = k + (w.nt - 1 - w.j);
+            o_b = w.b;
+            o_hq0 = hq0;
+            const uint4* q4 = reinterpret_cast<const uint4*>(q + ((size_t)w.b * Hq + hq0) * D);
+#pragma unroll
+            for (int i = 0; i < QPL; ++i)
+                if (lane + 32 * i < C::QPIECES)
+                    qv[i] = __ldg(q4 + lane + 32 * i);
+        }
+        ++o_tiles;
+        const int slot = (int)((unsigned long long)k % ns);
+        const uint32_t round = (uint32_t)((unsigned long long)k / ns);
         const bool aborted = __shfl_sync(0xffffffffu, *(volatile int*)&abort_flag, 0) != 0;
-        if (mine == warp && !aborted) {
-            const bool ok = __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], round & 1u, &abort_flag));
+        if (!aborted) {
+            // A parity wait cannot tell phase `round` from phase `round` - 2:
+            // wait on the full barrier only once the slot's previous tile is
+            // done (then its phase `round` - 1 has completed, and the parity
+            // names phase `round`).  Tiles are taken in order, so this almost
+            // never waits.
+            bool ok = true;
+            if (*(volatile int*)&consumed[slot] < (int)round) {
+                const uint64_t tw = global_ns();
+                for (uint32_t it = 0; *(volatile int*)&consumed[slot] < (int)round; ++it)
+                    if ((it & 63u) == 0 && (global_ns() - tw > kStreamWaitNs || *(volatile int*)&abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+            }
+            ok = __all_sync(0xffffffffu, ok) &&
+                 __all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], round & 1u, &abort_flag));
             if (!ok && lane == 0) {
                 atomicExch(&abort_flag, 1);
                 atomicExch(wsi, KIVI_ETIMEOUT);
             }
             if (ok) {
                 const uint8_t* sl = slots + (size_t)slot * C::SLOT;
+                if (newq) {
+#pragma unroll
+                    for (int i = 0; i < QPL; ++i)
+                        if (lane + 32 * i < C::QPIECES)
+                            wq[lane + 32 * i] = qv[i];
+                    __syncwarp();
+                }
+                const uint16_t* qh = reinterpret_cast<const uint16_t*>(wq);
                 const int t0 = walk_t0(w, C::TS, C::RT), n = walk_n(w, C::TS, C::RT);
                 if (walk_quant(w)) {
                     if (n == C::TS)
-                        consume_quant<BK, BV, NQB, D, C, true>(st, sl, t0, n, lgG, sl2, lg, qw, ub);
+                        consume_quant<BK, BV, NQB, D, C, true>(st, sl, qh, t0, n, lgG, sl2, lg, qw, ub);
                     else
-                        consume_quant<BK, BV, NQB, D, C, false>(st, sl, t0, n, lgG, sl2, lg, qw, ub);
+                        consume_quant<BK, BV, NQB, D, C, false>(st, sl, qh, t0, n, lgG, sl2, lg, qw, ub);
                 } else {
-                    qk_residual_stage<NQB, D, C>(sl, n, sl2, lg);
+                    qk_residual_stage<NQB, D, C>(sl, qh, n, sl2, lg);
                     __syncwarp();
                     softmax_stage<C, NQB>(st, lg, n, st.fv);
                     pv_residual_stage<NQB, D, C>(st, sl, n, lg);
                     __syncwarp();
                 }
-                if (lane == 0)
+                if (lane == 0) {
+                    *(volatile int*)&consumed[slot] = (int)round + 1;
                     mbar_arrive(&empty[slot]);
-            }
-        }
-        const bool seg_end = (w.j == w.nt - 1) || (k == ntiles - 1);
-        if (seg_end) {
-            // ---------------------------------------------- row segment merge
-            state_publish<BV, NQB, D, C>(st, lgG, warp, mbuf);
-            named_bar(1, 32 * NC);
-            const bool whole = seg_j0 == 0 && w.j == w.nt - 1;
-            float* dst_o;
-            float* dst_ml = nullptr;
-            if (whole) {
-                dst_o = out + ((size_t)w.b * Hq + hq0) * D;
-            } else {
-                const int slot_id = first_seg ? 0 : 1;
-                dst_o = ws + kStreamHeaderFloats + (size_t)(gridDim.x + 1) * kStreamLocInts +
-                        ((size_t)blockIdx.x * 2 + slot_id) * NQB * (D + 2);
-                dst_ml = dst_o + NQB * D;
-            }
-            for (int idx = threadIdx.x; idx < NQB * D; idx += 32 * NC) {
-                const int hh = idx / D, d = idx - hh * D;
-                float M = -INFINITY;
-#pragma unroll
-                for (int cw = 0; cw < NC; ++cw)
-                    M = fmaxf(M, mbuf[C::M_M + cw * NQB + hh]);
-                float o = 0.0f, L = 0.0f;
-                const int gg = d >> lgG;
-#pragma unroll
-                for (int cw = 0; cw < NC; ++cw) {
-                    const float mw = mbuf[C::M_M + cw * NQB + hh];
-                    const float e = mw > -INFINITY ? ex2(mw - M) : 0.0f;
-                    o = fmaf(e, mbuf[C::M_O + (cw * NQB + hh) * D + d] +
-                                    mbuf[C::M_Z + (cw * NQB + hh) * C::NGM + gg], o);
-                    L = fmaf(e, mbuf[C::M_L + cw * NQB + hh], L);
-                }
-                if (whole) {
-                    dst_o[hh * D + d] = o / L;
-                } else {
-                    dst_o[hh * D + d] = o;
-                    if (d == 0) {
-                        dst_ml[hh] = M;
-                        dst_ml[NQB + hh] = L;
-                    }
                 }
             }
-            named_bar(1, 32 * NC);
-            state_reset<C, NQB>(st);
-            first_seg = false;
         }
-        walk_next(w, c, RB, C::TS, C::RT);
-        if (seg_end)
-            seg_j0 = w.j;
-        if (++slot == ns) {
-            slot = 0;
-            ++round;
-        }
-        if (++mine == NC)
-            mine = 0;
     }
+    if (o_seg >= 0)
+        publish();
 }
 
 // --------------------------------------------------------------- combine ---
@@ -1153,18 +1336,22 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
 // takes the row in which range i ends, if range i is not empty, ends inside
 // a row, and holds that row's first tile; the ranges after it that start
 // inside the row hold its other pieces (their first row segment, slot 0).
-// Also writes zero outputs for sequences of length 0.
+// The range records are read in parallel, 128 ranges at a time.  Also writes
+// zero outputs for sequences of length 0.
 template <int NQB, int D>
 __global__ void __launch_bounds__(128)
 decode_stream_combine_kernel(const int32_t* __restrict__ len, int B, int Hq, int H, int NP,
                              const float* __restrict__ ws, float* __restrict__ out)
 {
+    constexpr int T = 128;
     const int N = gridDim.x, i = blockIdx.x;
     const int NQ = Hq / H;
+    __shared__ int s_last;
+    __shared__ float s_m[T][NQB], s_l[T][NQB];
     // zero rows of empty sequences (len is not written by the decode kernel)
     for (int b = i; b < B; b += N)
         if (len[b] == 0)
-            for (int x = threadIdx.x; x < Hq * D; x += blockDim.x)
+            for (int x = threadIdx.x; x < Hq * D; x += T)
                 out[(size_t)b * Hq * D + x] = 0.0f;
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int* rec = reinterpret_cast<const int*>(ws) + kStreamHeaderFloats;
@@ -1184,42 +1371,80 @@ decode_stream_combine_kernel(const int32_t* __restrict__ len, int B, int Hq, int
     const int h = rr / NP, pass = rr - h * NP;
     const int hq0 = h * NQ + pass * NQB;
     float* dst = out + ((size_t)b * Hq + hq0) * D;
-    __shared__ int s_last;
-    if (threadIdx.x == 0) {
-        // ranges that start inside the row (their record points into it at j > 0)
-        int k = i + 1;
-        while (k < N) {
+    // the last range k >= i + 1 that starts inside the row (its record points
+    // into the row at j > 0): every range from i + 1 to it does
+    if (threadIdx.x == 0)
+        s_last = N - 1;
+    __syncthreads();
+    for (int base = i + 1; base < N; base += T) {
+        const int k = base + (int)threadIdx.x;
+        if (k < N) {
             const int* rk = rec + k * kStreamLocInts;
             if (!(rk[2] == b && rk[3] == rr && rk[4] > 0))
-                break;
-            ++k;
+                atomicMin(&s_last, k - 1);
         }
-        s_last = k - 1;
+        __syncthreads();
+        if (s_last < base + T - 1)
+            break;
     }
-    __syncthreads();
     const int last = s_last;
     const int slot_i = row_first == g0 ? 0 : 1;
-    for (int idx = threadIdx.x; idx < NQB * D; idx += blockDim.x) {
-        const int hh = idx / D;
-        float M = -INFINITY;
-        for (int k = i; k <= last; ++k) {
-            if (k > i && gidx(k + 1) <= gidx(k))
-                continue;  // an empty range holds no piece
-            const float* p = part + ((size_t)k * 2 + (k == i ? slot_i : 0)) * pstride;
-            M = fmaxf(M, p[NQB * D + hh]);
-        }
-        float o = 0.0f, L = 0.0f;
-        for (int k = i; k <= last; ++k) {
-            if (k > i && gidx(k + 1) <= gidx(k))
-                continue;
-            const float* p = part + ((size_t)k * 2 + (k == i ? slot_i : 0)) * pstride;
-            const float m = p[NQB * D + hh];
-            const float e = m > -INFINITY ? ex2(m - M) : 0.0f;
-            o = fmaf(e, p[idx], o);
-            L = fmaf(e, p[NQB * D + NQB + hh], L);
-        }
-        dst[idx] = o / L;
+    const int P = last - i + 1;  // ranges i .. last; an empty one holds no piece
+    auto piece = [&](int k) { return part + ((size_t)k * 2 + (k == i ? slot_i : 0)) * pstride; };
+    // pass 1: the maxima over the pieces; pass 2: their weights and the sums.
+    // (m, l) of up to T pieces at a time go through shared memory; the sums
+    // run over the pieces in order, so the result does not depend on timing.
+    constexpr int ND = (D + T - 1) / T;  // channels per thread
+    float M[NQB], L[NQB], o[NQB][ND];
+#pragma unroll
+    for (int hh = 0; hh < NQB; ++hh) {
+        M[hh] = -INFINITY;
+        L[hh] = 0.0f;
+#pragma unroll
+        for (int u = 0; u < ND; ++u)
+            o[hh][u] = 0.0f;
     }
+    for (int pass2 = 0; pass2 < 2; ++pass2) {
+        for (int c0 = 0; c0 < P; c0 += T) {
+            const int t = (int)threadIdx.x, k = i + c0 + t;
+            const bool has = c0 + t < P && (k == i || gidx(k + 1) > gidx(k));
+#pragma unroll
+            for (int hh = 0; hh < NQB; ++hh) {
+                s_m[t][hh] = has ? piece(k)[NQB * D + hh] : -INFINITY;
+                s_l[t][hh] = has ? piece(k)[NQB * D + NQB + hh] : 0.0f;
+            }
+            __syncthreads();
+            const int nq = min(T, P - c0);
+            for (int q = 0; q < nq; ++q) {
+#pragma unroll
+                for (int hh = 0; hh < NQB; ++hh) {
+                    const float m = s_m[q][hh];
+                    if (pass2 == 0) {
+                        M[hh] = fmaxf(M[hh], m);
+                    } else if (m > -INFINITY) {
+                        const float e = ex2(m - M[hh]);
+                        L[hh] = fmaf(e, s_l[q][hh], L[hh]);
+                        const float* pq = piece(i + c0 + q) + hh * D;
+#pragma unroll
+                        for (int u = 0; u < ND; ++u) {
+                            const int d = t + u * T;
+                            if (d < D)
+                                o[hh][u] = fmaf(e, pq[d], o[hh][u]);
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        }
+    }
+#pragma unroll
+    for (int hh = 0; hh < NQB; ++hh)
+#pragma unroll
+        for (int u = 0; u < ND; ++u) {
+            const int d = (int)threadIdx.x + u * T;
+            if (d < D)
+                dst[hh * D + d] = o[hh][u] / L[hh];
+        }
 }
 
 // ---------------------------------------------------------------- launch ---
@@ -1232,12 +1457,12 @@ cudaError_t stream_launch(const kivi_cache& c, const uint16_t* q, int Hq, float 
     auto kern = decode_stream_kernel<BK, BV, NQB, D, NC>;
     constexpr int ns = stream_stages<C>();
     static_assert(ns >= 2, "the shared memory holds at least two stages");
-    const size_t smem = (size_t)ns * C::SLOT + C::FIXED_BYTES - 256 + 2 * (size_t)ns * 8;
+    const size_t smem = (size_t)ns * C::SLOT + C::FIXED_BYTES - kStreamStaticSmem + 2 * (size_t)ns * 8;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
     const int N = cmin(sm_count(), kMaxStreamCTAs);
-    kern<<<N, C::THREADS, smem, s>>>(c, q, Hq, sm, out, ws, ns);
+    kern<<<N, C::THREADS, smem, s>>>(c, q, Hq, sm, out, ws);
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
@@ -1260,12 +1485,6 @@ cudaError_t stream_launch(const kivi_cache& c, const uint16_t* q, int Hq, float 
     }
     return cudaGetLastError();
 }
-
-}  // namespace kivi
-
-namespace kivi {
-
-
 
 // Dispatch of the key and value widths and the query heads per pass for head
 // dimension D.
