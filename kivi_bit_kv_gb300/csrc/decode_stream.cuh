@@ -140,7 +140,6 @@ __host__ __device__ constexpr int round_up(int x, int m) { return (x + m - 1) / 
 
 constexpr int kMaxStreamCTAs = 1024;          // workspace sizing bound on the grid
 constexpr int kStreamStaticSmem = 512;        // room left for the kernel's static shared arrays
-constexpr int kStreamLocInts = 8;             // ints per CTA range record in the workspace
 constexpr int kStreamHeaderFloats = 4;        // workspace header (status word)
 constexpr int kStreamMaxStages = 32;          // stages of the ring (the consumed counters are static)
 
@@ -236,12 +235,11 @@ __host__ __device__ constexpr int stream_consumers()
                                                                           : stream_consumers<BK, BV, NQB, D, NC - 1>();
 }
 
-// Workspace of the streamed decode: header, the CTA range records and two
-// partial (o, m, l) slots per CTA.
+// Workspace of the streamed decode: header (status word) and two partial
+// (o, m, l) slots per CTA.
 inline size_t stream_ws_floats(int D, int NQB, int ctas)
 {
-    return (size_t)kStreamHeaderFloats + (size_t)(ctas + 1) * kStreamLocInts +
-           (size_t)ctas * 2 * NQB * (D + 2);
+    return (size_t)kStreamHeaderFloats + (size_t)ctas * 2 * NQB * (D + 2);
 }
 
 // ---------------------------------------------------------- tile walker ---
@@ -353,7 +351,8 @@ struct RangeStart {
 // lengths: two passes over the sequences (total, then location).
 template <int THREADS>
 __device__ __forceinline__ void locate_range(const kivi_cache& c, int RB, int TS, int RT, int k, int N,
-                                             RangeStart& r0, RangeStart& r1, long long* red, RangeStart* sh)
+                                             RangeStart& r0, RangeStart& r1, long long* red, RangeStart* sh,
+                                             long long* total = nullptr)
 {
     long long NT = 0;
     for (int base = 0; base < c.B; base += THREADS) {
@@ -385,6 +384,8 @@ __device__ __forceinline__ void locate_range(const kivi_cache& c, int RB, int TS
     __syncthreads();
     r0 = sh[0];
     r1 = sh[1];
+    if (total)
+        *total = NT;
 }
 
 // ------------------------------------------------------- consumer state ---
@@ -1007,9 +1008,13 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     __shared__ unsigned long long next_tile;  // the consumers' tile counter
     __shared__ int consumed[kStreamMaxStages];  // tiles finished per slot
 
-    // the combine kernel may start once every CTA is running; it waits for
-    // this grid's results in griddepcontrol.wait
+    // Launched as a programmatic dependent: the CTAs may be scheduled while
+    // the previous kernel of the stream drains, and wait here for its
+    // results before reading anything.  The combine kernel may start once
+    // every CTA of this grid is running; it waits for this grid's results in
+    // its own griddepcontrol.wait.
     asm volatile("griddepcontrol.launch_dependents;");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NQ = Hq / c.H, NP = NQ / NQB, RB = c.H * NP;
@@ -1025,20 +1030,6 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     RangeStart r0, r1;
     locate_range<C::THREADS>(c, RB, C::TS, C::RT, blockIdx.x, gridDim.x, r0, r1, red, sh_range);
     if (threadIdx.x == 0) {
-        int* rec = wsi + kStreamHeaderFloats + blockIdx.x * kStreamLocInts;
-        rec[0] = (int)(r0.g & 0xffffffff);
-        rec[1] = (int)(r0.g >> 32);
-        rec[2] = r0.b;
-        rec[3] = r0.rr;
-        rec[4] = r0.j;
-        if (blockIdx.x == gridDim.x - 1) {
-            int* e = rec + kStreamLocInts;
-            e[0] = (int)(r1.g & 0xffffffff);
-            e[1] = (int)(r1.g >> 32);
-            e[2] = r1.b;
-            e[3] = r1.rr;
-            e[4] = r1.j;
-        }
         for (int s = 0; s < ns; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -1191,8 +1182,7 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
             if (whole) {
                 dst_o = out + ((size_t)o_b * Hq + o_hq0) * D;
             } else {
-                dst_o = ws + kStreamHeaderFloats + (size_t)(gridDim.x + 1) * kStreamLocInts +
-                        ((size_t)blockIdx.x * 2 + (o_seg == 0 ? 0 : 1)) * NQB * (D + 2);
+                dst_o = ws + kStreamHeaderFloats + ((size_t)blockIdx.x * 2 + (o_seg == 0 ? 0 : 1)) * NQB * (D + 2);
                 dst_ml = dst_o + NQB * D;
             }
 #pragma unroll
@@ -1336,64 +1326,52 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
 // takes the row in which range i ends, if range i is not empty, ends inside
 // a row, and holds that row's first tile; the ranges after it that start
 // inside the row hold its other pieces (their first row segment, slot 0).
-// The range records are read in parallel, 128 ranges at a time.  Also writes
-// zero outputs for sequences of length 0.
-template <int NQB, int D>
+// The ranges are the decode kernel's (range k starts at tile NT k / N of the
+// NT tiles), found from len[] -- which the decode kernel does not write --
+// before the wait for the decode kernel's results, so that after it only the
+// pieces are read: their (m, l) pairs, then their o rows, all at once.  The
+// sums run over the pieces in order, so the result does not depend on
+// timing.  Also writes zero outputs for sequences of length 0.
+template <int NQB, int D, int TS, int RT>
 __global__ void __launch_bounds__(128)
-decode_stream_combine_kernel(const int32_t* __restrict__ len, int B, int Hq, int H, int NP,
-                             const float* __restrict__ ws, float* __restrict__ out)
+decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __restrict__ ws,
+                             float* __restrict__ out)
 {
     constexpr int T = 128;
     const int N = gridDim.x, i = blockIdx.x;
-    const int NQ = Hq / H;
-    __shared__ int s_last;
+    const int NQ = Hq / c.H, RB = c.H * NP;
+    __shared__ long long red[T / 32];
+    __shared__ RangeStart sh_range[2];
     __shared__ float s_m[T][NQB], s_l[T][NQB];
-    // zero rows of empty sequences (len is not written by the decode kernel)
-    for (int b = i; b < B; b += N)
-        if (len[b] == 0)
+    // the next decode kernel may be scheduled once every CTA of this grid
+    // runs (it waits for this grid's results before it reads anything)
+    asm volatile("griddepcontrol.launch_dependents;");
+    for (int b = i; b < c.B; b += N)
+        if (c.len[b] == 0)
             for (int x = threadIdx.x; x < Hq * D; x += T)
                 out[(size_t)b * Hq * D + x] = 0.0f;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    const int* rec = reinterpret_cast<const int*>(ws) + kStreamHeaderFloats;
-    auto gidx = [&](int k) {
-        return (long long)(unsigned)rec[k * kStreamLocInts] | ((long long)rec[k * kStreamLocInts + 1] << 32);
-    };
-    const long long g0 = gidx(i), g1 = gidx(i + 1);
-    const int* nx = rec + (i + 1) * kStreamLocInts;  // where range i ends
-    if (g1 <= g0 || nx[4] == 0 || nx[2] >= B)
+    RangeStart r0, r1;
+    long long NT = 0;
+    locate_range<T>(c, RB, TS, RT, i, N, r0, r1, red, sh_range, &NT);
+    const long long g0 = r0.g, g1 = r1.g;
+    if (g1 <= g0 || r1.j == 0 || r1.b >= c.B)
         return;
-    const int b = nx[2], rr = nx[3], jn = nx[4];
-    const long long row_first = g1 - jn;
+    const long long row_first = g1 - r1.j;
     if (row_first < g0)
         return;  // an earlier range holds the row's first tile
-    const float* part = ws + kStreamHeaderFloats + (size_t)(N + 1) * kStreamLocInts;
-    const size_t pstride = (size_t)NQB * (D + 2);
-    const int h = rr / NP, pass = rr - h * NP;
-    const int hq0 = h * NQ + pass * NQB;
-    float* dst = out + ((size_t)b * Hq + hq0) * D;
-    // the last range k >= i + 1 that starts inside the row (its record points
-    // into the row at j > 0): every range from i + 1 to it does
-    if (threadIdx.x == 0)
-        s_last = N - 1;
-    __syncthreads();
-    for (int base = i + 1; base < N; base += T) {
-        const int k = base + (int)threadIdx.x;
-        if (k < N) {
-            const int* rk = rec + k * kStreamLocInts;
-            if (!(rk[2] == b && rk[3] == rr && rk[4] > 0))
-                atomicMin(&s_last, k - 1);
-        }
-        __syncthreads();
-        if (s_last < base + T - 1)
-            break;
-    }
-    const int last = s_last;
+    const long long row_end = row_first + row_tiles(c.len[r1.b], c, TS, RT);
+    // ranges i + 1 .. last start inside the row: range k starts at NT k / N
+    const int last = (int)min((long long)N - 1, (row_end * N - 1) / NT);
+    auto X = [&](int k) { return NT * k / N; };
     const int slot_i = row_first == g0 ? 0 : 1;
     const int P = last - i + 1;  // ranges i .. last; an empty one holds no piece
+    const float* part = ws + kStreamHeaderFloats;
+    const size_t pstride = (size_t)NQB * (D + 2);
     auto piece = [&](int k) { return part + ((size_t)k * 2 + (k == i ? slot_i : 0)) * pstride; };
-    // pass 1: the maxima over the pieces; pass 2: their weights and the sums.
-    // (m, l) of up to T pieces at a time go through shared memory; the sums
-    // run over the pieces in order, so the result does not depend on timing.
+    const int h = r1.rr / NP, pass = r1.rr - h * NP;
+    float* dst = out + ((size_t)r1.b * Hq + h * NQ + pass * NQB) * D;
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
     constexpr int ND = (D + T - 1) / T;  // channels per thread
     float M[NQB], L[NQB], o[NQB][ND];
 #pragma unroll
@@ -1404,38 +1382,63 @@ decode_stream_combine_kernel(const int32_t* __restrict__ len, int B, int Hq, int
         for (int u = 0; u < ND; ++u)
             o[hh][u] = 0.0f;
     }
-    for (int pass2 = 0; pass2 < 2; ++pass2) {
-        for (int c0 = 0; c0 < P; c0 += T) {
-            const int t = (int)threadIdx.x, k = i + c0 + t;
-            const bool has = c0 + t < P && (k == i || gidx(k + 1) > gidx(k));
+    const int t = (int)threadIdx.x;
+    auto load_ml = [&](int c0) {
+        const int k = i + c0 + t;
+        const bool hk = c0 + t < P && (k == i || X(k + 1) > X(k));
 #pragma unroll
-            for (int hh = 0; hh < NQB; ++hh) {
-                s_m[t][hh] = has ? piece(k)[NQB * D + hh] : -INFINITY;
-                s_l[t][hh] = has ? piece(k)[NQB * D + NQB + hh] : 0.0f;
-            }
-            __syncthreads();
-            const int nq = min(T, P - c0);
-            for (int q = 0; q < nq; ++q) {
+        for (int hh = 0; hh < NQB; ++hh) {
+            s_m[t][hh] = hk ? piece(k)[NQB * D + hh] : -INFINITY;
+            s_l[t][hh] = hk ? piece(k)[NQB * D + NQB + hh] : 0.0f;
+        }
+    };
+    // pass 1: the maxima (a single chunk of pairs stays in shared memory)
+    for (int c0 = 0; c0 < P; c0 += T) {
+        load_ml(c0);
+        __syncthreads();
+        const int nq = min(T, P - c0);
+        for (int qq = 0; qq < nq; ++qq)
 #pragma unroll
-                for (int hh = 0; hh < NQB; ++hh) {
-                    const float m = s_m[q][hh];
-                    if (pass2 == 0) {
-                        M[hh] = fmaxf(M[hh], m);
-                    } else if (m > -INFINITY) {
-                        const float e = ex2(m - M[hh]);
-                        L[hh] = fmaf(e, s_l[q][hh], L[hh]);
-                        const float* pq = piece(i + c0 + q) + hh * D;
-#pragma unroll
-                        for (int u = 0; u < ND; ++u) {
-                            const int d = t + u * T;
-                            if (d < D)
-                                o[hh][u] = fmaf(e, pq[d], o[hh][u]);
-                        }
-                    }
-                }
-            }
+            for (int hh = 0; hh < NQB; ++hh)
+                M[hh] = fmaxf(M[hh], s_m[qq][hh]);
+        __syncthreads();
+    }
+    // pass 2: weights and sums, four pieces' rows loaded at a time
+    for (int c0 = 0; c0 < P; c0 += T) {
+        if (P > T) {
+            load_ml(c0);
             __syncthreads();
         }
+        const int nq = min(T, P - c0);
+        for (int q0 = 0; q0 < nq; q0 += 4) {
+            float e[4][NQB], v[4][NQB][ND];
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int hh = 0; hh < NQB; ++hh) {
+                    const float m = q0 + r < nq ? s_m[q0 + r][hh] : -INFINITY;
+                    e[r][hh] = m > -INFINITY ? ex2(m - M[hh]) : 0.0f;
+                    const float* pq = piece(i + c0 + q0 + r) + hh * D;
+#pragma unroll
+                    for (int u = 0; u < ND; ++u) {
+                        const int d = t + u * T;
+                        v[r][hh][u] = e[r][hh] != 0.0f && d < D ? pq[d] : 0.0f;
+                    }
+                }
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+#pragma unroll
+                for (int hh = 0; hh < NQB; ++hh) {
+                    if (e[r][hh] == 0.0f)
+                        continue;
+                    L[hh] = fmaf(e[r][hh], s_l[q0 + r][hh], L[hh]);
+#pragma unroll
+                    for (int u = 0; u < ND; ++u)
+                        o[hh][u] = fmaf(e[r][hh], v[r][hh][u], o[hh][u]);
+                }
+        }
+        if (P > T)
+            __syncthreads();
     }
 #pragma unroll
     for (int hh = 0; hh < NQB; ++hh)
@@ -1462,7 +1465,23 @@ cudaError_t stream_launch(const kivi_cache& c, const uint16_t* q, int Hq, float 
     if (e != cudaSuccess)
         return e;
     const int N = cmin(sm_count(), kMaxStreamCTAs);
-    kern<<<N, C::THREADS, smem, s>>>(c, q, Hq, sm, out, ws);
+    {
+        cudaLaunchConfig_t cf = {};
+        cf.gridDim = dim3(N);
+        cf.blockDim = dim3(C::THREADS);
+        cf.dynamicSmemBytes = smem;
+        cf.stream = s;
+        cudaLaunchAttribute at[1];
+        at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at[0].val.programmaticStreamSerializationAllowed = 1;
+        cf.attrs = at;
+        cf.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cf, kern, c, q, Hq, sm, out, ws);
+        if (e != cudaSuccess) {
+            (void)cudaGetLastError();
+            kern<<<N, C::THREADS, smem, s>>>(c, q, Hq, sm, out, ws);
+        }
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess)
         return e;
@@ -1477,11 +1496,11 @@ cudaError_t stream_launch(const kivi_cache& c, const uint16_t* q, int Hq, float 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, decode_stream_combine_kernel<NQB, D>, (const int32_t*)c.len, c.B, Hq, c.H, NP,
-                           (const float*)ws, out);
+    auto comb = decode_stream_combine_kernel<NQB, D, C::TS, C::RT>;
+    e = cudaLaunchKernelEx(&cfg, comb, c, Hq, NP, (const float*)ws, out);
     if (e != cudaSuccess) {
         (void)cudaGetLastError();
-        decode_stream_combine_kernel<NQB, D><<<N, 128, 0, s>>>(c.len, c.B, Hq, c.H, NP, ws, out);
+        comb<<<N, 128, 0, s>>>(c, Hq, NP, ws, out);
     }
     return cudaGetLastError();
 }
