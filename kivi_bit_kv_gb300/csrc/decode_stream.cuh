@@ -94,6 +94,18 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
                  "l"(src), "r"(bytes), "r"(smem_addr(b))
                  : "memory");
 }
+// The same with shared-memory addresses already converted.
+__device__ __forceinline__ void bulk_g2s_a(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                     dst),
+                 "l"(src), "r"(bytes), "r"(bar)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx_a(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
 constexpr uint64_t kStreamWaitNs = 2000000000ull;  // a wait on a stage gives up after 2 s
 
 // Nanoseconds of the global timer.
@@ -1055,13 +1067,24 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
 
     if (warp == NC) {
         // ------------------------------------------------------ producer
-        // lane 0 issues every copy: six bulk copies per quantized stage
+        // Lane 0 issues every copy: six bulk copies per quantized stage.  The
+        // issuing thread's own latency per stage bounds the stream, so the
+        // row's base pointers are formed once per row, the offsets inside a
+        // row are 32-bit, and shared-memory addresses are kept converted.
         if (lane != 0)
             return;
         Walk w = w0;
         int slot = 0;
         uint32_t round = 0;
         long long issued = 0;
+        const int NG = D >> lgG;
+        const int RG = c.R + c.G;
+        const uint32_t s_slots = smem_addr(slots), s_full = smem_addr(full);
+        const int32_t* kq_r = nullptr;
+        const int32_t* vq_r = nullptr;
+        const float *ks_r = nullptr, *kz_r = nullptr, *vs_r = nullptr, *vz_r = nullptr;
+        const uint16_t *kr_r = nullptr, *vr_r = nullptr;
+        bool new_row = true;
         for (long long k = 0; k < ntiles; ++k) {
             // the empty barrier of a slot completes once per tile taken from
             // it, in order, so its phase never runs more than one ahead
@@ -1070,39 +1093,49 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
                 atomicExch(wsi, KIVI_ETIMEOUT);
                 break;
             }
-            const int h = w.rr / NP;
-            const size_t bh = (size_t)w.b * c.H + h;
-            const int t0 = walk_t0(w, C::TS, C::RT), n = walk_n(w, C::TS, C::RT);
-            uint8_t* sl = slots + (size_t)slot * C::SLOT;
-            uint64_t* bar = &full[slot];
-            if (walk_quant(w)) {
-                const int nw = n / C::PK;
+            if (new_row) {
+                const size_t bh = (size_t)w.b * c.H + w.rr / NP;
+                kq_r = c.kq + bh * (size_t)(c.Tmax / C::PK) * D;
+                ks_r = c.kscale + bh * (size_t)(c.Tmax >> lgG) * D;
+                kz_r = c.kzero + bh * (size_t)(c.Tmax >> lgG) * D;
+                vq_r = c.vq + bh * (size_t)c.Tmax * C::DW;
+                vs_r = c.vscale + bh * (size_t)c.Tmax * NG;
+                vz_r = c.vzero + bh * (size_t)c.Tmax * NG;
+                kr_r = c.kres + bh * (size_t)RG * D;
+                vr_r = c.vres + bh * (size_t)RG * D;
+            }
+            const uint32_t sb = s_slots + (uint32_t)slot * C::SLOT;
+            const uint32_t bar = s_full + (uint32_t)slot * 8u;
+            if (w.j < w.nq) {
+                const int t0 = w.j * C::TS, n = min(C::TS, w.Tq - t0);
                 const int g0 = t0 >> lgG, ngr = ((t0 + n - 1) >> lgG) - g0 + 1;
-                const int NG = D >> lgG;
-                const size_t so = (bh * (size_t)(c.Tmax >> lgG) + g0) * D;
-                const size_t vo = bh * (size_t)c.Tmax + t0;
-                mbar_arrive_tx(bar, nw * D * 4 + 2 * ngr * D * 4 + n * C::DW * 4 + 2 * n * NG * 4);
-                bulk_g2s(sl + C::O_KW, c.kq + (bh * (size_t)(c.Tmax / C::PK) + t0 / C::PK) * D, nw * D * 4, bar);
-                bulk_g2s(sl + C::O_KS, c.kscale + so, ngr * D * 4, bar);
-                bulk_g2s(sl + C::O_KZ, c.kzero + so, ngr * D * 4, bar);
-                bulk_g2s(sl + C::O_VW, c.vq + vo * C::DW, n * C::DW * 4, bar);
-                bulk_g2s(sl + C::O_VS, c.vscale + vo * NG, n * NG * 4, bar);
-                bulk_g2s(sl + C::O_VZ, c.vzero + vo * NG, n * NG * 4, bar);
+                const uint32_t bw = (uint32_t)(n / C::PK) * (D * 4), bs = (uint32_t)ngr * (D * 4);
+                const uint32_t bv = (uint32_t)n * (C::DW * 4), bz = (uint32_t)(n * NG) * 4u;
+                mbar_arrive_tx_a(bar, bw + 2 * bs + bv + 2 * bz);
+                bulk_g2s_a(sb + C::O_KW, kq_r + (t0 / C::PK) * D, bw, bar);
+                bulk_g2s_a(sb + C::O_KS, ks_r + g0 * D, bs, bar);
+                bulk_g2s_a(sb + C::O_KZ, kz_r + g0 * D, bs, bar);
+                bulk_g2s_a(sb + C::O_VW, vq_r + t0 * C::DW, bv, bar);
+                bulk_g2s_a(sb + C::O_VS, vs_r + t0 * NG, bz, bar);
+                bulk_g2s_a(sb + C::O_VZ, vz_r + t0 * NG, bz, bar);
             } else {
                 // ring slots of tokens t0 .. t0+n-1: contiguous up to the ring's end
-                const int RG = c.R + c.G;
+                const int t0 = w.Tq + (w.j - w.nq) * C::RT, n = min(C::RT, w.len - t0);
                 const int s0 = t0 % RG, n1 = min(n, RG - s0);
-                const size_t ring = bh * RG * D;
-                mbar_arrive_tx(bar, 2 * n * D * 2);
-                bulk_g2s(sl + C::O_KR, c.kres + ring + (size_t)s0 * D, n1 * D * 2, bar);
-                bulk_g2s(sl + C::O_VR, c.vres + ring + (size_t)s0 * D, n1 * D * 2, bar);
+                mbar_arrive_tx_a(bar, 2u * n * D * 2);
+                bulk_g2s_a(sb + C::O_KR, kr_r + s0 * D, n1 * D * 2, bar);
+                bulk_g2s_a(sb + C::O_VR, vr_r + s0 * D, n1 * D * 2, bar);
                 if (n1 < n) {
-                    bulk_g2s(sl + C::O_KR + n1 * C::RROW, c.kres + ring, (n - n1) * D * 2, bar);
-                    bulk_g2s(sl + C::O_VR + n1 * C::RROW, c.vres + ring, (n - n1) * D * 2, bar);
+                    bulk_g2s_a(sb + C::O_KR + n1 * C::RROW, kr_r, (n - n1) * D * 2, bar);
+                    bulk_g2s_a(sb + C::O_VR + n1 * C::RROW, vr_r, (n - n1) * D * 2, bar);
                 }
             }
             ++issued;
-            walk_next(w, c, RB, C::TS, C::RT);
+            new_row = ++w.j >= w.nt;
+            if (new_row) {
+                --w.j;
+                walk_next(w, c, RB, C::TS, C::RT);
+            }
             if (++slot == ns) {
                 slot = 0;
                 ++round;
