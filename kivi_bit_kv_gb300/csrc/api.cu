@@ -6,6 +6,7 @@
 // unknown preset (vllm/model_executor/layers/quantization/turboquant/config.py,
 // `from_cache_dtype`).
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include <cstdarg>
 #include <cstdio>
@@ -37,6 +38,16 @@ int32_t ok()
 }
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// An NVTX range around each call that launches work, named after the call,
+// so that a timeline tool shows the host call above its kernels (the NVTX
+// calls do nothing unless such a tool is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange&) = delete;
+    NvtxRange& operator=(const NvtxRange&) = delete;
+};
 bool bits_ok(int b) { return b == 2 || b == 4 || b == 8; }
 
 int32_t check_sizes(const kivi_cache* c)
@@ -166,6 +177,7 @@ size_t kivi_cache_bytes(int32_t T, int32_t D, int32_t bits, int32_t G, int32_t R
 int32_t kivi_quant_keys(const kivi_cache* c, const uint16_t* K, int32_t T,
                         const int32_t* seq_lens, void* stream)
 {
+    NvtxRange range_("kivi_quant_keys");
     int32_t st = check_cache(c);
     if (st != KIVI_OK)
         return st;
@@ -181,6 +193,7 @@ int32_t kivi_quant_keys(const kivi_cache* c, const uint16_t* K, int32_t T,
 int32_t kivi_quant_values(const kivi_cache* c, const uint16_t* V, int32_t T,
                           const int32_t* seq_lens, void* stream)
 {
+    NvtxRange range_("kivi_quant_values");
     int32_t st = check_cache(c);
     if (st != KIVI_OK)
         return st;
@@ -196,6 +209,7 @@ int32_t kivi_quant_values(const kivi_cache* c, const uint16_t* V, int32_t T,
 int32_t kivi_dequant(const kivi_cache* c, int32_t which, uint16_t* out, int32_t T_out,
                      void* stream)
 {
+    NvtxRange range_("kivi_dequant");
     int32_t st = check_cache(c);
     if (st != KIVI_OK)
         return st;
@@ -211,6 +225,7 @@ int32_t kivi_dequant(const kivi_cache* c, int32_t which, uint16_t* out, int32_t 
 int32_t kivi_append_token(const kivi_cache* c, const uint16_t* k, const uint16_t* v,
                           int32_t* status, void* stream)
 {
+    NvtxRange range_("kivi_append_token");
     int32_t st = check_cache(c);
     if (st != KIVI_OK)
         return st;
@@ -265,6 +280,7 @@ extern "C" {
 int32_t kivi_decode_qk(const kivi_cache* c, const uint16_t* q, int32_t Hq, float sm_scale,
                        float* logits, int32_t ld_logits, void* stream)
 {
+    NvtxRange range_("kivi_decode_qk");
     int32_t st = check_cache(c);
     if (st != KIVI_OK || (st = check_heads(c, Hq)) != KIVI_OK ||
         (st = check_ptr(q, "q")) != KIVI_OK || (st = check_logits(c, logits, ld_logits)) != KIVI_OK)
@@ -284,6 +300,7 @@ size_t kivi_workspace_bytes(const kivi_cache* c, int32_t Hq)
 int32_t kivi_decode_pv(const kivi_cache* c, const float* logits, int32_t ld_logits, int32_t Hq,
                        float* out, void* ws, size_t ws_bytes_given, void* stream)
 {
+    NvtxRange range_("kivi_decode_pv");
     int32_t st = check_cache(c);
     if (st != KIVI_OK || (st = check_heads(c, Hq)) != KIVI_OK ||
         (st = check_logits(c, logits, ld_logits)) != KIVI_OK ||
@@ -303,6 +320,7 @@ int32_t kivi_decode_pv(const kivi_cache* c, const float* logits, int32_t ld_logi
 int32_t kivi_decode_attention(const kivi_cache* c, const uint16_t* q, int32_t Hq, float sm_scale,
                               float* out, void* ws, size_t ws_bytes_given, void* stream)
 {
+    NvtxRange range_("kivi_decode_attention");
     int32_t st = check_cache(c);
     if (st != KIVI_OK || (st = check_heads(c, Hq)) != KIVI_OK || (st = check_ptr(q, "q")) != KIVI_OK ||
         (st = check_ptr(out, "out")) != KIVI_OK || (st = check_ptr(ws, "ws")) != KIVI_OK)
@@ -365,6 +383,7 @@ static int32_t check_payload_buffer(const void* p, size_t bytes, const kivi_cach
 
 int32_t kivi_export(const kivi_cache* c, void* dst, size_t dst_bytes, int32_t* status, void* stream)
 {
+    NvtxRange range_("kivi_export");
     int32_t st = check_cache(c);
     if (st != KIVI_OK)
         return st;
@@ -377,6 +396,7 @@ int32_t kivi_export(const kivi_cache* c, void* dst, size_t dst_bytes, int32_t* s
 
 int32_t kivi_import(const kivi_cache* c, const void* src, size_t src_bytes, int32_t* status, void* stream)
 {
+    NvtxRange range_("kivi_import");
     int32_t st = check_cache(c);
     if (st != KIVI_OK)
         return st;
