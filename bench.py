@@ -37,6 +37,8 @@ sys.path.insert(0, ROOT)
 METRIC = "KV quant/dequant GB/s (fp16-equiv) & decode-attn tok/s; % of HBM roofline"
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 2 ** 20     # GB300 L2
+ROTATE_MIN_BYTES = 2 * L2_BYTES  # decode-only working sets rotate over at least this much
 
 
 # ------------------------------------------------------------------ setup --
@@ -51,6 +53,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-c2c", action="store_true")
+    p.add_argument("--no-workloads", action="store_true",
+                   help="skip the other workloads' per-kernel lines (run before the headline timing)")
+    p.add_argument("--workload-steps", type=int, default=200)
     p.add_argument("--decode", default="fused", choices=["fused", "split"],
                    help="decode through kivi_decode_attention (fused) or kivi_decode_qk + kivi_decode_pv")
     return p.parse_args()
@@ -245,6 +250,123 @@ def whole_job_value(bytes_per_rank: float, world: int, ms_per_step: float) -> fl
 
 # --------------------------------------------------------------- GPU arm --
 
+def cache_copies(w, lens, Tmax) -> int:
+    """Caches a decode-only workload rotates over, so that one step's packed
+    cache is gone from L2 when it comes round again (the copies together
+    hold at least twice the L2)."""
+    per = sum(w.H * (slice_bytes(w, int(n), 0) + slice_bytes(w, int(n), 1)) for n in lens)
+    return max(1, -(-ROTATE_MIN_BYTES // max(1, per)))
+
+
+def l2_note(kind: str, copies: int, per_copy: int) -> str:
+    if kind in ("full", "store"):
+        return "fp16 K/V and packed cache of a step larger than 2x L2 (no flush needed)"
+    if copies == 1:
+        return f"packed cache {per_copy / 2**20:.0f} MB, larger than 2x L2 (no rotation needed)"
+    return (f"{copies} caches of {per_copy / 2**20:.0f} MB rotated step by step "
+            f"({copies * per_copy / 2**20:.0f} MB, at least 2x L2)")
+
+
+def run_secondary(name, steps, warmup, dev, decode="fused") -> dict:
+    """Per-call times, algorithmic bytes and roofline fractions of another
+    workload, measured the same way as the headline one (bounded steps)."""
+    import numpy as np
+    import torch
+    from kivi_bit_kv_gb300 import KiviCache, abi
+    from kivi_bit_kv_gb300 import workloads as W
+    w = W.WORKLOADS[name]
+    kind = KINDS[name]
+    calls = step_calls(w, kind, decode)
+    grows = kind in ("decode", "stream")
+    lens0 = W.make_lengths(w).numpy().astype(np.int64)
+    n_app = warmup + steps if grows else 1
+    Tmax = (int(lens0.max()) + n_app + w.G) // w.G * w.G + w.G
+    seq_lens = None if w.ragged is None else torch.as_tensor(lens0.astype(np.int32), device=dev)
+    K, V = W.make_kv(w, device=dev)
+    ncp = cache_copies(w, lens0, Tmax) if grows else 1
+    caches = [KiviCache(w.B, w.H, w.D, w.bits_k, w.bits_v, w.G, w.R, Tmax, device=dev) for _ in range(ncp)]
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
+    ld = (Tmax + 3) // 4 * 4
+    logits = torch.empty((w.B, w.Hq, ld), dtype=torch.float32, device=dev) if decode == "split" else None
+    wss = [c.workspace(w.Hq) for c in caches]
+    if grows:
+        for c in caches:
+            abi.kivi_quant_keys(c, K, seq_lens)
+            abi.kivi_quant_values(c, V, seq_lens)
+        torch.cuda.synchronize(dev)
+        del K, V
+        torch.cuda.empty_cache()
+        kh = vh = None
+    else:
+        kh = torch.empty((w.B, w.H, w.T, w.D), dtype=torch.float16, device=dev)
+        vh = torch.empty_like(kh)
+    kn, vn = W.make_step_tokens(w, n_app, device=dev)
+    qs = torch.stack([W.make_q(w, dev, step=s) for s in range(n_app)]) if grows else W.make_q(w, dev)[None]
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i, ev=None):
+        c = caches[i % ncp]
+        j = i if grows else 0
+        fns = {
+            "quant_keys": lambda: abi.kivi_quant_keys(c, K, seq_lens),
+            "quant_values": lambda: abi.kivi_quant_values(c, V, seq_lens),
+            "dequant_keys": lambda: abi.kivi_dequant(c, 0, kh),
+            "dequant_values": lambda: abi.kivi_dequant(c, 1, vh),
+            "append": lambda: abi.kivi_append_token(c, kn[j], vn[j], status),
+            "decode_qk": lambda: abi.kivi_decode_qk(c, qs[j], logits),
+            "decode_pv": lambda: abi.kivi_decode_pv(c, logits, out, wss[i % ncp]),
+            "decode_attn": lambda: abi.kivi_decode_attention(c, qs[j], out, wss[i % ncp]),
+        }
+        for c_i, nm in enumerate(calls):
+            if ev is not None:
+                ev[2 * c_i].record(stream)
+            fns[nm]()
+            if ev is not None:
+                ev[2 * c_i + 1].record(stream)
+
+    for i in range(warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2 * len(calls))] for _ in range(steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for s_ in range(steps):
+        step(warmup + s_, evs[s_])
+    t1.record(stream)
+    torch.cuda.synchronize(dev)
+    assert int(status.item()) == 0, "a sequence ran out of capacity"
+    if "decode_attn" in calls:
+        for ws_ in wss:
+            assert int(ws_[:1].view(torch.int32).item()) == 0, "decode status word"
+    per_call = {c: sum(evs[s_][2 * i].elapsed_time(evs[s_][2 * i + 1]) for s_ in range(steps)) / steps
+                for i, c in enumerate(calls)}
+    ms_step = t0.elapsed_time(t1) / steps
+    if grows:
+        timed = [lens0 + (warmup + s_) // ncp + 1 for s_ in range(steps)]
+        pick = timed[:: max(1, len(timed) // 16)]
+        ab_list = [call_bytes(w, d, d) for d in pick]
+        ab = {k: sum(a[k] for a in ab_list) / len(ab_list) for k in ab_list[0]}
+    else:
+        ab = call_bytes(w, lens0, lens0 + 1)
+    hbm, _ = peaks()
+    kernels = {}
+    for c in calls:
+        gbs = ab[c] / (per_call[c] * 1e-3) / 1e9
+        kernels[c] = {"ms": round(per_call[c], 5), "alg_bytes": int(ab[c]), "gbs": round(gbs, 1),
+                      "frac": round(gbs / hbm, 3)}
+    per_copy = sum(w.H * (slice_bytes(w, int(n), 0) + slice_bytes(w, int(n), 1)) for n in lens0)
+    res = {"step": kind, "shape": [w.B, w.H, w.T, w.D], "Hq": w.Hq, "bits_k": w.bits_k, "bits_v": w.bits_v,
+           "steps": steps, "warmup": warmup, "ms_per_step": round(ms_step, 5), "kernels": kernels,
+           "l2": l2_note(kind, ncp, per_copy)}
+    if kind != "store":
+        dec_ms = sum(per_call[c] for c in calls if c.startswith("decode"))
+        res["decode_tok_s"] = round(w.B / (dec_ms * 1e-3), 1)
+    del caches, wss
+    torch.cuda.empty_cache()
+    return res
+
+
 def run_kivi(args, rank, world, local):
     import numpy as np
     import torch
@@ -258,27 +380,39 @@ def run_kivi(args, rank, world, local):
         dist.init_process_group("nccl" if dist.is_nccl_available() else "gloo")
     w = W.WORKLOADS[args.workload]
     kind = KINDS[w.name]
+    # the other workloads first, one after another on this GPU (their lines
+    # go into "workloads"); they also bring the clocks to their loaded state
+    others = {}
+    if world == 1 and not args.no_workloads:
+        for name in ("prefix_store_int4", "prefix_store_int8", "mistral_gqa", "streaming"):
+            if name != w.name:
+                others[name] = run_secondary(name, args.workload_steps, max(3, args.warmup // 4), dev,
+                                             args.decode)
     calls = step_calls(w, kind, args.decode)
     grows = kind in ("decode", "stream")
     n_app = (args.warmup + args.steps) if grows else 1
     lens0 = W.make_lengths(w).numpy().astype(np.int64)
     Tmax = (int(lens0.max()) + n_app + w.G) // w.G * w.G + w.G
     K, V = W.make_kv(w, device=dev)
-    cache = KiviCache(w.B, w.H, w.D, w.bits_k, w.bits_v, w.G, w.R, Tmax, device=dev)
+    ncp = cache_copies(w, lens0, Tmax) if grows else 1
+    caches = [KiviCache(w.B, w.H, w.D, w.bits_k, w.bits_v, w.G, w.R, Tmax, device=dev) for _ in range(ncp)]
+    cache = caches[0]
     seq_lens = None if w.ragged is None else torch.as_tensor(lens0.astype(np.int32), device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     ld = (Tmax + 3) // 4 * 4
     logits = torch.empty((w.B, w.Hq, ld), dtype=torch.float32, device=dev)
     out = torch.empty((w.B, w.Hq, w.D), dtype=torch.float32, device=dev)
-    ws = cache.workspace(w.Hq)
+    wss = [c.workspace(w.Hq) for c in caches]
+    ws = wss[0]
     kn, vn = W.make_step_tokens(w, n_app, device=dev)
     qs = torch.stack([W.make_q(w, dev, step=s) for s in range(n_app)]) if grows else W.make_q(w, dev)[None]
     if kind in ("full", "store"):
         kh = torch.empty((w.B, w.H, w.T, w.D), dtype=torch.float16, device=dev)
         vh = torch.empty_like(kh)
     else:  # encode the prefix once; the timed steps only append and decode
-        abi.kivi_quant_keys(cache, K, seq_lens)
-        abi.kivi_quant_values(cache, V, seq_lens)
+        for c in caches:
+            abi.kivi_quant_keys(c, K, seq_lens)
+            abi.kivi_quant_values(c, V, seq_lens)
         torch.cuda.synchronize(dev)
         del K, V
         torch.cuda.empty_cache()
@@ -286,15 +420,16 @@ def run_kivi(args, rank, world, local):
 
     def step(i, ev=None):
         j = i if grows else 0
+        c, wsc = caches[i % ncp], wss[i % ncp]
         fns = {
-            "quant_keys": lambda: abi.kivi_quant_keys(cache, K, seq_lens),
-            "quant_values": lambda: abi.kivi_quant_values(cache, V, seq_lens),
-            "dequant_keys": lambda: abi.kivi_dequant(cache, 0, kh),
-            "dequant_values": lambda: abi.kivi_dequant(cache, 1, vh),
-            "append": lambda: abi.kivi_append_token(cache, kn[j], vn[j], status),
-            "decode_qk": lambda: abi.kivi_decode_qk(cache, qs[j], logits),
-            "decode_pv": lambda: abi.kivi_decode_pv(cache, logits, out, ws),
-            "decode_attn": lambda: abi.kivi_decode_attention(cache, qs[j], out, ws),
+            "quant_keys": lambda: abi.kivi_quant_keys(c, K, seq_lens),
+            "quant_values": lambda: abi.kivi_quant_values(c, V, seq_lens),
+            "dequant_keys": lambda: abi.kivi_dequant(c, 0, kh),
+            "dequant_values": lambda: abi.kivi_dequant(c, 1, vh),
+            "append": lambda: abi.kivi_append_token(c, kn[j], vn[j], status),
+            "decode_qk": lambda: abi.kivi_decode_qk(c, qs[j], logits),
+            "decode_pv": lambda: abi.kivi_decode_pv(c, logits, out, wsc),
+            "decode_attn": lambda: abi.kivi_decode_attention(c, qs[j], out, wsc),
         }
         for c_i, name in enumerate(calls):
             if ev is not None:
@@ -320,13 +455,16 @@ def run_kivi(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     assert int(status.item()) == 0, "a sequence ran out of capacity"
+    if "decode_attn" in calls:
+        for wsc in wss:
+            assert int(wsc[:1].view(torch.int32).item()) == 0, "decode status word"
     per_call = {c: sum(evs[s][2 * i].elapsed_time(evs[s][2 * i + 1]) for s in range(args.steps)) / args.steps
                 for i, c in enumerate(calls)}
     ms_step = reduce_max(t0.elapsed_time(t1), dev) / args.steps
 
     # bytes per step, averaged over the timed steps (decode caches grow)
     if grows:
-        timed = [lens0 + args.warmup + s + 1 for s in range(args.steps)]
+        timed = [lens0 + (args.warmup + s) // ncp + 1 for s in range(args.steps)]
         pick = timed[:: max(1, len(timed) // 16)]
         ab_list = [call_bytes(w, d, d) for d in pick]
         ab = {k: sum(a[k] for a in ab_list) / len(ab_list) for k in ab_list[0]}
@@ -366,7 +504,8 @@ def run_kivi(args, rank, world, local):
                    "bits_k": w.bits_k, "bits_v": w.bits_v, "G": w.G, "R": w.R,
                    "ragged": list(w.ragged) if w.ragged else None,
                    "parallelism": f"replicas x{world}",
-                   "l2": "packed cache and fp16 K/V larger than L2 (no flush needed)"},
+                   "l2": l2_note(kind, ncp, sum(w.H * (slice_bytes(w, int(n), 0) + slice_bytes(w, int(n), 1))
+                                                for n in lens0))},
         "breakdown": breakdown,
         "roofline": {"bound": "hbm", "kernel": dominant, "achieved": dk["gbs"], "peak": hbm,
                      "peak_source": src, "unit": "GB/s", "frac": dk["frac"],
@@ -374,6 +513,8 @@ def run_kivi(args, rank, world, local):
         "gpu_launches": sum(LAUNCHES[c] for c in calls) * args.steps,
         "clocks": clk.summary(),
     }
+    if others:
+        line["workloads"] = others
     if kind == "full" and not args.no_e2e:
         line["e2e"] = run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq, calls)
     if kind == "full" and not args.no_c2c:
@@ -436,7 +577,7 @@ def run_e2e(args, w, cache, kh, vh, logits, out, ws, status, dev, world, eq, cal
     copy = torch.cuda.Stream(dev)
     ready = [torch.cuda.Event() for _ in range(2)]  # inputs of the buffer copied
     free = [torch.cuda.Event() for _ in range(2)]   # the buffer's last step done
-    n = max(3, args.steps // 20)
+    n = max(20, args.steps // 10)
 
     def issue_copy(i):
         b = i % 2
@@ -522,22 +663,33 @@ def _slice_fp16eq(w, T):
     return 2 * T * w.D * 2 * 3 + 2 * w.D * 2
 
 
-def cpu_baseline(w, K, V, q, kn, vn, budget_s: float = 10.0):
-    """The oracle as it stands on a bounded sample (about 10 s of CPU work)."""
-    from oracle import ref as R
-    cores = R.host_threads()
-    Ks, Vs, qs, ks, vs = _sample(w, K, V, q, kn, vn, cores, w.T)
+def _oracle_rate(R, w, K, V, q, kn, vn, threads: int, budget_s: float):
+    """fp16-equivalent GB/s of the oracle on `threads` host threads, over
+    rounds of `threads` (b, h) slices until budget_s has passed."""
+    Ks, Vs, qs, ks, vs = _sample(w, K, V, q, kn, vn, threads, w.T)
     done, t_start = 0, time.perf_counter()
     while True:
-        _oracle_pass(R, w, Ks, Vs, qs, ks, vs, cores)
+        _oracle_pass(R, w, Ks, Vs, qs, ks, vs, threads)
         done += 1
         el = time.perf_counter() - t_start
         if el >= budget_s:
             break
-    value = done * cores * _slice_fp16eq(w, w.T) / el / 1e9
+    return done * threads * _slice_fp16eq(w, w.T) / el / 1e9, done, el
+
+
+def cpu_baseline(w, K, V, q, kn, vn, budget_s: float = 10.0):
+    """The oracle as it stands on a bounded sample (about 10 s of CPU work
+    each): on every host core (the baseline of record) and on one thread."""
+    from oracle import ref as R
+    cores = R.host_threads()
+    value, done, el = _oracle_rate(R, w, K, V, q, kn, vn, cores, budget_s)
+    v1, done1, el1 = _oracle_rate(R, w, K, V, q, kn, vn, 1, budget_s)
     return {"value": round(value, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{done} rounds x {cores} (b,h) slices of {w.name} ({w.T} tokens each, full step "
-                      f"per slice: encode, materialize K and V, append, decode), {el:.1f} s"}
+                      f"per slice: encode, materialize K and V, append, decode), {el:.1f} s",
+            "single_thread": {"value": round(v1, 4), "unit": UNIT, "cores": 1,
+                              "sample": f"{done1} rounds x 1 slice, {el1:.1f} s"},
+            "of_record": "all cores"}
 
 
 def run_reference(args, rank, world):

@@ -67,6 +67,8 @@ extern "C" {
 #define KIVI_ECUDA      3 /* the CUDA launch reported an error                  */
 #define KIVI_ETIMEOUT   4 /* a bounded device wait gave up (workspace status)  */
 #define KIVI_EWORKSPACE 5 /* workspace smaller than kivi_workspace_bytes()      */
+#define KIVI_ECHECK     6 /* a device bounds check failed (a library built with
+                             KIVI_CHECKS defined; workspace status)           */
 
 /*
  * Cache descriptor: a plain struct of sizes and device pointers, owned and

@@ -14,7 +14,9 @@ import os
 import torch
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libkivi.so")
+# KIVI_LIB selects another in-tree build of the library (the bounds-checked
+# one, libkivi_checked.so); by default libkivi.so next to this file.
+LIB_PATH = os.environ.get("KIVI_LIB") or os.path.join(HERE, "libkivi.so")
 
 KIVI_OK = 0
 KIVI_EINVAL = 1
@@ -22,6 +24,7 @@ KIVI_ECAPACITY = 2
 KIVI_ECUDA = 3
 KIVI_ETIMEOUT = 4
 KIVI_EWORKSPACE = 5
+KIVI_ECHECK = 6
 
 (KIVI_BUF_KQ, KIVI_BUF_KSCALE, KIVI_BUF_KZERO, KIVI_BUF_VQ, KIVI_BUF_VSCALE, KIVI_BUF_VZERO,
  KIVI_BUF_KRES, KIVI_BUF_VRES, KIVI_BUF_LEN) = range(9)

@@ -41,23 +41,38 @@ def _deps() -> list[str]:
             + glob.glob(os.path.join(INCLUDE, "*.h")) + [__file__])
 
 
-def needs_build() -> bool:
-    if not os.path.exists(LIB):
+# Variants: "" (the library) and "checked" (KIVI_CHECKS defined: the streamed
+# decode checks every copy range, tile and output row on the device and
+# reports a failed check as KIVI_ECHECK in its workspace status word).
+VARIANT_FLAGS = {"": [], "checked": ["-DKIVI_CHECKS"]}
+
+
+def lib_path(variant: str = "") -> str:
+    return LIB if not variant else os.path.join(HERE, f"libkivi_{variant}.so")
+
+
+def needs_build(variant: str = "") -> bool:
+    lib = lib_path(variant)
+    if not os.path.exists(lib):
         return True
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return any(os.path.getmtime(p) > t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None) -> str:
-    """Compile libkivi.so if missing or stale; return its path."""
-    if not (force or needs_build()):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | None = None,
+          variant: str = "") -> str:
+    """Compile libkivi.so (or the variant's library) if missing or stale;
+    return its path."""
+    lib = lib_path(variant)
+    if not (force or needs_build(variant)):
+        return lib
+    bdir = BUILD if not variant else BUILD + "_" + variant
+    os.makedirs(bdir, exist_ok=True)
     nv = nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + VARIANT_FLAGS[variant] + list(extra_flags or [])
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [nv, *ARCH, *flags, "-c", src, "-o", obj]
         if verbose:
             cmd += ["-Xptxas", "-v"]
@@ -71,13 +86,13 @@ def build(force: bool = False, verbose: bool = False, extra_flags: list[str] | N
     srcs = sources()
     with ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nv, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart_static", "-lrt", "-ldl", "-lpthread"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":

@@ -130,6 +130,7 @@ const char* kivi_status_string(int32_t status)
     case KIVI_ECUDA: return "CUDA error";
     case KIVI_ETIMEOUT: return "device wait timed out";
     case KIVI_EWORKSPACE: return "workspace too small";
+    case KIVI_ECHECK: return "device bounds check failed";
     default: return "unknown status";
     }
 }

@@ -108,6 +108,21 @@ __device__ __forceinline__ void mbar_arrive_tx_a(uint32_t bar, uint32_t bytes)
 }
 constexpr uint64_t kStreamWaitNs = 2000000000ull;  // a wait on a stage gives up after 2 s
 
+// Bounds checks of a library built with KIVI_CHECKS defined: a failed check
+// records KIVI_ECHECK in the workspace status word (the first failure wins;
+// the host clears the word before the launch) and the access it guards is
+// skipped.  Without KIVI_CHECKS every check is true and compiles away.
+#ifdef KIVI_CHECKS
+__device__ __forceinline__ bool kivi_check(bool ok, int* status)
+{
+    if (!ok)
+        atomicCAS(status, KIVI_OK, KIVI_ECHECK);
+    return ok;
+}
+#else
+__device__ __forceinline__ bool kivi_check(bool, int*) { return true; }
+#endif
+
 // Nanoseconds of the global timer.
 __device__ __forceinline__ uint64_t global_ns()
 {
@@ -1055,8 +1070,10 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
             merged[i] = i - C::NMB;
         }
         next_tile = 0ull;
+#ifndef KIVI_CHECKS
         if (blockIdx.x == 0)
             wsi[0] = KIVI_OK;  // status word: KIVI_ETIMEOUT if a bounded wait gives up
+#endif
     }
     __syncthreads();
     const long long ntiles = r1.g - r0.g;
@@ -1111,23 +1128,42 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
                 const int g0 = t0 >> lgG, ngr = ((t0 + n - 1) >> lgG) - g0 + 1;
                 const uint32_t bw = (uint32_t)(n / C::PK) * (D * 4), bs = (uint32_t)ngr * (D * 4);
                 const uint32_t bv = (uint32_t)n * (C::DW * 4), bz = (uint32_t)(n * NG) * 4u;
-                mbar_arrive_tx_a(bar, bw + 2 * bs + bv + 2 * bz);
-                bulk_g2s_a(sb + C::O_KW, kq_r + (t0 / C::PK) * D, bw, bar);
-                bulk_g2s_a(sb + C::O_KS, ks_r + g0 * D, bs, bar);
-                bulk_g2s_a(sb + C::O_KZ, kz_r + g0 * D, bs, bar);
-                bulk_g2s_a(sb + C::O_VW, vq_r + t0 * C::DW, bv, bar);
-                bulk_g2s_a(sb + C::O_VS, vs_r + t0 * NG, bz, bar);
-                bulk_g2s_a(sb + C::O_VZ, vz_r + t0 * NG, bz, bar);
+                // the tile lies in the row's quantized tokens and in Tmax, each copy in its region
+                if (kivi_check(w.b < c.B && w.rr < RB && t0 >= 0 && n > 0 && t0 + n <= w.Tq &&
+                                   w.Tq <= c.Tmax && t0 % C::PK == 0 && n % C::PK == 0 &&
+                                   g0 + ngr <= (c.Tmax >> lgG) && C::O_KW + bw <= (uint32_t)C::O_KS &&
+                                   C::O_KS + bs <= (uint32_t)C::O_KZ && C::O_KZ + bs <= (uint32_t)C::O_VW &&
+                                   C::O_VW + bv <= (uint32_t)C::O_VS && C::O_VS + bz <= (uint32_t)C::O_VZ &&
+                                   C::O_VZ + bz <= (uint32_t)C::SLOT,
+                               wsi)) {
+                    mbar_arrive_tx_a(bar, bw + 2 * bs + bv + 2 * bz);
+                    bulk_g2s_a(sb + C::O_KW, kq_r + (t0 / C::PK) * D, bw, bar);
+                    bulk_g2s_a(sb + C::O_KS, ks_r + g0 * D, bs, bar);
+                    bulk_g2s_a(sb + C::O_KZ, kz_r + g0 * D, bs, bar);
+                    bulk_g2s_a(sb + C::O_VW, vq_r + t0 * C::DW, bv, bar);
+                    bulk_g2s_a(sb + C::O_VS, vs_r + t0 * NG, bz, bar);
+                    bulk_g2s_a(sb + C::O_VZ, vz_r + t0 * NG, bz, bar);
+                } else {
+                    mbar_arrive(&full[slot]);  // the stage completes without data
+                }
             } else {
                 // ring slots of tokens t0 .. t0+n-1: contiguous up to the ring's end
                 const int t0 = w.Tq + (w.j - w.nq) * C::RT, n = min(C::RT, w.len - t0);
                 const int s0 = t0 % RG, n1 = min(n, RG - s0);
-                mbar_arrive_tx_a(bar, 2u * n * D * 2);
-                bulk_g2s_a(sb + C::O_KR, kr_r + s0 * D, n1 * D * 2, bar);
-                bulk_g2s_a(sb + C::O_VR, vr_r + s0 * D, n1 * D * 2, bar);
-                if (n1 < n) {
-                    bulk_g2s_a(sb + C::O_KR + n1 * C::RROW, kr_r, (n - n1) * D * 2, bar);
-                    bulk_g2s_a(sb + C::O_VR + n1 * C::RROW, vr_r, (n - n1) * D * 2, bar);
+                // the tile lies in the row's residual tokens, inside the ring, each copy in its region
+                if (kivi_check(w.b < c.B && w.rr < RB && t0 >= w.Tq && n > 0 && n <= C::RT &&
+                                   t0 + n <= w.len && n <= RG && s0 + n1 <= RG && n - n1 <= s0 &&
+                                   C::O_KR + n * C::RROW <= C::O_VR && C::O_VR + n * C::RROW <= C::SLOT,
+                               wsi)) {
+                    mbar_arrive_tx_a(bar, 2u * n * D * 2);
+                    bulk_g2s_a(sb + C::O_KR, kr_r + s0 * D, n1 * D * 2, bar);
+                    bulk_g2s_a(sb + C::O_VR, vr_r + s0 * D, n1 * D * 2, bar);
+                    if (n1 < n) {
+                        bulk_g2s_a(sb + C::O_KR + n1 * C::RROW, kr_r, (n - n1) * D * 2, bar);
+                        bulk_g2s_a(sb + C::O_VR + n1 * C::RROW, vr_r, (n - n1) * D * 2, bar);
+                    }
+                } else {
+                    mbar_arrive(&full[slot]);
                 }
             }
             ++issued;
@@ -1212,6 +1248,7 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
             const unsigned mask = (unsigned)*(volatile int*)&pmask[buf];
             float* dst_o;
             float* dst_ml = nullptr;
+            const bool row_ok = kivi_check(o_b < c.B && o_hq0 + NQB <= Hq && (int)blockIdx.x < kMaxStreamCTAs, wsi);
             if (whole) {
                 dst_o = out + ((size_t)o_b * Hq + o_hq0) * D;
             } else {
@@ -1220,6 +1257,8 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
             }
 #pragma unroll
             for (int hh = 0; hh < NQB; ++hh) {
+                if (!row_ok)
+                    break;
                 float M = -INFINITY;
 #pragma unroll
                 for (int cw = 0; cw < NC; ++cw)
@@ -1330,7 +1369,11 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
                 }
                 const uint16_t* qh = reinterpret_cast<const uint16_t*>(wq);
                 const int t0 = walk_t0(w, C::TS, C::RT), n = walk_n(w, C::TS, C::RT);
-                if (walk_quant(w)) {
+                if (!kivi_check(w.b < c.B && t0 >= 0 && n > 0 && t0 + n <= w.len &&
+                                    n <= (walk_quant(w) ? C::TS : C::RT),
+                                wsi)) {
+                    // nothing to compute
+                } else if (walk_quant(w)) {
                     if (n == C::TS)
                         consume_quant<BK, BV, NQB, D, C, true>(st, sl, qh, t0, n, lgG, sl2, lg, qw, ub);
                     else
@@ -1404,6 +1447,10 @@ decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __
     const int h = r1.rr / NP, pass = r1.rr - h * NP;
     float* dst = out + ((size_t)r1.b * Hq + h * NQ + pass * NQB) * D;
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // the pieces are the grid's partial slots, the row one of the output's
+    if (!kivi_check(last < N && P >= 1 && r1.b < c.B && h * NQ + pass * NQB + NQB <= Hq,
+                    reinterpret_cast<int*>(const_cast<float*>(ws))))
+        return;
 
     constexpr int ND = (D + T - 1) / T;  // channels per thread
     float M[NQB], L[NQB], o[NQB][ND];
@@ -1498,6 +1545,12 @@ cudaError_t stream_launch(const kivi_cache& c, const uint16_t* q, int Hq, float 
     if (e != cudaSuccess)
         return e;
     const int N = cmin(sm_count(), kMaxStreamCTAs);
+#ifdef KIVI_CHECKS
+    // the status word starts at KIVI_OK before any CTA can record a check
+    e = cudaMemsetAsync(ws, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess)
+        return e;
+#endif
     {
         cudaLaunchConfig_t cf = {};
         cf.gridDim = dim3(N);

@@ -120,3 +120,22 @@ def test_reference_arm_runs_on_rank_0_only():
     from types import SimpleNamespace
     args = SimpleNamespace(workload="tiny", steps=1, warmup=1)
     assert bench.run_reference(args, rank=1, world=2) is None
+
+
+def test_decode_workloads_rotate_over_twice_the_l2():
+    """A decode-only workload whose packed cache would stay in L2 between
+    steps is timed over enough cache copies to hold at least 2x the L2."""
+    import numpy as np
+    from kivi_bit_kv_gb300 import workloads as W
+    for name in ("mistral_gqa", "streaming"):
+        w = W.WORKLOADS[name]
+        lens = W.make_lengths(w).numpy().astype(np.int64)
+        per = sum(w.H * (bench.slice_bytes(w, int(n), 0) + bench.slice_bytes(w, int(n), 1)) for n in lens)
+        n = bench.cache_copies(w, lens, w.Tmax)
+        assert n * per >= 2 * bench.L2_BYTES
+        assert (n - 1) * per < 2 * bench.L2_BYTES or n == 1
+        note = bench.l2_note(bench.KINDS[name], n, per)
+        assert ("rotated" in note) == (n > 1)
+    # the GQA cache (136 MB) is about one L2: it needs copies
+    w = W.WORKLOADS["mistral_gqa"]
+    assert bench.cache_copies(w, W.make_lengths(w).numpy(), w.Tmax) >= 2
