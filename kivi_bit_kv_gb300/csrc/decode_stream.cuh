@@ -174,6 +174,23 @@ constexpr int kStreamMaxStages = 32;          // stages of the ring (the consume
 // NQB query heads per pass, head dimension D and NC consumer warps.  Sizes
 // that depend on the group size G (32, 64 or 128) are taken at G = 32, the
 // largest.
+// Warp roles of the streamed decode: three warpgroups.  Warps 0..7 are the
+// consumers (NC of them take tiles, NC <= 8), warp 8 issues the key copies and
+// warp 9 the value copies of every stage, warps 10 and 11 only hand their
+// registers back.  The block is launched with 168 registers per thread
+// (384 threads); the consumer warpgroups then raise theirs to 224 and the
+// third lowers its to 56 (setmaxnreg): 2 x 128 x 224 + 128 x 56 = 384 x 168,
+// and each SM sub-partition holds two consumer warps and one other
+// (2 x 224 + 56 registers a lane, within its 16K).
+constexpr int kStreamWarps = 12;
+constexpr int kStreamConsumerWarps = 8;
+constexpr int kStreamLaunchRegs = 168;
+constexpr int kStreamConsumerRegs = 224;
+constexpr int kStreamOtherRegs = 56;
+static_assert(2 * 128 * kStreamConsumerRegs + 128 * kStreamOtherRegs == 32 * kStreamWarps * kStreamLaunchRegs,
+              "the register split uses exactly the registers the block is launched with");
+static_assert((2 * kStreamConsumerRegs + kStreamOtherRegs) * 32 <= 16384, "registers of one SM sub-partition");
+
 template <int BK, int BV, int NQB, int D, int NC>
 struct StreamCfg {
     using KT = KeyTile<BK, NQB>;
@@ -232,7 +249,7 @@ struct StreamCfg {
     static constexpr int M_END = round_up(M_Z + NC * NQB * NGM, 4);
     static constexpr int NMB = NC * NQB * D <= 2048 ? 4 : 2;
     static constexpr int FIXED_BYTES = 4 * (NC * WARP_FLOATS + NMB * M_END) + kStreamStaticSmem;
-    static constexpr int THREADS = 32 * (NC + 1);
+    static constexpr int THREADS = 32 * kStreamWarps;
     static_assert(TS % TOK == 0 && TS % 16 == 0 && RT % 16 == 0 && RT <= TS, "tile shape");
     static_assert(UB % 16 == 0 && TS % UB == 0, "weight batches");
     static_assert(UF % NQB == 0, "a fragment holds whole groups");
@@ -246,12 +263,10 @@ __host__ __device__ constexpr int stream_stages()
     return cmin((kStreamSmemBytes - C::FIXED_BYTES) / (C::SLOT + 16), kStreamMaxStages);
 }
 
-// Consumer warps of the streamed decode for a shape: up to seven (eight warps
-// with the producer, two per SM sub-partition, so each thread may hold up to
-// 255 registers), fewer when the shared memory would otherwise hold no more
-// stages than consumers -- every consumer then has a stage and at least one
-// more is in flight.
-constexpr int kStreamMaxConsumers = 7;
+// Consumer warps of the streamed decode for a shape: up to eight, fewer when
+// the shared memory would otherwise hold no more stages than consumers --
+// every consumer then has a stage and at least one more is in flight.
+constexpr int kStreamMaxConsumers = kStreamConsumerWarps;
 template <int BK, int BV, int NQB, int D, int NC = kStreamMaxConsumers>
 __host__ __device__ constexpr int stream_consumers()
 {
@@ -1020,7 +1035,7 @@ __device__ __forceinline__ void consume_quant(ConsumerState<C, NQB>& st, const u
 // ---------------------------------------------------------------- kernel ---
 
 template <int BK, int BV, int NQB, int D, int NC>
-__global__ void __launch_bounds__(32 * (NC + 1), 1)
+__global__ void __launch_bounds__(32 * kStreamWarps, 1)
 decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_scale,
                      float* __restrict__ out, float* __restrict__ ws)
 {
@@ -1058,7 +1073,7 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     locate_range<C::THREADS>(c, RB, C::TS, C::RT, blockIdx.x, gridDim.x, r0, r1, red, sh_range);
     if (threadIdx.x == 0) {
         for (int s = 0; s < ns; ++s) {
-            mbar_init(&full[s], 1);
+            mbar_init(&full[s], 2);  // the key and the value producer
             mbar_init(&empty[s], 1);
             consumed[s] = 0;
         }
@@ -1082,14 +1097,20 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     Walk w0{r0.b, r0.rr, r0.j, 0, 0, 0, 0};
     walk_load(w0, c, C::TS, C::RT);
 
-    if (warp == NC) {
-        // ------------------------------------------------------ producer
-        // Lane 0 issues every copy: six bulk copies per quantized stage.  The
-        // issuing thread's own latency per stage bounds the stream, so the
-        // row's base pointers are formed once per row, the offsets inside a
-        // row are 32-bit, and shared-memory addresses are kept converted.
-        if (lane != 0)
+    if (warp >= kStreamConsumerWarps) {
+        // the third warpgroup hands registers back (every warp of it, before
+        // any leaves)
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kStreamOtherRegs));
+        // ----------------------------------------------------- producers
+        // Lane 0 of warp 8 issues the key copies of every stage, lane 0 of
+        // warp 9 the value copies (three bulk copies each per quantized
+        // stage); each announces its own bytes on the stage's full barrier.
+        // The issuing thread's own latency per copy bounds the stream, hence
+        // two issuers, row base pointers formed once per row, 32-bit offsets
+        // inside a row and shared-memory addresses kept converted.
+        if (warp >= kStreamConsumerWarps + 2 || lane != 0)
             return;
+        const bool kp = warp == kStreamConsumerWarps;  // the key producer
         Walk w = w0;
         int slot = 0;
         uint32_t round = 0;
@@ -1129,22 +1150,24 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
                 const uint32_t bw = (uint32_t)(n / C::PK) * (D * 4), bs = (uint32_t)ngr * (D * 4);
                 const uint32_t bv = (uint32_t)n * (C::DW * 4), bz = (uint32_t)(n * NG) * 4u;
                 // the tile lies in the row's quantized tokens and in Tmax, each copy in its region
-                if (kivi_check(w.b < c.B && w.rr < RB && t0 >= 0 && n > 0 && t0 + n <= w.Tq &&
-                                   w.Tq <= c.Tmax && t0 % C::PK == 0 && n % C::PK == 0 &&
-                                   g0 + ngr <= (c.Tmax >> lgG) && C::O_KW + bw <= (uint32_t)C::O_KS &&
-                                   C::O_KS + bs <= (uint32_t)C::O_KZ && C::O_KZ + bs <= (uint32_t)C::O_VW &&
-                                   C::O_VW + bv <= (uint32_t)C::O_VS && C::O_VS + bz <= (uint32_t)C::O_VZ &&
-                                   C::O_VZ + bz <= (uint32_t)C::SLOT,
-                               wsi)) {
-                    mbar_arrive_tx_a(bar, bw + 2 * bs + bv + 2 * bz);
+                if (!kivi_check(w.b < c.B && w.rr < RB && t0 >= 0 && n > 0 && t0 + n <= w.Tq &&
+                                    w.Tq <= c.Tmax && t0 % C::PK == 0 && n % C::PK == 0 &&
+                                    g0 + ngr <= (c.Tmax >> lgG) && C::O_KW + bw <= (uint32_t)C::O_KS &&
+                                    C::O_KS + bs <= (uint32_t)C::O_KZ && C::O_KZ + bs <= (uint32_t)C::O_VW &&
+                                    C::O_VW + bv <= (uint32_t)C::O_VS && C::O_VS + bz <= (uint32_t)C::O_VZ &&
+                                    C::O_VZ + bz <= (uint32_t)C::SLOT,
+                                wsi)) {
+                    mbar_arrive(&full[slot]);  // the stage completes without data
+                } else if (kp) {
+                    mbar_arrive_tx_a(bar, bw + 2 * bs);
                     bulk_g2s_a(sb + C::O_KW, kq_r + (t0 / C::PK) * D, bw, bar);
                     bulk_g2s_a(sb + C::O_KS, ks_r + g0 * D, bs, bar);
                     bulk_g2s_a(sb + C::O_KZ, kz_r + g0 * D, bs, bar);
+                } else {
+                    mbar_arrive_tx_a(bar, bv + 2 * bz);
                     bulk_g2s_a(sb + C::O_VW, vq_r + t0 * C::DW, bv, bar);
                     bulk_g2s_a(sb + C::O_VS, vs_r + t0 * NG, bz, bar);
                     bulk_g2s_a(sb + C::O_VZ, vz_r + t0 * NG, bz, bar);
-                } else {
-                    mbar_arrive(&full[slot]);  // the stage completes without data
                 }
             } else {
                 // ring slots of tokens t0 .. t0+n-1: contiguous up to the ring's end
@@ -1155,13 +1178,12 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
                                    t0 + n <= w.len && n <= RG && s0 + n1 <= RG && n - n1 <= s0 &&
                                    C::O_KR + n * C::RROW <= C::O_VR && C::O_VR + n * C::RROW <= C::SLOT,
                                wsi)) {
-                    mbar_arrive_tx_a(bar, 2u * n * D * 2);
-                    bulk_g2s_a(sb + C::O_KR, kr_r + s0 * D, n1 * D * 2, bar);
-                    bulk_g2s_a(sb + C::O_VR, vr_r + s0 * D, n1 * D * 2, bar);
-                    if (n1 < n) {
-                        bulk_g2s_a(sb + C::O_KR + n1 * C::RROW, kr_r, (n - n1) * D * 2, bar);
-                        bulk_g2s_a(sb + C::O_VR + n1 * C::RROW, vr_r, (n - n1) * D * 2, bar);
-                    }
+                    const uint32_t o = kp ? C::O_KR : C::O_VR;
+                    const uint16_t* r = kp ? kr_r : vr_r;
+                    mbar_arrive_tx_a(bar, (uint32_t)n * D * 2);
+                    bulk_g2s_a(sb + o, r + s0 * D, n1 * D * 2, bar);
+                    if (n1 < n)
+                        bulk_g2s_a(sb + o + n1 * C::RROW, r, (n - n1) * D * 2, bar);
                 } else {
                     mbar_arrive(&full[slot]);
                 }
@@ -1188,6 +1210,10 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     }
 
     // ------------------------------------------------------------ consumer
+    // the two consumer warpgroups take the registers the third gave back
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kStreamConsumerRegs));
+    if (warp >= NC)
+        return;  // a consumer warp this shape has no shared memory for
     // The consumers take the range's tiles in order from a shared counter, so
     // a warp that falls behind (a merge, a slow tile) takes fewer of them and
     // holds up no one.  A row segment is the range's tiles of one row; a warp
@@ -1544,6 +1570,18 @@ cudaError_t stream_launch(const kivi_cache& c, const uint16_t* q, int Hq, float 
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
+    // the register split needs the block launched with kStreamLaunchRegs per
+    // thread: otherwise the consumers' setmaxnreg.inc could never be granted
+    static int launch_regs = -1;
+    if (launch_regs < 0) {
+        cudaFuncAttributes fa;
+        e = cudaFuncGetAttributes(&fa, kern);
+        if (e != cudaSuccess)
+            return e;
+        launch_regs = fa.numRegs;
+    }
+    if (launch_regs != kStreamLaunchRegs)
+        return cudaErrorInvalidConfiguration;
     const int N = cmin(sm_count(), kMaxStreamCTAs);
 #ifdef KIVI_CHECKS
     // the status word starts at KIVI_OK before any CTA can record a check

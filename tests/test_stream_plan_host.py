@@ -84,8 +84,8 @@ def test_every_shape_is_planned(plan):
 
 def test_stages_outnumber_consumers_and_fit(plan):
     for s in plan["shapes"]:
-        assert 1 <= s["NC"] <= 7, s
-        assert s["THREADS"] == 32 * (s["NC"] + 1)
+        assert 1 <= s["NC"] <= 8, s
+        assert s["THREADS"] == 384  # three warpgroups: 8 consumer warps, 2 producers, 2 idle
         assert s["ns"] >= s["NC"] + 1 and s["ns"] >= 2, s
         assert s["ns"] <= 32, s  # the per-slot consumed counters are a static array of 32
         dyn = s["ns"] * s["SLOT"] + s["FIXED"] - 512 + 2 * 8 * s["ns"]
