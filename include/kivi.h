@@ -354,6 +354,22 @@ int32_t kivi_export(const kivi_cache* c, void* dst, size_t dst_bytes,
 int32_t kivi_import(const kivi_cache* c, const void* src, size_t src_bytes,
                     int32_t* status, void* stream);
 
+/* ---------------------------------------------------- bounds-checked build */
+
+/*
+ * A library built with KIVI_CHECKS defined (the "checked" build variant)
+ * checks, on the device, every global access of the encode, materialize,
+ * append, payload and split-decode kernels against the arrays of the cache
+ * and the buffers of the call, and skips an access that falls outside them;
+ * the streamed fused decode checks its copies, tiles and output rows and
+ * reports in its workspace status word (kivi_decode_attention).  This call
+ * writes to *status (host memory) the status of the first failed check since
+ * the previous call -- KIVI_ECHECK -- or KIVI_OK, and clears the record.  It
+ * synchronizes the device.  In a library built without KIVI_CHECKS it writes
+ * KIVI_OK.  Returns KIVI_OK, KIVI_EINVAL (status is NULL) or KIVI_ECUDA.
+ */
+int32_t kivi_check_status(int32_t* status);
+
 #ifdef __cplusplus
 }
 #endif

@@ -36,6 +36,7 @@ EXPORTS = (
     "kivi_dequant", "kivi_append_token", "kivi_decode_qk", "kivi_decode_pv",
     "kivi_workspace_bytes", "kivi_decode_pv_noalloc", "kivi_decode_attention",
     "kivi_codec_fingerprint", "kivi_payload_bytes", "kivi_export", "kivi_import",
+    "kivi_check_status",
 )
 
 KIVI_PAYLOAD_MAGIC = 0x5056494B
@@ -98,6 +99,7 @@ def load(path: str | None = None):
         "kivi_payload_bytes": ([cp, vp], sz),
         "kivi_export": ([cp, vp, sz, vp, vp], i32),
         "kivi_import": ([cp, vp, sz, vp, vp], i32),
+        "kivi_check_status": ([C.POINTER(i32)], i32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(L, name)
@@ -320,3 +322,12 @@ def kivi_import(cache, src: torch.Tensor, status: torch.Tensor, stream=None):
     _check(load().kivi_import(C.byref(cache.desc), _payload_buf(src, "src", cache.device), src.numel(),
                               _dev(status, torch.int32, "status", cache.device),
                               _stream(stream, cache.device)), "kivi_import")
+
+
+def kivi_check_status() -> int:
+    """Status of the first failed device bounds check since the previous call
+    (KIVI_ECHECK) or KIVI_OK; always KIVI_OK in a library built without
+    KIVI_CHECKS.  Synchronizes the device."""
+    out = C.c_int32(-1)
+    _check(load().kivi_check_status(C.byref(out)), "kivi_check_status")
+    return int(out.value)

@@ -408,6 +408,27 @@ int32_t kivi_import(const kivi_cache* c, const void* src, size_t src_bytes, int3
                                         (cudaStream_t)stream));
 }
 
+int32_t kivi_check_status(int32_t* status)
+{
+    if (!status)
+        return fail(KIVI_EINVAL, "status is NULL");
+    int32_t first = KIVI_OK;
+#ifdef KIVI_CHECKS
+    const int32_t words[] = {kivi::check_word_quant(),    kivi::check_word_dequant(),
+                             kivi::check_word_append(),   kivi::check_word_payload(),
+                             kivi::check_word_decode(),   kivi::check_word_decode_d64(),
+                             kivi::check_word_decode_d128(), kivi::check_word_decode_d256()};
+    for (const int32_t w : words) {
+        if (w == KIVI_ECUDA)
+            return fail(KIVI_ECUDA, "reading the device check words failed");
+        if (first == KIVI_OK)
+            first = w;
+    }
+#endif
+    *status = first;
+    return ok();
+}
+
 }  // extern "C"
 
 namespace kivi {

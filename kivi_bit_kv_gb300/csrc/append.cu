@@ -24,7 +24,7 @@ __device__ __forceinline__ void flush_values(const kivi_cache& c, size_t bh, int
         uint4 raw[G / 8];
 #pragma unroll
         for (int v = 0; v < G / 8; ++v)
-            raw[v] = *reinterpret_cast<const uint4*>(src + v * 8);
+            raw[v] = ld_checked(reinterpret_cast<const uint4*>(src + v * 8));
         quant_store_value_group<BV, G>(c, bh, t, gi, raw);
     }
 }
@@ -43,8 +43,8 @@ __device__ __forceinline__ void flush_keys(const kivi_cache& c, size_t bh, int T
         uint4 raw[kLaneTokens];
 #pragma unroll
         for (int i = 0; i < kLaneTokens; ++i)
-            raw[i] = *reinterpret_cast<const uint4*>(c.kres + (bh * RG + (t0 + i) % RG) * D +
-                                                      (size_t)j * kLaneChans);
+            raw[i] = ld_checked(reinterpret_cast<const uint4*>(c.kres + (bh * RG + (t0 + i) % RG) * D +
+                                                                (size_t)j * kLaneChans));
         // RG and t0 are multiples of 16: the lane's 16 ring rows never wrap
         quant_store_key_lane<BK, S>(c, bh, t0, Tq / c.G, j, s, smask, raw,
                                     c.kres + (bh * RG + t0 % RG) * D + (size_t)j * kLaneChans, D);
@@ -58,7 +58,7 @@ append_kernel(kivi_cache c, const uint16_t* __restrict__ k, const uint16_t* __re
 {
     const size_t bh = blockIdx.x;
     const int b = (int)(bh / c.H), h = (int)(bh % c.H);
-    const int L = c.len[b];
+    const int L = ld_checked(c.len + b);
     if (L + 1 > c.Tmax) {
         if (h == 0 && threadIdx.x == 0)
             atomicExch(status, KIVI_ECAPACITY);
@@ -69,8 +69,8 @@ append_kernel(kivi_cache c, const uint16_t* __restrict__ k, const uint16_t* __re
     for (int i = threadIdx.x; i < D / kLaneChans; i += blockDim.x) {
         const size_t o = (bh * RG + slot) * D + (size_t)i * kLaneChans;
         const size_t in = bh * D + (size_t)i * kLaneChans;
-        *reinterpret_cast<uint4*>(c.kres + o) = *reinterpret_cast<const uint4*>(k + in);
-        *reinterpret_cast<uint4*>(c.vres + o) = *reinterpret_cast<const uint4*>(v + in);
+        st_checked(reinterpret_cast<uint4*>(c.kres + o), ld_checked(reinterpret_cast<const uint4*>(k + in)));
+        st_checked(reinterpret_cast<uint4*>(c.vres + o), ld_checked(reinterpret_cast<const uint4*>(v + in)));
     }
     const int Tq = quantized_tokens(L, G, c.R);
     if (L + 1 - Tq != RG)
@@ -98,9 +98,9 @@ __global__ void advance_len_kernel(int32_t* len, int B, int Tmax)
 {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < B) {
-        const int L = len[b];
+        const int L = ld_checked(len + b);
         if (L + 1 <= Tmax)
-            len[b] = L + 1;
+            st_checked(len + b, L + 1);
     }
 }
 
@@ -119,6 +119,7 @@ static void launch_append_bk(const kivi_cache& c, const uint16_t* k, const uint1
 cudaError_t launch_append(const kivi_cache& c, const uint16_t* k, const uint16_t* v,
                           int32_t* status, cudaStream_t s)
 {
+    KIVI_SET_CHECK_RANGES(c, s, {{k, (size_t)c.B * c.H * c.D * 2}, {v, (size_t)c.B * c.H * c.D * 2}, {status, 4}});
     switch (c.bits_k) {
     case 2: launch_append_bk<2>(c, k, v, status, s); break;
     case 4: launch_append_bk<4>(c, k, v, status, s); break;
@@ -127,5 +128,9 @@ cudaError_t launch_append(const kivi_cache& c, const uint16_t* k, const uint16_t
     advance_len_kernel<<<(c.B + 127) / 128, 128, 0, s>>>(c.len, c.B, c.Tmax);
     return cudaGetLastError();
 }
+
+#ifdef KIVI_CHECKS
+int32_t check_word_append() { return take_check_word(); }
+#endif
 
 }  // namespace kivi

@@ -58,7 +58,7 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
     const int C = D / gridDim.y, c0 = blockIdx.y * C;
     const int V = C / 4, rows = kCombineThreads / V;
     const int v = threadIdx.x % V, r0 = threadIdx.x / V;
-    const int n = len[bhq / Hq];  // not written by the chunk kernel: read before the wait
+    const int n = ld_checked(len + bhq / Hq);  // not written by the chunk kernel: read before the wait
     const int nv = decode_chunks(n, TC, S);
     const float* mrow = ws_m + bhq * nchunks;
     const float* lrow = ws_l + bhq * nchunks;
@@ -70,13 +70,13 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
     for (int i = 0; i < KP; ++i) {
         const int k = r0 + i * rows;
         if (k < nv) {
-            op[i] = o4[(size_t)k * (D / 4) + v];
-            mp[i] = mrow[k];
+            op[i] = ld_checked(o4 + (size_t)k * (D / 4) + v);
+            mp[i] = ld_checked(mrow + k);
         }
     }
     float m = -INFINITY, l = 0.0f;
     for (int k = threadIdx.x; k < nv; k += kCombineThreads)
-        merge_ml(m, l, mrow[k], lrow[k]);
+        merge_ml(m, l, ld_checked(mrow + k), ld_checked(lrow + k));
     for (int o = 16; o > 0; o >>= 1) {
         const float m2 = __shfl_xor_sync(0xffffffffu, m, o), l2 = __shfl_xor_sync(0xffffffffu, l, o);
         merge_ml(m, l, m2, l2);
@@ -103,8 +103,8 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
     }
 #pragma unroll 4
     for (int k = r0 + KP * rows; k < nv; k += rows) {
-        const float4 o = o4[(size_t)k * (D / 4) + v];
-        const float e = expf(mrow[k] - M);
+        const float4 o = ld_checked(o4 + (size_t)k * (D / 4) + v);
+        const float e = expf(ld_checked(mrow + k) - M);
         acc.x = fmaf(o.x, e, acc.x);
         acc.y = fmaf(o.y, e, acc.y);
         acc.z = fmaf(o.z, e, acc.z);
@@ -117,7 +117,7 @@ decode_combine_kernel(const int32_t* __restrict__ len, int Hq, int D, int nchunk
         float o = 0.0f;
         for (int r = 0; r < rows; ++r)
             o += pf[r * C + d];
-        out[bhq * D + c0 + d] = nv > 0 ? o / L : 0.0f;
+        st_checked(out + bhq * D + c0 + d, nv > 0 ? o / L : 0.0f);
     }
 }
 
@@ -133,6 +133,8 @@ static cudaError_t combine(const kivi_cache& c, int Hq, const float* ws_o, const
                            const float* ws_l, float* out, cudaStream_t s)
 {
     const int nch = pv_chunks(c, Hq);
+    KIVI_SET_CHECK_RANGES(c, s, {{ws_o, (size_t)c.B * Hq * nch * c.D * 4}, {ws_m, (size_t)c.B * Hq * nch * 4},
+                                 {ws_l, (size_t)c.B * Hq * nch * 4}, {out, (size_t)c.B * Hq * c.D * 4}});
     // channel slices per (b, hq): at least two CTAs per SM in all, 32 channels or more each
     const int rows = c.B * Hq;
     int ds = 1;
@@ -207,5 +209,9 @@ size_t stream_ws_bytes(const kivi_cache& c, int Hq)
     const int NQ = Hq / c.H;
     return stream_ws_floats(c.D, heads_per_pass(NQ), kMaxStreamCTAs) * sizeof(float);
 }
+
+#ifdef KIVI_CHECKS
+int32_t check_word_decode() { return take_check_word(); }
+#endif
 
 }  // namespace kivi

@@ -3,4 +3,7 @@
 
 namespace kivi {
 KIVI_DECODE_INSTANTIATE(128)
+#ifdef KIVI_CHECKS
+int32_t check_word_decode_d128() { return take_check_word(); }
+#endif
 }  // namespace kivi

@@ -38,7 +38,7 @@ __device__ __forceinline__ bool chunk_range(const kivi_cache& c, int TC, int S, 
     r.bh = bh;
     r.b = bh / c.H;
     r.h = bh - r.b * c.H;
-    r.n = c.len[r.b];
+    r.n = ld_checked(c.len + r.b);
     const int nch = decode_chunks(r.n, TC, S);
     r.ci = (int)(gridDim.x / BH) - 1 - y;
     if (r.ci >= nch)
@@ -107,7 +107,7 @@ decode_qk_kernel(kivi_cache c, const uint16_t* __restrict__ q, int Hq, float sm_
         stage_q<NQB, D>(q + ((size_t)r.b * Hq + hq0) * D, sm_scale, fk, qs, fac);
         __syncthreads();
         float* out = logits + ((size_t)r.b * Hq + hq0) * ldl;
-        auto sink = [&](int h, int t, float s) { out[(size_t)h * ldl + t] = s; };
+        auto sink = [&](int h, int t, float s) { st_checked(out + (size_t)h * ldl + t, s); };
         float lmax[2], rmax[NQB];  // unused here
         qk_quantized<BITS, NQB, D>(c.G, r.t_begin, r.tq_end, r.t_begin + warp * T::TOK, r.tq_end,
                                 kDecodeWarps * T::TOK, m.kw, m.ks, m.kz, qs, fac, sink, lmax);
@@ -176,7 +176,7 @@ decode_pv_kernel(kivi_cache c, const float* __restrict__ logits, int ldl, int Hq
             const float* lrow = logits + ((size_t)r.b * Hq + hq0 + h) * ldl + r.t_begin;
             mx[h] = -INFINITY;
             for (int t = threadIdx.x; t < n; t += kDecodeThreads) {
-                const float x = lrow[t];
+                const float x = ld_checked(lrow + t);
                 m.p[h * ps + t] = x;
                 mx[h] = fmaxf(mx[h], x);
             }
@@ -264,6 +264,7 @@ template <int D>
 cudaError_t launch_decode_qk_d(const kivi_cache& c, const uint16_t* q, int Hq, float sm_scale, float* logits,
                                int ld_logits, cudaStream_t s)
 {
+    KIVI_SET_CHECK_RANGES(c, s, {{q, (size_t)c.B * Hq * D * 2}, {logits, (size_t)c.B * Hq * ld_logits * 4}});
     KIVI_DECODE_DISPATCH(c.bits_k, Hq / c.H, qk_launch, c, q, Hq, sm_scale, logits, ld_logits, s)
 }
 
@@ -271,6 +272,10 @@ template <int D>
 cudaError_t launch_decode_pv_d(const kivi_cache& c, const float* logits, int ld_logits, int Hq, float* ws_o,
                                float* ws_m, float* ws_l, cudaStream_t s)
 {
+    KIVI_SET_CHECK_RANGES(c, s, {{logits, (size_t)c.B * Hq * ld_logits * 4},
+                                 {ws_o, (size_t)c.B * Hq * pv_chunks(c, Hq) * D * 4},
+                                 {ws_m, (size_t)c.B * Hq * pv_chunks(c, Hq) * 4},
+                                 {ws_l, (size_t)c.B * Hq * pv_chunks(c, Hq) * 4}});
     KIVI_DECODE_DISPATCH(c.bits_v, Hq / c.H, pv_launch, c, logits, ld_logits, Hq, ws_o, ws_m, ws_l, s)
 }
 

@@ -464,7 +464,7 @@ __device__ __forceinline__ void stage_q(const uint16_t* __restrict__ q, float sm
         const uint16_t* row = q + (size_t)h * D;
         float mx = 0.0f;
         for (int d = lane; d < D; d += 32)
-            mx = fmaxf(mx, fabsf(__half2float(__ushort_as_half(row[d]))));
+            mx = fmaxf(mx, fabsf(__half2float(__ushort_as_half(ld_checked(row + d)))));
         for (int m = 16; m > 0; m >>= 1)
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
         float inv = 1.0f, f = 1.0f;
@@ -476,7 +476,7 @@ __device__ __forceinline__ void stage_q(const uint16_t* __restrict__ q, float sm
         inv *= fk;
         f *= __frcp_rn(fk);  // exact: fk is a power of two
         for (int d = lane; d < D; d += 32)
-            qs[h * qstride + qpad(d)] = __half2float(__ushort_as_half(row[d])) * inv;
+            qs[h * qstride + qpad(d)] = __half2float(__ushort_as_half(ld_checked(row + d))) * inv;
         if (lane == 0)
             fac[h] = sm_scale * f;
     }
@@ -928,11 +928,11 @@ __device__ __forceinline__ void pv_unit(const kivi_cache& c, size_t bh, int t_be
                     X[i][2] = x.z;
                     X[i][3] = x.w;
                 } else if constexpr (T::NT == 2) {
-                    const uint2 x = ok ? __ldg(reinterpret_cast<const uint2*>(vr)) : make_uint2(0u, 0u);
+                    const uint2 x = ok ? ldg_checked(reinterpret_cast<const uint2*>(vr)) : make_uint2(0u, 0u);
                     X[i][0] = x.x;
                     X[i][1] = x.y;
                 } else {
-                    X[i][0] = ok ? __ldg(reinterpret_cast<const uint32_t*>(vr)) : 0u;
+                    X[i][0] = ok ? ldg_checked(reinterpret_cast<const uint32_t*>(vr)) : 0u;
                 }
             }
             uint2 b01, b23;
@@ -1028,7 +1028,7 @@ __device__ __forceinline__ void write_partials(int G, int nsplit, const float* o
             s += zs[w * zr + zi];
         for (int sp = 0; sp < nsplit; ++sp)
             s += o_part[(size_t)sp * NQB * D + idx];
-        ws_o[(row0 + (size_t)h * nchunks) * D + d] = s;
+        st_checked(ws_o + (row0 + (size_t)h * nchunks) * D + d, s);
     }
 #pragma unroll
     for (int h = 0; h < NQB; ++h)
@@ -1037,8 +1037,8 @@ __device__ __forceinline__ void write_partials(int G, int nsplit, const float* o
 #pragma unroll
             for (int w = 1; w < kDecodeWarps; ++w)
                 l += zs[w * zr + h * (NGv + 1) + NGv];
-            ws_m[row0 + (size_t)h * nchunks] = m[h];
-            ws_l[row0 + (size_t)h * nchunks] = l;
+            st_checked(ws_m + row0 + (size_t)h * nchunks, m[h]);
+            st_checked(ws_l + row0 + (size_t)h * nchunks, l);
         }
 }
 

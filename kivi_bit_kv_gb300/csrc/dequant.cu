@@ -33,7 +33,7 @@ dequant_keys_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
     const uint32_t two23 = two23_bits();
 
     for (int bh = blockIdx.y; bh < c.B * c.H; bh += gridDim.y) {
-        const int len = c.len[bh / c.H];
+        const int len = ld_checked(c.len + bh / c.H);
         const int n = min(len, T_out);
         if (t0 >= n)
             continue;
@@ -112,7 +112,7 @@ dequant_values_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
     auto phys = [&](int r, int ch) { return ch ^ (((r << lgNG) ^ (ch >> lgNV)) & 7); };
 
     for (int bh = blockIdx.y; bh < c.B * c.H; bh += gridDim.y) {
-        const int len = c.len[bh / c.H];
+        const int len = ld_checked(c.len + bh / c.H);
         const int n = min(len, T_out);
         const int Tq = quantized_tokens(len, c.G, c.R);
         uint32_t words[U][NW];
@@ -125,7 +125,8 @@ dequant_values_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
                 const size_t row = (size_t)bh * c.Tmax + t;
                 const uint32_t* src = reinterpret_cast<const uint32_t*>(c.vq) + row * (D / Cd::P) + gi * NW;
                 if constexpr (NW == 2) {
-                    const uint2 x = __ldcs(reinterpret_cast<const uint2*>(src));
+                    const uint2 x = KIVI_IN_RANGE(src, 8) ? __ldcs(reinterpret_cast<const uint2*>(src))
+                                                          : make_uint2(0u, 0u);
                     words[u][0] = x.x;
                     words[u][1] = x.y;
                 } else {
@@ -138,8 +139,8 @@ dequant_values_kernel(kivi_cache c, uint16_t* __restrict__ out, int T_out)
                         words[u][w + 3] = x.w;
                     }
                 }
-                sc[u] = __ldcs(c.vscale + row * NG + gi);
-                zr[u] = __ldcs(c.vzero + row * NG + gi);
+                sc[u] = KIVI_IN_RANGE(c.vscale + row * NG + gi, 4) ? __ldcs(c.vscale + row * NG + gi) : 0.0f;
+                zr[u] = KIVI_IN_RANGE(c.vzero + row * NG + gi, 4) ? __ldcs(c.vzero + row * NG + gi) : 0.0f;
             }
         }
 #pragma unroll
@@ -215,6 +216,7 @@ cudaError_t launch_dequant(const kivi_cache& c, int which, uint16_t* out, int T_
 {
     if (T_out <= 0)
         return cudaGetLastError();
+    KIVI_SET_CHECK_RANGES(c, s, {{out, (size_t)c.B * c.H * T_out * c.D * 2}});
     if (which == 0) {
         const int lanes = ((T_out + c.G - 1) / c.G) * (c.G / kLaneTokens) * (c.D / kLaneChans);
         const dim3 grid = dq_grid(c, (lanes + kDequantThreads - 1) / kDequantThreads);
@@ -232,5 +234,9 @@ cudaError_t launch_dequant(const kivi_cache& c, int which, uint16_t* out, int T_
     }
     return cudaGetLastError();
 }
+
+#ifdef KIVI_CHECKS
+int32_t check_word_dequant() { return take_check_word(); }
+#endif
 
 }  // namespace kivi

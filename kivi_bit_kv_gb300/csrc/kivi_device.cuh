@@ -8,12 +8,91 @@
 #pragma once
 
 #include <cuda_fp16.h>
+#include <cuda_runtime.h>
 #include <stdint.h>
 
 #include "kivi.h"
 #include "kivi_divm.h"
 
 namespace kivi {
+
+// ---------------------------------------------------------- checked build ---
+// With KIVI_CHECKS defined, every global access of the encode, materialize,
+// append, payload and split-decode kernels goes through KIVI_IN_RANGE: the
+// bytes [p, p + n) must lie in one of the ranges the launcher wrote into this
+// translation unit's table (the cache's arrays and the call's own buffers).
+// A failed check records KIVI_ECHECK in this unit's check word (the first
+// failure wins) and the access is skipped; kivi_check_status() reads and
+// clears the words of every unit.  Without KIVI_CHECKS the checks compile
+// away.
+#ifdef KIVI_CHECKS
+}  // namespace kivi
+#include <initializer_list>
+namespace kivi {
+constexpr int kCheckRanges = 16;
+struct CheckRange {
+    uintptr_t lo, hi;
+};
+static __constant__ CheckRange g_check_ranges[kCheckRanges];
+static __device__ int g_check_word;
+
+__device__ __forceinline__ bool in_ranges(const void* p, size_t n)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+#pragma unroll 1
+    for (int i = 0; i < kCheckRanges; ++i)
+        if (a >= g_check_ranges[i].lo && a + n <= g_check_ranges[i].hi)
+            return true;
+    atomicCAS(&g_check_word, KIVI_OK, KIVI_ECHECK);
+    return false;
+}
+#define KIVI_IN_RANGE(p, n) ::kivi::in_ranges((p), (n))
+
+// Writes the table of this translation unit: the arrays of cache c (their
+// sizes from kivi_buffer_bytes) and up to six buffers of the call.
+struct CallBuf {
+    const void* p;
+    size_t bytes;
+};
+static inline cudaError_t set_check_ranges(const kivi_cache& c, cudaStream_t s,
+                                           std::initializer_list<CallBuf> call = {})
+{
+    CheckRange r[kCheckRanges] = {};
+    int n = 0;
+    const void* arrays[9] = {c.kq, c.kscale, c.kzero, c.vq, c.vscale, c.vzero, c.kres, c.vres, c.len};
+    for (int i = 0; i < 9; ++i) {
+        const uintptr_t lo = reinterpret_cast<uintptr_t>(arrays[i]);
+        r[n++] = CheckRange{lo, lo + kivi_buffer_bytes(&c, i)};
+    }
+    for (const CallBuf& b : call)
+        if (b.p && n < kCheckRanges) {
+            const uintptr_t lo = reinterpret_cast<uintptr_t>(b.p);
+            r[n++] = CheckRange{lo, lo + b.bytes};
+        }
+    return cudaMemcpyToSymbolAsync(g_check_ranges, r, sizeof r, 0, cudaMemcpyHostToDevice, s);
+}
+// Reads and clears this translation unit's check word (synchronizes).
+static inline int32_t take_check_word()
+{
+    int32_t v = KIVI_OK;
+    const int32_t zero = KIVI_OK;
+    if (cudaMemcpyFromSymbol(&v, g_check_word, sizeof v) != cudaSuccess ||
+        cudaMemcpyToSymbol(g_check_word, &zero, sizeof zero) != cudaSuccess)
+        return KIVI_ECUDA;
+    return v;
+}
+#define KIVI_SET_CHECK_RANGES(c, s, ...)                                      \
+    do {                                                                      \
+        const cudaError_t e_ = ::kivi::set_check_ranges((c), (s), __VA_ARGS__); \
+        if (e_ != cudaSuccess)                                                \
+            return e_;                                                        \
+    } while (0)
+#else
+#define KIVI_IN_RANGE(p, n) true
+#define KIVI_SET_CHECK_RANGES(c, s, ...) \
+    do {                                 \
+    } while (0)
+#endif
 
 // Tokens one lane covers in a key tile (one int2 word; two int4 / four int8).
 constexpr int kLaneTokens = 16;
@@ -39,6 +118,10 @@ __host__ __device__ __forceinline__ int quantized_tokens(int T, int G, int R)
 // spinning -- and a warp barrier then publishes them to the warp.
 __device__ __forceinline__ void cp_async16(void* smem, const void* gmem)
 {
+    if (!KIVI_IN_RANGE(gmem, 16)) {
+        *reinterpret_cast<uint4*>(smem) = make_uint4(0u, 0u, 0u, 0u);
+        return;
+    }
     const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(sa), "l"(gmem) : "memory");
 }
@@ -51,19 +134,45 @@ __device__ __forceinline__ void cp_async_wait_prior() { asm volatile("cp.async.w
 
 __device__ __forceinline__ uint4 ld_stream(const void* p)   // read-once data
 {
+    if (!KIVI_IN_RANGE(p, 16))
+        return make_uint4(0u, 0u, 0u, 0u);
     return __ldcs(reinterpret_cast<const uint4*>(p));
 }
 __device__ __forceinline__ uint4 ld_nc(const void* p)       // read-only, may be shared
 {
+    if (!KIVI_IN_RANGE(p, 16))
+        return make_uint4(0u, 0u, 0u, 0u);
     return __ldg(reinterpret_cast<const uint4*>(p));
 }
 __device__ __forceinline__ float4 ld_nc_f4(const float* p)
 {
+    if (!KIVI_IN_RANGE(p, 16))
+        return make_float4(0.f, 0.f, 0.f, 0.f);
     return __ldg(reinterpret_cast<const float4*>(p));
 }
 __device__ __forceinline__ void st_stream(void* p, uint4 v)
 {
-    __stcs(reinterpret_cast<uint4*>(p), v);
+    if (KIVI_IN_RANGE(p, 16))
+        __stcs(reinterpret_cast<uint4*>(p), v);
+}
+// A global store of one value, bounds-checked in the checked build.
+template <class T>
+__device__ __forceinline__ void st_checked(T* p, T v)
+{
+    if (KIVI_IN_RANGE(p, sizeof(T)))
+        *p = v;
+}
+// A global load of one value (zero where a check fails).
+template <class T>
+__device__ __forceinline__ T ld_checked(const T* p)
+{
+    return KIVI_IN_RANGE(p, sizeof(T)) ? *p : T{};
+}
+// The same through the read-only path (data no kernel of the call writes).
+template <class T>
+__device__ __forceinline__ T ldg_checked(const T* p)
+{
+    return KIVI_IN_RANGE(p, sizeof(T)) ? __ldg(p) : T{};
 }
 
 __device__ __forceinline__ uint16_t u4_half(const uint4& v, int k)   // k in [0, 8)
@@ -414,10 +523,10 @@ __device__ __forceinline__ void quant_store_key_lane(const kivi_cache& c, size_t
         const size_t so = (bh * (size_t)(c.Tmax / c.G) + g) * D + (size_t)j * kLaneChans;
         float4* sp = reinterpret_cast<float4*>(c.kscale + so);
         float4* zp = reinterpret_cast<float4*>(c.kzero + so);
-        sp[0] = make_float4(scale[0], scale[1], scale[2], scale[3]);
-        sp[1] = make_float4(scale[4], scale[5], scale[6], scale[7]);
-        zp[0] = make_float4(zero[0], zero[1], zero[2], zero[3]);
-        zp[1] = make_float4(zero[4], zero[5], zero[6], zero[7]);
+        st_checked(sp, make_float4(scale[0], scale[1], scale[2], scale[3]));
+        st_checked(sp + 1, make_float4(scale[4], scale[5], scale[6], scale[7]));
+        st_checked(zp, make_float4(zero[0], zero[1], zero[2], zero[3]));
+        st_checked(zp + 1, make_float4(zero[4], zero[5], zero[6], zero[7]));
     }
 }
 
@@ -435,15 +544,15 @@ __device__ __forceinline__ void quant_store_value_group(const kivi_cache& c, siz
     const size_t row = bh * (size_t)c.Tmax + t;
     uint32_t* dst = reinterpret_cast<uint32_t*>(c.vq) + row * (c.D / Cd::P) + (size_t)gi * NW;
     if constexpr (NW == 2) {
-        *reinterpret_cast<uint2*>(dst) = make_uint2(words[0], words[1]);
+        st_checked(reinterpret_cast<uint2*>(dst), make_uint2(words[0], words[1]));
     } else {
 #pragma unroll
         for (int w = 0; w < NW; w += 4)
-            *reinterpret_cast<uint4*>(dst + w) = make_uint4(words[w], words[w + 1], words[w + 2], words[w + 3]);
+            st_checked(reinterpret_cast<uint4*>(dst + w), make_uint4(words[w], words[w + 1], words[w + 2], words[w + 3]));
     }
     const size_t so = row * (c.D / G) + gi;
-    c.vscale[so] = scale;
-    c.vzero[so] = zero;
+    st_checked(c.vscale + so, scale);
+    st_checked(c.vzero + so, zero);
 }
 
 }  // namespace kivi

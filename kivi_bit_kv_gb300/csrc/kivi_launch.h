@@ -66,6 +66,18 @@ cudaError_t launch_import(const kivi_cache& c, const void* src, size_t src_bytes
 int32_t check_decode_pv_args(const kivi_cache* c, const float* logits, int32_t ld_logits, int32_t Hq,
                              const float* out);
 
+#ifdef KIVI_CHECKS
+// Read and clear the check word of each translation unit with checked kernels.
+int32_t check_word_quant();
+int32_t check_word_dequant();
+int32_t check_word_append();
+int32_t check_word_payload();
+int32_t check_word_decode();
+int32_t check_word_decode_d64();
+int32_t check_word_decode_d128();
+int32_t check_word_decode_d256();
+#endif
+
 // Sets the message kivi_last_error() returns on this host thread; returns status.
 int32_t record_error(int32_t status, const char* message);
 

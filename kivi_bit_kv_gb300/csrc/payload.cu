@@ -68,7 +68,7 @@ __device__ __forceinline__ PayloadScan payload_scan(const kivi_cache& c, const i
     unsigned long long before = 0, total = 0;
     int bad = 0;
     for (int b = threadIdx.x; b < c.B; b += kPayloadThreads) {
-        const int n = lens[b];
+        const int n = ld_checked(lens + b);
         if (n < 0 || n > c.Tmax) {
             bad = 1;
             continue;
@@ -160,7 +160,7 @@ export_kernel(kivi_cache c, uint4* __restrict__ dst, size_t dst_units, uint64_t 
         return;  // len[] is the library's own state: cannot happen
     if (ps.total > dst_units) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-            *status = KIVI_EWORKSPACE;
+            st_checked(status, (int32_t)KIVI_EWORKSPACE);
         return;
     }
     if (blockIdx.x == 0 && blockIdx.y == 0) {
@@ -173,19 +173,19 @@ export_kernel(kivi_cache c, uint4* __restrict__ dst, size_t dst_units, uint64_t 
             else if (i == 2) w = (uint32_t)fingerprint;
             else if (i == 3) w = (uint32_t)(fingerprint >> 32);
             else if (i < 11) w = (uint32_t)fields[i - 4];
-            else if (i >= 16 && i - 16 < c.B) w = (uint32_t)c.len[i - 16];
-            hd[i] = w;
+            else if (i >= 16 && i - 16 < c.B) w = (uint32_t)ld_checked(c.len + (i - 16));
+            st_checked(hd + i, w);
         }
     }
     size_t off = ps.base;  // offset of slice (bh0 / H, 0)
     for (int bh = bh0 - bh0 % c.H; bh < bh1; ++bh) {
-        const SliceGeom g = slice_geom(c.len[bh / c.H], c.D, c.bits_k, c.bits_v, c.G, c.R);
+        const SliceGeom g = slice_geom(ld_checked(c.len + bh / c.H), c.D, c.bits_k, c.bits_v, c.G, c.R);
         const uint32_t U = (uint32_t)slice_units(g);
         if (bh >= bh0)
             for (uint32_t u = blockIdx.x * kPayloadThreads + threadIdx.x; u < U; u += gridDim.x * kPayloadThreads) {
                 uint32_t r;
                 const int s = section_of(g, u, r);
-                dst[off + u] = ld_nc(reinterpret_cast<const uint16_t*>(cache_unit(c, bh, g, s, r)));
+                st_checked(dst + off + u, ld_nc(reinterpret_cast<const uint16_t*>(cache_unit(c, bh, g, s, r))));
             }
         off += U;
     }
@@ -197,14 +197,14 @@ import_kernel(kivi_cache c, const uint4* __restrict__ src, size_t src_units, uin
 {
     const uint32_t* hd = reinterpret_cast<const uint32_t*>(src);
     const int32_t fields[7] = {c.B, c.H, c.D, c.bits_k, c.bits_v, c.G, c.R};
-    bool ok = hd[0] == KIVI_PAYLOAD_MAGIC && hd[1] == KIVI_PAYLOAD_VERSION && hd[2] == (uint32_t)fingerprint &&
-              hd[3] == (uint32_t)(fingerprint >> 32);
+    bool ok = ld_checked(hd) == KIVI_PAYLOAD_MAGIC && ld_checked(hd + 1) == KIVI_PAYLOAD_VERSION &&
+              ld_checked(hd + 2) == (uint32_t)fingerprint && ld_checked(hd + 3) == (uint32_t)(fingerprint >> 32);
 #pragma unroll
     for (int i = 0; i < 7; ++i)
-        ok = ok && (int32_t)hd[4 + i] == fields[i];
+        ok = ok && (int32_t)ld_checked(hd + 4 + i) == fields[i];
     if (!ok) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-            *status = KIVI_EINVAL;
+            st_checked(status, (int32_t)KIVI_EINVAL);
         return;
     }
     const int32_t* lens = reinterpret_cast<const int32_t*>(hd + 16);
@@ -214,22 +214,22 @@ import_kernel(kivi_cache c, const uint4* __restrict__ src, size_t src_units, uin
     const PayloadScan ps = payload_scan(c, lens, bh0 / c.H);
     if (ps.bad || ps.total > src_units) {
         if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0)
-            *status = ps.bad ? KIVI_ECAPACITY : KIVI_EWORKSPACE;
+            st_checked(status, (int32_t)(ps.bad ? KIVI_ECAPACITY : KIVI_EWORKSPACE));
         return;
     }
     size_t off = ps.base;  // offset of slice (bh0 / H, 0)
     for (int bh = bh0 - bh0 % c.H; bh < bh1; ++bh) {
-        const int b = bh / c.H, n = lens[b];
+        const int b = bh / c.H, n = ld_checked(lens + b);
         const SliceGeom g = slice_geom(n, c.D, c.bits_k, c.bits_v, c.G, c.R);
         const uint32_t U = (uint32_t)slice_units(g);
         if (bh >= bh0) {
             for (uint32_t u = blockIdx.x * kPayloadThreads + threadIdx.x; u < U; u += gridDim.x * kPayloadThreads) {
                 uint32_t r;
                 const int s = section_of(g, u, r);
-                *cache_unit(c, bh, g, s, r) = src[off + u];
+                st_checked(cache_unit(c, bh, g, s, r), ld_checked(src + off + u));
             }
             if (bh % c.H == 0 && blockIdx.x == 0 && threadIdx.x == 0)
-                c.len[b] = n;
+                st_checked(c.len + b, n);
         }
         off += U;
     }
@@ -256,6 +256,7 @@ size_t payload_bytes(const kivi_cache& c, const int32_t* lens)
 cudaError_t launch_export(const kivi_cache& c, void* dst, size_t dst_bytes, uint64_t fingerprint,
                           int32_t* status, cudaStream_t s)
 {
+    KIVI_SET_CHECK_RANGES(c, s, {{dst, dst_bytes}, {status, 4}});
     export_kernel<<<payload_grid(c), kPayloadThreads, 0, s>>>(c, static_cast<uint4*>(dst), dst_bytes / 16,
                                                              fingerprint, status);
     return cudaGetLastError();
@@ -264,9 +265,14 @@ cudaError_t launch_export(const kivi_cache& c, void* dst, size_t dst_bytes, uint
 cudaError_t launch_import(const kivi_cache& c, const void* src, size_t src_bytes, uint64_t fingerprint,
                           int32_t* status, cudaStream_t s)
 {
+    KIVI_SET_CHECK_RANGES(c, s, {{src, src_bytes}, {status, 4}});
     import_kernel<<<payload_grid(c), kPayloadThreads, 0, s>>>(c, static_cast<const uint4*>(src), src_bytes / 16,
                                                              fingerprint, status);
     return cudaGetLastError();
 }
+
+#ifdef KIVI_CHECKS
+int32_t check_word_payload() { return take_check_word(); }
+#endif
 
 }  // namespace kivi

@@ -43,9 +43,9 @@ quant_keys_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
 
     for (int bh = blockIdx.y; bh < c.B * c.H; bh += gridDim.y) {
         const int b = bh / c.H;
-        const int n = seq_lens ? min(max(seq_lens[b], 0), T) : T;
+        const int n = seq_lens ? min(max(ld_checked(seq_lens + b), 0), T) : T;
         if (blockIdx.x == 0 && threadIdx.x == 0 && bh % c.H == 0)
-            c.len[b] = n;
+            st_checked(c.len + b, n);
         if (g * c.G >= n)
             continue;  // uniform over the tile column
         const int Tq = quantized_tokens(n, c.G, c.R);
@@ -130,10 +130,10 @@ __device__ __forceinline__ void quant_store_key_lane_smem(const kivi_cache& c, s
         const size_t so = (bh * (size_t)(c.Tmax / c.G) + g) * D + (size_t)j * kLaneChans;
         float4* sp = reinterpret_cast<float4*>(c.kscale + so);
         float4* zp = reinterpret_cast<float4*>(c.kzero + so);
-        sp[0] = make_float4(scale[0], scale[1], scale[2], scale[3]);
-        sp[1] = make_float4(scale[4], scale[5], scale[6], scale[7]);
-        zp[0] = make_float4(zero[0], zero[1], zero[2], zero[3]);
-        zp[1] = make_float4(zero[4], zero[5], zero[6], zero[7]);
+        st_checked(sp, make_float4(scale[0], scale[1], scale[2], scale[3]));
+        st_checked(sp + 1, make_float4(scale[4], scale[5], scale[6], scale[7]));
+        st_checked(zp, make_float4(zero[0], zero[1], zero[2], zero[3]));
+        st_checked(zp + 1, make_float4(zero[4], zero[5], zero[6], zero[7]));
     }
     // codes: word = sum_i t_bits_i 2^(b i) - bias * sum_i 2^(b i) (mod 2^32)
     constexpr uint32_t kWordBias = kCodeBias * (uint32_t)(((1ull << (Cd::P * BITS)) - 1) /
@@ -202,7 +202,7 @@ quant_keys_staged_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
         bh = tile / tiles_per_seq;
         tt0 = (tile - bh * tiles_per_seq) * TT;
         const int b = bh / c.H;
-        n = seq_lens ? min(max(seq_lens[b], 0), T) : T;
+        n = seq_lens ? min(max(ld_checked(seq_lens + b), 0), T) : T;
     };
     auto prefetch = [&](int tile, int buf) {
         if (tile < ntiles) {
@@ -241,7 +241,7 @@ quant_keys_staged_kernel(kivi_cache c, const uint16_t* __restrict__ K, int T,
         int bh, tt0, n;
         tile_of(tile, bh, tt0, n);
         if (tt0 == 0 && threadIdx.x == 0 && bh % c.H == 0)
-            c.len[bh / c.H] = n;
+            st_checked(c.len + bh / c.H, n);
         const int g = tt0 / c.G + gl;
         const int t0 = g * c.G + s * kLaneTokens;
         const int lr = gl * c.G + s * kLaneTokens;  // first tile row of this lane
@@ -284,9 +284,9 @@ quant_values_kernel(kivi_cache c, const uint16_t* __restrict__ V, int T,
 
     for (int bh = blockIdx.y; bh < c.B * c.H; bh += gridDim.y) {
         const int b = bh / c.H;
-        const int n = seq_lens ? min(max(seq_lens[b], 0), T) : T;
+        const int n = seq_lens ? min(max(ld_checked(seq_lens + b), 0), T) : T;
         if (blockIdx.x == 0 && threadIdx.x == 0 && bh % c.H == 0)
-            c.len[b] = n;
+            st_checked(c.len + b, n);
         const int Tq = quantized_tokens(n, c.G, c.R);
         const uint16_t* src = V + (size_t)bh * T * D + gi * G;
         uint4 raw[U][NV];
@@ -318,7 +318,7 @@ __global__ void set_len_kernel(int32_t* len, int B, int T, const int32_t* __rest
 {
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b < B)
-        len[b] = seq_lens ? min(max(seq_lens[b], 0), T) : T;
+        st_checked(len + b, seq_lens ? min(max(ld_checked(seq_lens + b), 0), T) : T);
 }
 
 static dim3 encode_grid(const kivi_cache& c, int tiles)
@@ -373,6 +373,7 @@ static void key_launch_bits(const kivi_cache& c, const uint16_t* K, int T, const
 cudaError_t launch_quant_keys(const kivi_cache& c, const uint16_t* K, int T,
                               const int32_t* seq_lens, cudaStream_t s)
 {
+    KIVI_SET_CHECK_RANGES(c, s, {{K, (size_t)c.B * c.H * T * c.D * 2}, {seq_lens, (size_t)c.B * 4}});
     if (T > 0) {
         switch (c.bits_k) {
         case 2: key_launch_bits<2>(c, K, T, seq_lens, s); break;
@@ -402,6 +403,7 @@ static void quant_values_bits(const kivi_cache& c, const uint16_t* V, int T,
 cudaError_t launch_quant_values(const kivi_cache& c, const uint16_t* V, int T,
                                 const int32_t* seq_lens, cudaStream_t s)
 {
+    KIVI_SET_CHECK_RANGES(c, s, {{V, (size_t)c.B * c.H * T * c.D * 2}, {seq_lens, (size_t)c.B * 4}});
     if (T > 0) {
         switch (c.bits_v) {
         case 2: quant_values_bits<2>(c, V, T, seq_lens, s); break;
@@ -413,5 +415,9 @@ cudaError_t launch_quant_values(const kivi_cache& c, const uint16_t* V, int T,
     }
     return cudaGetLastError();
 }
+
+#ifdef KIVI_CHECKS
+int32_t check_word_quant() { return take_check_word(); }
+#endif
 
 }  // namespace kivi
