@@ -277,11 +277,17 @@ __host__ __device__ constexpr int stream_consumers()
                                                                           : stream_consumers<BK, BV, NQB, D, NC - 1>();
 }
 
-// Workspace of the streamed decode: header (status word) and two partial
-// (o, m, l) slots per CTA.
+// Workspace of the streamed decode: header (status word), two partial
+// (o, m, l) slots per CTA, and per CTA a descriptor of the row its range
+// ends in (kStreamDescInts ints) for the combine kernel.
+constexpr int kStreamDescInts = 8;
+__host__ __device__ inline size_t stream_partial_floats(int D, int NQB, int ctas)
+{
+    return (size_t)ctas * 2 * NQB * (D + 2);
+}
 inline size_t stream_ws_floats(int D, int NQB, int ctas)
 {
-    return (size_t)kStreamHeaderFloats + (size_t)ctas * 2 * NQB * (D + 2);
+    return (size_t)kStreamHeaderFloats + stream_partial_floats(D, NQB, ctas) + (size_t)ctas * kStreamDescInts;
 }
 
 // ---------------------------------------------------------- tile walker ---
@@ -1070,8 +1076,34 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     int* wsi = reinterpret_cast<int*>(ws);
 
     RangeStart r0, r1;
-    locate_range<C::THREADS>(c, RB, C::TS, C::RT, blockIdx.x, gridDim.x, r0, r1, red, sh_range);
+    long long NT = 0;
+    locate_range<C::THREADS>(c, RB, C::TS, C::RT, blockIdx.x, gridDim.x, r0, r1, red, sh_range, &NT);
+    // zero outputs of empty sequences b = blockIdx.x mod gridDim.x (no tile writes them)
+    for (int b = blockIdx.x; b < c.B; b += gridDim.x)
+        if (c.len[b] == 0)
+            for (int x = threadIdx.x; x < Hq * D; x += C::THREADS)
+                out[(size_t)b * Hq * D + x] = 0.0f;
     if (threadIdx.x == 0) {
+        // The row in which this range ends, for the combine kernel: cut (the
+        // range ends inside it and holds its first tile), its sequence and
+        // row, the partial slot of this CTA's piece, the last range with a
+        // piece (range k starts at tile NT k / N), and NT.
+        int* dsc = wsi + kStreamHeaderFloats + stream_partial_floats(D, NQB, gridDim.x) +
+                   (size_t)blockIdx.x * kStreamDescInts;
+        const long long g0 = r0.g, g1 = r1.g, row_first = g1 - r1.j;
+        const bool cut = g1 > g0 && r1.j != 0 && r1.b < c.B && row_first >= g0;
+        int last = 0;
+        if (cut) {
+            const long long row_end = row_first + row_tiles(c.len[r1.b], c, C::TS, C::RT);
+            last = (int)min((long long)gridDim.x - 1, (row_end * gridDim.x - 1) / NT);
+        }
+        dsc[0] = cut ? 1 : 0;
+        dsc[1] = r1.b;
+        dsc[2] = r1.rr;
+        dsc[3] = row_first == g0 ? 0 : 1;
+        dsc[4] = last;
+        dsc[5] = (int)(NT & 0xffffffff);
+        dsc[6] = (int)(NT >> 32);
         for (int s = 0; s < ns; ++s) {
             mbar_init(&full[s], 2);  // the key and the value producer
             mbar_init(&empty[s], 1);
@@ -1428,12 +1460,12 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
 // takes the row in which range i ends, if range i is not empty, ends inside
 // a row, and holds that row's first tile; the ranges after it that start
 // inside the row hold its other pieces (their first row segment, slot 0).
-// The ranges are the decode kernel's (range k starts at tile NT k / N of the
-// NT tiles), found from len[] -- which the decode kernel does not write --
-// before the wait for the decode kernel's results, so that after it only the
-// pieces are read: their (m, l) pairs, then their o rows, all at once.  The
-// sums run over the pieces in order, so the result does not depend on
-// timing.  Also writes zero outputs for sequences of length 0.
+// Decode CTA i leaves that row in its descriptor (cut or not, the row, the
+// slot of its own piece, the last range with a piece, and the tile count NT
+// that places range k at tile NT k / N), so after its wait this kernel reads
+// the descriptor, then the pieces' (m, l) pairs, then their o rows, four
+// pieces at a time.  The sums run over the pieces in order, so the result
+// does not depend on timing.
 template <int NQB, int D, int TS, int RT>
 __global__ void __launch_bounds__(128)
 decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __restrict__ ws,
@@ -1441,40 +1473,27 @@ decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __
 {
     constexpr int T = 128;
     const int N = gridDim.x, i = blockIdx.x;
-    const int NQ = Hq / c.H, RB = c.H * NP;
-    __shared__ long long red[T / 32];
-    __shared__ RangeStart sh_range[2];
+    const int NQ = Hq / c.H;
     __shared__ float s_m[T][NQB], s_l[T][NQB];
     // the next decode kernel may be scheduled once every CTA of this grid
     // runs (it waits for this grid's results before it reads anything)
     asm volatile("griddepcontrol.launch_dependents;");
-    for (int b = i; b < c.B; b += N)
-        if (c.len[b] == 0)
-            for (int x = threadIdx.x; x < Hq * D; x += T)
-                out[(size_t)b * Hq * D + x] = 0.0f;
-    RangeStart r0, r1;
-    long long NT = 0;
-    locate_range<T>(c, RB, TS, RT, i, N, r0, r1, red, sh_range, &NT);
-    const long long g0 = r0.g, g1 = r1.g;
-    if (g1 <= g0 || r1.j == 0 || r1.b >= c.B)
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int* dsc = reinterpret_cast<const int*>(ws) + kStreamHeaderFloats + stream_partial_floats(D, NQB, N) +
+                     (size_t)i * kStreamDescInts;
+    if (dsc[0] == 0)
         return;
-    const long long row_first = g1 - r1.j;
-    if (row_first < g0)
-        return;  // an earlier range holds the row's first tile
-    const long long row_end = row_first + row_tiles(c.len[r1.b], c, TS, RT);
-    // ranges i + 1 .. last start inside the row: range k starts at NT k / N
-    const int last = (int)min((long long)N - 1, (row_end * N - 1) / NT);
+    const int rb = dsc[1], rr = dsc[2], slot_i = dsc[3], last = dsc[4];
+    const long long NT = (long long)(unsigned)dsc[5] | ((long long)dsc[6] << 32);
     auto X = [&](int k) { return NT * k / N; };
-    const int slot_i = row_first == g0 ? 0 : 1;
     const int P = last - i + 1;  // ranges i .. last; an empty one holds no piece
     const float* part = ws + kStreamHeaderFloats;
     const size_t pstride = (size_t)NQB * (D + 2);
     auto piece = [&](int k) { return part + ((size_t)k * 2 + (k == i ? slot_i : 0)) * pstride; };
-    const int h = r1.rr / NP, pass = r1.rr - h * NP;
-    float* dst = out + ((size_t)r1.b * Hq + h * NQ + pass * NQB) * D;
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    const int h = rr / NP, pass = rr - h * NP;
+    float* dst = out + ((size_t)rb * Hq + h * NQ + pass * NQB) * D;
     // the pieces are the grid's partial slots, the row one of the output's
-    if (!kivi_check(last < N && P >= 1 && r1.b < c.B && h * NQ + pass * NQB + NQB <= Hq,
+    if (!kivi_check(last < N && P >= 1 && rb < c.B && h * NQ + pass * NQB + NQB <= Hq,
                     reinterpret_cast<int*>(const_cast<float*>(ws))))
         return;
 
