@@ -526,6 +526,48 @@ __device__ __forceinline__ float warp_max_stat(const float* p, int n)
     return warp_max_nonneg(mx);
 }
 
+// The largest key statistic (first nk floats at pk) and the largest value
+// statistic (first nv at pv) of a tile, per warp, each at most MAXK / MAXV
+// floats: all loads issued first, tree maxima, one integer reduction each
+// (the two chains are independent, so their latencies overlap).
+template <int MAXK, int MAXV>
+__device__ __forceinline__ void warp_max_stats2(const float* pk, int nk, const float* pv, int nv, float& mk,
+                                                float& mv)
+{
+    constexpr int LK = (MAXK + 127) / 128, LV = (MAXV + 127) / 128;
+    const int lane = threadIdx.x & 31;
+    float4 k4[LK], v4[LV];
+#pragma unroll
+    for (int u = 0; u < LK; ++u) {
+        const int i = 4 * lane + 128 * u;
+        k4[u] = i < nk ? *reinterpret_cast<const float4*>(pk + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll
+    for (int u = 0; u < LV; ++u) {
+        const int i = 4 * lane + 128 * u;
+        v4[u] = i < nv ? *reinterpret_cast<const float4*>(pv + i) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    float a[LK], b[LV];
+#pragma unroll
+    for (int u = 0; u < LK; ++u)
+        a[u] = fmaxf(fmaxf(k4[u].x, k4[u].y), fmaxf(k4[u].z, k4[u].w));
+#pragma unroll
+    for (int u = 0; u < LV; ++u)
+        b[u] = fmaxf(fmaxf(v4[u].x, v4[u].y), fmaxf(v4[u].z, v4[u].w));
+#pragma unroll
+    for (int w = 1; w < LK; w *= 2)
+#pragma unroll
+        for (int u = 0; u + w < LK; u += 2 * w)
+            a[u] = fmaxf(a[u], a[u + w]);
+#pragma unroll
+    for (int w = 1; w < LV; w *= 2)
+#pragma unroll
+        for (int u = 0; u + w < LV; u += 2 * w)
+            b[u] = fmaxf(b[u], b[u + w]);
+    mk = warp_max_nonneg(a[0]);
+    mv = warp_max_nonneg(b[0]);
+}
+
 // q . K_hat of one key warp tile (tokens tok0 .. tok0 + TOK of the stage,
 // valid below n) into the logit rows lg[h][lg_phys(t)] for valid tokens.
 // kst0: the stage's first key statistic row is group kst0; t0: first token
@@ -1000,8 +1042,10 @@ __device__ __forceinline__ void consume_quant(ConsumerState<C, NQB>& st, const u
     const int n = FULL ? C::TS : n_rt;
     const int NG = D >> lgG;
     const int ngr = ((t0 + n - 1) >> lgG) - (t0 >> lgG) + 1;
-    const float smax_k = warp_max_stat(reinterpret_cast<const float*>(sl + C::O_KS), ngr * D);
-    const float smax_v = warp_max_stat(reinterpret_cast<const float*>(sl + C::O_VS), n * NG);
+    float smax_k, smax_v;
+    warp_max_stats2<C::KSR * D, C::TS * C::NGM>(reinterpret_cast<const float*>(sl + C::O_KS), ngr * D,
+                                               reinterpret_cast<const float*>(sl + C::O_VS), n * NG, smax_k,
+                                               smax_v);
     float fac[NQB];
 #pragma unroll
     for (int hh = 0; hh < NQB; ++hh) {
@@ -1358,13 +1402,19 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
         o_seg = -1;
         o_tiles = 0;
     };
+    // The warp reserves its next tile while it works on the current one (the
+    // counter's round trip is then off the critical path).  The smallest
+    // unfinished tile is always some warp's current tile, whose slot's
+    // previous tile is finished, so the reservations cannot deadlock.
+    unsigned long long kk_next = 0;
+    if (lane == 0)
+        kk_next = atomicAdd(&next_tile, 1ull);
     for (;;) {
-        unsigned long long kk = 0;
-        if (lane == 0)
-            kk = atomicAdd(&next_tile, 1ull);
-        const long long k = (long long)__shfl_sync(0xffffffffu, kk, 0);
+        const long long k = (long long)__shfl_sync(0xffffffffu, kk_next, 0);
         if (k >= ntiles)
             break;
+        if (lane == 0)
+            kk_next = atomicAdd(&next_tile, 1ull);
         const int crossed = walk_skip(w, c, RB, C::TS, C::RT, (int)(k - kw));
         kw = k;
         if (crossed) {
