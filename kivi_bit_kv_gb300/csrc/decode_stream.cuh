@@ -695,35 +695,42 @@ __device__ __forceinline__ void softmax_stage(ConsumerState<C, NQB>& st, float* 
         }
     }
     float alpha[NQB];
+    bool same = fv_new == st.fv;  // no rescaling at all: common once the maxima settle
 #pragma unroll
     for (int h = 0; h < NQB; ++h) {
         mt[h] = warp_max(mt[h]);
         const float mn = fmaxf(st.m[h], mt[h]);
-        alpha[h] = ex2(st.m[h] - mn);  // 0 while the state is empty
+        alpha[h] = ex2(st.m[h] - mn);  // 0 while the state is empty; 1 if the maximum stays
+        same = same && alpha[h] == 1.0f;
         st.m[h] = mn;
-        st.l[h] *= alpha[h];
-#pragma unroll
-        for (int g = 0; g < C::NGM; ++g)
-            st.z[h][g] *= alpha[h];
-#pragma unroll
-        for (int i = 0; i < C::CPL; ++i)
-            st.r[h][i] *= alpha[h];
     }
-    // o is kept in units of 1 / fv: rescale to the new value weight scale
-    const float ratio = fv_new * __frcp_rn(st.fv);  // exact: powers of two
-    st.fv = fv_new;
-    const int tg = lane & 3;
-    const float ro0 = seln<NQB>(alpha, pv_col_head<C, NQB>(tg, 0)) * ratio;
-    const float ro1 = seln<NQB>(alpha, pv_col_head<C, NQB>(tg, 1)) * ratio;
+    if (!same) {  // warp-uniform: every lane holds the same maxima and scales
 #pragma unroll
-    for (int sg = 0; sg < C::NSEG; ++sg)
+        for (int h = 0; h < NQB; ++h) {
+            st.l[h] *= alpha[h];
 #pragma unroll
-        for (int j = 0; j < C::NTV; ++j) {
-            st.o[sg][j][0] *= ro0;
-            st.o[sg][j][1] *= ro1;
-            st.o[sg][j][2] *= ro0;
-            st.o[sg][j][3] *= ro1;
+            for (int g = 0; g < C::NGM; ++g)
+                st.z[h][g] *= alpha[h];
+#pragma unroll
+            for (int i = 0; i < C::CPL; ++i)
+                st.r[h][i] *= alpha[h];
         }
+        // o is kept in units of 1 / fv: rescale to the new value weight scale
+        const float ratio = fv_new * __frcp_rn(st.fv);  // exact: powers of two
+        st.fv = fv_new;
+        const int tg = lane & 3;
+        const float ro0 = seln<NQB>(alpha, pv_col_head<C, NQB>(tg, 0)) * ratio;
+        const float ro1 = seln<NQB>(alpha, pv_col_head<C, NQB>(tg, 1)) * ratio;
+#pragma unroll
+        for (int sg = 0; sg < C::NSEG; ++sg)
+#pragma unroll
+            for (int j = 0; j < C::NTV; ++j) {
+                st.o[sg][j][0] *= ro0;
+                st.o[sg][j][1] *= ro1;
+                st.o[sg][j][2] *= ro0;
+                st.o[sg][j][3] *= ro1;
+            }
+    }
 #pragma unroll
     for (int u = 0; u < (C::TS + 63) / 64; ++u) {
         const int t = 2 * (lane + 32 * u);
@@ -1423,13 +1430,13 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
         }
         if (o_seg >= 0 && o_seg != seg)
             publish();
-        const int h = w.rr / NP, pass = w.rr - h * NP;
-        const int hq0 = h * NQ + pass * NQB;
         // a new segment (a new row): its query heads go to the warp's scratch
         // once the tile's wait is over; the loads start now
         const bool newq = o_seg < 0;
         uint4 qv[QPL];
         if (newq) {
+            const int h = w.rr / NP, pass = w.rr - h * NP;
+            const int hq0 = h * NQ + pass * NQB;
             o_seg = seg;
             o_start = seg_start;
             o_rowend = k + (w.nt - 1 - w.j);
