@@ -224,9 +224,9 @@ struct StreamCfg {
     static constexpr int R_END = O_VR + RT * RROW;
     static constexpr int SLOT = round_up(cmax(Q_END, R_END), 128);
     // per-consumer scratch (floats): logits / probabilities [NQB][LS]
-    // (two floats of padding per 16 tokens), the scaled query [NQB][QWS],
-    // the value weights [2 parts][UNITS][UTS] fp16 for UB tokens at a time,
-    // the row's query heads [NQB][D] fp16
+    // (two floats of padding per 16 tokens), the scaled query [NQB][QWS]
+    // and, over it once q . K is done, the value weights [2 parts][UNITS][UTS]
+    // fp16 for UB tokens at a time, then the row's query heads [NQB][D] fp16
     static constexpr int LS = TS + TS / 8;
     static constexpr int QWS = D + 4;
     static constexpr int UNITS = NGM * NQB;            // value weight units (group, head)
@@ -236,18 +236,19 @@ struct StreamCfg {
     static constexpr int UTS = UB + 8;                 // halves per weight row
     static constexpr int W_LG = 0;
     static constexpr int W_QW = W_LG + NQB * LS;
-    static constexpr int W_UB = W_QW + NQB * QWS;
-    static constexpr int W_Q = round_up(W_UB + UNITS * UTS, 4);  // the row's query heads, fp16
+    static constexpr int W_UB = W_QW;
+    static constexpr int W_Q = round_up(W_UB + cmax(NQB * QWS, UNITS * UTS), 4);
     static constexpr int QPIECES = NQB * D / 8;                  // 16-byte pieces of them
     static constexpr int WARP_FLOATS = W_Q + NQB * D / 2;
     // merge buffer (floats): o [NC][NQB][D], m, l [NC][NQB], z [NC][NQB][NGM];
-    // NMB of them, used by row segments in turn
+    // NMB of them, used by row segments in turn (two leave a twelfth stage
+    // room at int2, D = 128)
     static constexpr int M_O = 0;
     static constexpr int M_M = M_O + NC * NQB * D;
     static constexpr int M_L = M_M + NC * NQB;
     static constexpr int M_Z = M_L + NC * NQB;
     static constexpr int M_END = round_up(M_Z + NC * NQB * NGM, 4);
-    static constexpr int NMB = NC * NQB * D <= 2048 ? 4 : 2;
+    static constexpr int NMB = 2;
     static constexpr int FIXED_BYTES = 4 * (NC * WARP_FLOATS + NMB * M_END) + kStreamStaticSmem;
     static constexpr int THREADS = 32 * kStreamWarps;
     static_assert(TS % TOK == 0 && TS % 16 == 0 && RT % 16 == 0 && RT <= TS, "tile shape");

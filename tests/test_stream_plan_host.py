@@ -152,11 +152,12 @@ def test_warp_scratch(plan):
         nqb = s["nqb"]
         assert s["LS"] >= s["TS"] + 2 * ((s["TS"] - 1) // 16) + 1  # padded logit rows
         assert s["W_QW"] == s["W_LG"] + nqb * s["LS"]
-        assert s["W_UB"] == s["W_QW"] + nqb * s["QWS"]
+        # the value weights overlay the scaled query (dead once q . K is done)
+        assert s["W_UB"] == s["W_QW"]
         assert s["UNITS"] == s["NGM"] * nqb
         assert s["UB"] % 16 == 0 and s["TS"] % s["UB"] == 0 and s["UTS"] >= s["UB"]
         # 2 parts x UNITS rows of UTS fp16 weights
-        assert s["W_UB"] + s["UNITS"] * s["UTS"] <= s["W_Q"]
+        assert s["W_UB"] + s["UNITS"] * s["UTS"] <= s["W_Q"] and s["W_QW"] + nqb * s["QWS"] <= s["W_Q"]
         # the row's query heads, fp16, in 16-byte pieces
         assert s["W_Q"] % 4 == 0 and s["W_Q"] + nqb * s["D"] // 2 <= s["WARP_FLOATS"]
         assert s["WARP_FLOATS"] % 4 == 0 and s["QWS"] % 4 == 0 and s["LS"] % 2 == 0
