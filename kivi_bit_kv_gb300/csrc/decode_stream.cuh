@@ -1522,8 +1522,9 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
 // slot of its own piece, the last range with a piece, and the tile count NT
 // that places range k at tile NT k / N), so after its wait this kernel reads
 // the descriptor, then the pieces' (m, l) pairs, then their o rows, four
-// pieces at a time.  The sums run over the pieces in order, so the result
-// does not depend on timing.
+// pieces at a time; a row of at most four pieces (the usual case) has its
+// pairs and rows read in one round.  The sums run over the pieces in order,
+// so the result does not depend on timing.
 template <int NQB, int D, int TS, int RT>
 __global__ void __launch_bounds__(128)
 decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __restrict__ ws,
@@ -1556,6 +1557,52 @@ decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __
         return;
 
     constexpr int ND = (D + T - 1) / T;  // channels per thread
+    const int t = (int)threadIdx.x;
+    if (P <= 4) {
+        // the common case: every load of the row in one round (the sums run
+        // in the same order as below, so the result is the same)
+        float mr[4][NQB], lr[4][NQB], v[4][NQB][ND];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+            const int k = i + r;
+            const bool hk = r < P && (k == i || X(k + 1) > X(k));
+            const float* pc = piece(k);
+#pragma unroll
+            for (int hh = 0; hh < NQB; ++hh) {
+                mr[r][hh] = hk ? pc[NQB * D + hh] : -INFINITY;
+                lr[r][hh] = hk ? pc[NQB * D + NQB + hh] : 0.0f;
+#pragma unroll
+                for (int u = 0; u < ND; ++u)
+                    v[r][hh][u] = hk && t + u * T < D ? pc[hh * D + t + u * T] : 0.0f;
+            }
+        }
+#pragma unroll
+        for (int hh = 0; hh < NQB; ++hh) {
+            float Mh = -INFINITY;
+#pragma unroll
+            for (int r = 0; r < 4; ++r)
+                Mh = fmaxf(Mh, mr[r][hh]);
+            float Lh = 0.0f, oh[ND];
+#pragma unroll
+            for (int u = 0; u < ND; ++u)
+                oh[u] = 0.0f;
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                const float e = mr[r][hh] > -INFINITY ? ex2(mr[r][hh] - Mh) : 0.0f;
+                if (e == 0.0f)
+                    continue;
+                Lh = fmaf(e, lr[r][hh], Lh);
+#pragma unroll
+                for (int u = 0; u < ND; ++u)
+                    oh[u] = fmaf(e, v[r][hh][u], oh[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < ND; ++u)
+                if (t + u * T < D)
+                    dst[hh * D + t + u * T] = oh[u] / Lh;
+        }
+        return;
+    }
     float M[NQB], L[NQB], o[NQB][ND];
 #pragma unroll
     for (int hh = 0; hh < NQB; ++hh) {
@@ -1565,7 +1612,6 @@ decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __
         for (int u = 0; u < ND; ++u)
             o[hh][u] = 0.0f;
     }
-    const int t = (int)threadIdx.x;
     auto load_ml = [&](int c0) {
         const int k = i + c0 + t;
         const bool hk = c0 + t < P && (k == i || X(k + 1) > X(k));
