@@ -14,18 +14,24 @@
 // output written; a row cut by a range boundary leaves one partial (o, m, l)
 // per CTA, merged by decode_stream_combine_kernel.
 //
-// Pipeline.  Warp NC of the CTA is the producer: for every tile of the range
-// one of its threads waits for a free stage, announces the stage's byte count
-// on the stage's mbarrier and issues 1-D bulk copies (cp.async.bulk, the TMA
-// engine), global to shared: seven per quantized tile (the row's query, the
-// packed key word-rows, key scales, key zeros, packed value rows, value
-// scales, value zeros; each a contiguous range of its buffer) and three or
-// five per residual tile (query, key and value ring slots, which wrap at most
-// once).  Warps 0 .. NC-1 are consumers: consumer w takes tiles w,
-// w + NC, ... of the range, waits for its stage, computes the whole tile and
-// releases the stage.  Each consumer keeps its own online-softmax state
-// (running maximum m, sums l, the weighted value sums); at the end of every
-// row segment the consumers merge their states through shared memory.
+// Pipeline.  A CTA is three warpgroups (setmaxnreg: the two consumer
+// warpgroups at 224 registers a thread, the third at 56).  In the third,
+// lane 0 of warp 8 issues the key copies of every tile of the range and lane
+// 0 of warp 9 the value copies: each waits for a free stage of the ring,
+// announces its bytes on the stage's full mbarrier and issues 1-D bulk copies
+// (cp.async.bulk, the TMA engine), global to shared -- three per quantized
+// tile (packed word-rows, scales, zeros of its side; each a contiguous range
+// of its buffer) and one or two per residual tile (the ring slots, which
+// wrap at most once).  Warps 0 .. NC-1 are consumers: they take the range's
+// tiles in order from a shared counter (each reserves its next tile while it
+// computes the current one), wait for the tile's stage, compute the whole
+// tile and release the stage.  The query heads of a row are loaded from
+// global memory into the warp's scratch when the warp starts a row.  Each
+// consumer keeps its own online-softmax state (running maximum m, sums l,
+// the weighted value sums) per row segment (the range's tiles of one row);
+// when it moves on, it publishes the state to one of two merge buffers, and
+// the warp that completes the segment's tile count merges the states and
+// writes the row's output (or the CTA's partial for a cut row).
 //
 // A quantized tile, per consumer warp:
 //   1. q . K_hat on the warp-level tensor cores (decode_mma.cuh: codes as
