@@ -8,8 +8,11 @@
 // cut into tiles: ceil(Tq/TS) quantized tiles of TS tokens (the last one
 // shorter), then ceil((n - Tq)/RT) residual tiles of RT fp16 tokens.  Both
 // kinds move about the same number of bytes.  One CTA runs per SM; CTA i takes
-// the contiguous range [i NT / N, (i+1) NT / N) of the NT tiles of all rows in
-// order, so the load is balanced whatever the (device-side, ragged) lengths.
+// a contiguous range of the tiles of all rows in order, cut where the running
+// weight of the tiles (each tile one unit, each row a fixed extra for its
+// start and finish) crosses i/N of the total, so the load is balanced
+// whatever the (device-side, ragged) lengths and however many rows a range
+// touches.
 // A row that lies wholly inside one CTA's range is finished there and its
 // output written; a row cut by a range boundary leaves one partial (o, m, l)
 // per CTA, merged by decode_stream_combine_kernel.
@@ -362,85 +365,137 @@ __device__ __forceinline__ int walk_n(const Walk& w, int TS, int RT)
     return w.j < w.nq ? min(TS, w.Tq - t0) : min(RT, w.len - t0);
 }
 
-// Tiles of sequence b's rows (each of the RB rows of b holds nt tiles).
-__device__ __forceinline__ int row_tiles(int len, const kivi_cache& c, int TS, int RT)
-{
-    const int Tq = quantized_tokens(len, c.G, c.R);
-    return (Tq + TS - 1) / TS + (len - Tq + RT - 1) / RT;
-}
 
-// Exclusive prefix sum of v over the CTA (THREADS threads) and its total.
+// Exclusive prefix sums of the pairs (v.x, v.y) over the CTA (THREADS
+// threads) and their totals; red holds 2 x THREADS / 32 values.
 template <int THREADS>
-__device__ __forceinline__ long long cta_exscan(long long v, long long& total, long long* red)
+__device__ __forceinline__ longlong2 cta_exscan2(longlong2 v, longlong2& total, long long* red)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    long long x = v;
+    long long x = v.x, y = v.y;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const long long y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o)
-            x += y;
+        const long long ux = __shfl_up_sync(0xffffffffu, x, o);
+        const long long uy = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) {
+            x += ux;
+            y += uy;
+        }
     }
-    if (lane == 31)
-        red[warp] = x;
+    if (lane == 31) {
+        red[2 * warp] = x;
+        red[2 * warp + 1] = y;
+    }
     __syncthreads();
-    long long off = 0, tot = 0;
+    long long ox = 0, oy = 0, tx = 0, ty = 0;
 #pragma unroll
     for (int w = 0; w < THREADS / 32; ++w) {
-        const long long r = red[w];
-        off += w < warp ? r : 0;
-        tot += r;
+        const long long rx = red[2 * w], ry = red[2 * w + 1];
+        ox += w < warp ? rx : 0;
+        oy += w < warp ? ry : 0;
+        tx += rx;
+        ty += ry;
     }
     __syncthreads();
-    total = tot;
-    return off + x - v;
+    total = make_longlong2(tx, ty);
+    return make_longlong2(ox + x - v.x, oy + y - v.y);
 }
 
-// CTA range record: first tile (global index) and its position.
+// CTA range record: first tile (global index) and its position; wend: the
+// split weight at the end of that tile's row.
 struct RangeStart {
-    long long g;
+    long long g, wend;
     int b, rr, j;
 };
 
+// The split of the tiles among the CTAs weighs each quantized tile
+// kStreamTileWeight, each residual tile kStreamResWeight, and each row
+// row_extra(NQB) more, put on the row's first tile: starting and finishing a
+// row segment (the query load, the state merge over NQB heads, the partial
+// tiles) costs a CTA about as much as two tiles per head, so ranges of equal
+// tile counts end at different times when their numbers of rows differ (on
+// B = 64 ragged rows of 1024-8192 tokens, CTA end times spread from 262 to
+// 291 us with equal tile counts).  Measured: a residual tile weighs as much
+// as a quantized one (heavier or lighter residual weights were slower).
+constexpr int kStreamTileWeight = 8;
+constexpr int kStreamResWeight = 8;
+__host__ __device__ constexpr int row_extra(int NQB) { return 16 * NQB; }
+
+// A row's tiles for the split: nq quantized, nr residual.
+struct RowTiles {
+    int nq, nr;
+};
+__device__ __forceinline__ RowTiles row_tile_counts(int len, const kivi_cache& c, int TS, int RT)
+{
+    const int Tq = quantized_tokens(len, c.G, c.R);
+    return RowTiles{(Tq + TS - 1) / TS, (len - Tq + RT - 1) / RT};
+}
+template <int NQB>
+__device__ __forceinline__ long long row_weight(RowTiles t)
+{
+    return t.nq + t.nr > 0
+               ? (long long)t.nq * kStreamTileWeight + (long long)t.nr * kStreamResWeight + row_extra(NQB)
+               : 0;
+}
+// The tile of a row whose weight interval holds offset off (< the row's
+// weight): tile 0 covers the row's extra and its own weight.
+template <int NQB>
+__device__ __forceinline__ int tile_at(RowTiles t, long long off)
+{
+    const long long x = off - row_extra(NQB);
+    const long long q = (long long)t.nq * kStreamTileWeight;
+    const int j = x < q ? (int)(x / kStreamTileWeight) : t.nq + (int)((x - q) / kStreamResWeight);
+    return x < 0 ? 0 : j;
+}
+
 // Start of CTA k's range and of CTA k+1's (the end), from the device-side
-// lengths: two passes over the sequences (total, then location).
-template <int THREADS>
+// lengths: two passes over the sequences (totals, then location).  With Wtot
+// the weight of all tiles, range k starts at the tile whose weight interval
+// holds Wtot k / N (tile 0 of a row covers the row's weight and its own), so
+// a range may be empty; *total receives Wtot.
+template <int THREADS, int NQB>
 __device__ __forceinline__ void locate_range(const kivi_cache& c, int RB, int TS, int RT, int k, int N,
                                              RangeStart& r0, RangeStart& r1, long long* red, RangeStart* sh,
                                              long long* total = nullptr)
 {
-    long long NT = 0;
+    long long W = 0, NT = 0;
     for (int base = 0; base < c.B; base += THREADS) {
         const int b = base + (int)threadIdx.x;
-        const long long v = b < c.B ? (long long)RB * row_tiles(c.len[b], c, TS, RT) : 0;
-        long long tot;
-        cta_exscan<THREADS>(v, tot, red);
-        NT += tot;
+        const RowTiles t = b < c.B ? row_tile_counts(c.len[b], c, TS, RT) : RowTiles{0, 0};
+        longlong2 tot;
+        cta_exscan2<THREADS>(make_longlong2(RB * row_weight<NQB>(t), (long long)RB * (t.nq + t.nr)), tot, red);
+        W += tot.x;
+        NT += tot.y;
     }
-    const long long X[2] = {NT * k / N, NT * (k + 1) / N};
+    const long long X[2] = {W * k / N, W * (k + 1) / N};
     if (threadIdx.x < 2)
-        sh[threadIdx.x] = RangeStart{X[threadIdx.x], c.B, 0, 0};
+        sh[threadIdx.x] = RangeStart{NT, W, c.B, 0, 0};
     __syncthreads();
-    long long ex0 = 0;
+    long long ew = 0, et = 0;
     for (int base = 0; base < c.B; base += THREADS) {
         const int b = base + (int)threadIdx.x;
-        const int nt = b < c.B ? row_tiles(c.len[b], c, TS, RT) : 0;
-        const long long v = (long long)RB * nt;
-        long long tot;
-        const long long ex = ex0 + cta_exscan<THREADS>(v, tot, red);
+        const RowTiles t = b < c.B ? row_tile_counts(c.len[b], c, TS, RT) : RowTiles{0, 0};
+        const int nt = t.nq + t.nr;
+        const long long wr = row_weight<NQB>(t);
+        longlong2 tot;
+        const longlong2 ex = cta_exscan2<THREADS>(make_longlong2(RB * wr, (long long)RB * nt), tot, red);
+        const long long xw = ew + ex.x, xt = et + ex.y;
 #pragma unroll
         for (int i = 0; i < 2; ++i)
-            if (v > 0 && ex <= X[i] && X[i] < ex + v) {
-                const long long w = X[i] - ex;
-                sh[i] = RangeStart{X[i], b, (int)(w / nt), (int)(w % nt)};
+            if (nt > 0 && xw <= X[i] && X[i] < xw + RB * wr) {
+                const long long o = X[i] - xw;
+                const int rr = (int)(o / wr);
+                const int j = tile_at<NQB>(t, o - rr * wr);
+                sh[i] = RangeStart{xt + (long long)rr * nt + j, xw + (rr + 1) * wr, b, rr, j};
             }
-        ex0 += tot;
+        ew += tot.x;
+        et += tot.y;
     }
     __syncthreads();
     r0 = sh[0];
     r1 = sh[1];
     if (total)
-        *total = NT;
+        *total = W;
 }
 
 // ------------------------------------------------------- consumer state ---
@@ -1106,7 +1161,7 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     using C = StreamCfg<BK, BV, NQB, D, NC>;
     constexpr int ns = stream_stages<C>();  // stages of the ring
     extern __shared__ __align__(128) uint8_t smem[];
-    __shared__ long long red[C::THREADS / 32];
+    __shared__ long long red[2 * (C::THREADS / 32)];
     __shared__ RangeStart sh_range[2];
     __shared__ int abort_flag;
     // per merge buffer: warps published (bit mask), tiles published, last segment merged
@@ -1134,8 +1189,8 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     int* wsi = reinterpret_cast<int*>(ws);
 
     RangeStart r0, r1;
-    long long NT = 0;
-    locate_range<C::THREADS>(c, RB, C::TS, C::RT, blockIdx.x, gridDim.x, r0, r1, red, sh_range, &NT);
+    long long W = 0;  // split weight of all tiles
+    locate_range<C::THREADS, NQB>(c, RB, C::TS, C::RT, blockIdx.x, gridDim.x, r0, r1, red, sh_range, &W);
     // zero outputs of empty sequences b = blockIdx.x mod gridDim.x (no tile writes them)
     for (int b = blockIdx.x; b < c.B; b += gridDim.x)
         if (c.len[b] == 0)
@@ -1144,24 +1199,21 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     if (threadIdx.x == 0) {
         // The row in which this range ends, for the combine kernel: cut (the
         // range ends inside it and holds its first tile), its sequence and
-        // row, the partial slot of this CTA's piece, the last range with a
-        // piece (range k starts at tile NT k / N), and NT.
+        // row, the partial slot of this CTA's piece, and the last range with
+        // a piece: the last k whose split point W k / N lies before the
+        // row's end weight r1.wend.
         int* dsc = wsi + kStreamHeaderFloats + stream_partial_floats(D, NQB, gridDim.x) +
                    (size_t)blockIdx.x * kStreamDescInts;
         const long long g0 = r0.g, g1 = r1.g, row_first = g1 - r1.j;
         const bool cut = g1 > g0 && r1.j != 0 && r1.b < c.B && row_first >= g0;
         int last = 0;
-        if (cut) {
-            const long long row_end = row_first + row_tiles(c.len[r1.b], c, C::TS, C::RT);
-            last = (int)min((long long)gridDim.x - 1, (row_end * gridDim.x - 1) / NT);
-        }
+        if (cut)
+            last = (int)min((long long)gridDim.x - 1, (r1.wend * gridDim.x - 1) / W);
         dsc[0] = cut ? 1 : 0;
         dsc[1] = r1.b;
         dsc[2] = r1.rr;
         dsc[3] = row_first == g0 ? 0 : 1;
         dsc[4] = last;
-        dsc[5] = (int)(NT & 0xffffffff);
-        dsc[6] = (int)(NT >> 32);
         for (int s = 0; s < ns; ++s) {
             mbar_init(&full[s], 2);  // the key and the value producer
             mbar_init(&empty[s], 1);
@@ -1182,8 +1234,13 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
     }
     __syncthreads();
     const long long ntiles = r1.g - r0.g;
-    if (ntiles <= 0)
+    if (ntiles <= 0) {
+        // an empty range inside a cut row: its slot 0 holds no piece, which
+        // the combine reads as the maximum -inf
+        if (threadIdx.x < NQB && kivi_check((int)blockIdx.x < kMaxStreamCTAs, wsi))
+            ws[kStreamHeaderFloats + (size_t)blockIdx.x * 2 * NQB * (D + 2) + NQB * D + threadIdx.x] = -INFINITY;
         return;
+    }
     Walk w0{r0.b, r0.rr, r0.j, 0, 0, 0, 0};
     walk_load(w0, c, C::TS, C::RT);
 
@@ -1522,15 +1579,16 @@ decode_stream_kernel(const kivi_cache c, const uint16_t* __restrict__ q, int Hq,
 
 // Merges the partials of the rows that CTA ranges cut: CTA i of this grid
 // takes the row in which range i ends, if range i is not empty, ends inside
-// a row, and holds that row's first tile; the ranges after it that start
-// inside the row hold its other pieces (their first row segment, slot 0).
-// Decode CTA i leaves that row in its descriptor (cut or not, the row, the
-// slot of its own piece, the last range with a piece, and the tile count NT
-// that places range k at tile NT k / N), so after its wait this kernel reads
-// the descriptor, then the pieces' (m, l) pairs, then their o rows, four
-// pieces at a time; a row of at most four pieces (the usual case) has its
-// pairs and rows read in one round.  The sums run over the pieces in order,
-// so the result does not depend on timing.
+// a row, and holds that row's first tile; the ranges after it up to the one
+// holding the row's last tile hold its other pieces (their first row
+// segment, slot 0), or nothing if they are empty (their slot 0 then holds
+// the maximum -inf, a piece of weight zero).  Decode CTA i leaves that row
+// in its descriptor (cut or not, the row, the slot of its own piece, the
+// last range with a piece), so after its wait this kernel reads the
+// descriptor, then the pieces' (m, l) pairs, then their o rows, four pieces
+// at a time; a row of at most four pieces (the usual case) has its pairs and
+// rows read in one round.  The sums run over the pieces in order, so the
+// result does not depend on timing.
 template <int NQB, int D, int TS, int RT>
 __global__ void __launch_bounds__(128)
 decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __restrict__ ws,
@@ -1549,8 +1607,6 @@ decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __
     if (dsc[0] == 0)
         return;
     const int rb = dsc[1], rr = dsc[2], slot_i = dsc[3], last = dsc[4];
-    const long long NT = (long long)(unsigned)dsc[5] | ((long long)dsc[6] << 32);
-    auto X = [&](int k) { return NT * k / N; };
     const int P = last - i + 1;  // ranges i .. last; an empty one holds no piece
     const float* part = ws + kStreamHeaderFloats;
     const size_t pstride = (size_t)NQB * (D + 2);
@@ -1571,7 +1627,7 @@ decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
             const int k = i + r;
-            const bool hk = r < P && (k == i || X(k + 1) > X(k));
+            const bool hk = r < P;
             const float* pc = piece(k);
 #pragma unroll
             for (int hh = 0; hh < NQB; ++hh) {
@@ -1620,7 +1676,7 @@ decode_stream_combine_kernel(const kivi_cache c, int Hq, int NP, const float* __
     }
     auto load_ml = [&](int c0) {
         const int k = i + c0 + t;
-        const bool hk = c0 + t < P && (k == i || X(k + 1) > X(k));
+        const bool hk = c0 + t < P;
 #pragma unroll
         for (int hh = 0; hh < NQB; ++hh) {
             s_m[t][hh] = hk ? piece(k)[NQB * D + hh] : -INFINITY;
