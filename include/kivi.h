@@ -231,8 +231,9 @@ int32_t kivi_decode_pv(const kivi_cache* c, const float* logits,
  * q: fp16 [B][Hq][D]; out: fp32 [B][Hq][D]; ws: device, >=
  * kivi_workspace_bytes(c, Hq) bytes, 16-byte aligned, contents need not be
  * initialized.  One persistent kernel (one CTA per SM, each taking a
- * contiguous share of all rows' tiles) and a combine kernel for the rows that
- * two CTAs share: two kernels on `stream`.  A sequence with len[b] == 0 gets
+ * contiguous share of all rows' tiles, the shares balanced by a weight that
+ * counts each row's start as well as its tiles) and a combine kernel for the
+ * rows that CTA shares cut: two kernels on `stream`.  A sequence with len[b] == 0 gets
  * out = 0.  The first 4 bytes of ws receive a status word: KIVI_OK, or
  * KIVI_ETIMEOUT if a bounded wait inside the kernel gave up (after two
  * seconds; the outputs are then invalid).  Calls that share a workspace must
