@@ -451,8 +451,8 @@ __device__ __forceinline__ int tile_at(RowTiles t, long long off)
 // Start of CTA k's range and of CTA k+1's (the end), from the device-side
 // lengths: two passes over the sequences (totals, then location).  With Wtot
 // the weight of all tiles, range k starts at the tile whose weight interval
-// holds Wtot k / N (tile 0 of a row covers the row's weight and its own), so
-// a range may be empty; *total receives Wtot.
+// holds Wtot k / N (tile 0 of a row covers the row's extra weight and its
+// own), so a range may be empty; *total receives Wtot.
 template <int THREADS, int NQB>
 __device__ __forceinline__ void locate_range(const kivi_cache& c, int RB, int TS, int RT, int k, int N,
                                              RangeStart& r0, RangeStart& r1, long long* red, RangeStart* sh,
