@@ -139,3 +139,28 @@ def test_decode_workloads_rotate_over_twice_the_l2():
     # the GQA cache (136 MB) is about one L2: it needs copies
     w = W.WORKLOADS["mistral_gqa"]
     assert bench.cache_copies(w, W.make_lengths(w).numpy(), w.Tmax) >= 2
+
+
+def test_timed_region_starts_behind_a_device_busy_wait():
+    """queue_ahead issues one device-side busy wait of the requested length
+    (in clock cycles at up to 2.07 GHz) through torch.cuda._sleep, and does
+    nothing where that call does not exist: with the queue empty at the start
+    event, the first call's events would also time the host's launch of it."""
+    calls = []
+
+    class _Cuda:
+        @staticmethod
+        def _sleep(cycles):
+            calls.append(cycles)
+
+    class _Torch:
+        cuda = _Cuda
+
+    bench.queue_ahead(_Torch, ms=2.0)
+    assert calls == [int(2.0 * 2.07e6)]
+
+    class _NoSleep:
+        cuda = type("cuda", (), {})
+
+    bench.queue_ahead(_NoSleep)  # no busy wait available: no error
+    assert calls == [int(2.0 * 2.07e6)]
