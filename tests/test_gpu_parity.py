@@ -143,6 +143,31 @@ def test_more_slices_than_a_grid_dimension(cuda):
     torch.cuda.empty_cache()
 
 
+def test_fused_decode_many_ragged_sequences(cuda):
+    """More sequences than the fused decode's CTA has threads (1000 > 384),
+    ragged from 0 to 300 tokens with empty ones among them: the tile split
+    then scans the lengths in several passes carrying running totals, many
+    ranges hold several short rows and some rows are cut between CTAs.  Every
+    row is compared with the oracle (empty sequences must give zeros)."""
+    B, H, Hq, D, bk, bv, G, Rr = 1000, 1, 2, 64, 2, 4, 32, 32
+    g = np.random.default_rng(41)
+    lens = g.integers(0, 301, size=B)
+    lens[g.choice(B, 40, replace=False)] = 0
+    T = int(lens.max())
+    Tmax = roundup(T + 8, G)
+    K = f16_host((B, H, T, D), 42, 2.0)
+    V = f16_host((B, H, T, D), 43)
+    q = f16_host((B, Hq, D), 44)
+    cache = new_cache(B, H, D, bk, bv, G, Rr, Tmax, cuda)
+    gpu_encode(cache, K, V, lens.tolist())
+    rc = R.RefCache(B, H, D, bk, bv, G, Rr, Tmax).encode(np16(K), np16(V), seq_lens=lens.tolist())
+    lg, o, fo = gpu_decode(cache, q)
+    rlg, ro = rc.attention(np16(q))
+    compare_attention(lg[:, :, :T], o, rlg, ro, rc.lens, fused=fo)
+    del cache
+    torch.cuda.empty_cache()
+
+
 def test_decode_is_deterministic(cuda):
     B, H, Hq, D, T = 2, 2, 4, 128, 3000
     K, V = f16_host((B, H, T, D), 5, 2.0), f16_host((B, H, T, D), 6)
