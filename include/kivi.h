@@ -216,6 +216,9 @@ int32_t kivi_decode_qk(const kivi_cache* c, const uint16_t* q, int32_t Hq,
  * parallel; per-chunk partial results go to the caller's workspace `ws`
  * (device, >= kivi_workspace_bytes(c, Hq) bytes, 16-byte aligned) and a
  * second kernel combines them.  A sequence with len[b] == 0 gets out = 0.
+ * The chunking and every sum's order are fixed, so kivi_decode_qk followed
+ * by kivi_decode_pv gives the same bits from run to run (the fused
+ * kivi_decode_attention is faster and agrees with it to rounding order).
  */
 int32_t kivi_decode_pv(const kivi_cache* c, const float* logits,
                        int32_t ld_logits, int32_t Hq, float* out, void* ws,
@@ -237,7 +240,9 @@ int32_t kivi_decode_pv(const kivi_cache* c, const float* logits,
  * out = 0.  The first 4 bytes of ws receive a status word: KIVI_OK, or
  * KIVI_ETIMEOUT if a bounded wait inside the kernel gave up (after two
  * seconds; the outputs are then invalid).  Calls that share a workspace must
- * not overlap on the GPU.
+ * not overlap on the GPU.  Which consumer warp takes which tile varies from
+ * run to run, so results agree from run to run to rounding order, not bit
+ * for bit; kivi_decode_qk + kivi_decode_pv is the deterministic path.
  */
 int32_t kivi_decode_attention(const kivi_cache* c, const uint16_t* q,
                               int32_t Hq, float sm_scale, float* out,
